@@ -381,9 +381,9 @@ def corruption(p: float, vocab: int, length: int, seed: int = SEED_CORRUPT, requ
 
 
 def fc_taps(n_rows: int, width: int, seed: int = SEED_PROMPT) -> np.ndarray:
-    """Tapped target features N(0, 1) as bf16 bits [n_rows][width] (the draft-alone workload)."""
+    """Tapped target features N(0, 1) as float32 [n_rows][width] (the draft-alone workload)."""
     rng = np.random.default_rng([seed, 77])
-    return bf16_bits(rng.standard_normal((n_rows, width), dtype=np.float32))
+    return rng.standard_normal((n_rows, width), dtype=np.float32)
 
 
 def activations(m: int, k: int, seed: int) -> np.ndarray:

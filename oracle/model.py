@@ -3,9 +3,9 @@ forward, acceptance, commit and snapshot. TEST INFRASTRUCTURE ONLY: imported by 
 smoke check and by the benchmark's CPU-baseline leg; never by the library.
 
 Plain and slow on purpose. Every product runs in dfl_oracle.c (double, ascending k); everything else
-here is double-precision numpy on one row at a time; a value is rounded to float32 where the model
-stores it and to bf16 at the three rounding points of the model:
-  R1  every product's input is bf16,  R2  keys and values are stored as bf16,  R3  taps are bf16.
+here is double-precision numpy on one row at a time. Activations, keys, values and taps are the pages'
+"floats" (KV planes of "2 x 256 floats per position"; taps of "(P+tokens)*T*H floats"): every value is
+rounded to float32 where the model stores it. Weights are Q4_1 or bf16 as stored.
 
 Sources (pages, by title and section):
   * 1bit engine PR "npu forward: Gemma4 verifies a draft in one batched pass; KV row width per layer",
@@ -118,6 +118,7 @@ class Target:
         # a mutant that counts every layer at one width, to show the tests catch it
         self.widths = [width_mutant if (width_mutant and w[l]) else w[l] for l in range(cfg.n_layers)]
         self.planes: Dict[int, np.ndarray] = {l: np.zeros(0, F32) for l in range(cfg.n_layers) if cfg.is_owner(l)}
+        self.record = None               # optional dict: per-layer intermediates of the last forward
         self.n = 0                       # committed positions
         self.pending = 0                 # rows of the last forward not yet committed
         self.taps = np.zeros((0, len(self.tap_layers) * cfg.hidden), F32)
@@ -167,7 +168,7 @@ class Target:
             p = f"t{l}."
             own, nkv = c.kv_owner[l], c.kv_heads[l]
             base = c.rope_base_full if c.layer_type[l] else c.rope_base_sliding
-            h = nat.bf16r(rmsnorm(x, self.norm[p + "attn_norm"], c.eps))
+            h = rmsnorm(x, self.norm[p + "attn_norm"], c.eps)
             y = nat.linear_q41(h, W[p + "wqkv"] if own == l else W[p + "wq"])
             q = y[:, : nq * hd].reshape(k, nq, hd)
             q = np.stack([rope(rmsnorm(q[i], self.norm[p + "q_norm"], c.eps), pos[i], base) for i in range(k)])
@@ -175,7 +176,7 @@ class Target:
                 kk = y[:, nq * hd:(nq + nkv) * hd].reshape(k, nkv, hd)
                 vv = y[:, (nq + nkv) * hd:(nq + 2 * nkv) * hd]
                 kk = np.stack([rope(rmsnorm(kk[i], self.norm[p + "k_norm"], c.eps), pos[i], base) for i in range(k)])
-                rows = np.concatenate([nat.bf16r(kk).reshape(k, -1), nat.bf16r(vv)], axis=1)
+                rows = np.concatenate([kk.reshape(k, -1), vv], axis=1).astype(F32)
                 self.planes[l] = np.concatenate([self.planes[l], rows.reshape(-1)])
             width = self.widths[own]
             plane = self.planes[own].reshape(-1, width) if width == 2 * nkv * hd else None
@@ -192,31 +193,36 @@ class Target:
                     Kj = plane[lo:hi, g * hd:(g + 1) * hd]
                     Vj = plane[lo:hi, (nkv + g) * hd:(nkv + g + 1) * hd]
                     o[i, hq] = attend(q[i, hq], Kj, Vj, 1.0 / np.sqrt(hd))
-            y = nat.linear_q41(nat.bf16r(o.reshape(k, nq * hd)), W[p + "wo"])
+            if self.record is not None:
+                self.record[l] = {"h": h.copy(), "qkv": y.copy(), "q": q.reshape(k, -1).copy(),
+                                  "o": o.reshape(k, nq * hd).copy()}
+            y = nat.linear_q41(o.reshape(k, nq * hd), W[p + "wo"])
             x = add(x, rmsnorm(y, self.norm[p + "post_attn_norm"], c.eps))
-            b = nat.bf16r(rmsnorm(x, self.norm[p + "pre_ffn_norm"], c.eps))
+            b = rmsnorm(x, self.norm[p + "pre_ffn_norm"], c.eps)
             gu = nat.linear_q41(b, W[p + "wgu"])
             F = c.ffn[l]
-            a = nat.bf16r((silu(gu[:, :F]) * np.asarray(gu[:, F:], F64)).astype(F32))
+            a = (silu(gu[:, :F]) * np.asarray(gu[:, F:], F64)).astype(F32)
             y = nat.linear_q41(a, W[p + "wd"])
             x = add(x, rmsnorm(y, self.norm[p + "post_ffn_norm"], c.eps))
             if c.ple_dim:
                 P = c.ple_dim
-                t = nat.linear_q41(nat.bf16r(x), W[p + "wple_g"])
-                z = nat.bf16r((silu(t) * np.asarray(ple[:, l * P:(l + 1) * P], F64)).astype(F32))
+                t = nat.linear_q41(x, W[p + "wple_g"])
+                z = (silu(t) * np.asarray(ple[:, l * P:(l + 1) * P], F64)).astype(F32)
                 y = nat.linear_q41(z, W[p + "wple_p"])
                 x = add(x, rmsnorm(y, self.norm[p + "ple_norm"], c.eps))
                 x = (np.asarray(x, F64) * F64(np.float32(self.lam[l]))).astype(F32)
             if l in self.tap_layers:
                 ti = self.tap_layers.index(l)
-                taps[:, ti * H:(ti + 1) * H] = nat.bf16r(x)
+                taps[:, ti * H:(ti + 1) * H] = x
+            if self.record is not None:
+                self.record[l]["x"] = x.copy()
         self.last_hidden = x
         self.pending = k
         self.taps = np.concatenate([self.taps, taps])
         return self.head(x)
 
     def head(self, x: np.ndarray) -> np.ndarray:
-        return nat.linear_bf16(nat.bf16r(rmsnorm(x, self.norm["final_norm"], self.cfg.eps)), self.W["head"])
+        return nat.linear_bf16(rmsnorm(x, self.norm["final_norm"], self.cfg.eps), self.W["head"])
 
 
 # ---- draft -------------------------------------------------------------------------------------------
@@ -249,19 +255,19 @@ class Draft:
         self.ctx_v = [a[:n].copy() for a in self.ctx_v]
 
     def context_rows(self, taps: np.ndarray) -> np.ndarray:
-        """c_j = RMSNorm_hidden(bf16(concat taps_j) . fc) for each row of taps."""
+        """c_j = RMSNorm_hidden(concat taps_j . fc) for each row of taps."""
         d = self.cfg
-        return rmsnorm(nat.linear_bf16(nat.bf16r(taps), self.W["d.fc"]), self.norm["d.hidden_norm"], d.eps)
+        return rmsnorm(nat.linear_bf16(taps, self.W["d.fc"]), self.norm["d.hidden_norm"], d.eps)
 
     def append_ctx(self, taps: np.ndarray) -> None:
         """Make the rows `taps` (positions n_ctx, n_ctx+1, ...) context: each layer's key and value of
-        bf16(c_j), with the key normed and rotated at position j."""
+        c_j, with the key normed and rotated at position j."""
         d = self.cfg
         r = taps.shape[0]
         if r == 0:
             return
         pos = self.n_ctx + np.arange(r)
-        cb = nat.bf16r(self.context_rows(taps))
+        cb = self.context_rows(taps)
         nq, hd = d.n_heads, d.head_dim
         for l in range(d.n_layers):
             p = f"d{l}."
@@ -269,8 +275,8 @@ class Draft:
             y = nat.linear_q41(cb, Wkv)
             kk = y[:, : self.kv].reshape(r, d.n_kv_heads, hd)
             kk = np.stack([rope(rmsnorm(kk[i], self.norm[p + "k_norm"], d.eps), pos[i], d.rope_base) for i in range(r)])
-            self.ctx_k[l] = np.concatenate([self.ctx_k[l], nat.bf16r(kk.reshape(r, -1))])
-            self.ctx_v[l] = np.concatenate([self.ctx_v[l], nat.bf16r(y[:, self.kv:])])
+            self.ctx_k[l] = np.concatenate([self.ctx_k[l], kk.reshape(r, -1)])
+            self.ctx_v[l] = np.concatenate([self.ctx_v[l], y[:, self.kv:]])
 
     def block(self, token: int, emb: np.ndarray, head: np.ndarray):
         """Draft block at positions n..n+B-1 (n = context rows held) for rows [token, mask, ...].
@@ -285,14 +291,14 @@ class Draft:
         grp = nq // nkv
         for l in range(d.n_layers):
             p = f"d{l}."
-            h = nat.bf16r(rmsnorm(x, self.norm[p + "attn_norm"], d.eps))
+            h = rmsnorm(x, self.norm[p + "attn_norm"], d.eps)
             y = nat.linear_q41(h, W[p + "wqkv"])
             q = y[:, : nq * hd].reshape(B, nq, hd)
             q = np.stack([rope(rmsnorm(q[i], self.norm[p + "q_norm"], d.eps), pos[i], d.rope_base) for i in range(B)])
             kk = y[:, nq * hd:(nq + nkv) * hd].reshape(B, nkv, hd)
             kk = np.stack([rope(rmsnorm(kk[i], self.norm[p + "k_norm"], d.eps), pos[i], d.rope_base) for i in range(B)])
-            Kb = nat.bf16r(kk.reshape(B, -1))
-            Vb = nat.bf16r(y[:, (nq + nkv) * hd:])
+            Kb = kk.reshape(B, -1)
+            Vb = y[:, (nq + nkv) * hd:]
             Kall = np.concatenate([self.ctx_k[l][lo:n], Kb])
             Vall = np.concatenate([self.ctx_v[l][lo:n], Vb])
             o = np.zeros((B, nq, hd), F32)
@@ -301,11 +307,11 @@ class Draft:
                     g = hq // grp
                     o[i, hq] = attend(q[i, hq], Kall[:, g * hd:(g + 1) * hd], Vall[:, g * hd:(g + 1) * hd],
                                       1.0 / np.sqrt(hd))
-            x = add(x, nat.linear_q41(nat.bf16r(o.reshape(B, -1)), W[p + "wo"]))
-            b = nat.bf16r(rmsnorm(x, self.norm[p + "ffn_norm"], d.eps))
+            x = add(x, nat.linear_q41(o.reshape(B, -1), W[p + "wo"]))
+            b = rmsnorm(x, self.norm[p + "ffn_norm"], d.eps)
             gu = nat.linear_q41(b, W[p + "wgu"])
-            a = nat.bf16r((silu(gu[:, : d.ffn]) * np.asarray(gu[:, d.ffn:], F64)).astype(F32))
+            a = (silu(gu[:, : d.ffn]) * np.asarray(gu[:, d.ffn:], F64)).astype(F32)
             x = add(x, nat.linear_q41(a, W[p + "wd"]))
         self.last_hidden = x
-        logits = nat.linear_bf16(nat.bf16r(rmsnorm(x[1:], self.norm["d.final_norm"], d.eps)), head)
+        logits = nat.linear_bf16(rmsnorm(x[1:], self.norm["d.final_norm"], d.eps), head)
         return np.array([argmax_first(r) for r in logits], np.int32), logits
