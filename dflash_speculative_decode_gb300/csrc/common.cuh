@@ -1,0 +1,236 @@
+// common.cuh -- device helpers and kernel interfaces shared by the library's own CUDA sources.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace dfl {
+
+constexpr int kMaxRows = 16;           // rows of one pass (R_max)
+constexpr int kWarpsPerCta = 4;        // GEMM CTA: 4 warps, each two 16-column tiles
+constexpr int kMaxChunksPerSplit = 16; // 64-wide K chunks one GEMM CTA stages in shared memory
+constexpr int kSplitTargetWarps = 152 * 16;
+
+// Device-resident counters of the current pass. The host writes them with k_set_state before each
+// pass so a captured graph replays at any position.
+struct DevState {
+    int n;                 // positions held (committed) at the start of the pass
+    int k;                 // rows of this pass
+    int draft_n;           // positions whose taps are already draft context
+    int ctx_rows;          // committed rows this draft pass makes context (draft_n .. draft_n+ctx_rows-1)
+    int accepted;          // accepted length of the last verify
+    int sampled;           // 1: sample with temperature, 0: greedy
+    float temperature;
+    int pad0;
+    unsigned long long seed;
+    int rows[kMaxRows];    // tokens of the verify rows (row 0 = last token)
+    int target[kMaxRows];  // target token per verify row
+    int props[kMaxRows];   // draft proposals for positions n+1..n+block-1
+    int last_tok;          // row 0 of the last draft block
+    int err;               // sticky device-side error bits
+};
+
+struct SetStateArgs {
+    int n, k, draft_n, ctx_rows, sampled, use_draft_rows, last_tok;
+    float temperature;
+    unsigned long long seed;
+    int rows[kMaxRows];
+};
+
+// ---- small device helpers ------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// Round to nearest even bf16 (finite inputs).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+    uint32_t u = __float_as_uint(f);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return uint16_t(u >> 16);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// D = A * B + D for one m16n8k16 bf16 tile, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 4-bit codes pairs of a packed word -> bf16x2 registers holding the codes exactly.
+// bits [4s, 4s+4) and [16+4s, 16+4s+4) of w become the low and high bf16 of register s.
+// 0x4300 is bf16 128.0 whose last mantissa bit is worth 1, so (0x4300 | q) is 128 + q; subtracting
+// 128 leaves q exactly.
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r);
+    const __nv_bfloat162 off = __floats2bfloat162_rn(128.0f, 128.0f);
+    v = __hsub2(v, off);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide sum with a fixed reduction order (deterministic). blockDim.x a multiple of 32, <= 1024.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (w == 0) {
+        t = lane < nw ? red[lane] : 0.f;
+        t = warp_sum(t);
+        if (lane == 0) red[32] = t;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+// ---- GEMM interface ---------------------------------------------------------------------------------
+enum WFmt { W_Q41 = 0, W_BF16 = 1 };
+enum Epi { EPI_F32 = 0, EPI_GLU = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
+enum XIn { X_BF16 = 0, X_F32 = 1 };   // activation type of a product
+enum ArgmaxDst { AM_VERIFY = 0, AM_DRAFT = 1 };
+
+struct GemmArgs {
+    const uint8_t *img;    // tile image
+    int K, C, N;           // logical K, chunks of 64 along padded K, output columns
+    int M;                 // rows (<= 16)
+    int S;                 // K splits
+    const void *x;         // activations [M][ldx]: fp32 (X_F32) or bf16 (X_BF16)
+    int ldx;
+    int x_row0;            // first activation row used
+    void *y;               // fp32 output
+    int ldy;
+    float *part;           // split-K partials [S][M][N]
+    int *cnt;              // arrival counters [N/32] (zero between launches)
+    const uint16_t *ext;   // EPI_SILU_MUL: bf16 multiplier [M][lde]
+    int lde;
+    // EPI_ARGMAX
+    float *logits;         // optional fp32 [M][ldl] store of the raw products
+    int ldl;
+    float *am_val;         // per-CTA partial maxima [gridDim.x][M]
+    int *am_idx;
+    int *am_cnt;           // CTA arrival counter (zero between launches)
+    DevState *st;
+    int am_dst;            // AM_VERIFY: st->target[m] and st->accepted; AM_DRAFT: st->props[m]
+};
+
+// launchers (gemm.cu)
+int gemm_splits(int C, int N, int fmt);
+size_t gemm_scratch_floats(int S, int M, int N);
+cudaError_t launch_gemm(int fmt, int epi, int xin, const GemmArgs &a, cudaStream_t s);
+cudaError_t launch_pack_q41(const uint8_t *src, int K, int N, uint8_t *img, cudaStream_t s);
+cudaError_t launch_pack_bf16(const uint16_t *src, int K, int N, uint8_t *img, cudaStream_t s);
+inline int padded_k(int K) { return (K + 63) / 64 * 64; }
+inline size_t q41_image_bytes(int K, int N) { return size_t(N / 16) * (padded_k(K) / 64) * 640; }
+inline size_t bf16_image_bytes(int K, int N) { return size_t(N / 16) * (padded_k(K) / 64) * 2048; }
+
+// ---- row and attention interfaces (rows.cu) ------------------------------------------------------
+struct RowArgs {
+    int M, H;
+    float *x;              // fp32 residual [M][H]
+    const float *y;        // fp32 product [M][ldy] to add (nullable)
+    int ldy;
+    const uint16_t *w_post;   // RMSNorm weight applied to y before the add (nullable: plain add)
+    float lambda;          // multiply x after the add (1 = none)
+    float *tap;            // tap store base (nullable), row of position p at tap + p*ld_tap + tap_off
+    int ld_tap, tap_off;
+    const uint16_t *w_next;   // RMSNorm weight for the output (nullable: output = x)
+    float *out;            // [M][ld_out] (nullable)
+    int ld_out;
+    float eps;
+    const DevState *st;
+    int pos_from_ctx;      // tap positions: 0 = st->n + m, 1 = st->draft_n + m
+    int rows_from_ctx;     // 1: only rows < st->ctx_rows are live (the rest are written as zeros)
+};
+
+struct EmbedArgs {
+    int M, H;
+    const uint16_t *emb;   // bf16 [vocab][H]
+    float scale;
+    const DevState *st;
+    int use_draft;         // 0: tokens st->rows[m]; 1: draft block [st->last_tok, mask...]
+    int mask_token;
+    float *x;              // fp32 [M][H]
+    const uint16_t *ple;   // bf16 [vocab][ple_w] (nullable)
+    int ple_w;
+    uint16_t *ple_out;     // bf16 [M][ple_w]
+};
+
+struct QkArgs {
+    int M, nq, nkv, hd;
+    const float *qkv;      // fp32 [M][ldq] (q | k | v)
+    int ldq;
+    int row0;              // first row of qkv that belongs to this group of rows
+    const uint16_t *q_norm, *k_norm;
+    float eps;
+    const float2 *rope;    // (cos, sin) table [max_pos][hd/2]
+    const DevState *st;
+    int pos_mode;          // 0: st->n + m, 1: st->n + m (draft block), 2: st->draft_n + m (draft context)
+    int live_from_ctx;     // 1: only rows < st->ctx_rows are live
+    float *q_out;          // fp32 [M][nq][hd] (nullable: no query)
+    float *k_store, *v_store;      // [cap][nkv][hd] (nullable: no append)
+    int cap;               // ring capacity (slot = pos % cap)
+};
+
+struct AttnArgs {
+    int M, nq, nkv, hd;
+    const float *q;        // fp32 [M][nq][hd]
+    const float *kA, *vA;      // positional store [capA][nkv][hd]
+    int capA;
+    const float *kB, *vB;      // block store [nB][nkv][hd] (nullable)
+    int nB;
+    int window;            // mode 0: keys p-window+1..p (0 = all of 0..p); mode 1: context window
+    int mode;              // 0: target (causal, keys in A up to the row's own position)
+                           // 1: draft (A keys max(0,n-window)..n-1 for every row, plus all B keys)
+    const DevState *st;
+    float scale;
+    float *part_acc;       // [nq][max_chunks][M][hd]
+    float *part_ml;        // [nq][max_chunks][M][2]
+    int *cnt;              // [nq] arrival counters (zero between launches)
+    int max_chunks;
+    float *out;            // [M][nq*hd]
+};
+
+struct SampleArgs {
+    const float *logits;   // [M][V]
+    int M, V, ld;
+    DevState *st;
+    int *cnt;
+};
+
+cudaError_t launch_set_state(DevState *st, const SetStateArgs &a, cudaStream_t s);
+cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t s);
+cudaError_t launch_rows(const RowArgs &a, cudaStream_t s);
+cudaError_t launch_qk(const QkArgs &a, cudaStream_t s);
+cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s);
+cudaError_t launch_rope_table(float2 *tab, int max_pos, int hd, double base, cudaStream_t s);
+cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const uint16_t *w_norm, float eps,
+                             float *dst, int ld_dst, const DevState *st, int live_from_ctx, cudaStream_t s);
+cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, float *dst, int ld_dst,
+                             cudaStream_t s);
+cudaError_t launch_commit(DevState *st, int keep, cudaStream_t s);
+
+constexpr int kAttnChunk = 32;   // keys per attention work item
+
+}  // namespace dfl

@@ -1,0 +1,1152 @@
+// engine.cu -- host engine behind the C ABI (include/dfl.h): arena layout, tensor packing, the
+// sequence of kernels of a verify / prefill chunk / draft block, and the index arithmetic of commit,
+// snapshot and restore.
+//
+// State (1bit engine PR "npu forward: Gemma4 verifies a draft in one batched pass; KV row width per
+// layer", "What changes" item 1): one KV plane per layer that holds its own, counted at that layer's
+// width (2 * kv_heads * head_dim floats per position); a KV-shared layer holds none and reads its
+// owner's; positions held are counted over owner planes. Sliding planes are rings of W + R_max - 1
+// slots (a verify writes up to R_max rows before knowing how many survive, and the oldest key a later
+// row needs is W - 1 behind it), full planes are linear. commit_verify_rows only moves the position
+// counter: rows past it are overwritten by the next pass.
+#include <algorithm>
+#include <cctype>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "dfl.h"
+
+namespace dfl {
+int head_grid(int C, int M, int N);
+size_t attn_smem(int M, int hd);
+}  // namespace dfl
+
+using namespace dfl;
+
+namespace {
+
+struct QMat {
+    uint8_t *img = nullptr;
+    int K = 0, N = 0, C = 0, S = 1;
+    bool q41 = true;
+    bool loaded = false;
+};
+struct Vec {
+    uint16_t *p = nullptr;
+    size_t n = 0;
+    bool loaded = false;
+};
+struct TLayer {
+    int type = 0, owner = 0, nkv = 0, ffn = 0, cap = 0;
+    QMat qkv, o, gu, d, pg, pp;
+    Vec attn_norm, q_norm, k_norm, post_attn_norm, pre_ffn_norm, post_ffn_norm, ple_norm, lam;
+    float lambda = 1.f;
+    float *K = nullptr, *V = nullptr;
+};
+struct DLayer {
+    QMat qkv, o, gu, d;
+    Vec attn_norm, q_norm, k_norm, ffn_norm;
+    float *K = nullptr, *V = nullptr;
+};
+
+struct Arena {
+    uint8_t *base = nullptr;
+    size_t off = 0;
+    template <typename T>
+    T *take(size_t count) {
+        off = (off + 255) / 256 * 256;
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+uint64_t fnv1a(const void *p, size_t n) {
+    const uint8_t *b = static_cast<const uint8_t *>(p);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return h;
+}
+
+constexpr uint32_t kSnapMagic = 0x53464C44u;   // "DLFS"
+
+struct SnapHeader {
+    uint32_t magic, version;
+    uint64_t cfg_hash;
+    int32_t n, draft_n;
+    uint64_t bytes;
+    uint8_t pad[224];
+};
+static_assert(sizeof(SnapHeader) == 256, "header size");
+
+}  // namespace
+
+struct dfl_ctx {
+    dfl_config cfg{};
+    cudaStream_t stream = nullptr;
+    // weights
+    Vec emb, final_norm, ple_table, d_hidden_norm, d_final_norm;
+    QMat head, fc;
+    std::vector<TLayer> tl;
+    std::vector<DLayer> dl;
+    float2 *rope_s = nullptr, *rope_f = nullptr, *rope_d = nullptr;
+    int rope_rows = 0;
+    // state
+    DevState *st = nullptr;
+    float *taps = nullptr;
+    int TH = 0, cap_sliding = 0, cap_draft = 0, ctx_fuse = 0;
+    // workspace
+    float *x = nullptr, *x_d = nullptr, *y = nullptr, *y_fc = nullptr, *qkv = nullptr, *q = nullptr;
+    float *part = nullptr, *logits = nullptr, *dlogits = nullptr, *att_acc = nullptr, *att_ml = nullptr, *am_val = nullptr;
+    float *h = nullptr, *hcat = nullptr, *hb = nullptr, *o = nullptr, *a = nullptr, *z = nullptr;
+    float *tapbuf = nullptr, *kB = nullptr, *vB = nullptr;
+    uint16_t *ple_rows = nullptr;
+    int *cnt = nullptr, *att_cnt = nullptr, *am_idx = nullptr, *am_cnt = nullptr, *smp_cnt = nullptr;
+    int *counters_begin = nullptr;
+    size_t counters_bytes = 0;
+    int att_max_chunks = 0, nq_max = 0, qkv_max = 0;
+    // host mirror of the state
+    int n = 0, draft_n = 0, pending = 0, last_accepted = -1, draft_at = -1;
+    bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
+    int last_k = 0;
+    int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
+    std::string err;
+};
+
+namespace {
+
+int fail(dfl_ctx *c, int code, const std::string &msg) {
+    if (c) c->err = msg;
+    return code;
+}
+
+#define DFL_CK(call)                                                                          \
+    do {                                                                                      \
+        cudaError_t e_ = (call);                                                              \
+        if (e_ != cudaSuccess) return fail(c, DFL_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+    } while (0)
+
+std::string validate(const dfl_config *g) {
+    auto bad = [](const char *f) { return std::string("configuration: ") + f; };
+    if (g->n_layers < 1 || g->n_layers > DFL_MAX_LAYERS) return bad("n_layers out of range 1..64");
+    if (g->hidden < 64 || g->hidden % 64 || g->hidden > 4096) return bad("hidden must be a multiple of 64, <= 4096");
+    if (g->vocab < 16 || g->vocab % 16) return bad("vocab must be a multiple of 16");
+    if (g->head_dim != 64 && g->head_dim != 128 && g->head_dim != 256) return bad("head_dim must be 64, 128 or 256");
+    if (g->n_heads < 1 || (g->n_heads * g->head_dim) % 64) return bad("n_heads * head_dim must be a multiple of 64");
+    if (g->window < 1) return bad("window must be >= 1");
+    if (g->ple_dim < 0 || g->ple_dim % 32) return bad("ple_dim must be a multiple of 32");
+    for (int l = 0; l < g->n_layers; ++l) {
+        const int o = g->kv_owner[l], t = g->layer_type[l], kv = g->kv_heads[l];
+        if (t != DFL_SLIDING && t != DFL_FULL) return bad("layer_type must be 0 or 1");
+        if (kv < 1 || g->n_heads % kv) return bad("kv_heads must divide n_heads");
+        if (o < 0 || o > l) return bad("kv_owner must be an earlier layer or the layer itself");
+        if (o != l && (g->kv_owner[o] != o || g->layer_type[o] != t || g->kv_heads[o] != kv))
+            return bad("a KV-shared layer's owner must hold its own plane, of the same type and kv_heads");
+        if (g->ffn[l] < 64 || g->ffn[l] % 64) return bad("ffn must be a multiple of 64");
+        if (((g->n_heads + 2 * kv) * g->head_dim) % 32) return bad("q|k|v width must be a multiple of 32");
+    }
+    if (g->d_layers < 1 || g->d_layers > DFL_MAX_LAYERS) return bad("d_layers out of range");
+    if (g->d_head_dim != 64 && g->d_head_dim != 128 && g->d_head_dim != 256) return bad("d_head_dim must be 64, 128 or 256");
+    if (g->d_heads < 1 || g->d_kv_heads < 1 || g->d_heads % g->d_kv_heads) return bad("d_kv_heads must divide d_heads");
+    if ((g->d_heads * g->d_head_dim) % 64) return bad("d_heads * d_head_dim must be a multiple of 64");
+    if (g->d_ffn < 64 || g->d_ffn % 64) return bad("d_ffn must be a multiple of 64");
+    if (g->d_window < 0) return bad("d_window must be >= 0");
+    if (g->block < 2 || g->block > DFL_MAX_ROWS) return bad("block must be 2..16");
+    if (g->n_taps < 1 || g->n_taps > DFL_MAX_TAPS) return bad("n_taps must be 1..8");
+    for (int i = 0; i < g->n_taps; ++i) {
+        if (g->taps[i] < 0 || g->taps[i] >= g->n_layers) return bad("tap layer out of range");
+        if (i && g->taps[i] <= g->taps[i - 1]) return bad("taps must be ascending");
+    }
+    if (g->mask_token < 0 || g->mask_token >= g->vocab) return bad("mask_token out of range");
+    if (g->max_ctx < 1 || g->max_ctx > (1 << 20)) return bad("max_ctx out of range");
+    if (!(g->eps > 0.f) || !(g->d_eps > 0.f)) return bad("eps must be > 0");
+    return {};
+}
+
+QMat qmat(int K, int N, bool q41) {
+    QMat m;
+    m.K = K;
+    m.N = N;
+    m.C = padded_k(K) / 64;
+    m.S = gemm_splits(m.C, N, q41 ? W_Q41 : W_BF16);
+    m.q41 = q41;
+    return m;
+}
+
+// Lay out every buffer. With null bases only the sizes are computed.
+void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
+    const dfl_config &g = c->cfg;
+    const int H = g.hidden, V = g.vocab, NL = g.n_layers, hd = g.head_dim, nq = g.n_heads, P = g.ple_dim;
+    const int R = kMaxRows;
+    c->TH = g.n_taps * H;
+    c->cap_sliding = g.window + R - 1;
+    c->cap_draft = g.d_window > 0 ? g.d_window : g.max_ctx + R;
+    c->ctx_fuse = R - g.block;
+    c->rope_rows = g.max_ctx + 2 * R;
+
+    size_t part_floats = 0;
+    int cnt_n = 1;
+    auto qm = [&](QMat &m, int K, int N, bool q41) {
+        m = qmat(K, N, q41);
+        m.img = W.take<uint8_t>(q41 ? q41_image_bytes(K, N) : bf16_image_bytes(K, N));
+        part_floats = std::max(part_floats, gemm_scratch_floats(m.S, R, N));
+        cnt_n = std::max(cnt_n, N / 32);
+    };
+    auto vec = [&](Vec &v, size_t n) {
+        v.n = n;
+        v.p = W.take<uint16_t>(n);
+    };
+    vec(c->emb, (size_t)V * H);
+    qm(c->head, H, V, false);
+    vec(c->final_norm, H);
+    if (P) vec(c->ple_table, (size_t)V * NL * P);
+    c->tl.assign(NL, TLayer());
+    c->qkv_max = 0;
+    int ffn_max = g.d_ffn;
+    for (int l = 0; l < NL; ++l) {
+        TLayer &L = c->tl[l];
+        L.type = g.layer_type[l];
+        L.owner = g.kv_owner[l];
+        L.nkv = g.kv_heads[l];
+        L.ffn = g.ffn[l];
+        ffn_max = std::max(ffn_max, L.ffn);
+        const bool own = L.owner == l;
+        const int nqkv = (nq + (own ? 2 * L.nkv : 0)) * hd;
+        c->qkv_max = std::max(c->qkv_max, nqkv);
+        vec(L.attn_norm, H);
+        vec(L.q_norm, hd);
+        if (own) vec(L.k_norm, hd);
+        vec(L.post_attn_norm, H);
+        vec(L.pre_ffn_norm, H);
+        vec(L.post_ffn_norm, H);
+        qm(L.qkv, H, nqkv, true);
+        qm(L.o, nq * hd, H, true);
+        qm(L.gu, H, 2 * L.ffn, true);
+        qm(L.d, L.ffn, H, true);
+        if (P) {
+            vec(L.ple_norm, H);
+            vec(L.lam, 1);
+            qm(L.pg, H, P, true);
+            qm(L.pp, P, H, true);
+        }
+    }
+    const int dq = g.d_heads, dkv = g.d_kv_heads, dhd = g.d_head_dim;
+    qm(c->fc, c->TH, H, false);
+    vec(c->d_hidden_norm, H);
+    vec(c->d_final_norm, H);
+    c->dl.assign(g.d_layers, DLayer());
+    for (int l = 0; l < g.d_layers; ++l) {
+        DLayer &D = c->dl[l];
+        vec(D.attn_norm, H);
+        vec(D.q_norm, dhd);
+        vec(D.k_norm, dhd);
+        vec(D.ffn_norm, H);
+        qm(D.qkv, H, (dq + 2 * dkv) * dhd, true);
+        qm(D.o, dq * dhd, H, true);
+        qm(D.gu, H, 2 * g.d_ffn, true);
+        qm(D.d, g.d_ffn, H, true);
+    }
+    c->qkv_max = std::max(c->qkv_max, (dq + 2 * dkv) * dhd);
+    c->rope_s = W.take<float2>((size_t)c->rope_rows * (hd / 2));
+    c->rope_f = W.take<float2>((size_t)c->rope_rows * (hd / 2));
+    c->rope_d = W.take<float2>((size_t)c->rope_rows * (dhd / 2));
+
+    // state
+    c->st = S.take<DevState>(1);
+    for (int l = 0; l < NL; ++l) {
+        TLayer &L = c->tl[l];
+        if (L.owner != l) continue;
+        L.cap = L.type == DFL_SLIDING ? c->cap_sliding : g.max_ctx + R;
+        L.K = S.take<float>((size_t)L.cap * L.nkv * hd);
+        L.V = S.take<float>((size_t)L.cap * L.nkv * hd);
+    }
+    for (int l = 0; l < g.d_layers; ++l) {
+        c->dl[l].K = S.take<float>((size_t)c->cap_draft * dkv * dhd);
+        c->dl[l].V = S.take<float>((size_t)c->cap_draft * dkv * dhd);
+    }
+    c->taps = S.take<float>((size_t)(g.max_ctx + 2 * R) * c->TH);
+
+    // workspace
+    c->nq_max = std::max(nq, dq);
+    const int hd_max = std::max(hd, dhd);
+    const int att_max = std::max(nq * hd, dq * dhd);
+    c->x = X.take<float>((size_t)R * H);
+    c->x_d = X.take<float>((size_t)R * H);
+    c->y = X.take<float>((size_t)R * H);
+    c->y_fc = X.take<float>((size_t)R * H);
+    c->qkv = X.take<float>((size_t)R * c->qkv_max);
+    c->q = X.take<float>((size_t)R * att_max);
+    c->h = X.take<float>((size_t)R * H);
+    c->hcat = X.take<float>((size_t)R * H);
+    c->hb = X.take<float>((size_t)R * H);
+    c->o = X.take<float>((size_t)R * att_max);
+    c->a = X.take<float>((size_t)R * ffn_max);
+    c->z = X.take<float>((size_t)R * std::max(P, 32));
+    c->ple_rows = X.take<uint16_t>((size_t)R * std::max(NL * P, 32));
+    c->tapbuf = X.take<float>((size_t)R * c->TH);
+    c->kB = X.take<float>((size_t)R * dkv * dhd);
+    c->vB = X.take<float>((size_t)R * dkv * dhd);
+    c->part = X.take<float>(std::max<size_t>(part_floats, 1));
+    c->att_max_chunks = (g.max_ctx + R + kAttnChunk - 1) / kAttnChunk + 2;
+    c->att_acc = X.take<float>((size_t)c->nq_max * c->att_max_chunks * R * hd_max);
+    c->att_ml = X.take<float>((size_t)c->nq_max * c->att_max_chunks * R * 2);
+    c->am_val = X.take<float>((size_t)152 * 4 * kMaxRows);
+    c->am_idx = X.take<int>((size_t)152 * 4 * kMaxRows);
+    c->logits = X.take<float>((size_t)R * V);
+    c->dlogits = X.take<float>((size_t)R * V);
+    // counters that must read zero between launches, contiguous so one memset clears them
+    X.off = (X.off + 255) / 256 * 256;
+    const size_t cbeg = X.off;
+    c->cnt = X.take<int>(cnt_n);
+    c->att_cnt = X.take<int>(c->nq_max);
+    c->am_cnt = X.take<int>(1);
+    c->smp_cnt = X.take<int>(1);
+    c->counters_begin = c->cnt;
+    c->counters_bytes = X.off - cbeg;
+}
+
+bool is_tap(const dfl_config &g, int l, int *ti) {
+    for (int i = 0; i < g.n_taps; ++i)
+        if (g.taps[i] == l) {
+            *ti = i;
+            return true;
+        }
+    return false;
+}
+
+// ---- one product -----------------------------------------------------------------------------------
+cudaError_t gemm(dfl_ctx *c, const QMat &W, const float *x, int ldx, int row0, int M, int epi, void *y, int ldy,
+                 const uint16_t *ext = nullptr, int lde = 0) {
+    GemmArgs a{};
+    a.img = W.img;
+    a.K = W.K;
+    a.C = W.C;
+    a.N = W.N;
+    a.M = M;
+    a.S = W.S;
+    a.x = x;
+    a.ldx = ldx;
+    a.x_row0 = row0;
+    a.y = y;
+    a.ldy = ldy;
+    a.part = c->part;
+    a.cnt = c->cnt;
+    a.ext = ext;
+    a.lde = lde;
+    return launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, X_F32, a, c->stream);
+}
+
+cudaError_t head(dfl_ctx *c, const float *x, int row0, int M, float *logits, int dst) {
+    GemmArgs a{};
+    a.img = c->head.img;
+    a.K = c->head.K;
+    a.C = c->head.C;
+    a.N = c->head.N;
+    a.M = M;
+    a.S = 1;
+    a.x = x;
+    a.ldx = c->cfg.hidden;
+    a.x_row0 = row0;
+    a.logits = logits;
+    a.ldl = c->cfg.vocab;
+    a.am_val = c->am_val;
+    a.am_idx = c->am_idx;
+    a.am_cnt = c->am_cnt;
+    a.st = c->st;
+    a.am_dst = dst;
+    return launch_gemm(W_BF16, EPI_ARGMAX, X_F32, a, c->stream);
+}
+
+RowArgs rows(dfl_ctx *c, int M, float *x) {
+    RowArgs r{};
+    r.M = M;
+    r.H = c->cfg.hidden;
+    r.x = x;
+    r.lambda = 1.f;
+    r.eps = c->cfg.eps;
+    r.st = c->st;
+    r.ld_out = c->cfg.hidden;
+    return r;
+}
+
+int set_state(dfl_ctx *c, int k, const int32_t *rows_in, bool draft_rows, int ctx_rows, int last_tok,
+              const dfl_sampling *s) {
+    SetStateArgs a{};
+    a.n = c->n;
+    a.k = k;
+    a.draft_n = c->draft_n;
+    a.ctx_rows = ctx_rows;
+    a.use_draft_rows = draft_rows ? 1 : 0;
+    a.last_tok = last_tok;
+    a.sampled = (s && s->temperature > 0.f) ? 1 : 0;
+    a.temperature = a.sampled ? s->temperature : 1.f;
+    a.seed = s ? s->seed : 0;
+    for (int i = 0; i < kMaxRows; ++i) a.rows[i] = (rows_in && i < k) ? rows_in[i] : 0;
+    DFL_CK(launch_set_state(c->st, a, c->stream));
+    return DFL_OK;
+}
+
+// ---- target pass: k rows at positions n..n+k-1 ---------------------------------------------------------
+int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
+    const dfl_config &g = c->cfg;
+    const int H = g.hidden, NL = g.n_layers, hd = g.head_dim, nq = g.n_heads, P = g.ple_dim;
+    EmbedArgs ea{};
+    ea.M = k;
+    ea.H = H;
+    ea.emb = c->emb.p;
+    ea.scale = g.emb_scale;
+    ea.st = c->st;
+    ea.x = c->x;
+    ea.ple = P ? c->ple_table.p : nullptr;
+    ea.ple_w = NL * P;
+    ea.ple_out = c->ple_rows;
+    DFL_CK(launch_embed(ea, c->stream));
+    RowArgs r0 = rows(c, k, c->x);
+    r0.w_next = c->tl[0].attn_norm.p;
+    r0.out = c->h;
+    DFL_CK(launch_rows(r0, c->stream));
+    const int last_layer = (c->stop_layer >= 0 && c->stop_layer < NL) ? c->stop_layer : NL - 1;
+    if (last_layer < NL - 1) do_head = false;
+    for (int l = 0; l <= last_layer; ++l) {
+        TLayer &L = c->tl[l];
+        TLayer &O = c->tl[L.owner];
+        const bool own = L.owner == l;
+        const int nqkv = L.qkv.N;
+        DFL_CK(gemm(c, L.qkv, c->h, H, 0, k, EPI_F32, c->qkv, nqkv));
+        QkArgs qa{};
+        qa.M = k;
+        qa.nq = nq;
+        qa.nkv = L.nkv;
+        qa.hd = hd;
+        qa.qkv = c->qkv;
+        qa.ldq = nqkv;
+        qa.q_norm = L.q_norm.p;
+        qa.k_norm = own ? L.k_norm.p : nullptr;
+        qa.eps = g.eps;
+        qa.rope = L.type == DFL_SLIDING ? c->rope_s : c->rope_f;
+        qa.st = c->st;
+        qa.q_out = c->q;
+        qa.k_store = own ? L.K : nullptr;
+        qa.v_store = own ? L.V : nullptr;
+        qa.cap = L.cap;
+        DFL_CK(launch_qk(qa, c->stream));
+        AttnArgs aa{};
+        aa.M = k;
+        aa.nq = nq;
+        aa.nkv = L.nkv;
+        aa.hd = hd;
+        aa.q = c->q;
+        aa.kA = O.K;
+        aa.vA = O.V;
+        aa.capA = O.cap;
+        aa.window = L.type == DFL_SLIDING ? g.window : 0;
+        aa.mode = 0;
+        aa.st = c->st;
+        aa.scale = 1.0f / sqrtf((float)hd);
+        aa.part_acc = c->att_acc;
+        aa.part_ml = c->att_ml;
+        aa.cnt = c->att_cnt;
+        aa.max_chunks = c->att_max_chunks;
+        aa.out = c->o;
+        DFL_CK(launch_attn(aa, 2 * 152, c->stream));
+        DFL_CK(gemm(c, L.o, c->o, nq * hd, 0, k, EPI_F32, c->y, H));
+        RowArgs r1 = rows(c, k, c->x);
+        r1.y = c->y;
+        r1.ldy = H;
+        r1.w_post = L.post_attn_norm.p;
+        r1.w_next = L.pre_ffn_norm.p;
+        r1.out = c->h;
+        DFL_CK(launch_rows(r1, c->stream));
+        DFL_CK(gemm(c, L.gu, c->h, H, 0, k, EPI_GLU, c->a, L.ffn));
+        DFL_CK(gemm(c, L.d, c->a, L.ffn, 0, k, EPI_F32, c->y, H));
+        const uint16_t *next = l + 1 < NL ? c->tl[l + 1].attn_norm.p : c->final_norm.p;
+        int ti = 0;
+        const bool tap = is_tap(g, l, &ti);
+        RowArgs r2 = rows(c, k, c->x);
+        r2.y = c->y;
+        r2.ldy = H;
+        r2.w_post = L.post_ffn_norm.p;
+        r2.out = c->h;
+        if (P) {
+            DFL_CK(launch_rows(r2, c->stream));   // out = bf16(x): the gate's input
+            DFL_CK(gemm(c, L.pg, c->h, H, 0, k, EPI_SILU_MUL, c->z, P, c->ple_rows + (size_t)l * P, NL * P));
+            DFL_CK(gemm(c, L.pp, c->z, P, 0, k, EPI_F32, c->y, H));
+            r2 = rows(c, k, c->x);
+            r2.y = c->y;
+            r2.ldy = H;
+            r2.w_post = L.ple_norm.p;
+            r2.lambda = L.lambda;
+            r2.out = c->h;
+        }
+        r2.w_next = next;
+        if (tap) {
+            r2.tap = c->taps;
+            r2.ld_tap = c->TH;
+            r2.tap_off = ti * H;
+        }
+        DFL_CK(launch_rows(r2, c->stream));
+    }
+    if (do_head) {
+        float *lg = (c->keep_logits || sampled) ? c->logits : nullptr;
+        DFL_CK(head(c, c->h, 0, k, lg, AM_VERIFY));
+        if (sampled) {
+            SampleArgs sa{};
+            sa.logits = c->logits;
+            sa.M = k;
+            sa.V = g.vocab;
+            sa.ld = g.vocab;
+            sa.st = c->st;
+            sa.cnt = c->smp_cnt;
+            DFL_CK(launch_sample(sa, c->stream));
+        }
+        c->have_logits = lg != nullptr;
+    }
+    return DFL_OK;
+}
+
+// ---- draft context rows: fc of the taps, hidden norm, then each layer's key and value ---------------
+// rows draft_n .. draft_n + r - 1 (device st->ctx_rows = r) into activation rows `row0..` of hctx.
+int ctx_rows_prologue(dfl_ctx *c, int M, float *hdst) {
+    const dfl_config &g = c->cfg;
+    DFL_CK(launch_copy_taps(c->taps, c->TH, c->st, M, c->tapbuf, c->TH, c->stream));
+    DFL_CK(gemm(c, c->fc, c->tapbuf, c->TH, 0, M, EPI_F32, c->y_fc, g.hidden));
+    DFL_CK(launch_cast_rows(c->y_fc, g.hidden, M, g.hidden, c->d_hidden_norm.p, g.d_eps, hdst, g.hidden, c->st, 1,
+                            c->stream));
+    return DFL_OK;
+}
+
+QkArgs draft_qk(dfl_ctx *c, int l) {
+    const dfl_config &g = c->cfg;
+    QkArgs qa{};
+    qa.nq = g.d_heads;
+    qa.nkv = g.d_kv_heads;
+    qa.hd = g.d_head_dim;
+    qa.qkv = c->qkv;
+    qa.ldq = c->dl[l].qkv.N;
+    qa.q_norm = c->dl[l].q_norm.p;
+    qa.k_norm = c->dl[l].k_norm.p;
+    qa.eps = g.d_eps;
+    qa.rope = c->rope_d;
+    qa.st = c->st;
+    return qa;
+}
+
+// a pass that only makes r <= 16 committed rows draft context
+int run_ctx_only(dfl_ctx *c, int r) {
+    const dfl_config &g = c->cfg;
+    int rc = set_state(c, 0, nullptr, false, r, -1, nullptr);
+    if (rc) return rc;
+    rc = ctx_rows_prologue(c, kMaxRows, c->hcat);
+    if (rc) return rc;
+    for (int l = 0; l < g.d_layers; ++l) {
+        DLayer &D = c->dl[l];
+        DFL_CK(gemm(c, D.qkv, c->hcat, g.hidden, 0, kMaxRows, EPI_F32, c->qkv, D.qkv.N));
+        QkArgs qa = draft_qk(c, l);
+        qa.M = kMaxRows;
+        qa.row0 = 0;
+        qa.pos_mode = 2;
+        qa.live_from_ctx = 1;
+        qa.k_store = D.K;
+        qa.v_store = D.V;
+        qa.cap = c->cap_draft;
+        DFL_CK(launch_qk(qa, c->stream));
+    }
+    c->draft_n += r;
+    return DFL_OK;
+}
+
+int catch_up(dfl_ctx *c, int leave) {
+    while (c->n - c->draft_n > leave) {
+        const int r = std::min(kMaxRows, c->n - c->draft_n);
+        const int rc = run_ctx_only(c, r);
+        if (rc) return rc;
+    }
+    return DFL_OK;
+}
+
+int run_draft(dfl_ctx *c, int last_tok) {
+    const dfl_config &g = c->cfg;
+    const int H = g.hidden, B = g.block, F = c->ctx_fuse;
+    const int r = c->n - c->draft_n;   // <= F after catch_up
+    int rc = set_state(c, B, nullptr, false, r, last_tok, nullptr);
+    if (rc) return rc;
+    if (F > 0) {
+        rc = ctx_rows_prologue(c, F, c->hcat + (size_t)B * H);
+        if (rc) return rc;
+    }
+    EmbedArgs ea{};
+    ea.M = B;
+    ea.H = H;
+    ea.emb = c->emb.p;
+    ea.scale = g.d_emb_scale;
+    ea.st = c->st;
+    ea.use_draft = 1;
+    ea.mask_token = g.mask_token;
+    ea.x = c->x_d;
+    DFL_CK(launch_embed(ea, c->stream));
+    RowArgs r0 = rows(c, B, c->x_d);
+    r0.eps = g.d_eps;
+    r0.w_next = c->dl[0].attn_norm.p;
+    r0.out = c->hcat;
+    DFL_CK(launch_rows(r0, c->stream));
+    const int dq = g.d_heads, dhd = g.d_head_dim;
+    for (int l = 0; l < g.d_layers; ++l) {
+        DLayer &D = c->dl[l];
+        DFL_CK(gemm(c, D.qkv, c->hcat, H, 0, B + F, EPI_F32, c->qkv, D.qkv.N));
+        QkArgs qb = draft_qk(c, l);
+        qb.M = B;
+        qb.pos_mode = 1;
+        qb.q_out = c->q;
+        qb.k_store = c->kB;
+        qb.v_store = c->vB;
+        qb.cap = 0;
+        DFL_CK(launch_qk(qb, c->stream));
+        if (F > 0) {
+            QkArgs qc = draft_qk(c, l);
+            qc.M = F;
+            qc.row0 = B;
+            qc.pos_mode = 2;
+            qc.live_from_ctx = 1;
+            qc.k_store = D.K;
+            qc.v_store = D.V;
+            qc.cap = c->cap_draft;
+            DFL_CK(launch_qk(qc, c->stream));
+        }
+        AttnArgs aa{};
+        aa.M = B;
+        aa.nq = dq;
+        aa.nkv = g.d_kv_heads;
+        aa.hd = dhd;
+        aa.q = c->q;
+        aa.kA = D.K;
+        aa.vA = D.V;
+        aa.capA = c->cap_draft;
+        aa.kB = c->kB;
+        aa.vB = c->vB;
+        aa.nB = B;
+        aa.window = g.d_window;
+        aa.mode = 1;
+        aa.st = c->st;
+        aa.scale = 1.0f / sqrtf((float)dhd);
+        aa.part_acc = c->att_acc;
+        aa.part_ml = c->att_ml;
+        aa.cnt = c->att_cnt;
+        aa.max_chunks = c->att_max_chunks;
+        aa.out = c->o;
+        DFL_CK(launch_attn(aa, 2 * 152, c->stream));
+        DFL_CK(gemm(c, D.o, c->o, dq * dhd, 0, B, EPI_F32, c->y, H));
+        RowArgs r1 = rows(c, B, c->x_d);
+        r1.eps = g.d_eps;
+        r1.y = c->y;
+        r1.ldy = H;
+        r1.w_next = D.ffn_norm.p;
+        r1.out = c->hb;
+        DFL_CK(launch_rows(r1, c->stream));
+        DFL_CK(gemm(c, D.gu, c->hb, H, 0, B, EPI_GLU, c->a, g.d_ffn));
+        DFL_CK(gemm(c, D.d, c->a, g.d_ffn, 0, B, EPI_F32, c->y, H));
+        RowArgs r2 = rows(c, B, c->x_d);
+        r2.eps = g.d_eps;
+        r2.y = c->y;
+        r2.ldy = H;
+        r2.w_next = l + 1 < g.d_layers ? c->dl[l + 1].attn_norm.p : c->d_final_norm.p;
+        r2.out = l + 1 < g.d_layers ? c->hcat : c->hb;
+        DFL_CK(launch_rows(r2, c->stream));
+    }
+    float *lg = c->keep_logits ? c->dlogits : nullptr;
+    DFL_CK(head(c, c->hb, 1, B - 1, lg, AM_DRAFT));
+    c->have_dlogits = lg != nullptr;
+    c->draft_n += r;
+    return DFL_OK;
+}
+
+int read_state(dfl_ctx *c, DevState *out) {
+    DFL_CK(cudaMemcpyAsync(out, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
+    DFL_CK(cudaStreamSynchronize(c->stream));
+    return DFL_OK;
+}
+
+int check_tokens(dfl_ctx *c, const int32_t *t, int n) {
+    for (int i = 0; i < n; ++i)
+        if (t[i] < 0 || t[i] >= c->cfg.vocab) return fail(c, DFL_E_INVALID_ARG, "token id out of range");
+    return DFL_OK;
+}
+
+int ready(dfl_ctx *c) {
+    auto chk = [&](bool ok, const char *what) { return ok ? DFL_OK : fail(c, DFL_E_STATE, std::string("tensor not loaded: ") + what); };
+    int rc;
+    if ((rc = chk(c->emb.loaded && c->head.loaded && c->final_norm.loaded, "emb/head/final_norm"))) return rc;
+    if (c->cfg.ple_dim && (rc = chk(c->ple_table.loaded, "ple_table"))) return rc;
+    for (size_t l = 0; l < c->tl.size(); ++l) {
+        const TLayer &L = c->tl[l];
+        bool ok = L.qkv.loaded && L.o.loaded && L.gu.loaded && L.d.loaded && L.attn_norm.loaded && L.q_norm.loaded &&
+                  L.post_attn_norm.loaded && L.pre_ffn_norm.loaded && L.post_ffn_norm.loaded;
+        if (L.owner == (int)l) ok = ok && L.k_norm.loaded;
+        if (c->cfg.ple_dim) ok = ok && L.pg.loaded && L.pp.loaded && L.ple_norm.loaded && L.lam.loaded;
+        if ((rc = chk(ok, ("t" + std::to_string(l) + ".*").c_str()))) return rc;
+    }
+    if ((rc = chk(c->fc.loaded && c->d_hidden_norm.loaded && c->d_final_norm.loaded, "d.fc/d.hidden_norm/d.final_norm")))
+        return rc;
+    for (size_t l = 0; l < c->dl.size(); ++l) {
+        const DLayer &D = c->dl[l];
+        const bool ok = D.qkv.loaded && D.o.loaded && D.gu.loaded && D.d.loaded && D.attn_norm.loaded &&
+                        D.q_norm.loaded && D.k_norm.loaded && D.ffn_norm.loaded;
+        if ((rc = chk(ok, ("d" + std::to_string(l) + ".*").c_str()))) return rc;
+    }
+    return DFL_OK;
+}
+
+size_t snapshot_size(const dfl_ctx *c, int n, int draft_n) {
+    const dfl_config &g = c->cfg;
+    size_t b = sizeof(SnapHeader);
+    for (int l = 0; l < g.n_layers; ++l) {
+        const TLayer &L = c->tl[l];
+        if (L.owner != l) continue;
+        const size_t row = (size_t)L.nkv * g.head_dim * 4;
+        const size_t rows = L.type == DFL_SLIDING ? (size_t)L.cap : (size_t)n;
+        b += 2 * rows * row;
+    }
+    b += (size_t)g.d_layers * 2 * c->cap_draft * g.d_kv_heads * g.d_head_dim * 4;
+    b += (size_t)(n - draft_n) * c->TH * 4;
+    return b;
+}
+
+}  // namespace
+
+// =====================================================================================================
+// C ABI
+// =====================================================================================================
+extern "C" {
+
+int dfl_required_bytes(const dfl_config *cfg, dfl_sizes *out) {
+    if (!cfg || !out) return DFL_E_INVALID_ARG;
+    if (!validate(cfg).empty()) return DFL_E_INVALID_ARG;
+    dfl_ctx tmp;
+    tmp.cfg = *cfg;
+    Arena W, S, X;
+    plan(&tmp, W, S, X);
+    out->weights_bytes = W.off;
+    out->state_bytes = S.off;
+    out->workspace_bytes = X.off;
+    return DFL_OK;
+}
+
+int dfl_init(const dfl_config *cfg, const dfl_buffers *buf, void *stream, dfl_ctx **out) {
+    if (!cfg || !buf || !out) return DFL_E_INVALID_ARG;
+    *out = nullptr;
+    if (!validate(cfg).empty()) return DFL_E_INVALID_ARG;
+    if (!buf->weights || !buf->state || !buf->workspace) return DFL_E_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(buf->weights) | reinterpret_cast<uintptr_t>(buf->state) |
+         reinterpret_cast<uintptr_t>(buf->workspace)) & 255)
+        return DFL_E_INVALID_ARG;
+    dfl_ctx *c = new dfl_ctx();
+    c->cfg = *cfg;
+    c->stream = static_cast<cudaStream_t>(stream);
+    Arena W, S, X;
+    W.base = static_cast<uint8_t *>(buf->weights);
+    S.base = static_cast<uint8_t *>(buf->state);
+    X.base = static_cast<uint8_t *>(buf->workspace);
+    plan(c, W, S, X);
+    auto bail = [&](cudaError_t e, const char *what) {
+        delete c;
+        (void)e;
+        (void)what;
+        return DFL_E_CUDA;
+    };
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(buf->state, 0, S.off, c->stream)) != cudaSuccess) return bail(e, "memset state");
+    if ((e = cudaMemsetAsync(c->counters_begin, 0, c->counters_bytes, c->stream)) != cudaSuccess) return bail(e, "memset");
+    const dfl_config &g = c->cfg;
+    if ((e = launch_rope_table(c->rope_s, c->rope_rows, g.head_dim, g.rope_base_sliding, c->stream)) != cudaSuccess ||
+        (e = launch_rope_table(c->rope_f, c->rope_rows, g.head_dim, g.rope_base_full, c->stream)) != cudaSuccess ||
+        (e = launch_rope_table(c->rope_d, c->rope_rows, g.d_head_dim, g.d_rope_base, c->stream)) != cudaSuccess)
+        return bail(e, "rope table");
+    if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) return bail(e, "sync");
+    *out = c;
+    return DFL_OK;
+}
+
+int dfl_load_tensor(dfl_ctx *c, const char *name, const void *src, size_t bytes) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (!name || !src) return fail(c, DFL_E_INVALID_ARG, "null name or source");
+    const dfl_config &g = c->cfg;
+    const std::string s(name);
+    QMat *m = nullptr;
+    Vec *v = nullptr;
+    TLayer *tlay = nullptr;
+    auto field = [&](const std::string &f, int layer, bool draft) -> bool {
+        if (draft) {
+            DLayer &D = c->dl[layer];
+            if (f == "attn_norm") v = &D.attn_norm;
+            else if (f == "q_norm") v = &D.q_norm;
+            else if (f == "k_norm") v = &D.k_norm;
+            else if (f == "ffn_norm") v = &D.ffn_norm;
+            else if (f == "wqkv") m = &D.qkv;
+            else if (f == "wo") m = &D.o;
+            else if (f == "wgu") m = &D.gu;
+            else if (f == "wd") m = &D.d;
+            else return false;
+            return true;
+        }
+        TLayer &L = c->tl[layer];
+        const bool own = L.owner == layer;
+        tlay = &L;
+        if (f == "attn_norm") v = &L.attn_norm;
+        else if (f == "q_norm") v = &L.q_norm;
+        else if (f == "k_norm" && own) v = &L.k_norm;
+        else if (f == "post_attn_norm") v = &L.post_attn_norm;
+        else if (f == "pre_ffn_norm") v = &L.pre_ffn_norm;
+        else if (f == "post_ffn_norm") v = &L.post_ffn_norm;
+        else if (f == "ple_norm" && g.ple_dim) v = &L.ple_norm;
+        else if (f == "lambda" && g.ple_dim) v = &L.lam;
+        else if ((f == "wqkv" && own) || (f == "wq" && !own)) m = &L.qkv;
+        else if (f == "wo") m = &L.o;
+        else if (f == "wgu") m = &L.gu;
+        else if (f == "wd") m = &L.d;
+        else if (f == "wple_g" && g.ple_dim) m = &L.pg;
+        else if (f == "wple_p" && g.ple_dim) m = &L.pp;
+        else return false;
+        return true;
+    };
+    bool ok = false;
+    if (s == "emb") v = &c->emb, ok = true;
+    else if (s == "head") m = &c->head, ok = true;
+    else if (s == "final_norm") v = &c->final_norm, ok = true;
+    else if (s == "ple_table" && g.ple_dim) v = &c->ple_table, ok = true;
+    else if (s == "d.fc") m = &c->fc, ok = true;
+    else if (s == "d.hidden_norm") v = &c->d_hidden_norm, ok = true;
+    else if (s == "d.final_norm") v = &c->d_final_norm, ok = true;
+    else if (s.size() > 2 && (s[0] == 't' || s[0] == 'd') && isdigit((unsigned char)s[1])) {
+        const size_t dot = s.find('.');
+        if (dot != std::string::npos) {
+            const int layer = atoi(s.substr(1, dot - 1).c_str());
+            const bool draft = s[0] == 'd';
+            if (layer >= 0 && layer < (draft ? g.d_layers : g.n_layers)) ok = field(s.substr(dot + 1), layer, draft);
+        }
+    }
+    if (!ok) return fail(c, DFL_E_INVALID_ARG, "unknown tensor name: " + s);
+    if (m) {
+        const size_t want = m->q41 ? (size_t)m->N * (m->K / 32) * 20 : (size_t)m->N * m->K * 2;
+        if (bytes != want) return fail(c, DFL_E_INVALID_ARG, s + ": expected " + std::to_string(want) + " bytes");
+        if (m->q41) DFL_CK(launch_pack_q41(static_cast<const uint8_t *>(src), m->K, m->N, m->img, c->stream));
+        else DFL_CK(launch_pack_bf16(static_cast<const uint16_t *>(src), m->K, m->N, m->img, c->stream));
+        m->loaded = true;
+        return DFL_OK;
+    }
+    if (bytes != v->n * 2) return fail(c, DFL_E_INVALID_ARG, s + ": expected " + std::to_string(v->n * 2) + " bytes");
+    DFL_CK(cudaMemcpyAsync(v->p, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
+    if (tlay && v == &tlay->lam) {
+        uint16_t b = 0;
+        DFL_CK(cudaMemcpyAsync(&b, src, 2, cudaMemcpyDeviceToHost, c->stream));
+        DFL_CK(cudaStreamSynchronize(c->stream));
+        uint32_t u = uint32_t(b) << 16;
+        float f;
+        memcpy(&f, &u, 4);
+        tlay->lambda = f;
+    }
+    v->loaded = true;
+    return DFL_OK;
+}
+
+int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s, int32_t *next_tok) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (!tokens || n < 1) return fail(c, DFL_E_INVALID_ARG, "prefill needs at least one token");
+    if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending: commit it first");
+    if (c->draft_only) return fail(c, DFL_E_STATE, "context holds draft-only rows");
+    if ((long)c->n + n > c->cfg.max_ctx) return fail(c, DFL_E_CAPACITY, "prefill exceeds max_ctx");
+    int rc = ready(c);
+    if (rc) return rc;
+    if ((rc = check_tokens(c, tokens, n))) return rc;
+    const bool sampled = s && s->temperature > 0.f;
+    int done = 0, last_k = 0;
+    while (done < n) {
+        const int k = std::min(kMaxRows, n - done);
+        const bool last = done + k == n;
+        if ((rc = set_state(c, k, tokens + done, false, 0, -1, s))) return rc;
+        if ((rc = run_target(c, k, last, sampled))) return rc;
+        c->n += k;
+        done += k;
+        last_k = k;
+    }
+    if ((rc = catch_up(c, 0))) return rc;
+    DevState hs;
+    if ((rc = read_state(c, &hs))) return rc;
+    if (next_tok) *next_tok = hs.target[last_k - 1];
+    c->last_k = last_k;
+    c->draft_at = -1;
+    return DFL_OK;
+}
+
+int dfl_draft_block(dfl_ctx *c, int32_t last_tok, int32_t *proposals) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending: commit it first");
+    if (last_tok < 0 || last_tok >= c->cfg.vocab) return fail(c, DFL_E_INVALID_ARG, "token id out of range");
+    if ((long)c->n + c->cfg.block > c->cfg.max_ctx + kMaxRows) return fail(c, DFL_E_CAPACITY, "block past max_ctx");
+    int rc = ready(c);
+    if (rc) return rc;
+    if ((rc = catch_up(c, c->ctx_fuse))) return rc;
+    if ((rc = run_draft(c, last_tok))) return rc;
+    c->draft_at = c->n;
+    if (proposals) {
+        DevState hs;
+        if ((rc = read_state(c, &hs))) return rc;
+        for (int i = 0; i < c->cfg.block - 1; ++i) proposals[i] = hs.props[i];
+    }
+    return DFL_OK;
+}
+
+int dfl_verify_block(dfl_ctx *c, const int32_t *rows_in, int k, const dfl_sampling *s, int32_t *target_tok,
+                     int32_t *accepted) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending: commit it first");
+    if (c->draft_only) return fail(c, DFL_E_STATE, "context holds draft-only rows");
+    if (k < 1 || k > kMaxRows) return fail(c, DFL_E_UNSUPPORTED, "k must be 1..16");
+    if ((long)c->n + k > c->cfg.max_ctx) return fail(c, DFL_E_CAPACITY, "verify exceeds max_ctx");
+    int rc = ready(c);
+    if (rc) return rc;
+    if (rows_in) {
+        if ((rc = check_tokens(c, rows_in, k))) return rc;
+    } else {
+        if (c->draft_at != c->n) return fail(c, DFL_E_STATE, "rows = NULL needs a draft block at this position");
+        if (k > c->cfg.block) return fail(c, DFL_E_INVALID_ARG, "k exceeds the draft block");
+    }
+    const bool sampled = s && s->temperature > 0.f;
+    if ((rc = set_state(c, k, rows_in, rows_in == nullptr, 0, -1, s))) return rc;
+    if ((rc = run_target(c, k, true, sampled))) return rc;
+    DevState hs;
+    if ((rc = read_state(c, &hs))) return rc;
+    if (target_tok)
+        for (int i = 0; i < k; ++i) target_tok[i] = hs.target[i];
+    if (accepted) *accepted = hs.accepted;
+    c->pending = k;
+    c->last_k = k;
+    c->last_accepted = hs.accepted;
+    return DFL_OK;
+}
+
+int dfl_commit_verify_rows(dfl_ctx *c, int keep) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (!c->pending) return fail(c, DFL_E_STATE, "no pending verify");
+    if (keep == DFL_KEEP_ACCEPTED) keep = std::min(c->last_accepted + 1, c->pending);
+    if (keep < 0 || keep > c->pending) return fail(c, DFL_E_INVALID_ARG, "keep must be 0..k");
+    c->n += keep;
+    c->pending = 0;
+    c->draft_at = -1;
+    return DFL_OK;
+}
+
+int64_t dfl_snapshot_bytes(const dfl_ctx *c) {
+    if (!c) return -1;
+    return (int64_t)snapshot_size(c, c->n, c->draft_n);
+}
+
+int dfl_snapshot(dfl_ctx *c, void *dst, size_t bytes) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (c->pending) return fail(c, DFL_E_STATE, "snapshot needs the committed state");
+    if (!dst) return fail(c, DFL_E_INVALID_ARG, "null destination");
+    const size_t need = snapshot_size(c, c->n, c->draft_n);
+    if (bytes < need) return fail(c, DFL_E_INVALID_ARG, "snapshot buffer too small");
+    const dfl_config &g = c->cfg;
+    SnapHeader hdr{};
+    hdr.magic = kSnapMagic;
+    hdr.version = 1;
+    hdr.cfg_hash = fnv1a(&c->cfg, sizeof(dfl_config));
+    hdr.n = c->n;
+    hdr.draft_n = c->draft_n;
+    hdr.bytes = need;
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    DFL_CK(cudaMemcpyAsync(d, &hdr, sizeof hdr, cudaMemcpyHostToDevice, c->stream));
+    size_t off = sizeof hdr;
+    for (int l = 0; l < g.n_layers; ++l) {
+        const TLayer &L = c->tl[l];
+        if (L.owner != l) continue;
+        const size_t row = (size_t)L.nkv * g.head_dim * 4;
+        const size_t rows = L.type == DFL_SLIDING ? (size_t)L.cap : (size_t)c->n;
+        DFL_CK(cudaMemcpyAsync(d + off, L.K, rows * row, cudaMemcpyDeviceToDevice, c->stream));
+        off += rows * row;
+        DFL_CK(cudaMemcpyAsync(d + off, L.V, rows * row, cudaMemcpyDeviceToDevice, c->stream));
+        off += rows * row;
+    }
+    const size_t dbytes = (size_t)c->cap_draft * g.d_kv_heads * g.d_head_dim * 4;
+    for (int l = 0; l < g.d_layers; ++l) {
+        DFL_CK(cudaMemcpyAsync(d + off, c->dl[l].K, dbytes, cudaMemcpyDeviceToDevice, c->stream));
+        off += dbytes;
+        DFL_CK(cudaMemcpyAsync(d + off, c->dl[l].V, dbytes, cudaMemcpyDeviceToDevice, c->stream));
+        off += dbytes;
+    }
+    const size_t tb = (size_t)(c->n - c->draft_n) * c->TH * 4;
+    if (tb) DFL_CK(cudaMemcpyAsync(d + off, c->taps + (size_t)c->draft_n * c->TH, tb, cudaMemcpyDeviceToDevice, c->stream));
+    DFL_CK(cudaStreamSynchronize(c->stream));   // the header came from host memory on this stack
+    return DFL_OK;
+}
+
+int dfl_restore(dfl_ctx *c, const void *src, size_t bytes) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (c->pending) return fail(c, DFL_E_STATE, "restore needs the committed state");
+    if (!src || bytes < sizeof(SnapHeader)) return fail(c, DFL_E_INVALID_ARG, "snapshot too small");
+    SnapHeader hdr;
+    DFL_CK(cudaMemcpyAsync(&hdr, src, sizeof hdr, cudaMemcpyDeviceToHost, c->stream));
+    DFL_CK(cudaStreamSynchronize(c->stream));
+    const dfl_config &g = c->cfg;
+    if (hdr.magic != kSnapMagic || hdr.version != 1) return fail(c, DFL_E_INVALID_ARG, "not a snapshot");
+    if (hdr.cfg_hash != fnv1a(&c->cfg, sizeof(dfl_config))) return fail(c, DFL_E_INVALID_ARG, "snapshot of another configuration");
+    if (hdr.n < 0 || hdr.n > g.max_ctx || hdr.draft_n < 0 || hdr.draft_n > hdr.n)
+        return fail(c, DFL_E_INVALID_ARG, "corrupt snapshot header");
+    const size_t need = snapshot_size(c, hdr.n, hdr.draft_n);
+    if (hdr.bytes != need || bytes < need) return fail(c, DFL_E_INVALID_ARG, "snapshot size mismatch");
+    const uint8_t *s = static_cast<const uint8_t *>(src);
+    size_t off = sizeof hdr;
+    for (int l = 0; l < g.n_layers; ++l) {
+        const TLayer &L = c->tl[l];
+        if (L.owner != l) continue;
+        const size_t row = (size_t)L.nkv * g.head_dim * 4;
+        const size_t rows = L.type == DFL_SLIDING ? (size_t)L.cap : (size_t)hdr.n;
+        DFL_CK(cudaMemcpyAsync(L.K, s + off, rows * row, cudaMemcpyDeviceToDevice, c->stream));
+        off += rows * row;
+        DFL_CK(cudaMemcpyAsync(L.V, s + off, rows * row, cudaMemcpyDeviceToDevice, c->stream));
+        off += rows * row;
+    }
+    const size_t dbytes = (size_t)c->cap_draft * g.d_kv_heads * g.d_head_dim * 4;
+    for (int l = 0; l < g.d_layers; ++l) {
+        DFL_CK(cudaMemcpyAsync(c->dl[l].K, s + off, dbytes, cudaMemcpyDeviceToDevice, c->stream));
+        off += dbytes;
+        DFL_CK(cudaMemcpyAsync(c->dl[l].V, s + off, dbytes, cudaMemcpyDeviceToDevice, c->stream));
+        off += dbytes;
+    }
+    const size_t tb = (size_t)(hdr.n - hdr.draft_n) * c->TH * 4;
+    if (tb) DFL_CK(cudaMemcpyAsync(c->taps + (size_t)hdr.draft_n * c->TH, s + off, tb, cudaMemcpyDeviceToDevice, c->stream));
+    c->n = hdr.n;
+    c->draft_n = hdr.draft_n;
+    c->draft_at = -1;
+    c->draft_only = false;
+    return DFL_OK;
+}
+
+int dfl_kv_widths(const dfl_ctx *c, int32_t *out) {
+    if (!c || !out) return DFL_E_INVALID_ARG;
+    for (int l = 0; l < c->cfg.n_layers; ++l)
+        out[l] = c->tl[l].owner == l ? 2 * c->tl[l].nkv * c->cfg.head_dim : 0;
+    return DFL_OK;
+}
+
+int64_t dfl_positions_held(const dfl_ctx *c) { return c ? c->n : -1; }
+
+int dfl_set_option(dfl_ctx *c, int option, int value) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (option == DFL_OPT_KEEP_LOGITS) c->keep_logits = value != 0;
+    else if (option == DFL_OPT_GRAPHS) (void)value;
+    else if (option == DFL_OPT_STOP_LAYER) c->stop_layer = value;
+    else return fail(c, DFL_E_INVALID_ARG, "unknown option");
+    return DFL_OK;
+}
+
+int dfl_read_logits(dfl_ctx *c, int which, float *dst, int rows) {
+    if (!c || !dst) return DFL_E_INVALID_ARG;
+    const int V = c->cfg.vocab;
+    if (which == 0) {
+        if (!c->have_logits) return fail(c, DFL_E_STATE, "no verify logits kept");
+        if (rows < 1 || rows > c->last_k) return fail(c, DFL_E_INVALID_ARG, "rows out of range");
+        DFL_CK(cudaMemcpyAsync(dst, c->logits, (size_t)rows * V * 4, cudaMemcpyDeviceToHost, c->stream));
+    } else if (which == 1) {
+        if (!c->have_dlogits) return fail(c, DFL_E_STATE, "no draft logits kept");
+        if (rows < 1 || rows > c->cfg.block - 1) return fail(c, DFL_E_INVALID_ARG, "rows out of range");
+        DFL_CK(cudaMemcpyAsync(dst, c->dlogits, (size_t)rows * V * 4, cudaMemcpyDeviceToHost, c->stream));
+    } else {
+        return fail(c, DFL_E_INVALID_ARG, "which must be 0 or 1");
+    }
+    DFL_CK(cudaStreamSynchronize(c->stream));
+    return DFL_OK;
+}
+
+int dfl_read_taps(dfl_ctx *c, int pos0, int rows, float *dst) {
+    if (!c || !dst) return DFL_E_INVALID_ARG;
+    if (pos0 < 0 || rows < 1 || pos0 + rows > c->cfg.max_ctx + kMaxRows) return fail(c, DFL_E_INVALID_ARG, "rows out of range");
+    DFL_CK(cudaMemcpyAsync(dst, c->taps + (size_t)pos0 * c->TH, (size_t)rows * c->TH * 4, cudaMemcpyDeviceToHost, c->stream));
+    DFL_CK(cudaStreamSynchronize(c->stream));
+    return DFL_OK;
+}
+
+int dfl_draft_append_taps(dfl_ctx *c, const void *src, int rows) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (!src || rows < 1) return fail(c, DFL_E_INVALID_ARG, "bad taps");
+    if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending");
+    if ((long)c->n + rows > c->cfg.max_ctx) return fail(c, DFL_E_CAPACITY, "taps exceed max_ctx");
+    int rc = ready(c);
+    if (rc) return rc;
+    DFL_CK(cudaMemcpyAsync(c->taps + (size_t)c->n * c->TH, src, (size_t)rows * c->TH * 4, cudaMemcpyDeviceToDevice,
+                           c->stream));
+    c->n += rows;
+    c->draft_only = true;
+    c->draft_at = -1;
+    return catch_up(c, 0);
+}
+
+int dfl_debug_read(dfl_ctx *c, const char *name, void *dst, size_t bytes) {
+    if (!c || !name || !dst) return DFL_E_INVALID_ARG;
+    const std::string s(name);
+    const void *src = nullptr;
+    size_t have = 0;
+    const size_t R = kMaxRows, H = c->cfg.hidden;
+    if (s == "x") src = c->x, have = R * H * 4;
+    else if (s == "h") src = c->h, have = R * H * 4;
+    else if (s == "y") src = c->y, have = R * H * 4;
+    else if (s == "qkv") src = c->qkv, have = R * c->qkv_max * 4;
+    else if (s == "q") src = c->q, have = R * std::max(c->cfg.n_heads * c->cfg.head_dim, c->cfg.d_heads * c->cfg.d_head_dim) * 4;
+    else if (s == "o") src = c->o, have = R * std::max(c->cfg.n_heads * c->cfg.head_dim, c->cfg.d_heads * c->cfg.d_head_dim) * 4;
+    else if (s == "x_d") src = c->x_d, have = R * H * 4;
+    else return fail(c, DFL_E_INVALID_ARG, "unknown buffer " + s);
+    if (bytes > have) return fail(c, DFL_E_INVALID_ARG, "read past the buffer");
+    DFL_CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, c->stream));
+    DFL_CK(cudaStreamSynchronize(c->stream));
+    return DFL_OK;
+}
+
+const char *dfl_last_error(const dfl_ctx *c) { return c ? c->err.c_str() : "null context"; }
+
+void dfl_destroy(dfl_ctx *c) { delete c; }
+
+int64_t dfl_q41_image_bytes(int K, int N) {
+    if (K < 32 || K % 32 || N < 32 || N % 32) return -1;
+    return (int64_t)q41_image_bytes(K, N);
+}
+
+int dfl_q41_pack(const void *src, int K, int N, void *img, void *stream) {
+    if (!src || !img || K < 32 || K % 32 || N < 32 || N % 32) return DFL_E_INVALID_ARG;
+    return launch_pack_q41(static_cast<const uint8_t *>(src), K, N, static_cast<uint8_t *>(img),
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+}
+
+// scratch = arrival counters (N/32 ints, at offset 0, rounded up to 256 bytes), then the partial sums
+int64_t dfl_q41_gemm_scratch_bytes(int K, int N, int M) {
+    if (K < 32 || K % 32 || N < 32 || N % 32 || M < 1 || M > kMaxRows) return -1;
+    const int C = padded_k(K) / 64;
+    const int S = gemm_splits(C, N, W_Q41);
+    return (int64_t)((size_t)(N / 32 * 4 + 255) / 256 * 256 + gemm_scratch_floats(S, M, N) * 4);
+}
+
+int dfl_q41_gemm(const void *img, int K, int N, const void *x, int M, float *y, void *scratch, size_t scratch_bytes,
+                 void *stream) {
+    const int64_t need = dfl_q41_gemm_scratch_bytes(K, N, M);
+    if (need < 0 || !img || !x || !y || !scratch || (int64_t)scratch_bytes < need) return DFL_E_INVALID_ARG;
+    const int C = padded_k(K) / 64;
+    GemmArgs a{};
+    a.img = static_cast<const uint8_t *>(img);
+    a.K = K;
+    a.C = C;
+    a.N = N;
+    a.M = M;
+    a.S = gemm_splits(C, N, W_Q41);
+    a.x = static_cast<const uint16_t *>(x);
+    a.ldx = K;
+    a.y = y;
+    a.ldy = N;
+    const size_t cbytes = (size_t)(N / 32 * 4 + 255) / 256 * 256;
+    a.cnt = static_cast<int *>(scratch);
+    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + cbytes);
+    return launch_gemm(W_Q41, EPI_F32, X_BF16, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,218 @@
+/*
+ * dfl.h -- C ABI of one DFlash speculative-decode step over Q4_1 weights on one GB300 (sm_103a).
+ *
+ * The step (pages, by title and section):
+ *   1. Draft: an 8-row block [last token, mask x 7] conditioned on the target's tapped layer outputs
+ *      through the draft's fc projection proposes up to 7 tokens in one pass (model card
+ *      "Nemotron-3.5-Bolt-E4B-DFlash-NPU2", spec table and "How it is used"; 1bit engine PR "a Gemma4
+ *      pack stops re-reading its weights every token; tools/dflash_acceptance", item 2).
+ *   2. Verify: one batched pass of the target over the k drafted rows, every projection one M-row
+ *      product, attention over per-layer-width KV planes: sliding and full layers, and KV-shared
+ *      layers that read their owner's plane and append nothing (1bit engine PR "npu forward: Gemma4
+ *      verifies a draft in one batched pass; KV row width per layer", "What changes").
+ *   3. Accept the longest agreeing prefix plus one target token (greedy, first maximum; or sampled
+ *      per position), then commit_verify_rows: keep that many rows, pure index arithmetic.
+ *
+ * Conventions
+ *  - Every call returns DFL_OK (0) or a negative DFL_E_* code; dfl_last_error() gives the message.
+ *    On any error the state (positions held, planes, draft context) is unchanged.
+ *  - Memory: the library never allocates device memory. The caller allocates the three device buffers
+ *    sized by dfl_required_bytes() and keeps them alive until dfl_destroy(). Device pointers below
+ *    are marked "device"; everything else is host memory.
+ *  - Calls enqueue work on the stream given to dfl_init(). Calls with host outputs (tokens, counts,
+ *    logits) synchronise that stream before returning, so the outputs are valid on return. Calls
+ *    without host outputs return without synchronising.
+ *  - Numbers: activations, KV planes and taps are fp32 (the pages' "floats"); weights are Q4_1 or bf16.
+ *  - Formats: bf16 = upper half of IEEE binary32. Q4_1 matrix ("container" layout): uint8
+ *    [N][K/32][20]; block = fp16 scale d, fp16 minimum m, 16 bytes of 4-bit codes, element i of the
+ *    block in byte 4 + i/2 (low nibble for even i); weight w = d*q + m ("Q4_1: 5 bits per weight with
+ *    scales and minimums", model card spec table). N = output columns, K = inputs (reduction).
+ *  - Not thread-safe: one host thread per context.
+ */
+#ifndef DFL_H
+#define DFL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFL_MAX_LAYERS 64
+#define DFL_MAX_TAPS 8
+#define DFL_MAX_ROWS 16          /* rows of one verify or prefill chunk (R_max) */
+
+enum {
+    DFL_OK = 0,
+    DFL_E_INVALID_ARG = -1,      /* bad pointer, size, token id or configuration */
+    DFL_E_STATE = -2,            /* call not legal in the current state (e.g. verify while pending) */
+    DFL_E_CAPACITY = -3,         /* positions would exceed max_ctx */
+    DFL_E_UNSUPPORTED = -4,      /* e.g. k > DFL_MAX_ROWS, a shape the kernels do not take */
+    DFL_E_CUDA = -5,             /* a CUDA call failed; the message names it */
+    DFL_E_TIMEOUT = -6           /* a bounded device wait gave up */
+};
+
+enum { DFL_SLIDING = 0, DFL_FULL = 1 };
+
+/* Model and capacity. Layer l is KV-shared when kv_owner[l] != l: it reads the plane of layer
+ * kv_owner[l] (the last non-shared layer of the same attention type) and appends nothing. */
+typedef struct dfl_config {
+    /* target */
+    int32_t n_layers, hidden, vocab, n_heads, head_dim;
+    int32_t window;                        /* sliding window: keys p-window+1..p visible to position p */
+    int32_t ple_dim;                       /* per-layer-embedding width; 0 = none (and no layer scalar) */
+    int32_t layer_type[DFL_MAX_LAYERS];    /* DFL_SLIDING / DFL_FULL */
+    int32_t kv_heads[DFL_MAX_LAYERS];
+    int32_t kv_owner[DFL_MAX_LAYERS];
+    int32_t ffn[DFL_MAX_LAYERS];
+    float rope_base_sliding, rope_base_full, eps, emb_scale;
+    /* draft (hidden width = target hidden) */
+    int32_t d_layers, d_ffn, d_heads, d_kv_heads, d_head_dim;
+    int32_t d_window;                      /* context keys visible to a block; 0 = all */
+    int32_t block;                         /* rows of a draft block (proposals = block - 1) */
+    int32_t n_taps, mask_token;
+    int32_t taps[DFL_MAX_TAPS];            /* target layers whose outputs feed fc, ascending */
+    float d_rope_base, d_eps, d_emb_scale;
+    /* capacity */
+    int32_t max_ctx;                       /* positions the KV arena holds */
+} dfl_config;
+
+typedef struct dfl_sizes {
+    uint64_t weights_bytes;                /* packed weight image, tables */
+    uint64_t state_bytes;                  /* KV planes, draft context, taps, device counters */
+    uint64_t workspace_bytes;              /* activations and reduction scratch of one pass */
+} dfl_sizes;
+
+typedef struct dfl_buffers {
+    void *weights;                         /* device, >= weights_bytes, 256-byte aligned */
+    void *state;                           /* device, >= state_bytes, 256-byte aligned */
+    void *workspace;                       /* device, >= workspace_bytes, 256-byte aligned */
+} dfl_buffers;
+
+/* Sampling: temperature > 0 samples every verified position with the uniform
+ * U(seed, position) = top 53 bits of SplitMix64(seed XOR position * 0x9E3779B97F4A7C15) * 2^-53,
+ * and picks the smallest token whose running sum of exp((l - max)/T) exceeds U * sum.
+ * A NULL dfl_sampling, or temperature <= 0, means greedy (first maximum). */
+typedef struct dfl_sampling {
+    float temperature;
+    uint64_t seed;
+} dfl_sampling;
+
+typedef struct dfl_ctx dfl_ctx;
+
+/* Sizes of the three device buffers for a configuration. Fails with DFL_E_INVALID_ARG or
+ * DFL_E_UNSUPPORTED on a configuration the library does not take (it states which field). */
+int dfl_required_bytes(const dfl_config *cfg, dfl_sizes *out);
+
+/* Create a context over caller-owned device buffers (sizes from dfl_required_bytes) and a CUDA
+ * stream (cudaStream_t, may be NULL for the legacy stream). Positions held start at 0. Every tensor
+ * must then be given once with dfl_load_tensor before the first pass. The context does not own the
+ * buffers or the stream. */
+int dfl_init(const dfl_config *cfg, const dfl_buffers *buf, void *cuda_stream, dfl_ctx **out);
+
+/* Load one tensor from DEVICE memory in its container format; the library packs it into its own
+ * layout in the weights buffer (Q4_1 matrices into a tile-major image of the same bytes per weight).
+ * Names: "emb" bf16 [vocab][hidden]; "head" bf16 [vocab][hidden]; "final_norm" bf16 [hidden];
+ * "ple_table" bf16 [vocab][n_layers*ple_dim]; per target layer l, "t<l>.": attn_norm, q_norm,
+ * k_norm (owners), post_attn_norm, pre_ffn_norm, post_ffn_norm, ple_norm (bf16), lambda (bf16 [1]),
+ * wqkv (owners: q|k|v) or wq (shared), wo, wgu (gate|up), wd, wple_g, wple_p (Q4_1);
+ * draft: "d.fc" bf16 [hidden][n_taps*hidden], "d.hidden_norm", "d.final_norm", and per draft
+ * layer "d<l>.": attn_norm, q_norm, k_norm, ffn_norm, wqkv, wo, wgu, wd.
+ * `bytes` must equal the tensor's container size. The source may be freed once the stream has
+ * passed this call (it is read by kernels enqueued here). */
+int dfl_load_tensor(dfl_ctx *ctx, const char *name, const void *dev_src, size_t bytes);
+
+/* Prefill (extend the context): run the n tokens at positions held..held+n-1 in chunks of at most
+ * DFL_MAX_ROWS rows, commit them, bring the draft context up to date, and write the target's token
+ * for the next position to *next_tok (greedy or sampled). Fails with DFL_E_CAPACITY if held + n + 1
+ * exceeds max_ctx. */
+int dfl_prefill(dfl_ctx *ctx, const int32_t *tokens, int n, const dfl_sampling *s, int32_t *next_tok);
+
+/* Draft block at positions held..held+block-1 for rows [last_tok, mask x (block-1)]: first makes the
+ * committed rows not yet in the draft context into context (fc of their taps, then each draft layer's
+ * key and value), then runs the block. Proposals (block-1 tokens for positions held+1..) are kept on
+ * the device for dfl_verify_block(rows = NULL) and copied to `proposals` when it is not NULL. */
+int dfl_draft_block(dfl_ctx *ctx, int32_t last_tok, int32_t *proposals);
+
+/* Batched verify of k rows at positions held..held+k-1. rows = [last token, proposal 1, ..,
+ * proposal k-1]; rows == NULL takes last_tok of the last draft block and its k-1 first proposals.
+ * Writes the target's token for positions held+1..held+k to target_tok[0..k-1] (if not NULL) and
+ * the accepted length a (longest prefix with proposal i == target token i-1) to *accepted (if not
+ * NULL). The rows stay pending until dfl_commit_verify_rows. k in 1..DFL_MAX_ROWS. */
+int dfl_verify_block(dfl_ctx *ctx, const int32_t *rows, int k, const dfl_sampling *s,
+                     int32_t *target_tok, int32_t *accepted);
+
+/* commit_verify_rows: keep the first `keep` rows of the pending verify (0 <= keep <= k); positions
+ * held become held + keep. Pure index arithmetic: no data moves; later rows are overwritten by the
+ * next pass. keep = DFL_KEEP_ACCEPTED keeps accepted + 1 rows (the accepted proposals and the row of
+ * the last token) as counted by the last verify. */
+#define DFL_KEEP_ACCEPTED (-1)
+int dfl_commit_verify_rows(dfl_ctx *ctx, int keep);
+
+/* Snapshot of the committed state (positions held, every owner plane, the draft context, the taps
+ * of committed rows not yet in the draft context) into a DEVICE buffer of at least
+ * dfl_snapshot_bytes() bytes; restore replaces the state with a snapshot taken from a context with
+ * the same configuration. Both need the committed state (no pending verify). KV-shared layers have no
+ * plane and contribute nothing. */
+int64_t dfl_snapshot_bytes(const dfl_ctx *ctx);
+int dfl_snapshot(dfl_ctx *ctx, void *dev_dst, size_t bytes);
+int dfl_restore(dfl_ctx *ctx, const void *dev_src, size_t bytes);
+
+/* Per-layer KV row width in floats per position: 2 * kv_heads * head_dim for a layer with its own
+ * plane, 0 for a KV-shared layer. out: n_layers entries. */
+int dfl_kv_widths(const dfl_ctx *ctx, int32_t *out);
+
+/* Positions held (committed), counted over owner planes only. -1 on a NULL context. */
+int64_t dfl_positions_held(const dfl_ctx *ctx);
+
+/* Options. DFL_OPT_KEEP_LOGITS = 1 makes verify and draft passes also store their fp32 logits
+ * (otherwise only the fused argmax runs); DFL_OPT_GRAPHS = 0 launches kernels one by one instead of
+ * replaying captured CUDA graphs; DFL_OPT_STOP_LAYER = l >= 0 (inspection only) makes target passes
+ * stop after layer l, without the head, so dfl_debug_read shows that layer's intermediates; -1 = off. */
+enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3 };
+int dfl_set_option(dfl_ctx *ctx, int option, int value);
+
+/* Copy the fp32 logits of the last pass (rows x vocab, row-major) to host memory. which = 0: the
+ * last verify or prefill chunk (rows <= its k); which = 1: the last draft block (rows 1..block-1,
+ * rows <= block-1). Needs DFL_OPT_KEEP_LOGITS. */
+int dfl_read_logits(dfl_ctx *ctx, int which, float *host_dst, int rows);
+
+/* Copy the fp32 taps of positions pos0..pos0+rows-1 (n_taps*hidden each) to host memory. */
+int dfl_read_taps(dfl_ctx *ctx, int pos0, int rows, float *host_dst);
+
+/* Draft-only context: make `rows` rows of given taps (DEVICE fp32 [rows][n_taps*hidden]) context at
+ * positions held..held+rows-1 and advance positions held, without running the target. A context used
+ * this way refuses dfl_verify_block and dfl_prefill (DFL_E_STATE). */
+int dfl_draft_append_taps(dfl_ctx *ctx, const void *dev_taps, int rows);
+
+/* Inspection: copy the first `bytes` of an internal buffer of the last pass to host memory. Names:
+ * "x" [16][hidden] residual rows, "h" [16][hidden] next product input, "y" [16][hidden] last projection
+ * output, "qkv" [16][width], "q" [16][heads*head_dim] (normed, rotated), "o" [16][heads*head_dim]
+ * attention output, "x_d" [16][hidden] draft residual rows; all fp32. */
+int dfl_debug_read(dfl_ctx *ctx, const char *name, void *host_dst, size_t bytes);
+
+const char *dfl_last_error(const dfl_ctx *ctx);
+void dfl_destroy(dfl_ctx *ctx);
+
+/* ---- the Q4_1 product on its own (used for the isolated GEMM measurements) ----------------------- */
+
+/* Bytes of the packed tile image of a K x N Q4_1 matrix (K padded up to a multiple of 64). */
+int64_t dfl_q41_image_bytes(int K, int N);
+/* Pack a container-layout Q4_1 matrix (DEVICE) into the tile image (DEVICE). */
+int dfl_q41_pack(const void *dev_src, int K, int N, void *dev_image, void *cuda_stream);
+/* Scratch bytes dfl_q41_gemm needs for K, N, M. */
+int64_t dfl_q41_gemm_scratch_bytes(int K, int N, int M);
+/* y[m][n] = sum_k x[m][k] * w[k][n] (fp32), x bf16 DEVICE [M][K], y fp32 DEVICE [M][N], from the tile
+ * image; M in 1..16; N a multiple of 32. The scratch (DEVICE, >= dfl_q41_gemm_scratch_bytes) holds
+ * arrival counters (first N/32 ints) and split-K partial sums; it must be zeroed once before the first
+ * call (each call leaves the counters zero). Calls on one scratch must not overlap on the GPU. The
+ * result does not depend on M (fixed reduction order). */
+int dfl_q41_gemm(const void *dev_image, int K, int N, const void *dev_x, int M, float *dev_y,
+                 void *dev_scratch, size_t scratch_bytes, void *cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFL_H */

@@ -1,0 +1,70 @@
+"""CPU: the C-ABI library builds, loads without a GPU, and exports every entry point include/dfl.h
+declares; the Python binding names the same set."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dfl.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dfl_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    from dflash_speculative_decode_gb300 import build
+    path = build.build()
+    L = ctypes.CDLL(path)
+    names = _declared()
+    assert len(names) >= 20
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_header():
+    from dflash_speculative_decode_gb300 import _abi
+    assert sorted(_abi.SIGNATURES) == _declared()
+
+
+def test_required_bytes_without_gpu():
+    """Size planning is host arithmetic: it runs without a device."""
+    import gen
+    from dflash_speculative_decode_gb300 import _abi
+    L = _abi.lib()
+    for pc in (gen.tiny_pair(), gen.tiny_shared_pair(), gen.e4b_pair()):
+        cfg = _abi.config_from_pair(pc)
+        sz = _abi.dfl_sizes()
+        assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == 0
+        assert sz.weights_bytes > 0 and sz.state_bytes > 0 and sz.workspace_bytes > 0
+    e4b = _abi.config_from_pair(gen.e4b_pair())
+    sz = _abi.dfl_sizes()
+    L.dfl_required_bytes(ctypes.byref(e4b), ctypes.byref(sz))
+    # Q4_1 layer weights (0.625 B/weight) + bf16 embedding, head, PLE table and fc
+    assert 11.5e9 < sz.weights_bytes < 13.5e9
+
+
+def test_bad_configuration_is_refused():
+    import gen
+    from dflash_speculative_decode_gb300 import _abi
+    L = _abi.lib()
+    sz = _abi.dfl_sizes()
+    cfg = _abi.config_from_pair(gen.tiny_pair())
+    cfg.kv_owner[2] = 3                       # a later layer cannot own an earlier layer's plane
+    assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == _abi.DFL_E_INVALID_ARG
+    cfg = _abi.config_from_pair(gen.tiny_pair())
+    cfg.block = 17
+    assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == _abi.DFL_E_INVALID_ARG
+    cfg = _abi.config_from_pair(gen.tiny_shared_pair())
+    cfg.kv_owner[5] = 3                       # owner of another attention type
+    assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == _abi.DFL_E_INVALID_ARG
+
+
+def test_q41_sizes():
+    from dflash_speculative_decode_gb300 import _abi
+    L = _abi.lib()
+    assert L.dfl_q41_image_bytes(2560, 4096) == 2560 * 4096 * 5 // 8
+    assert L.dfl_q41_image_bytes(32, 64) == 64 * 64 * 5 // 8      # K padded to 64
+    assert L.dfl_q41_image_bytes(30, 64) == -1
+    assert L.dfl_q41_gemm_scratch_bytes(2560, 4096, 17) == -1
