@@ -1,0 +1,385 @@
+"""Benchmark: DFlash speculative decode (block 8) on the E4B-shaped synthetic pair at 1k context.
+
+One JSON line on stdout. A step is one speculative pass: draft block -> plant proposals -> batched
+verify of 8 rows -> accept -> commit_verify_rows. `value` is decode tokens/s with every input resident
+in HBM (weights, KV state, the planted-proposal table); `e2e` is the same loop through the host-buffer
+calls (proposals copied in from host memory, proposals and target tokens copied out every step).
+`roofline` reports the Q4_1 products (the dominant kernel) against the measured HBM copy bandwidth;
+`cpu_baseline` times the oracle on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference] [--workload e4b|gemm]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gen  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+METRIC = "spec-decode tok/s (block 8, 1 GB300); Q4_1 verify-GEMM HBM GB/s vs 8 TB/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "src": "measured"}
+    return dict(PEAKS_FALLBACK, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    def __init__(self, index=0):
+        self.index, self.samples, self.proc = index, [], None
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------------------------------
+def e4b_workload(args):
+    pc = gen.e4b_pair(max_ctx=args.ctx + 512 + 64)
+    return pc, {"workload": f"e4b-pair ctx {args.ctx} block 8 greedy, planted drafts p={args.p}, "
+                            f"512-token decodes", "target": "42 layers hidden 2560 ffn 10240/20480 12x256 heads, "
+                            "PLE 256, vocab 262144, Q4_1", "draft": "5 layers hidden 2560 ffn 5120 32/8x128, fc 5x2560",
+                "context": args.ctx, "generated_per_decode": 512, "corruption_p": args.p,
+                "l2": "weights streamed per step (6.4 GB) exceed the 129 MB L2"}
+
+
+def load_engine(pc, keep=False, workers=None):
+    from dflash_speculative_decode_gb300 import Engine, config_from_pair
+    eng = Engine(config_from_pair(pc))
+    kept = {} if keep else None
+    workers = workers or min(16, os.cpu_count() or 1)
+    t0 = time.time()
+    for name, arr in gen.iter_tensors(pc, workers=workers):
+        eng.load_tensor(name, arr)
+        if keep:
+            kept[name] = arr
+    return eng, kept, time.time() - t0
+
+
+def planted_table(torch, eng, pc, first, n_gen, p):
+    """Plain greedy decode on the GPU from the prefilled state (untimed) gives the target's own tokens G;
+    the planted proposal for absolute position q is G[q] unless the position is corrupted
+    (gen.corruption, keyed by q). Returns the prefix snapshot (taken before the decode)."""
+    snap = eng.dfl_snapshot()
+    P = eng.dfl_positions_held()
+    toks = [first]
+    while len(toks) < n_gen:
+        tt, _ = eng.dfl_verify_block([toks[-1]])
+        eng.dfl_commit_verify_rows(1)
+        toks.append(int(tt[0]))
+    L = pc.max_ctx + 32
+    G = np.zeros(L, np.int32)
+    G[P:P + len(toks)] = toks
+    cor = gen.corruption(p, pc.target.vocab, L)
+    table = cor.propose(G, np.arange(L))
+    return snap, toks, torch.from_numpy(table).cuda()
+
+
+def run_steps(eng, torch, table_dev, first_tok, snap, n0, steps, n_gen, host_rows=None):
+    """`steps` speculative passes; a 512-token decode that runs out restarts from the prefix snapshot.
+    Device mode: proposals planted from the device table. Host mode (host_rows = host table): proposals
+    read back to host, planted there, and passed in host memory."""
+    from dflash_speculative_decode_gb300 import DFL_KEEP_ACCEPTED
+    B = eng.cfg.block
+    tokens = 0
+    last = first_tok
+    produced = 1
+    for _ in range(steps):
+        if produced >= n_gen:
+            eng.dfl_restore(snap)
+            last, produced = first_tok, 1
+        if host_rows is None:
+            eng.dfl_draft_block(last, want=False)
+            eng.dfl_plant_proposals(table_dev)
+            tt, a = eng.dfl_verify_block(None, k=B)
+        else:
+            n = eng.dfl_positions_held()
+            eng.dfl_draft_block(last, want=True)
+            rows = np.concatenate([[last], host_rows[n + 1:n + B]]).astype(np.int32)
+            tt, a = eng.dfl_verify_block(rows)
+        eng.dfl_commit_verify_rows(DFL_KEEP_ACCEPTED)
+        last = int(tt[a])
+        tokens += a + 1
+        produced += a + 1
+    return tokens
+
+
+def bench_cuda(args):
+    import torch
+    from dflash_speculative_decode_gb300 import build
+    from dflash_speculative_decode_gb300._abi import DFL_OPT_PROFILE
+    build.build()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    pc, cfgdesc = e4b_workload(args)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    eng, W, t_load = load_engine(pc, keep=want_cpu)
+    prompt = gen.prompt(pc.target.vocab, args.ctx)
+    t0 = time.time()
+    first = eng.dfl_prefill(prompt)
+    torch.cuda.synchronize()
+    t_prefill = time.time() - t0
+    snap, plain, table = planted_table(torch, eng, pc, first, 512, args.p)
+    eng.dfl_restore(snap)
+    n0 = eng.dfl_positions_held()
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    run_steps(eng, torch, table, first, snap, n0, args.warmup, 512)
+    eng.dfl_restore(snap)
+    # timed: device-resident loop
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = Clocks(local)
+    clk.start()
+    l0 = eng.dfl_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    toks = run_steps(eng, torch, table, first, snap, n0, args.steps, 512)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = eng.dfl_launch_count() - l0
+    ms = e0.elapsed_time(e1)
+    clocks = clk.stop()
+    if world > 1:
+        t = torch.tensor([ms, toks], dtype=torch.float64, device="cuda")
+        mx = t.clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+        ms, toks_all = float(mx[0]), float(t[1])
+    else:
+        toks_all = toks
+    value = toks_all / (ms / 1e3)
+
+    # e2e: host-buffer calls
+    eng.dfl_restore(snap)
+    host_table = table.cpu().numpy()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    toks_e2e = run_steps(eng, torch, table, first, snap, n0, args.steps, 512, host_rows=host_table)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t1
+
+    # roofline: per-launch events on the products over the same steps
+    eng.dfl_restore(snap)
+    eng.dfl_set_option(DFL_OPT_PROFILE, 1)
+    run_steps(eng, torch, table, first, snap, n0, args.steps, 512)
+    q_n, q_ms, q_bytes = eng.dfl_profile_read(0)
+    h_n, h_ms, h_bytes = eng.dfl_profile_read(2)
+    f_n, f_ms, f_bytes = eng.dfl_profile_read(1)
+    eng.dfl_set_option(DFL_OPT_PROFILE, 0)
+    pk = peaks()
+    achieved = q_bytes / (q_ms / 1e3) / 1e9 if q_ms else 0.0
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+            "kernel": "k_gemm (Q4_1 products of draft and verify)", "peak_source": pk["src"],
+            "launches": q_n, "avg_launch_us": round(q_ms * 1e3 / max(q_n, 1), 2),
+            "bytes_per_launch": round(q_bytes / max(q_n, 1)),
+            "frac_vs_8TBs": round(achieved / 8000.0, 4),
+            "head": {"achieved": round(h_bytes / (h_ms / 1e3) / 1e9, 1) if h_ms else None, "launches": h_n,
+                     "avg_launch_us": round(h_ms * 1e3 / max(h_n, 1), 2)},
+            "products_share_of_step": round((q_ms + h_ms + f_ms) / ms, 3) if ms else None}
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "fp32 activations, Q4_1/bf16 weights",
+           "data": "synthetic (seeded random-init weights of the E4B-shaped pair, uniform prompt)",
+           "config": dict(cfgdesc, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+           "tokens_per_step": round(toks_all / world / args.steps, 3),
+           "e2e": {"value": round(toks_e2e / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * pc.draft.block,
+                   "d2h_bytes_per_step": 4 * (pc.draft.block - 1) + 4 * pc.draft.block + 4},
+           "gpu_launches": launches, "roofline": roof, "clocks": clocks,
+           "setup_s": {"load": round(t_load, 1), "prefill": round(t_prefill, 2)}}
+    if want_cpu:
+        out["cpu_baseline"] = cpu_baseline(pc, W, args, out["tokens_per_step"])
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def cpu_baseline(pc, W, args, tokens_per_step):
+    """The oracle (C products, one row at a time, OpenMP over output columns) on a bounded sample of the
+    same workload: one speculative pass (draft block + 8-row verify) of the E4B pair after a 4-token
+    prefix; tokens/s = the GPU run's tokens per pass / the oracle's time per pass."""
+    import oracle
+    oracle.build()
+    pair = oracle.Pair(pc, W)
+    prompt = gen.prompt(pc.target.vocab, 4)
+    first, _ = pair.prefill(prompt, oracle.Sampler())
+    t0 = time.time()
+    pair.sync_draft()
+    dp, _ = pair.draft.block(first, W["emb"], W["head"])
+    pair.verify([first] + [int(v) for v in dp], oracle.Sampler())
+    dt = time.time() - t0
+    return {"value": round(tokens_per_step / dt, 4), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": "one speculative pass (draft block + 8-row verify) of the E4B pair "
+                                        "at a 4-token context, scaled by the GPU run's tokens per pass",
+            "seconds_per_pass": round(dt, 2)}
+
+
+def bench_reference(args):
+    """The oracle as the reference arm, on the machine's host cores: K timed speculative passes (draft block
+    + 8-row verify + commit) of the E4B pair on a bounded sample of the workload (4-token context).
+    A pass costs the oracle the same whatever the proposals, so tokens/s = the planted stream's expected
+    tokens per pass at corruption p, 1 + sum_{i=1..7} (1-p)^i, over the measured time per pass."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    pc, cfgdesc = e4b_workload(args)
+    W = gen.generate(pc, workers=min(16, os.cpu_count() or 1))
+    pair = oracle.Pair(pc, W)
+    sm = oracle.Sampler()
+    first, _ = pair.prefill(gen.prompt(pc.target.vocab, 4), sm)
+    last, t_timed = first, 0.0
+    for i in range(args.warmup + args.steps):
+        t0 = time.time()
+        pair.sync_draft()
+        dp, _ = pair.draft.block(last, W["emb"], W["head"])
+        tt, _, _ = pair.verify([last] + [int(v) for v in dp], sm)
+        a = oracle.accept_length([int(v) for v in dp], tt[:-1])
+        pair.target.commit(a + 1)
+        last = tt[a]
+        if i >= args.warmup:
+            t_timed += time.time() - t0
+    per_pass = 1.0 + sum((1.0 - args.p) ** i for i in range(1, pc.draft.block))
+    value = per_pass * args.steps / t_timed
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_timed / args.steps, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp64 arithmetic, fp32 storage",
+           "data": "synthetic", "config": dict(cfgdesc, sample="4-token context"),
+           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": "speculative passes of the E4B pair at a 4-token context, "
+                                      f"{per_pass:.3f} tokens per pass (planted p={args.p})"},
+           "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def bench_gemm(args):
+    """Isolated Q4_1 product sweep: rows M in {1,2,4,8,16}; 100 seeded weight buffers per shape cycled
+    so the weights come from HBM; bf16 activations N(0,1)."""
+    import ctypes
+    import torch
+    from dflash_speculative_decode_gb300 import _abi, build
+    build.build()
+    L = _abi.lib()
+    pk = peaks()
+    dev = torch.device("cuda:0")
+    st = torch.cuda.current_stream()
+    res = []
+    shapes = [(2560, 10240), (10240, 2560), (2560, 4096), (2560, 20480), (20480, 2560)]
+    for K, N in shapes:
+        nbuf = max(8, min(100, int(8e9 // (K * N * 0.625))))
+        imgs = []
+        src = torch.from_numpy(gen.make_tensor(gen.TensorSpec("sweep", "q41", (N, K), 0.02), seed=5).reshape(-1)).to(dev)
+        for i in range(nbuf):
+            img = torch.empty(L.dfl_q41_image_bytes(K, N), dtype=torch.uint8, device=dev)
+            L.dfl_q41_pack(ctypes.c_void_p(src.data_ptr()), K, N, ctypes.c_void_p(img.data_ptr()),
+                           ctypes.c_void_p(st.cuda_stream))
+            imgs.append(img)
+        del src
+        for M in (1, 2, 4, 8, 16):
+            x = torch.from_numpy(gen.activations(M, K, seed=M).view(np.int16)).to(dev)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            sb = L.dfl_q41_gemm_scratch_bytes(K, N, M)
+            scratch = torch.zeros(sb, dtype=torch.uint8, device=dev)
+
+            def once(i):
+                L.dfl_q41_gemm(ctypes.c_void_p(imgs[i % nbuf].data_ptr()), K, N, ctypes.c_void_p(x.data_ptr()), M,
+                               ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(scratch.data_ptr()), sb,
+                               ctypes.c_void_p(st.cuda_stream))
+            for i in range(max(args.warmup, 3)):
+                once(i)
+            reps = 100
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(st)
+            for i in range(reps):
+                once(i)
+            e1.record(st)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            by = K * N * 0.625 + M * K * 2 + M * N * 4
+            gbs = by / (us * 1e-6) / 1e9
+            res.append({"K": K, "N": N, "M": M, "us": round(us, 2), "GB/s": round(gbs, 1),
+                        "frac_measured": round(gbs / pk["hbm_gbs"], 3), "frac_8TBs": round(gbs / 8000, 3)})
+        del imgs
+        torch.cuda.empty_cache()
+    print(json.dumps({"workload": "isolated Q4_1 product sweep", "peak_gbs": pk["hbm_gbs"], "results": res}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm"])
+    ap.add_argument("--ctx", type=int, default=1024)
+    ap.add_argument("--p", type=float, default=0.3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return bench_reference(args)
+    if args.workload == "gemm":
+        return bench_gemm(args)
+    return bench_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libdfl.so")
 MAX_LAYERS, MAX_TAPS, MAX_ROWS = 64, 8, 16
 DFL_OK, DFL_E_INVALID_ARG, DFL_E_STATE, DFL_E_CAPACITY, DFL_E_UNSUPPORTED, DFL_E_CUDA, DFL_E_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 DFL_KEEP_ACCEPTED = -1
-DFL_OPT_KEEP_LOGITS, DFL_OPT_GRAPHS, DFL_OPT_STOP_LAYER = 1, 2, 3
+DFL_OPT_KEEP_LOGITS, DFL_OPT_GRAPHS, DFL_OPT_STOP_LAYER, DFL_OPT_PROFILE = 1, 2, 3, 4
 ERRORS = {DFL_E_INVALID_ARG: "DFL_E_INVALID_ARG", DFL_E_STATE: "DFL_E_STATE", DFL_E_CAPACITY: "DFL_E_CAPACITY",
           DFL_E_UNSUPPORTED: "DFL_E_UNSUPPORTED", DFL_E_CUDA: "DFL_E_CUDA", DFL_E_TIMEOUT: "DFL_E_TIMEOUT"}
 
@@ -76,6 +76,9 @@ SIGNATURES = {
     "dfl_read_taps": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, P(ctypes.c_float)]),
     "dfl_draft_append_taps": (ctypes.c_int, [vp, vp, ctypes.c_int]),
     "dfl_debug_read": (ctypes.c_int, [vp, ctypes.c_char_p, vp, ctypes.c_size_t]),
+    "dfl_plant_proposals": (ctypes.c_int, [vp, vp, ctypes.c_int]),
+    "dfl_launch_count": (ctypes.c_int64, [vp]),
+    "dfl_profile_read": (ctypes.c_int, [vp, ctypes.c_int, P(ctypes.c_int64), P(ctypes.c_double), P(ctypes.c_double)]),
     "dfl_last_error": (ctypes.c_char_p, [vp]),
     "dfl_destroy": (None, [vp]),
     "dfl_q41_image_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int]),
@@ -254,6 +257,19 @@ class Engine:
         out = np.zeros(shape, dtype)
         self._check(self.L.dfl_debug_read(self.ctx, name.encode(), out.ctypes.data_as(vp), out.nbytes), "dfl_debug_read")
         return out
+
+    def dfl_plant_proposals(self, table_dev):
+        self._check(self.L.dfl_plant_proposals(self.ctx, ctypes.c_void_p(table_dev.data_ptr()), table_dev.numel()),
+                    "dfl_plant_proposals")
+
+    def dfl_launch_count(self) -> int:
+        return int(self.L.dfl_launch_count(self.ctx))
+
+    def dfl_profile_read(self, cls: int):
+        n, ms, by = ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+        self._check(self.L.dfl_profile_read(self.ctx, cls, ctypes.byref(n), ctypes.byref(ms), ctypes.byref(by)),
+                    "dfl_profile_read")
+        return n.value, ms.value, by.value
 
     def dfl_draft_append_taps(self, taps_dev):
         rows = taps_dev.shape[0]

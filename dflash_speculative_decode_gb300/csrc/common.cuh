@@ -229,7 +229,7 @@ cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const u
                              float *dst, int ld_dst, const DevState *st, int live_from_ctx, cudaStream_t s);
 cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, float *dst, int ld_dst,
                              cudaStream_t s);
-cudaError_t launch_commit(DevState *st, int keep, cudaStream_t s);
+cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStream_t s);
 
 constexpr int kAttnChunk = 32;   // keys per attention work item
 

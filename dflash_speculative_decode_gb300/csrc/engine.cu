@@ -114,6 +114,13 @@ struct dfl_ctx {
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
     int last_k = 0;
     int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
+    long long launches = 0;                       // kernels this context has launched
+    bool profile = false;                         // bracket product launches with events
+    std::vector<cudaEvent_t> ev_pool;
+    struct Rec { int cls; double bytes; size_t ev; };
+    std::vector<Rec> recs;                        // pending profiled launches
+    double prof_ms[4] = {0, 0, 0, 0}, prof_bytes[4] = {0, 0, 0, 0};
+    long long prof_n[4] = {0, 0, 0, 0};
     std::string err;
 };
 
@@ -128,6 +135,13 @@ int fail(dfl_ctx *c, int code, const std::string &msg) {
     do {                                                                                      \
         cudaError_t e_ = (call);                                                              \
         if (e_ != cudaSuccess) return fail(c, DFL_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+    } while (0)
+
+// a row/attention/control kernel launch (products count themselves)
+#define DFL_LAUNCH(call)                                                                      \
+    do {                                                                                      \
+        c->launches += 1;                                                                     \
+        DFL_CK(call);                                                                         \
     } while (0)
 
 std::string validate(const dfl_config *g) {
@@ -319,8 +333,31 @@ bool is_tap(const dfl_config &g, int l, int *ti) {
 }
 
 // ---- one product -----------------------------------------------------------------------------------
+// profiled launch classes: 0 = Q4_1 products, 1 = bf16 products (fc), 2 = head
+cudaError_t prof_begin(dfl_ctx *c, size_t *slot) {
+    if (!c->profile) return cudaSuccess;
+    const size_t need = c->recs.size() * 2 + 2;
+    while (c->ev_pool.size() < need) {
+        cudaEvent_t e;
+        cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) return r;
+        c->ev_pool.push_back(e);
+    }
+    *slot = c->recs.size() * 2;
+    return cudaEventRecord(c->ev_pool[*slot], c->stream);
+}
+
+cudaError_t prof_end(dfl_ctx *c, size_t slot, int cls, double bytes) {
+    if (!c->profile) return cudaSuccess;
+    c->recs.push_back({cls, bytes, slot});
+    return cudaEventRecord(c->ev_pool[slot + 1], c->stream);
+}
+
 cudaError_t gemm(dfl_ctx *c, const QMat &W, const float *x, int ldx, int row0, int M, int epi, void *y, int ldy,
                  const uint16_t *ext = nullptr, int lde = 0) {
+    size_t slot = 0;
+    cudaError_t e = prof_begin(c, &slot);
+    if (e != cudaSuccess) return e;
     GemmArgs a{};
     a.img = W.img;
     a.K = W.K;
@@ -337,10 +374,17 @@ cudaError_t gemm(dfl_ctx *c, const QMat &W, const float *x, int ldx, int row0, i
     a.cnt = c->cnt;
     a.ext = ext;
     a.lde = lde;
-    return launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, X_F32, a, c->stream);
+    c->launches += 1;
+    e = launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, X_F32, a, c->stream);
+    if (e != cudaSuccess) return e;
+    const double bytes = (W.q41 ? 0.625 : 2.0) * W.K * (double)W.N + 4.0 * M * W.K + 4.0 * M * W.N;
+    return prof_end(c, slot, W.q41 ? 0 : 1, bytes);
 }
 
 cudaError_t head(dfl_ctx *c, const float *x, int row0, int M, float *logits, int dst) {
+    size_t slot = 0;
+    cudaError_t e = prof_begin(c, &slot);
+    if (e != cudaSuccess) return e;
     GemmArgs a{};
     a.img = c->head.img;
     a.K = c->head.K;
@@ -358,7 +402,11 @@ cudaError_t head(dfl_ctx *c, const float *x, int row0, int M, float *logits, int
     a.am_cnt = c->am_cnt;
     a.st = c->st;
     a.am_dst = dst;
-    return launch_gemm(W_BF16, EPI_ARGMAX, X_F32, a, c->stream);
+    c->launches += 1;
+    e = launch_gemm(W_BF16, EPI_ARGMAX, X_F32, a, c->stream);
+    if (e != cudaSuccess) return e;
+    const double bytes = 2.0 * a.K * (double)a.N + 4.0 * M * a.K + (logits ? 4.0 * M * a.N : 0.0);
+    return prof_end(c, slot, 2, bytes);
 }
 
 RowArgs rows(dfl_ctx *c, int M, float *x) {
@@ -386,7 +434,7 @@ int set_state(dfl_ctx *c, int k, const int32_t *rows_in, bool draft_rows, int ct
     a.temperature = a.sampled ? s->temperature : 1.f;
     a.seed = s ? s->seed : 0;
     for (int i = 0; i < kMaxRows; ++i) a.rows[i] = (rows_in && i < k) ? rows_in[i] : 0;
-    DFL_CK(launch_set_state(c->st, a, c->stream));
+    DFL_LAUNCH(launch_set_state(c->st, a, c->stream));
     return DFL_OK;
 }
 
@@ -404,11 +452,11 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
     ea.ple = P ? c->ple_table.p : nullptr;
     ea.ple_w = NL * P;
     ea.ple_out = c->ple_rows;
-    DFL_CK(launch_embed(ea, c->stream));
+    DFL_LAUNCH(launch_embed(ea, c->stream));
     RowArgs r0 = rows(c, k, c->x);
     r0.w_next = c->tl[0].attn_norm.p;
     r0.out = c->h;
-    DFL_CK(launch_rows(r0, c->stream));
+    DFL_LAUNCH(launch_rows(r0, c->stream));
     const int last_layer = (c->stop_layer >= 0 && c->stop_layer < NL) ? c->stop_layer : NL - 1;
     if (last_layer < NL - 1) do_head = false;
     for (int l = 0; l <= last_layer; ++l) {
@@ -433,7 +481,7 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
         qa.k_store = own ? L.K : nullptr;
         qa.v_store = own ? L.V : nullptr;
         qa.cap = L.cap;
-        DFL_CK(launch_qk(qa, c->stream));
+        DFL_LAUNCH(launch_qk(qa, c->stream));
         AttnArgs aa{};
         aa.M = k;
         aa.nq = nq;
@@ -452,7 +500,7 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.cnt = c->att_cnt;
         aa.max_chunks = c->att_max_chunks;
         aa.out = c->o;
-        DFL_CK(launch_attn(aa, 2 * 152, c->stream));
+        DFL_LAUNCH(launch_attn(aa, 2 * 152, c->stream));
         DFL_CK(gemm(c, L.o, c->o, nq * hd, 0, k, EPI_F32, c->y, H));
         RowArgs r1 = rows(c, k, c->x);
         r1.y = c->y;
@@ -460,7 +508,7 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
         r1.w_post = L.post_attn_norm.p;
         r1.w_next = L.pre_ffn_norm.p;
         r1.out = c->h;
-        DFL_CK(launch_rows(r1, c->stream));
+        DFL_LAUNCH(launch_rows(r1, c->stream));
         DFL_CK(gemm(c, L.gu, c->h, H, 0, k, EPI_GLU, c->a, L.ffn));
         DFL_CK(gemm(c, L.d, c->a, L.ffn, 0, k, EPI_F32, c->y, H));
         const uint16_t *next = l + 1 < NL ? c->tl[l + 1].attn_norm.p : c->final_norm.p;
@@ -472,7 +520,7 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
         r2.w_post = L.post_ffn_norm.p;
         r2.out = c->h;
         if (P) {
-            DFL_CK(launch_rows(r2, c->stream));   // out = bf16(x): the gate's input
+            DFL_LAUNCH(launch_rows(r2, c->stream));   // out = bf16(x): the gate's input
             DFL_CK(gemm(c, L.pg, c->h, H, 0, k, EPI_SILU_MUL, c->z, P, c->ple_rows + (size_t)l * P, NL * P));
             DFL_CK(gemm(c, L.pp, c->z, P, 0, k, EPI_F32, c->y, H));
             r2 = rows(c, k, c->x);
@@ -488,7 +536,7 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
             r2.ld_tap = c->TH;
             r2.tap_off = ti * H;
         }
-        DFL_CK(launch_rows(r2, c->stream));
+        DFL_LAUNCH(launch_rows(r2, c->stream));
     }
     if (do_head) {
         float *lg = (c->keep_logits || sampled) ? c->logits : nullptr;
@@ -501,7 +549,7 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
             sa.ld = g.vocab;
             sa.st = c->st;
             sa.cnt = c->smp_cnt;
-            DFL_CK(launch_sample(sa, c->stream));
+            DFL_LAUNCH(launch_sample(sa, c->stream));
         }
         c->have_logits = lg != nullptr;
     }
@@ -512,9 +560,9 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
 // rows draft_n .. draft_n + r - 1 (device st->ctx_rows = r) into activation rows `row0..` of hctx.
 int ctx_rows_prologue(dfl_ctx *c, int M, float *hdst) {
     const dfl_config &g = c->cfg;
-    DFL_CK(launch_copy_taps(c->taps, c->TH, c->st, M, c->tapbuf, c->TH, c->stream));
+    DFL_LAUNCH(launch_copy_taps(c->taps, c->TH, c->st, M, c->tapbuf, c->TH, c->stream));
     DFL_CK(gemm(c, c->fc, c->tapbuf, c->TH, 0, M, EPI_F32, c->y_fc, g.hidden));
-    DFL_CK(launch_cast_rows(c->y_fc, g.hidden, M, g.hidden, c->d_hidden_norm.p, g.d_eps, hdst, g.hidden, c->st, 1,
+    DFL_LAUNCH(launch_cast_rows(c->y_fc, g.hidden, M, g.hidden, c->d_hidden_norm.p, g.d_eps, hdst, g.hidden, c->st, 1,
                             c->stream));
     return DFL_OK;
 }
@@ -553,7 +601,7 @@ int run_ctx_only(dfl_ctx *c, int r) {
         qa.k_store = D.K;
         qa.v_store = D.V;
         qa.cap = c->cap_draft;
-        DFL_CK(launch_qk(qa, c->stream));
+        DFL_LAUNCH(launch_qk(qa, c->stream));
     }
     c->draft_n += r;
     return DFL_OK;
@@ -587,12 +635,12 @@ int run_draft(dfl_ctx *c, int last_tok) {
     ea.use_draft = 1;
     ea.mask_token = g.mask_token;
     ea.x = c->x_d;
-    DFL_CK(launch_embed(ea, c->stream));
+    DFL_LAUNCH(launch_embed(ea, c->stream));
     RowArgs r0 = rows(c, B, c->x_d);
     r0.eps = g.d_eps;
     r0.w_next = c->dl[0].attn_norm.p;
     r0.out = c->hcat;
-    DFL_CK(launch_rows(r0, c->stream));
+    DFL_LAUNCH(launch_rows(r0, c->stream));
     const int dq = g.d_heads, dhd = g.d_head_dim;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
@@ -604,7 +652,7 @@ int run_draft(dfl_ctx *c, int last_tok) {
         qb.k_store = c->kB;
         qb.v_store = c->vB;
         qb.cap = 0;
-        DFL_CK(launch_qk(qb, c->stream));
+        DFL_LAUNCH(launch_qk(qb, c->stream));
         if (F > 0) {
             QkArgs qc = draft_qk(c, l);
             qc.M = F;
@@ -614,7 +662,7 @@ int run_draft(dfl_ctx *c, int last_tok) {
             qc.k_store = D.K;
             qc.v_store = D.V;
             qc.cap = c->cap_draft;
-            DFL_CK(launch_qk(qc, c->stream));
+            DFL_LAUNCH(launch_qk(qc, c->stream));
         }
         AttnArgs aa{};
         aa.M = B;
@@ -637,7 +685,7 @@ int run_draft(dfl_ctx *c, int last_tok) {
         aa.cnt = c->att_cnt;
         aa.max_chunks = c->att_max_chunks;
         aa.out = c->o;
-        DFL_CK(launch_attn(aa, 2 * 152, c->stream));
+        DFL_LAUNCH(launch_attn(aa, 2 * 152, c->stream));
         DFL_CK(gemm(c, D.o, c->o, dq * dhd, 0, B, EPI_F32, c->y, H));
         RowArgs r1 = rows(c, B, c->x_d);
         r1.eps = g.d_eps;
@@ -645,7 +693,7 @@ int run_draft(dfl_ctx *c, int last_tok) {
         r1.ldy = H;
         r1.w_next = D.ffn_norm.p;
         r1.out = c->hb;
-        DFL_CK(launch_rows(r1, c->stream));
+        DFL_LAUNCH(launch_rows(r1, c->stream));
         DFL_CK(gemm(c, D.gu, c->hb, H, 0, B, EPI_GLU, c->a, g.d_ffn));
         DFL_CK(gemm(c, D.d, c->a, g.d_ffn, 0, B, EPI_F32, c->y, H));
         RowArgs r2 = rows(c, B, c->x_d);
@@ -654,7 +702,7 @@ int run_draft(dfl_ctx *c, int last_tok) {
         r2.ldy = H;
         r2.w_next = l + 1 < g.d_layers ? c->dl[l + 1].attn_norm.p : c->d_final_norm.p;
         r2.out = l + 1 < g.d_layers ? c->hcat : c->hb;
-        DFL_CK(launch_rows(r2, c->stream));
+        DFL_LAUNCH(launch_rows(r2, c->stream));
     }
     float *lg = c->keep_logits ? c->dlogits : nullptr;
     DFL_CK(head(c, c->hb, 1, B - 1, lg, AM_DRAFT));
@@ -1039,6 +1087,11 @@ int dfl_set_option(dfl_ctx *c, int option, int value) {
     if (option == DFL_OPT_KEEP_LOGITS) c->keep_logits = value != 0;
     else if (option == DFL_OPT_GRAPHS) (void)value;
     else if (option == DFL_OPT_STOP_LAYER) c->stop_layer = value;
+    else if (option == DFL_OPT_PROFILE) {
+        c->profile = value != 0;
+        c->recs.clear();
+        for (int i = 0; i < 4; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
+    }
     else return fail(c, DFL_E_INVALID_ARG, "unknown option");
     return DFL_OK;
 }
@@ -1104,9 +1157,43 @@ int dfl_debug_read(dfl_ctx *c, const char *name, void *dst, size_t bytes) {
     return DFL_OK;
 }
 
+int dfl_plant_proposals(dfl_ctx *c, const int32_t *dev_table, int table_len) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (!dev_table) return fail(c, DFL_E_INVALID_ARG, "null table");
+    if (c->draft_at != c->n || c->pending) return fail(c, DFL_E_STATE, "planting needs a draft block at this position");
+    if ((long)c->n + c->cfg.block > table_len) return fail(c, DFL_E_INVALID_ARG, "table shorter than the block's positions");
+    DFL_LAUNCH(launch_plant(c->st, dev_table, c->cfg.block - 1, c->stream));
+    return DFL_OK;
+}
+
+int64_t dfl_launch_count(const dfl_ctx *c) { return c ? c->launches : -1; }
+
+int dfl_profile_read(dfl_ctx *c, int cls, int64_t *launches, double *ms, double *bytes) {
+    if (!c || cls < 0 || cls > 2) return DFL_E_INVALID_ARG;
+    if (!c->recs.empty()) {
+        DFL_CK(cudaStreamSynchronize(c->stream));
+        for (const auto &r : c->recs) {
+            float t = 0.f;
+            DFL_CK(cudaEventElapsedTime(&t, c->ev_pool[r.ev], c->ev_pool[r.ev + 1]));
+            c->prof_ms[r.cls] += t;
+            c->prof_bytes[r.cls] += r.bytes;
+            c->prof_n[r.cls] += 1;
+        }
+        c->recs.clear();
+    }
+    if (launches) *launches = c->prof_n[cls];
+    if (ms) *ms = c->prof_ms[cls];
+    if (bytes) *bytes = c->prof_bytes[cls];
+    return DFL_OK;
+}
+
 const char *dfl_last_error(const dfl_ctx *c) { return c ? c->err.c_str() : "null context"; }
 
-void dfl_destroy(dfl_ctx *c) { delete c; }
+void dfl_destroy(dfl_ctx *c) {
+    if (!c) return;
+    for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+    delete c;
+}
 
 int64_t dfl_q41_image_bytes(int K, int N) {
     if (K < 32 || K % 32 || N < 32 || N % 32) return -1;

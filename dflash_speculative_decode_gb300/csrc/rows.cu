@@ -36,6 +36,17 @@ cudaError_t launch_set_state(DevState *st, const SetStateArgs &a, cudaStream_t s
     return cudaGetLastError();
 }
 
+// planted drafts: the proposals for positions n+1..n+count become table[n+1..n+count]
+__global__ void k_plant(DevState *st, const int32_t *table, int count) {
+    const int i = threadIdx.x;
+    if (i < count) st->props[i] = table[st->n + 1 + i];
+}
+
+cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStream_t s) {
+    k_plant<<<1, 32, 0, s>>>(st, table, count);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------------------------------
 // x[m] = emb[token_m] * scale (fp32); the row's per-layer-embedding inputs are a plain table row.
 __global__ void k_embed(EmbedArgs a) {

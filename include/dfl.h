@@ -169,8 +169,10 @@ int64_t dfl_positions_held(const dfl_ctx *ctx);
 /* Options. DFL_OPT_KEEP_LOGITS = 1 makes verify and draft passes also store their fp32 logits
  * (otherwise only the fused argmax runs); DFL_OPT_GRAPHS = 0 launches kernels one by one instead of
  * replaying captured CUDA graphs; DFL_OPT_STOP_LAYER = l >= 0 (inspection only) makes target passes
- * stop after layer l, without the head, so dfl_debug_read shows that layer's intermediates; -1 = off. */
-enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3 };
+ * stop after layer l, without the head, so dfl_debug_read shows that layer's intermediates; -1 = off;
+ * DFL_OPT_PROFILE = 1 brackets every product launch with CUDA events on the context's stream (read with
+ * dfl_profile_read; setting the option clears the totals). */
+enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3, DFL_OPT_PROFILE = 4 };
 int dfl_set_option(dfl_ctx *ctx, int option, int value);
 
 /* Copy the fp32 logits of the last pass (rows x vocab, row-major) to host memory. which = 0: the
@@ -191,6 +193,20 @@ int dfl_draft_append_taps(dfl_ctx *ctx, const void *dev_taps, int rows);
  * output, "qkv" [16][width], "q" [16][heads*head_dim] (normed, rotated), "o" [16][heads*head_dim]
  * attention output, "x_d" [16][hidden] draft residual rows; all fp32. */
 int dfl_debug_read(dfl_ctx *ctx, const char *name, void *host_dst, size_t bytes);
+
+/* Planted drafts (measurement workloads that control acceptance): after dfl_draft_block, replace its
+ * proposals on the device with dev_table[held+1 .. held+block-1], a DEVICE int32 table indexed by
+ * absolute position with at least held+block entries. The draft block itself has run. */
+int dfl_plant_proposals(dfl_ctx *ctx, const int32_t *dev_table, int table_len);
+
+/* Kernels this context has launched so far (every launch counted once). */
+int64_t dfl_launch_count(const dfl_ctx *ctx);
+
+/* Totals of the launches profiled while DFL_OPT_PROFILE was on, per class: 0 = Q4_1 products,
+ * 1 = bf16 products (fc), 2 = the bf16 head with its fused argmax. *ms = summed event time of the
+ * launches; *bytes = their algorithmic bytes (weights at 0.625 B (Q4_1) or 2 B (bf16) per weight,
+ * fp32 activations in and products out). Synchronises the stream. */
+int dfl_profile_read(dfl_ctx *ctx, int cls, int64_t *launches, double *ms, double *bytes);
 
 const char *dfl_last_error(const dfl_ctx *ctx);
 void dfl_destroy(dfl_ctx *ctx);
