@@ -83,11 +83,11 @@ class Clocks:
 # workload
 # ---------------------------------------------------------------------------------------------------
 def e4b_workload(args):
-    pc = gen.e4b_pair(max_ctx=args.ctx + 512 + 64)
+    pc = gen.e4b_pair(max_ctx=args.ctx + args.gen + 64)
     return pc, {"workload": f"e4b-pair ctx {args.ctx} block 8 greedy, planted drafts p={args.p}, "
-                            f"512-token decodes", "target": "42 layers hidden 2560 ffn 10240/20480 12x256 heads, "
+                            f"{args.gen}-token decodes", "target": "42 layers hidden 2560 ffn 10240/20480 12x256 heads, "
                             "PLE 256, vocab 262144, Q4_1", "draft": "5 layers hidden 2560 ffn 5120 32/8x128, fc 5x2560",
-                "context": args.ctx, "generated_per_decode": 512, "corruption_p": args.p,
+                "context": args.ctx, "generated_per_decode": args.gen, "corruption_p": args.p,
                 "l2": "weights streamed per step (6.4 GB) exceed the 129 MB L2"}
 
 
@@ -171,14 +171,15 @@ def bench_cuda(args):
     first = eng.dfl_prefill(prompt)
     torch.cuda.synchronize()
     t_prefill = time.time() - t0
-    snap, plain, table = planted_table(torch, eng, pc, first, 512, args.p)
+    snap, plain, table = planted_table(torch, eng, pc, first, args.gen, args.p)
     eng.dfl_restore(snap)
     n0 = eng.dfl_positions_held()
     stream = torch.cuda.current_stream()
 
     # warm-up
-    run_steps(eng, torch, table, first, snap, n0, args.warmup, 512)
+    run_steps(eng, torch, table, first, snap, n0, args.warmup, args.gen)
     eng.dfl_restore(snap)
+    sys.stderr.write(f"[bench] kernel launches before the timed region: {eng.dfl_launch_count()}\n")
     # timed: device-resident loop
     if world > 1:
         torch.distributed.barrier()
@@ -188,7 +189,7 @@ def bench_cuda(args):
     l0 = eng.dfl_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    toks = run_steps(eng, torch, table, first, snap, n0, args.steps, 512)
+    toks = run_steps(eng, torch, table, first, snap, n0, args.steps, args.gen)
     e1.record(stream)
     torch.cuda.synchronize()
     launches = eng.dfl_launch_count() - l0
@@ -209,14 +210,14 @@ def bench_cuda(args):
     host_table = table.cpu().numpy()
     torch.cuda.synchronize()
     t1 = time.perf_counter()
-    toks_e2e = run_steps(eng, torch, table, first, snap, n0, args.steps, 512, host_rows=host_table)
+    toks_e2e = run_steps(eng, torch, table, first, snap, n0, args.steps, args.gen, host_rows=host_table)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t1
 
     # roofline: per-launch events on the products over the same steps
     eng.dfl_restore(snap)
     eng.dfl_set_option(DFL_OPT_PROFILE, 1)
-    run_steps(eng, torch, table, first, snap, n0, args.steps, 512)
+    run_steps(eng, torch, table, first, snap, n0, args.steps, args.gen)
     q_n, q_ms, q_bytes = eng.dfl_profile_read(0)
     h_n, h_ms, h_bytes = eng.dfl_profile_read(2)
     f_n, f_ms, f_bytes = eng.dfl_profile_read(1)
@@ -372,6 +373,7 @@ def main():
     ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm"])
     ap.add_argument("--ctx", type=int, default=1024)
     ap.add_argument("--p", type=float, default=0.3)
+    ap.add_argument("--gen", type=int, default=512, help="tokens per decode before restarting from the prefix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -10,7 +10,7 @@ namespace dfl {
 
 constexpr int kMaxRows = 16;           // rows of one pass (R_max)
 constexpr int kWarpsPerCta = 4;        // GEMM CTA: 4 warps, each two 16-column tiles
-constexpr int kMaxChunksPerSplit = 16; // 64-wide K chunks one GEMM CTA stages in shared memory
+constexpr int kMaxChunksPerSplit = 8;  // 64-wide K chunks one GEMM CTA stages in shared memory
 constexpr int kSplitTargetWarps = 152 * 16;
 
 // Device-resident counters of the current pass. The host writes them with k_set_state before each
@@ -79,6 +79,21 @@ __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w) {
     v = __hsub2(v, off);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start
+// while its predecessor is still running. Everything before pdl_wait() must touch only data no earlier
+// kernel writes (weights); pdl_wait() returns once the predecessor grid has completed and its writes are
+// visible. pdl_trigger() lets the successor be scheduled (once every CTA of this grid has triggered or
+// exited). Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory"); }
 
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
@@ -230,6 +245,23 @@ cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const u
 cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, float *dst, int ld_dst,
                              cudaStream_t s);
 cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStream_t s);
+
+// Launch with programmatic stream serialization (kernels begin with pdl_wait()).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 constexpr int kAttnChunk = 32;   // keys per attention work item
 

@@ -14,6 +14,8 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <functional>
+#include <map>
 #include <string>
 #include <vector>
 
@@ -117,10 +119,21 @@ struct dfl_ctx {
     long long launches = 0;                       // kernels this context has launched
     bool profile = false;                         // bracket product launches with events
     std::vector<cudaEvent_t> ev_pool;
+    size_t ev_next = 0, ev_reserved = 0;          // slots [0, ev_reserved) belong to captured graphs
     struct Rec { int cls; double bytes; size_t ev; };
-    std::vector<Rec> recs;                        // pending profiled launches
+    std::vector<Rec> recs;                        // profiled launches not yet read
     double prof_ms[4] = {0, 0, 0, 0}, prof_bytes[4] = {0, 0, 0, 0};
     long long prof_n[4] = {0, 0, 0, 0};
+    // captured passes
+    bool use_graphs = true, capturing = false;
+    cudaStream_t cap_stream = nullptr;
+    struct Graph {
+        cudaGraphExec_t exec = nullptr;
+        std::vector<Rec> recs;                    // profiled launches inside the graph
+        long long launches = 0;                   // kernels per replay
+        bool pending = false;                     // replayed since its events were last read
+    };
+    std::map<uint64_t, Graph> graphs;
     std::string err;
 };
 
@@ -336,14 +349,15 @@ bool is_tap(const dfl_config &g, int l, int *ti) {
 // profiled launch classes: 0 = Q4_1 products, 1 = bf16 products (fc), 2 = head
 cudaError_t prof_begin(dfl_ctx *c, size_t *slot) {
     if (!c->profile) return cudaSuccess;
-    const size_t need = c->recs.size() * 2 + 2;
+    const size_t need = c->ev_next + 2;
     while (c->ev_pool.size() < need) {
         cudaEvent_t e;
         cudaError_t r = cudaEventCreate(&e);
         if (r != cudaSuccess) return r;
         c->ev_pool.push_back(e);
     }
-    *slot = c->recs.size() * 2;
+    *slot = c->ev_next;
+    c->ev_next += 2;
     return cudaEventRecord(c->ev_pool[*slot], c->stream);
 }
 
@@ -409,6 +423,79 @@ cudaError_t head(dfl_ctx *c, const float *x, int row0, int M, float *logits, int
     return prof_end(c, slot, 2, bytes);
 }
 
+// fold finished profiled launches into the totals
+cudaError_t harvest(dfl_ctx *c, std::vector<dfl_ctx::Rec> &recs) {
+    if (recs.empty()) return cudaSuccess;
+    cudaError_t e = cudaEventSynchronize(c->ev_pool[recs.back().ev + 1]);
+    if (e != cudaSuccess) return e;
+    for (const auto &r : recs) {
+        float t = 0.f;
+        e = cudaEventElapsedTime(&t, c->ev_pool[r.ev], c->ev_pool[r.ev + 1]);
+        if (e != cudaSuccess) return e;
+        c->prof_ms[r.cls] += t;
+        c->prof_bytes[r.cls] += r.bytes;
+        c->prof_n[r.cls] += 1;
+    }
+    return cudaSuccess;
+}
+
+// Run a pass body either directly or as a CUDA graph captured once per key (on a private stream,
+// replayed on the context's stream). The body must only enqueue kernels.
+int run_graph(dfl_ctx *c, uint64_t key, const std::function<int()> &body) {
+    if (!c->use_graphs) {
+        const int rc = body();
+        if (rc) return rc;
+        if (c->profile) {
+            DFL_CK(harvest(c, c->recs));
+            c->recs.clear();
+            c->ev_next = c->ev_reserved;
+        }
+        return DFL_OK;
+    }
+    key = key * 2 + (c->profile ? 1 : 0);
+    auto it = c->graphs.find(key);
+    if (it == c->graphs.end()) {
+        if (!c->cap_stream) DFL_CK(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
+        cudaStream_t user = c->stream;
+        c->stream = c->cap_stream;
+        c->capturing = true;
+        const long long l0 = c->launches;
+        c->recs.clear();
+        c->ev_next = c->ev_reserved;
+        cudaError_t e = cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal);
+        int rc = e == cudaSuccess ? body() : DFL_E_CUDA;
+        cudaGraph_t g = nullptr;
+        cudaError_t e2 = cudaStreamEndCapture(c->cap_stream, &g);
+        c->stream = user;
+        c->capturing = false;
+        if (e != cudaSuccess) return fail(c, DFL_E_CUDA, std::string("cudaStreamBeginCapture: ") + cudaGetErrorString(e));
+        if (rc) {
+            if (g) cudaGraphDestroy(g);
+            return rc;
+        }
+        if (e2 != cudaSuccess) return fail(c, DFL_E_CUDA, std::string("cudaStreamEndCapture: ") + cudaGetErrorString(e2));
+        dfl_ctx::Graph G;
+        e = cudaGraphInstantiate(&G.exec, g, 0);
+        cudaGraphDestroy(g);
+        if (e != cudaSuccess) return fail(c, DFL_E_CUDA, std::string("cudaGraphInstantiate: ") + cudaGetErrorString(e));
+        G.launches = c->launches - l0;
+        c->launches = l0;
+        G.recs = c->recs;
+        c->recs.clear();
+        c->ev_reserved = c->ev_next;
+        it = c->graphs.emplace(key, G).first;
+    }
+    dfl_ctx::Graph &G = it->second;
+    if (G.pending) {
+        DFL_CK(harvest(c, G.recs));
+        G.pending = false;
+    }
+    DFL_CK(cudaGraphLaunch(G.exec, c->stream));
+    c->launches += G.launches;
+    G.pending = c->profile && !G.recs.empty();
+    return DFL_OK;
+}
+
 RowArgs rows(dfl_ctx *c, int M, float *x) {
     RowArgs r{};
     r.M = M;
@@ -439,7 +526,7 @@ int set_state(dfl_ctx *c, int k, const int32_t *rows_in, bool draft_rows, int ct
 }
 
 // ---- target pass: k rows at positions n..n+k-1 ---------------------------------------------------------
-int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
+int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
     const dfl_config &g = c->cfg;
     const int H = g.hidden, NL = g.n_layers, hd = g.head_dim, nq = g.n_heads, P = g.ple_dim;
     EmbedArgs ea{};
@@ -551,8 +638,18 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
             sa.cnt = c->smp_cnt;
             DFL_LAUNCH(launch_sample(sa, c->stream));
         }
-        c->have_logits = lg != nullptr;
     }
+    return DFL_OK;
+}
+
+// A target pass of k rows at positions n..n+k-1 (the device counters are set beforehand).
+int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
+    const bool early = c->stop_layer >= 0 && c->stop_layer < c->cfg.n_layers - 1;
+    const uint64_t key = (1ull << 40) | (uint64_t)k | (uint64_t)do_head << 8 | (uint64_t)sampled << 9 |
+                         (uint64_t)c->keep_logits << 10 | (uint64_t)(c->stop_layer + 1) << 12;
+    const int rc = run_graph(c, key, [&] { return target_body(c, k, do_head, sampled); });
+    if (rc) return rc;
+    if (do_head && !early) c->have_logits = c->keep_logits || sampled;
     return DFL_OK;
 }
 
@@ -616,14 +713,11 @@ int catch_up(dfl_ctx *c, int leave) {
     return DFL_OK;
 }
 
-int run_draft(dfl_ctx *c, int last_tok) {
+int draft_body(dfl_ctx *c) {
     const dfl_config &g = c->cfg;
     const int H = g.hidden, B = g.block, F = c->ctx_fuse;
-    const int r = c->n - c->draft_n;   // <= F after catch_up
-    int rc = set_state(c, B, nullptr, false, r, last_tok, nullptr);
-    if (rc) return rc;
     if (F > 0) {
-        rc = ctx_rows_prologue(c, F, c->hcat + (size_t)B * H);
+        const int rc = ctx_rows_prologue(c, F, c->hcat + (size_t)B * H);
         if (rc) return rc;
     }
     EmbedArgs ea{};
@@ -706,10 +800,23 @@ int run_draft(dfl_ctx *c, int last_tok) {
     }
     float *lg = c->keep_logits ? c->dlogits : nullptr;
     DFL_CK(head(c, c->hb, 1, B - 1, lg, AM_DRAFT));
-    c->have_dlogits = lg != nullptr;
+    return DFL_OK;
+}
+
+// Draft block at positions n..n+block-1; first makes the r <= ctx_fuse committed rows not yet in the
+// draft context into context (fused into the same pass).
+int run_draft(dfl_ctx *c, int last_tok) {
+    const int r = c->n - c->draft_n;
+    int rc = set_state(c, c->cfg.block, nullptr, false, r, last_tok, nullptr);
+    if (rc) return rc;
+    rc = run_graph(c, (2ull << 40) | (uint64_t)c->keep_logits, [&] { return draft_body(c); });
+    if (rc) return rc;
+    c->have_dlogits = c->keep_logits;
     c->draft_n += r;
     return DFL_OK;
 }
+
+
 
 int read_state(dfl_ctx *c, DevState *out) {
     DFL_CK(cudaMemcpyAsync(out, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
@@ -1085,11 +1192,14 @@ int64_t dfl_positions_held(const dfl_ctx *c) { return c ? c->n : -1; }
 int dfl_set_option(dfl_ctx *c, int option, int value) {
     if (!c) return DFL_E_INVALID_ARG;
     if (option == DFL_OPT_KEEP_LOGITS) c->keep_logits = value != 0;
-    else if (option == DFL_OPT_GRAPHS) (void)value;
+    else if (option == DFL_OPT_GRAPHS) c->use_graphs = value != 0;
     else if (option == DFL_OPT_STOP_LAYER) c->stop_layer = value;
     else if (option == DFL_OPT_PROFILE) {
+        DFL_CK(cudaStreamSynchronize(c->stream));
+        for (auto &kv : c->graphs) kv.second.pending = false;
         c->profile = value != 0;
         c->recs.clear();
+        c->ev_next = c->ev_reserved;
         for (int i = 0; i < 4; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
     }
     else return fail(c, DFL_E_INVALID_ARG, "unknown option");
@@ -1170,17 +1280,14 @@ int64_t dfl_launch_count(const dfl_ctx *c) { return c ? c->launches : -1; }
 
 int dfl_profile_read(dfl_ctx *c, int cls, int64_t *launches, double *ms, double *bytes) {
     if (!c || cls < 0 || cls > 2) return DFL_E_INVALID_ARG;
-    if (!c->recs.empty()) {
-        DFL_CK(cudaStreamSynchronize(c->stream));
-        for (const auto &r : c->recs) {
-            float t = 0.f;
-            DFL_CK(cudaEventElapsedTime(&t, c->ev_pool[r.ev], c->ev_pool[r.ev + 1]));
-            c->prof_ms[r.cls] += t;
-            c->prof_bytes[r.cls] += r.bytes;
-            c->prof_n[r.cls] += 1;
+    DFL_CK(cudaStreamSynchronize(c->stream));
+    DFL_CK(harvest(c, c->recs));
+    c->recs.clear();
+    for (auto &kv : c->graphs)
+        if (kv.second.pending) {
+            DFL_CK(harvest(c, kv.second.recs));
+            kv.second.pending = false;
         }
-        c->recs.clear();
-    }
     if (launches) *launches = c->prof_n[cls];
     if (ms) *ms = c->prof_ms[cls];
     if (bytes) *bytes = c->prof_bytes[cls];
@@ -1191,7 +1298,10 @@ const char *dfl_last_error(const dfl_ctx *c) { return c ? c->err.c_str() : "null
 
 void dfl_destroy(dfl_ctx *c) {
     if (!c) return;
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second.exec);
     for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     delete c;
 }
 

@@ -117,52 +117,64 @@ cudaError_t launch_pack_bf16(const uint16_t *src, int K, int N, uint8_t *img, cu
 // shared load.
 __device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo, uint16_t hi) { return uint32_t(lo) | (uint32_t(hi) << 16); }
 
+// Copy the raw activation slice rows [0, M) x inputs [64*c0, 64*(c0+nch)) into shared memory with
+// 16-byte asynchronous copies (one round trip), zero beyond K.
+template <int XIN>
+__device__ __forceinline__ void stage_raw(uint8_t *raw, const GemmArgs &a, int row0, int c0, int nch) {
+    constexpr int E = XIN ? 4 : 2;                     // bytes per element
+    const int rowbytes = nch * 64 * E;
+    const int k0 = 64 * c0;
+    const int kend = min(a.K, 64 * (c0 + nch));
+    const int live = (kend - k0) * E;                  // bytes of a row inside K (multiple of 64)
+    const int per_row = rowbytes / 16;
+    for (int e = threadIdx.x; e < a.M * per_row; e += blockDim.x) {
+        const int m = e / per_row, off = (e % per_row) * 16;
+        uint8_t *dst = raw + m * rowbytes + off;
+        if (off < live)
+            cp_async16(dst, reinterpret_cast<const uint8_t *>(a.x) + ((long)(row0 + m) * a.ldx + k0) * E + off);
+        else
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_wait_all();
+}
+
+template <int XIN>
+__device__ __forceinline__ float raw_at(const uint8_t *raw, int rowbytes, int m, int k) {
+    if (XIN) return reinterpret_cast<const float *>(raw + m * rowbytes)[k];
+    return bf16_to_f32(reinterpret_cast<const uint16_t *>(raw + m * rowbytes)[k]);
+}
+
+// Fragments and per-32-block sums from the raw slice (after a barrier).
 template <int MT, int XIN>
-__device__ __forceinline__ void stage_x(uint32_t *xs, const GemmArgs &a, int row0, int c0, int nch) {
+__device__ __forceinline__ void stage_frags(uint32_t *xs, float *sums, const uint8_t *raw, const GemmArgs &a, int nch,
+                                            bool want_sums) {
     constexpr int W = XIN ? 4 : 2;
+    const int rowbytes = nch * 64 * (XIN ? 4 : 2);
     for (int e = threadIdx.x; e < nch * MT * 4 * 32; e += blockDim.x) {
         const int L = e & 31, ks = (e >> 5) & 3, tt = (e >> 7) % MT, cc = (e >> 7) / MT;
         const int tok = 8 * tt + (L >> 2), tq = L & 3;
-        const int k0 = 64 * (c0 + cc) + 16 * ks + 2 * tq;
+        const int k = 64 * cc + 16 * ks + 2 * tq;
         uint32_t w[4] = {0u, 0u, 0u, 0u};
         if (tok < a.M) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const int k = k0 + 8 * hh;
-                if (k >= a.K) continue;
-                if (XIN) {
-                    const float2 v = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(a.x) +
-                                                                       (long)(row0 + tok) * a.ldx + k);
-                    const uint16_t h0 = f32_to_bf16(v.x), h1 = f32_to_bf16(v.y);
-                    const uint16_t l0 = f32_to_bf16(v.x - bf16_to_f32(h0)), l1 = f32_to_bf16(v.y - bf16_to_f32(h1));
-                    w[hh] = pack_bf16x2(h0, h1);
-                    w[2 + hh] = pack_bf16x2(l0, l1);
-                } else {
-                    w[hh] = *reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint16_t *>(a.x) +
-                                                                 (long)(row0 + tok) * a.ldx + k);
-                }
+                const float v0 = raw_at<XIN>(raw, rowbytes, tok, k + 8 * hh);
+                const float v1 = raw_at<XIN>(raw, rowbytes, tok, k + 8 * hh + 1);
+                const uint16_t h0 = f32_to_bf16(v0), h1 = f32_to_bf16(v1);
+                w[hh] = pack_bf16x2(h0, h1);
+                if (XIN) w[2 + hh] = pack_bf16x2(f32_to_bf16(v0 - bf16_to_f32(h0)), f32_to_bf16(v1 - bf16_to_f32(h1)));
             }
         }
         uint32_t *d = xs + (size_t)e * W;
         if (XIN) *reinterpret_cast<uint4 *>(d) = make_uint4(w[0], w[1], w[2], w[3]);
         else *reinterpret_cast<uint2 *>(d) = make_uint2(w[0], w[1]);
     }
-}
-
-// Per 32-input block sums of the activations, [cc][block][16 tokens], in ascending k.
-template <int XIN>
-__device__ __forceinline__ void stage_sums(float *sums, const GemmArgs &a, int row0, int c0, int nch) {
+    if (!want_sums) return;
     for (int e = threadIdx.x; e < nch * 32; e += blockDim.x) {
         const int tok = e & 15, blk = (e >> 4) & 1, cc = e >> 5;
         float s = 0.f;
-        if (tok < a.M) {
-            const int kb = 64 * (c0 + cc) + 32 * blk;
-            for (int i = 0; i < 32; ++i) {
-                if (kb + i >= a.K) break;
-                s += XIN ? reinterpret_cast<const float *>(a.x)[(long)(row0 + tok) * a.ldx + kb + i]
-                         : bf16_to_f32(reinterpret_cast<const uint16_t *>(a.x)[(long)(row0 + tok) * a.ldx + kb + i]);
-            }
-        }
+        if (tok < a.M)
+            for (int i = 0; i < 32; ++i) s += raw_at<XIN>(raw, rowbytes, tok, 64 * cc + 32 * blk + i);
         sums[e] = s;
     }
 }
@@ -282,15 +294,49 @@ __global__ void __launch_bounds__(128) k_gemm(GemmArgs a) {
     const int nch = c1 - c0;
     uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
     float *sums = reinterpret_cast<float *>(smem + (size_t)nch * MT * 4 * 32 * (XIN ? 16 : 8));
-    stage_x<MT, XIN>(xs, a, a.x_row0, c0, nch);
-    if (FMT == W_Q41) stage_sums<XIN>(sums, a, a.x_row0, c0, nch);
-    __syncthreads();
+    uint8_t *raw = reinterpret_cast<uint8_t *>(sums + nch * 32);
 
     const int ngroups = a.N / 32;
     const int ng = blockIdx.x * kWarpsPerCta + warp;
-    if (ng >= ngroups) return;
-    const int nt0 = (EPI == EPI_GLU) ? ng : 2 * ng;
-    const int nt1 = (EPI == EPI_GLU) ? ng + ngroups : 2 * ng + 1;
+    const bool active = ng < ngroups;
+    const int nt0 = active ? ((EPI == EPI_GLU) ? ng : 2 * ng) : 0;
+    const int nt1 = active ? ((EPI == EPI_GLU) ? ng + ngroups : 2 * ng + 1) : 0;
+
+    // the first weight chunks are requested before the activations are staged, so the two latencies overlap
+    constexpr int PQ = 4, PB = 2;
+    constexpr int TB = FMT == W_Q41 ? 640 : 2048;
+    const uint8_t *base0 = a.img + ((size_t)nt0 * a.C + c0) * TB;
+    const uint8_t *base1 = a.img + ((size_t)nt1 * a.C + c0) * TB;
+    uint4 nb[PQ][2], sc[PQ][2];
+    uint4 w[PB][2][4];
+    if (active) {
+        if (FMT == W_Q41) {
+#pragma unroll
+            for (int p = 0; p < PQ; ++p)
+                if (p < nch) {
+                    nb[p][0] = ldg_stream(base0 + p * 640 + 16 * lane);
+                    nb[p][1] = ldg_stream(base1 + p * 640 + 16 * lane);
+                    sc[p][0] = ldg_stream(base0 + p * 640 + 512 + 16 * g);
+                    sc[p][1] = ldg_stream(base1 + p * 640 + 512 + 16 * g);
+                }
+        } else {
+#pragma unroll
+            for (int p = 0; p < PB; ++p)
+                if (p < nch)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        w[p][0][ks] = ldg_stream(base0 + p * 2048 + 512 * ks + 16 * lane);
+                        w[p][1][ks] = ldg_stream(base1 + p * 2048 + 512 * ks + 16 * lane);
+                    }
+        }
+    }
+    pdl_wait();          // the activations are written by the previous kernel
+    pdl_trigger();
+    stage_raw<XIN>(raw, a, a.x_row0, c0, nch);
+    __syncthreads();
+    stage_frags<MT, XIN>(xs, sums, raw, a, nch, FMT == W_Q41);
+    __syncthreads();
+    if (!active) return;
 
     float acc[2][MT][4];
 #pragma unroll
@@ -299,25 +345,13 @@ __global__ void __launch_bounds__(128) k_gemm(GemmArgs a) {
         for (int tt = 0; tt < MT; ++tt) acc[j][tt][0] = acc[j][tt][1] = acc[j][tt][2] = acc[j][tt][3] = 0.f;
 
     if (FMT == W_Q41) {
-        constexpr int P = 4;
-        const uint8_t *base0 = a.img + ((size_t)nt0 * a.C + c0) * 640;
-        const uint8_t *base1 = a.img + ((size_t)nt1 * a.C + c0) * 640;
-        uint4 nb[P][2], sc[P][2];
+        for (int cb = 0; cb < nch; cb += PQ) {
 #pragma unroll
-        for (int p = 0; p < P; ++p)
-            if (p < nch) {
-                nb[p][0] = ldg_stream(base0 + p * 640 + 16 * lane);
-                nb[p][1] = ldg_stream(base1 + p * 640 + 16 * lane);
-                sc[p][0] = ldg_stream(base0 + p * 640 + 512 + 16 * g);
-                sc[p][1] = ldg_stream(base1 + p * 640 + 512 + 16 * g);
-            }
-        for (int cb = 0; cb < nch; cb += P) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
+            for (int p = 0; p < PQ; ++p) {
                 const int cc = cb + p;
                 if (cc < nch) {
                     q41_chunk<MT, XIN>(acc, nb[p], sc[p], xs, sums, cc, lane);
-                    const int nx = cc + P;
+                    const int nx = cc + PQ;
                     if (nx < nch) {
                         nb[p][0] = ldg_stream(base0 + (size_t)nx * 640 + 16 * lane);
                         nb[p][1] = ldg_stream(base1 + (size_t)nx * 640 + 16 * lane);
@@ -328,25 +362,13 @@ __global__ void __launch_bounds__(128) k_gemm(GemmArgs a) {
             }
         }
     } else {
-        constexpr int P = 2;
-        const uint8_t *base0 = a.img + ((size_t)nt0 * a.C + c0) * 2048;
-        const uint8_t *base1 = a.img + ((size_t)nt1 * a.C + c0) * 2048;
-        uint4 w[P][2][4];
+        for (int cb = 0; cb < nch; cb += PB) {
 #pragma unroll
-        for (int p = 0; p < P; ++p)
-            if (p < nch)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    w[p][0][ks] = ldg_stream(base0 + p * 2048 + 512 * ks + 16 * lane);
-                    w[p][1][ks] = ldg_stream(base1 + p * 2048 + 512 * ks + 16 * lane);
-                }
-        for (int cb = 0; cb < nch; cb += P) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
+            for (int p = 0; p < PB; ++p) {
                 const int cc = cb + p;
                 if (cc < nch) {
                     bf16_chunk<MT, XIN>(acc, w[p], xs, cc, lane);
-                    const int nx = cc + P;
+                    const int nx = cc + PB;
                     if (nx < nch)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
@@ -386,10 +408,22 @@ __global__ void __launch_bounds__(128) k_gemm(GemmArgs a) {
                 if (tok >= a.M) continue;
                 const int r = g + 8 * (i >> 1);
                 float v0 = 0.f, v1 = 0.f;
-                for (int s2 = 0; s2 < a.S; ++s2) {
-                    const float *Ps = a.part + (size_t)s2 * a.M * a.N + (long)tok * a.N;
-                    v0 += __ldcg(Ps + 16 * nt0 + r);
-                    v1 += __ldcg(Ps + 16 * nt1 + r);
+                const float *Pb = a.part + (long)tok * a.N;
+                const size_t stride = (size_t)a.M * a.N;
+                int s2 = 0;
+                for (; s2 + 8 <= a.S; s2 += 8) {
+                    float u0[8], u1[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        u0[q] = __ldcg(Pb + (s2 + q) * stride + 16 * nt0 + r);
+                        u1[q] = __ldcg(Pb + (s2 + q) * stride + 16 * nt1 + r);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v0 += u0[q], v1 += u1[q];
+                }
+                for (; s2 < a.S; ++s2) {
+                    v0 += __ldcg(Pb + s2 * stride + 16 * nt0 + r);
+                    v1 += __ldcg(Pb + s2 * stride + 16 * nt1 + r);
                 }
                 acc[0][tt][i] = v0;
                 acc[1][tt][i] = v1;
@@ -406,6 +440,28 @@ __global__ void __launch_bounds__(128) k_gemm(GemmArgs a) {
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
 template <int MT>
+__device__ __forceinline__ void stage_head_x(uint32_t *xs, const GemmArgs &a) {
+    for (int e = threadIdx.x; e < a.C * MT * 4 * 32; e += blockDim.x) {
+        const int L = e & 31, ks = (e >> 5) & 3, tt = (e >> 7) % MT, cc = (e >> 7) / MT;
+        const int tok = 8 * tt + (L >> 2), tq = L & 3;
+        const int k = 64 * cc + 16 * ks + 2 * tq;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (tok < a.M) {
+            const float *xr = reinterpret_cast<const float *>(a.x) + (long)(a.x_row0 + tok) * a.ldx;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int kk = k + 8 * hh;
+                const float2 v = kk < a.K ? *reinterpret_cast<const float2 *>(xr + kk) : make_float2(0.f, 0.f);
+                const uint16_t h0 = f32_to_bf16(v.x), h1 = f32_to_bf16(v.y);
+                w[hh] = pack_bf16x2(h0, h1);
+                w[2 + hh] = pack_bf16x2(f32_to_bf16(v.x - bf16_to_f32(h0)), f32_to_bf16(v.y - bf16_to_f32(h1)));
+            }
+        }
+        *reinterpret_cast<uint4 *>(xs + (size_t)e * 4) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <int MT>
 __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float wval[kWarpsPerCta][kMaxRows];
@@ -413,8 +469,6 @@ __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
-    stage_x<MT, 1>(xs, a, a.x_row0, 0, a.C);
-    __syncthreads();
 
     const int ntiles = a.N / 16;
     const int gw = blockIdx.x * kWarpsPerCta + warp, nw = gridDim.x * kWarpsPerCta;
@@ -444,6 +498,11 @@ __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
 #pragma unroll
     for (int p = 0; p < P; ++p)
         if (p < units) load(p, w[p]);
+    // the activations are staged while the first weight chunks are in flight
+    pdl_wait();
+    pdl_trigger();
+    stage_head_x<MT>(xs, a);
+    __syncthreads();
     float acc[2][MT][4];
     for (int ub = 0; ub < units; ub += P) {
 #pragma unroll
@@ -553,14 +612,15 @@ int gemm_splits(int C, int N, int fmt) {
 
 size_t gemm_scratch_floats(int S, int M, int N) { return S > 1 ? (size_t)S * M * N : 0; }
 
-size_t gemm_smem(int C, int S, int MT, int XIN, int fmt) {
+size_t gemm_smem(int C, int S, int MT, int XIN, int fmt, int M) {
+    (void)fmt;
     const int maxch = (C + S - 1) / S;
-    return (size_t)maxch * MT * 4 * 32 * (XIN ? 16 : 8) + (fmt == W_Q41 ? (size_t)maxch * 128 : 0);
+    return (size_t)maxch * MT * 4 * 32 * (XIN ? 16 : 8) + (size_t)maxch * 128 + (size_t)M * maxch * 64 * (XIN ? 4 : 2);
 }
 
 template <int FMT, int MT, int EPI, int XIN>
 static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    const size_t smem = gemm_smem(a.C, a.S, MT, XIN, FMT);
+    const size_t smem = gemm_smem(a.C, a.S, MT, XIN, FMT, a.M);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm<FMT, MT, EPI, XIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -569,8 +629,7 @@ static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     }
     const int ngroups = a.N / 32;
     dim3 grid((ngroups + kWarpsPerCta - 1) / kWarpsPerCta, a.S);
-    k_gemm<FMT, MT, EPI, XIN><<<grid, 128, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_gemm<FMT, MT, EPI, XIN>, grid, dim3(128), smem, s, a);
 }
 
 template <int MT>
@@ -586,8 +645,7 @@ static cudaError_t run_head(const GemmArgs &a, cudaStream_t s) {
     int grid = 152 * per_sm;
     const int ntiles = a.N / 16;
     if (grid * kWarpsPerCta > ntiles) grid = (ntiles + kWarpsPerCta - 1) / kWarpsPerCta;
-    k_head<MT><<<grid, 128, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_head<MT>, dim3(grid), dim3(128), smem, s, a);
 }
 
 int head_grid(int C, int M, int N) {

@@ -14,6 +14,8 @@ namespace dfl {
 
 // ---------------------------------------------------------------------------------------------------
 __global__ void k_set_state(DevState *st, SetStateArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int i = threadIdx.x;
     int r = 0;
     if (i < kMaxRows) r = a.use_draft_rows ? (i == 0 ? st->last_tok : st->props[i - 1]) : a.rows[i];
@@ -32,24 +34,26 @@ __global__ void k_set_state(DevState *st, SetStateArgs a) {
 }
 
 cudaError_t launch_set_state(DevState *st, const SetStateArgs &a, cudaStream_t s) {
-    k_set_state<<<1, 32, 0, s>>>(st, a);
-    return cudaGetLastError();
+    return launch_pdl(k_set_state, dim3(1), dim3(32), 0, s, st, a);
 }
 
 // planted drafts: the proposals for positions n+1..n+count become table[n+1..n+count]
 __global__ void k_plant(DevState *st, const int32_t *table, int count) {
+    pdl_wait();
+    pdl_trigger();
     const int i = threadIdx.x;
     if (i < count) st->props[i] = table[st->n + 1 + i];
 }
 
 cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStream_t s) {
-    k_plant<<<1, 32, 0, s>>>(st, table, count);
-    return cudaGetLastError();
+    return launch_pdl(k_plant, dim3(1), dim3(32), 0, s, st, table, count);
 }
 
 // ---------------------------------------------------------------------------------------------------
 // x[m] = emb[token_m] * scale (fp32); the row's per-layer-embedding inputs are a plain table row.
 __global__ void k_embed(EmbedArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x;
     const int tok = a.use_draft ? (m == 0 ? a.st->last_tok : a.mask_token) : a.st->rows[m];
     const uint16_t *e = a.emb + (long)tok * a.H;
@@ -61,8 +65,7 @@ __global__ void k_embed(EmbedArgs a) {
 }
 
 cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t s) {
-    k_embed<<<a.M, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_embed, dim3(a.M), dim3(256), 0, s, a);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -72,6 +75,8 @@ constexpr int kRowThreads = 256;
 constexpr int kRowMaxPer = 16;   // hidden <= 4096
 
 __global__ void __launch_bounds__(kRowThreads) k_rows(RowArgs a) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[33];
     const int m = blockIdx.x;
     const bool live = !a.rows_from_ctx || m < a.st->ctx_rows;
@@ -143,14 +148,15 @@ __global__ void __launch_bounds__(kRowThreads) k_rows(RowArgs a) {
 
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
     if (a.H > kRowThreads * kRowMaxPer) return cudaErrorInvalidValue;
-    k_rows<<<a.M, kRowThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_rows, dim3(a.M), dim3(kRowThreads), 0, s, a);
 }
 
 // dst[m] = RMSNorm(src[m], w) for live rows (m < st->ctx_rows when live_from_ctx), zeros else.
 __global__ void __launch_bounds__(kRowThreads) k_cast_rows(const float *src, int ld_src, int H, const uint16_t *w,
                                                            float eps, float *dst, int ld_dst, const DevState *st,
                                                            int live_from_ctx) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[33];
     const int m = blockIdx.x;
     const bool live = !live_from_ctx || m < st->ctx_rows;
@@ -174,8 +180,7 @@ __global__ void __launch_bounds__(kRowThreads) k_cast_rows(const float *src, int
 cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const uint16_t *w_norm, float eps,
                              float *dst, int ld_dst, const DevState *st, int live_from_ctx, cudaStream_t s) {
     if (H > kRowThreads * kRowMaxPer) return cudaErrorInvalidValue;
-    k_cast_rows<<<M, kRowThreads, 0, s>>>(src, ld_src, H, w_norm, eps, dst, ld_dst, st, live_from_ctx);
-    return cudaGetLastError();
+    return launch_pdl(k_cast_rows, dim3(M), dim3(kRowThreads), 0, s, src, ld_src, H, w_norm, eps, dst, ld_dst, st, live_from_ctx);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -183,6 +188,8 @@ cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const u
 // absolute position, from a (cos, sin) table computed in double precision. Keys and values are
 // stored into their plane slot (pos % cap), or into the block store (slot = row).
 __global__ void k_qk(QkArgs a) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[33];
     const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.hd / 2;
     const bool live = !a.live_from_ctx || m < a.st->ctx_rows;
@@ -220,8 +227,7 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t s) {
     const int heads = (a.q_out ? a.nq : 0) + (a.k_store ? a.nkv : 0);
     if (heads == 0) return cudaSuccess;
     if (a.hd / 2 < 32 || a.hd / 2 > 1024 || (a.hd / 2) % 32) return cudaErrorInvalidValue;
-    k_qk<<<dim3(a.M, heads), a.hd / 2, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_qk, dim3(a.M, heads), dim3(a.hd / 2), 0, s, a);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -246,6 +252,8 @@ __device__ __forceinline__ void attn_range(const AttnArgs &a, int n, int &lo, in
 }
 
 __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_last;
     const int hd = a.hd, ks = hd + 1;   // key row stride in floats (odd: conflict-free column reads)
@@ -378,8 +386,7 @@ cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t s) {
         attr = true;
     }
     if (a.hd % 32 || a.M > kMaxRows || a.nB > kAttnChunk) return cudaErrorInvalidValue;
-    k_attn<<<grid, kAttnThreads, attn_smem(a.M, a.hd), s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_attn, dim3(grid), dim3(kAttnThreads), attn_smem(a.M, a.hd), s, a);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -396,6 +403,8 @@ constexpr int kSampleThreads = 1024;
 // Row m's token for position n+m+1: the smallest j whose running sum of exp((l_j - max)/T) exceeds
 // U * total (running sums in double; each thread sums a contiguous segment, then a block scan).
 __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleArgs a) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float redf[33];
     __shared__ double wsum[32];
     __shared__ int s_tok, s_last;
@@ -474,8 +483,7 @@ __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleArgs a) {
 }
 
 cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s) {
-    k_sample<<<a.M, kSampleThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_sample, dim3(a.M), dim3(kSampleThreads), 0, s, a);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -503,6 +511,8 @@ namespace dfl {
 
 // dst[m] = taps row of position st->draft_n + m for m < st->ctx_rows, zeros for the other rows.
 __global__ void k_copy_taps(const float *taps, int ld, const DevState *st, float *dst, int ld_dst) {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x;
     const bool live = m < st->ctx_rows;
     const float *src = taps + (long)(st->draft_n + (live ? m : 0)) * ld;
@@ -512,8 +522,7 @@ __global__ void k_copy_taps(const float *taps, int ld, const DevState *st, float
 
 cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, float *dst, int ld_dst,
                              cudaStream_t s) {
-    k_copy_taps<<<M, 256, 0, s>>>(taps, ld, st, dst, ld_dst);
-    return cudaGetLastError();
+    return launch_pdl(k_copy_taps, dim3(M), dim3(256), 0, s, taps, ld, st, dst, ld_dst);
 }
 
 }  // namespace dfl
