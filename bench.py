@@ -312,8 +312,9 @@ def bench_reference(args):
 
 
 def bench_gemm(args):
-    """Isolated Q4_1 product sweep: rows M in {1,2,4,8,16}; 100 seeded weight buffers per shape cycled
-    so the weights come from HBM; bf16 activations N(0,1)."""
+    """Isolated Q4_1 product sweep: rows M in {1,2,4,8,16}; up to 100 packed weight buffers per shape
+    cycled so the weights come from HBM (8 GB of images); activations N(0,1) rounded to bf16, packed
+    once into the operand format (resident); 100 timed launches per point."""
     import ctypes
     import torch
     from dflash_speculative_decode_gb300 import _abi, build
@@ -324,8 +325,11 @@ def bench_gemm(args):
     st = torch.cuda.current_stream()
     res = []
     shapes = [(2560, 10240), (10240, 2560), (2560, 4096), (2560, 20480), (20480, 2560)]
+    if args.gemm_shape:
+        shapes = [tuple(int(v) for v in args.gemm_shape.split("x"))]
+    rows = [int(v) for v in args.gemm_rows.split(",")]
     for K, N in shapes:
-        nbuf = max(8, min(100, int(8e9 // (K * N * 0.625))))
+        nbuf = max(8, min(args.gemm_bufs, int(8e9 // (K * N * 0.625))))
         imgs = []
         src = torch.from_numpy(gen.make_tensor(gen.TensorSpec("sweep", "q41", (N, K), 0.02), seed=5).reshape(-1)).to(dev)
         for i in range(nbuf):
@@ -334,28 +338,40 @@ def bench_gemm(args):
                            ctypes.c_void_p(st.cuda_stream))
             imgs.append(img)
         del src
-        for M in (1, 2, 4, 8, 16):
-            x = torch.from_numpy(gen.activations(M, K, seed=M).view(np.int16)).to(dev)
+        for M in rows:
+            xb = gen.activations(M, K, seed=M)
+            x = torch.from_numpy((xb.astype(np.uint32) << 16).view(np.float32)).to(dev)   # bf16 values as fp32
+            act = torch.empty(L.dfl_act_bytes(M, K), dtype=torch.uint8, device=dev)
+            L.dfl_act_pack(ctypes.c_void_p(x.data_ptr()), M, K, ctypes.c_void_p(act.data_ptr()),
+                           ctypes.c_void_p(st.cuda_stream))
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
             sb = L.dfl_q41_gemm_scratch_bytes(K, N, M)
-            scratch = torch.zeros(sb, dtype=torch.uint8, device=dev)
+            scratch = torch.zeros(max(sb, 256), dtype=torch.uint8, device=dev)
 
             def once(i):
-                L.dfl_q41_gemm(ctypes.c_void_p(imgs[i % nbuf].data_ptr()), K, N, ctypes.c_void_p(x.data_ptr()), M,
+                L.dfl_q41_gemm(ctypes.c_void_p(imgs[i % nbuf].data_ptr()), K, N, ctypes.c_void_p(act.data_ptr()), M,
                                ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(scratch.data_ptr()), sb,
                                ctypes.c_void_p(st.cuda_stream))
             for i in range(max(args.warmup, 3)):
                 once(i)
+            # 100 launches captured in one CUDA graph: the timing sees the GPU, not the Python launch rate
             reps = 100
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                cs = torch.cuda.current_stream()
+                for i in range(reps):
+                    L.dfl_q41_gemm(ctypes.c_void_p(imgs[i % nbuf].data_ptr()), K, N, ctypes.c_void_p(act.data_ptr()),
+                                   M, ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(scratch.data_ptr()), sb,
+                                   ctypes.c_void_p(cs.cuda_stream))
+            g.replay()
             torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
-            for i in range(reps):
-                once(i)
+            g.replay()
             e1.record(st)
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1e3 / reps
-            by = K * N * 0.625 + M * K * 2 + M * N * 4
+            by = K * N * 0.625 + M * K * 4 + M * N * 4   # weights, operand-format activations, fp32 out
             gbs = by / (us * 1e-6) / 1e9
             res.append({"K": K, "N": N, "M": M, "us": round(us, 2), "GB/s": round(gbs, 1),
                         "frac_measured": round(gbs / pk["hbm_gbs"], 3), "frac_8TBs": round(gbs / 8000, 3)})
@@ -374,6 +390,9 @@ def main():
     ap.add_argument("--ctx", type=int, default=1024)
     ap.add_argument("--p", type=float, default=0.3)
     ap.add_argument("--gen", type=int, default=512, help="tokens per decode before restarting from the prefix")
+    ap.add_argument("--gemm-bufs", type=int, default=100, help="weight images cycled by the product sweep")
+    ap.add_argument("--gemm-shape", default="", help="one KxN shape for the product sweep")
+    ap.add_argument("--gemm-rows", default="1,2,4,8,16", help="row counts of the product sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -83,6 +83,8 @@ SIGNATURES = {
     "dfl_destroy": (None, [vp]),
     "dfl_q41_image_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int]),
     "dfl_q41_pack": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
+    "dfl_act_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int]),
+    "dfl_act_pack": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
     "dfl_q41_gemm_scratch_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "dfl_q41_gemm": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]),
 }

@@ -10,8 +10,6 @@ namespace dfl {
 
 constexpr int kMaxRows = 16;           // rows of one pass (R_max)
 constexpr int kWarpsPerCta = 4;        // GEMM CTA: 4 warps, each two 16-column tiles
-constexpr int kMaxChunksPerSplit = 8;  // 64-wide K chunks one GEMM CTA stages in shared memory
-constexpr int kSplitTargetWarps = 152 * 16;
 
 // Device-resident counters of the current pass. The host writes them with k_set_state before each
 // pass so a captured graph replays at any position.
@@ -67,10 +65,9 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Four 4-bit codes pairs of a packed word -> bf16x2 registers holding the codes exactly.
-// bits [4s, 4s+4) and [16+4s, 16+4s+4) of w become the low and high bf16 of register s.
-// 0x4300 is bf16 128.0 whose last mantissa bit is worth 1, so (0x4300 | q) is 128 + q; subtracting
-// 128 leaves q exactly.
+// Two 4-bit codes of a packed word -> a bf16x2 register holding the codes exactly: bits [0, 4) and
+// [16, 20) of w become the low and high bf16. 0x4300 is bf16 128.0 whose last mantissa bit is worth 1,
+// so (0x4300 | q) is 128 + q; subtracting 128 leaves q exactly.
 __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w) {
     uint32_t r;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
@@ -94,6 +91,31 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory"); }
+
+// ---- activation operand format ---------------------------------------------------------------------
+// An activation matrix of up to 16 rows and K inputs (K % 16 == 0) that feeds a product is stored as
+// the B fragments of mma.m16n8k16: fp32 x = hi + lo with hi = bf16(x), lo = bf16(x - hi) (exact to
+// 2^-17 relative). Row tok, 16-input group kb, lane column t = 0..3 own 16 bytes at word
+// ((tok * K/16 + kb) * 4 + t) * 4: {hi(2t, 2t+1), hi(2t+8, 2t+9), lo(2t, 2t+1), lo(2t+8, 2t+9)},
+// inputs counted within the group, the lower input in the low half. Beside it, sums[kb * 16 + tok]
+// holds the fp32 sum of the row's 16 inputs of group kb (the Q4_1 minimum term).
+// act_store writes one element and returns hi + lo.
+__device__ __forceinline__ float act_store(uint32_t *f, int K, int tok, int k, float v) {
+    const int r = k & 15, t = (r & 7) >> 1, w = r >> 3, half = r & 1;
+    uint16_t *p = reinterpret_cast<uint16_t *>(f + (((long)tok * (K >> 4) + (k >> 4)) * 4 + t) * 4);
+    const uint16_t hi = f32_to_bf16(v);
+    const uint16_t lo = f32_to_bf16(v - bf16_to_f32(hi));
+    p[2 * w + half] = hi;
+    p[2 * (w + 2) + half] = lo;
+    return bf16_to_f32(hi) + bf16_to_f32(lo);
+}
+
+// Sum over the 16 lanes of a half warp (all 32 lanes must call).
+__device__ __forceinline__ float half_warp_sum(float v) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
@@ -122,20 +144,21 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // ---- GEMM interface ---------------------------------------------------------------------------------
 enum WFmt { W_Q41 = 0, W_BF16 = 1 };
 enum Epi { EPI_F32 = 0, EPI_GLU = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
-enum XIn { X_BF16 = 0, X_F32 = 1 };   // activation type of a product
 enum ArgmaxDst { AM_VERIFY = 0, AM_DRAFT = 1 };
 
 struct GemmArgs {
     const uint8_t *img;    // tile image
     int K, C, N;           // logical K, chunks of 64 along padded K, output columns
     int M;                 // rows (<= 16)
-    int S;                 // K splits
-    const void *x;         // activations [M][ldx]: fp32 (X_F32) or bf16 (X_BF16)
-    int ldx;
+    const uint32_t *xf;    // activations, operand format (K inputs)
+    const float *xs;       // their per-16 sums
     int x_row0;            // first activation row used
-    void *y;               // fp32 output
+    float *y;              // EPI_F32: fp32 output [M][ldy]
     int ldy;
-    float *part;           // split-K partials [S][M][N]
+    uint32_t *yf;          // EPI_GLU / EPI_SILU_MUL: output in operand format (N/2 or N inputs)
+    float *ys;
+    float *part;           // segment partials [N/32][maxseg][16][32]
+    int maxseg;
     int *cnt;              // arrival counters [N/32] (zero between launches)
     const uint16_t *ext;   // EPI_SILU_MUL: bf16 multiplier [M][lde]
     int lde;
@@ -150,9 +173,13 @@ struct GemmArgs {
 };
 
 // launchers (gemm.cu)
-int gemm_splits(int C, int N, int fmt);
-size_t gemm_scratch_floats(int S, int M, int N);
-cudaError_t launch_gemm(int fmt, int epi, int xin, const GemmArgs &a, cudaStream_t s);
+int gemm_grid(int C, int N);
+int gemm_maxseg(int C, int N);
+size_t gemm_scratch_floats(int C, int N);
+cudaError_t launch_gemm(int fmt, int epi, const GemmArgs &a, cudaStream_t s);
+cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *sums, cudaStream_t s);
+inline size_t act_words(int K) { return (size_t)kMaxRows * K; }          // fragment words of a 16-row buffer
+inline size_t act_sums(int K) { return (size_t)(K / 16) * kMaxRows; }     // sum floats
 cudaError_t launch_pack_q41(const uint8_t *src, int K, int N, uint8_t *img, cudaStream_t s);
 cudaError_t launch_pack_bf16(const uint16_t *src, int K, int N, uint8_t *img, cudaStream_t s);
 inline int padded_k(int K) { return (K + 63) / 64 * 64; }
@@ -170,8 +197,9 @@ struct RowArgs {
     float *tap;            // tap store base (nullable), row of position p at tap + p*ld_tap + tap_off
     int ld_tap, tap_off;
     const uint16_t *w_next;   // RMSNorm weight for the output (nullable: output = x)
-    float *out;            // [M][ld_out] (nullable)
-    int ld_out;
+    uint32_t *outf;        // output rows in operand format with H inputs (nullable)
+    float *outs;           // their per-16 sums
+    int out_row0;          // first output row
     float eps;
     const DevState *st;
     int pos_from_ctx;      // tap positions: 0 = st->n + m, 1 = st->draft_n + m
@@ -223,7 +251,8 @@ struct AttnArgs {
     float *part_ml;        // [nq][max_chunks][M][2]
     int *cnt;              // [nq] arrival counters (zero between launches)
     int max_chunks;
-    float *out;            // [M][nq*hd]
+    uint32_t *outf;        // [M][nq*hd] in operand format
+    float *outs;
 };
 
 struct SampleArgs {
@@ -241,9 +270,9 @@ cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s);
 cudaError_t launch_rope_table(float2 *tab, int max_pos, int hd, double base, cudaStream_t s);
 cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const uint16_t *w_norm, float eps,
-                             float *dst, int ld_dst, const DevState *st, int live_from_ctx, cudaStream_t s);
-cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, float *dst, int ld_dst,
+                             uint32_t *dstf, float *dsts, int row0, const DevState *st, int live_from_ctx,
                              cudaStream_t s);
+cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, uint32_t *dstf, cudaStream_t s);
 cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStream_t s);
 
 // Launch with programmatic stream serialization (kernels begin with pdl_wait()).

@@ -33,9 +33,14 @@ namespace {
 
 struct QMat {
     uint8_t *img = nullptr;
-    int K = 0, N = 0, C = 0, S = 1;
+    int K = 0, N = 0, C = 0, maxseg = 1;
     bool q41 = true;
     bool loaded = false;
+};
+// a 16-row activation buffer in the products' operand format
+struct Act {
+    uint32_t *f = nullptr;
+    float *s = nullptr;
 };
 struct Vec {
     uint16_t *p = nullptr;
@@ -104,8 +109,8 @@ struct dfl_ctx {
     // workspace
     float *x = nullptr, *x_d = nullptr, *y = nullptr, *y_fc = nullptr, *qkv = nullptr, *q = nullptr;
     float *part = nullptr, *logits = nullptr, *dlogits = nullptr, *att_acc = nullptr, *att_ml = nullptr, *am_val = nullptr;
-    float *h = nullptr, *hcat = nullptr, *hb = nullptr, *o = nullptr, *a = nullptr, *z = nullptr;
-    float *tapbuf = nullptr, *kB = nullptr, *vB = nullptr;
+    Act h, hcat, hb, o, a, z, tapbuf;
+    float *kB = nullptr, *vB = nullptr;
     uint16_t *ple_rows = nullptr;
     int *cnt = nullptr, *att_cnt = nullptr, *am_idx = nullptr, *am_cnt = nullptr, *smp_cnt = nullptr;
     int *counters_begin = nullptr;
@@ -199,7 +204,7 @@ QMat qmat(int K, int N, bool q41) {
     m.K = K;
     m.N = N;
     m.C = padded_k(K) / 64;
-    m.S = gemm_splits(m.C, N, q41 ? W_Q41 : W_BF16);
+    m.maxseg = gemm_maxseg(m.C, N);
     m.q41 = q41;
     return m;
 }
@@ -220,7 +225,7 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     auto qm = [&](QMat &m, int K, int N, bool q41) {
         m = qmat(K, N, q41);
         m.img = W.take<uint8_t>(q41 ? q41_image_bytes(K, N) : bf16_image_bytes(K, N));
-        part_floats = std::max(part_floats, gemm_scratch_floats(m.S, R, N));
+        part_floats = std::max(part_floats, gemm_scratch_floats(m.C, N));
         cnt_n = std::max(cnt_n, N / 32);
     };
     auto vec = [&](Vec &v, size_t n) {
@@ -307,14 +312,18 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     c->y_fc = X.take<float>((size_t)R * H);
     c->qkv = X.take<float>((size_t)R * c->qkv_max);
     c->q = X.take<float>((size_t)R * att_max);
-    c->h = X.take<float>((size_t)R * H);
-    c->hcat = X.take<float>((size_t)R * H);
-    c->hb = X.take<float>((size_t)R * H);
-    c->o = X.take<float>((size_t)R * att_max);
-    c->a = X.take<float>((size_t)R * ffn_max);
-    c->z = X.take<float>((size_t)R * std::max(P, 32));
+    auto act = [&](Act &A, int K) {
+        A.f = X.take<uint32_t>(act_words(K));
+        A.s = X.take<float>(act_sums(K));
+    };
+    act(c->h, H);
+    act(c->hcat, H);
+    act(c->hb, H);
+    act(c->o, att_max);
+    act(c->a, ffn_max);
+    act(c->z, std::max(P, 32));
     c->ple_rows = X.take<uint16_t>((size_t)R * std::max(NL * P, 32));
-    c->tapbuf = X.take<float>((size_t)R * c->TH);
+    act(c->tapbuf, c->TH);
     c->kB = X.take<float>((size_t)R * dkv * dhd);
     c->vB = X.take<float>((size_t)R * dkv * dhd);
     c->part = X.take<float>(std::max<size_t>(part_floats, 1));
@@ -358,17 +367,21 @@ cudaError_t prof_begin(dfl_ctx *c, size_t *slot) {
     }
     *slot = c->ev_next;
     c->ev_next += 2;
-    return cudaEventRecord(c->ev_pool[*slot], c->stream);
+    // inside a capture the record must become a node of the graph (timestamped at every replay)
+    return c->capturing ? cudaEventRecordWithFlags(c->ev_pool[*slot], c->stream, cudaEventRecordExternal)
+                        : cudaEventRecord(c->ev_pool[*slot], c->stream);
 }
 
 cudaError_t prof_end(dfl_ctx *c, size_t slot, int cls, double bytes) {
     if (!c->profile) return cudaSuccess;
     c->recs.push_back({cls, bytes, slot});
-    return cudaEventRecord(c->ev_pool[slot + 1], c->stream);
+    return c->capturing ? cudaEventRecordWithFlags(c->ev_pool[slot + 1], c->stream, cudaEventRecordExternal)
+                        : cudaEventRecord(c->ev_pool[slot + 1], c->stream);
 }
 
-cudaError_t gemm(dfl_ctx *c, const QMat &W, const float *x, int ldx, int row0, int M, int epi, void *y, int ldy,
-                 const uint16_t *ext = nullptr, int lde = 0) {
+// y = x . W for M rows; EPI_F32 writes fp32 rows to y, EPI_GLU / EPI_SILU_MUL write `out` in operand format
+cudaError_t gemm(dfl_ctx *c, const QMat &W, const Act &x, int row0, int M, int epi, float *y, int ldy,
+                 const Act *out = nullptr, const uint16_t *ext = nullptr, int lde = 0) {
     size_t slot = 0;
     cudaError_t e = prof_begin(c, &slot);
     if (e != cudaSuccess) return e;
@@ -378,24 +391,26 @@ cudaError_t gemm(dfl_ctx *c, const QMat &W, const float *x, int ldx, int row0, i
     a.C = W.C;
     a.N = W.N;
     a.M = M;
-    a.S = W.S;
-    a.x = x;
-    a.ldx = ldx;
+    a.xf = x.f;
+    a.xs = x.s;
     a.x_row0 = row0;
     a.y = y;
     a.ldy = ldy;
+    a.yf = out ? out->f : nullptr;
+    a.ys = out ? out->s : nullptr;
     a.part = c->part;
+    a.maxseg = W.maxseg;
     a.cnt = c->cnt;
     a.ext = ext;
     a.lde = lde;
     c->launches += 1;
-    e = launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, X_F32, a, c->stream);
+    e = launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, a, c->stream);
     if (e != cudaSuccess) return e;
     const double bytes = (W.q41 ? 0.625 : 2.0) * W.K * (double)W.N + 4.0 * M * W.K + 4.0 * M * W.N;
     return prof_end(c, slot, W.q41 ? 0 : 1, bytes);
 }
 
-cudaError_t head(dfl_ctx *c, const float *x, int row0, int M, float *logits, int dst) {
+cudaError_t head(dfl_ctx *c, const Act &x, int row0, int M, float *logits, int dst) {
     size_t slot = 0;
     cudaError_t e = prof_begin(c, &slot);
     if (e != cudaSuccess) return e;
@@ -405,9 +420,8 @@ cudaError_t head(dfl_ctx *c, const float *x, int row0, int M, float *logits, int
     a.C = c->head.C;
     a.N = c->head.N;
     a.M = M;
-    a.S = 1;
-    a.x = x;
-    a.ldx = c->cfg.hidden;
+    a.xf = x.f;
+    a.xs = x.s;
     a.x_row0 = row0;
     a.logits = logits;
     a.ldl = c->cfg.vocab;
@@ -417,7 +431,7 @@ cudaError_t head(dfl_ctx *c, const float *x, int row0, int M, float *logits, int
     a.st = c->st;
     a.am_dst = dst;
     c->launches += 1;
-    e = launch_gemm(W_BF16, EPI_ARGMAX, X_F32, a, c->stream);
+    e = launch_gemm(W_BF16, EPI_ARGMAX, a, c->stream);
     if (e != cudaSuccess) return e;
     const double bytes = 2.0 * a.K * (double)a.N + 4.0 * M * a.K + (logits ? 4.0 * M * a.N : 0.0);
     return prof_end(c, slot, 2, bytes);
@@ -504,7 +518,6 @@ RowArgs rows(dfl_ctx *c, int M, float *x) {
     r.lambda = 1.f;
     r.eps = c->cfg.eps;
     r.st = c->st;
-    r.ld_out = c->cfg.hidden;
     return r;
 }
 
@@ -542,7 +555,8 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
     DFL_LAUNCH(launch_embed(ea, c->stream));
     RowArgs r0 = rows(c, k, c->x);
     r0.w_next = c->tl[0].attn_norm.p;
-    r0.out = c->h;
+    r0.outf = c->h.f;
+    r0.outs = c->h.s;
     DFL_LAUNCH(launch_rows(r0, c->stream));
     const int last_layer = (c->stop_layer >= 0 && c->stop_layer < NL) ? c->stop_layer : NL - 1;
     if (last_layer < NL - 1) do_head = false;
@@ -551,7 +565,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         TLayer &O = c->tl[L.owner];
         const bool own = L.owner == l;
         const int nqkv = L.qkv.N;
-        DFL_CK(gemm(c, L.qkv, c->h, H, 0, k, EPI_F32, c->qkv, nqkv));
+        DFL_CK(gemm(c, L.qkv, c->h, 0, k, EPI_F32, c->qkv, nqkv));
         QkArgs qa{};
         qa.M = k;
         qa.nq = nq;
@@ -586,18 +600,20 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.part_ml = c->att_ml;
         aa.cnt = c->att_cnt;
         aa.max_chunks = c->att_max_chunks;
-        aa.out = c->o;
+        aa.outf = c->o.f;
+        aa.outs = c->o.s;
         DFL_LAUNCH(launch_attn(aa, 2 * 152, c->stream));
-        DFL_CK(gemm(c, L.o, c->o, nq * hd, 0, k, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, L.o, c->o, 0, k, EPI_F32, c->y, H));
         RowArgs r1 = rows(c, k, c->x);
         r1.y = c->y;
         r1.ldy = H;
         r1.w_post = L.post_attn_norm.p;
         r1.w_next = L.pre_ffn_norm.p;
-        r1.out = c->h;
+        r1.outf = c->h.f;
+        r1.outs = c->h.s;
         DFL_LAUNCH(launch_rows(r1, c->stream));
-        DFL_CK(gemm(c, L.gu, c->h, H, 0, k, EPI_GLU, c->a, L.ffn));
-        DFL_CK(gemm(c, L.d, c->a, L.ffn, 0, k, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, L.gu, c->h, 0, k, EPI_GLU, nullptr, 0, &c->a));
+        DFL_CK(gemm(c, L.d, c->a, 0, k, EPI_F32, c->y, H));
         const uint16_t *next = l + 1 < NL ? c->tl[l + 1].attn_norm.p : c->final_norm.p;
         int ti = 0;
         const bool tap = is_tap(g, l, &ti);
@@ -605,17 +621,19 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         r2.y = c->y;
         r2.ldy = H;
         r2.w_post = L.post_ffn_norm.p;
-        r2.out = c->h;
+        r2.outf = c->h.f;
+        r2.outs = c->h.s;
         if (P) {
-            DFL_LAUNCH(launch_rows(r2, c->stream));   // out = bf16(x): the gate's input
-            DFL_CK(gemm(c, L.pg, c->h, H, 0, k, EPI_SILU_MUL, c->z, P, c->ple_rows + (size_t)l * P, NL * P));
-            DFL_CK(gemm(c, L.pp, c->z, P, 0, k, EPI_F32, c->y, H));
+            DFL_LAUNCH(launch_rows(r2, c->stream));   // out = x: the gate's input
+            DFL_CK(gemm(c, L.pg, c->h, 0, k, EPI_SILU_MUL, nullptr, 0, &c->z, c->ple_rows + (size_t)l * P, NL * P));
+            DFL_CK(gemm(c, L.pp, c->z, 0, k, EPI_F32, c->y, H));
             r2 = rows(c, k, c->x);
             r2.y = c->y;
             r2.ldy = H;
             r2.w_post = L.ple_norm.p;
             r2.lambda = L.lambda;
-            r2.out = c->h;
+            r2.outf = c->h.f;
+            r2.outs = c->h.s;
         }
         r2.w_next = next;
         if (tap) {
@@ -655,12 +673,13 @@ int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
 
 // ---- draft context rows: fc of the taps, hidden norm, then each layer's key and value ---------------
 // rows draft_n .. draft_n + r - 1 (device st->ctx_rows = r) into activation rows `row0..` of hctx.
-int ctx_rows_prologue(dfl_ctx *c, int M, float *hdst) {
+// rows draft_n .. draft_n + st->ctx_rows - 1 become rows row0.. of hcat: RMSNorm_hidden(fc . taps)
+int ctx_rows_prologue(dfl_ctx *c, int M, int row0) {
     const dfl_config &g = c->cfg;
-    DFL_LAUNCH(launch_copy_taps(c->taps, c->TH, c->st, M, c->tapbuf, c->TH, c->stream));
-    DFL_CK(gemm(c, c->fc, c->tapbuf, c->TH, 0, M, EPI_F32, c->y_fc, g.hidden));
-    DFL_LAUNCH(launch_cast_rows(c->y_fc, g.hidden, M, g.hidden, c->d_hidden_norm.p, g.d_eps, hdst, g.hidden, c->st, 1,
-                            c->stream));
+    DFL_LAUNCH(launch_copy_taps(c->taps, c->TH, c->st, M, c->tapbuf.f, c->stream));
+    DFL_CK(gemm(c, c->fc, c->tapbuf, 0, M, EPI_F32, c->y_fc, g.hidden));
+    DFL_LAUNCH(launch_cast_rows(c->y_fc, g.hidden, M, g.hidden, c->d_hidden_norm.p, g.d_eps, c->hcat.f, c->hcat.s, row0,
+                                c->st, 1, c->stream));
     return DFL_OK;
 }
 
@@ -685,11 +704,11 @@ int run_ctx_only(dfl_ctx *c, int r) {
     const dfl_config &g = c->cfg;
     int rc = set_state(c, 0, nullptr, false, r, -1, nullptr);
     if (rc) return rc;
-    rc = ctx_rows_prologue(c, kMaxRows, c->hcat);
+    rc = ctx_rows_prologue(c, kMaxRows, 0);
     if (rc) return rc;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
-        DFL_CK(gemm(c, D.qkv, c->hcat, g.hidden, 0, kMaxRows, EPI_F32, c->qkv, D.qkv.N));
+        DFL_CK(gemm(c, D.qkv, c->hcat, 0, kMaxRows, EPI_F32, c->qkv, D.qkv.N));
         QkArgs qa = draft_qk(c, l);
         qa.M = kMaxRows;
         qa.row0 = 0;
@@ -717,7 +736,7 @@ int draft_body(dfl_ctx *c) {
     const dfl_config &g = c->cfg;
     const int H = g.hidden, B = g.block, F = c->ctx_fuse;
     if (F > 0) {
-        const int rc = ctx_rows_prologue(c, F, c->hcat + (size_t)B * H);
+        const int rc = ctx_rows_prologue(c, F, B);
         if (rc) return rc;
     }
     EmbedArgs ea{};
@@ -733,12 +752,13 @@ int draft_body(dfl_ctx *c) {
     RowArgs r0 = rows(c, B, c->x_d);
     r0.eps = g.d_eps;
     r0.w_next = c->dl[0].attn_norm.p;
-    r0.out = c->hcat;
+    r0.outf = c->hcat.f;
+    r0.outs = c->hcat.s;
     DFL_LAUNCH(launch_rows(r0, c->stream));
     const int dq = g.d_heads, dhd = g.d_head_dim;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
-        DFL_CK(gemm(c, D.qkv, c->hcat, H, 0, B + F, EPI_F32, c->qkv, D.qkv.N));
+        DFL_CK(gemm(c, D.qkv, c->hcat, 0, B + F, EPI_F32, c->qkv, D.qkv.N));
         QkArgs qb = draft_qk(c, l);
         qb.M = B;
         qb.pos_mode = 1;
@@ -778,24 +798,28 @@ int draft_body(dfl_ctx *c) {
         aa.part_ml = c->att_ml;
         aa.cnt = c->att_cnt;
         aa.max_chunks = c->att_max_chunks;
-        aa.out = c->o;
+        aa.outf = c->o.f;
+        aa.outs = c->o.s;
         DFL_LAUNCH(launch_attn(aa, 2 * 152, c->stream));
-        DFL_CK(gemm(c, D.o, c->o, dq * dhd, 0, B, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, D.o, c->o, 0, B, EPI_F32, c->y, H));
         RowArgs r1 = rows(c, B, c->x_d);
         r1.eps = g.d_eps;
         r1.y = c->y;
         r1.ldy = H;
         r1.w_next = D.ffn_norm.p;
-        r1.out = c->hb;
+        r1.outf = c->hb.f;
+        r1.outs = c->hb.s;
         DFL_LAUNCH(launch_rows(r1, c->stream));
-        DFL_CK(gemm(c, D.gu, c->hb, H, 0, B, EPI_GLU, c->a, g.d_ffn));
-        DFL_CK(gemm(c, D.d, c->a, g.d_ffn, 0, B, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, D.gu, c->hb, 0, B, EPI_GLU, nullptr, 0, &c->a));
+        DFL_CK(gemm(c, D.d, c->a, 0, B, EPI_F32, c->y, H));
         RowArgs r2 = rows(c, B, c->x_d);
         r2.eps = g.d_eps;
         r2.y = c->y;
         r2.ldy = H;
         r2.w_next = l + 1 < g.d_layers ? c->dl[l + 1].attn_norm.p : c->d_final_norm.p;
-        r2.out = l + 1 < g.d_layers ? c->hcat : c->hb;
+        const Act &nxt = l + 1 < g.d_layers ? c->hcat : c->hb;
+        r2.outf = nxt.f;
+        r2.outs = nxt.s;
         DFL_LAUNCH(launch_rows(r2, c->stream));
     }
     float *lg = c->keep_logits ? c->dlogits : nullptr;
@@ -920,6 +944,7 @@ int dfl_init(const dfl_config *cfg, const dfl_buffers *buf, void *stream, dfl_ct
         (e = launch_rope_table(c->rope_d, c->rope_rows, g.d_head_dim, g.d_rope_base, c->stream)) != cudaSuccess)
         return bail(e, "rope table");
     if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) return bail(e, "sync");
+    c->launches = 3;   // the rope tables
     *out = c;
     return DFL_OK;
 }
@@ -986,8 +1011,8 @@ int dfl_load_tensor(dfl_ctx *c, const char *name, const void *src, size_t bytes)
     if (m) {
         const size_t want = m->q41 ? (size_t)m->N * (m->K / 32) * 20 : (size_t)m->N * m->K * 2;
         if (bytes != want) return fail(c, DFL_E_INVALID_ARG, s + ": expected " + std::to_string(want) + " bytes");
-        if (m->q41) DFL_CK(launch_pack_q41(static_cast<const uint8_t *>(src), m->K, m->N, m->img, c->stream));
-        else DFL_CK(launch_pack_bf16(static_cast<const uint16_t *>(src), m->K, m->N, m->img, c->stream));
+        if (m->q41) DFL_LAUNCH(launch_pack_q41(static_cast<const uint8_t *>(src), m->K, m->N, m->img, c->stream));
+        else DFL_LAUNCH(launch_pack_bf16(static_cast<const uint16_t *>(src), m->K, m->N, m->img, c->stream));
         m->loaded = true;
         return DFL_OK;
     }
@@ -1254,11 +1279,9 @@ int dfl_debug_read(dfl_ctx *c, const char *name, void *dst, size_t bytes) {
     size_t have = 0;
     const size_t R = kMaxRows, H = c->cfg.hidden;
     if (s == "x") src = c->x, have = R * H * 4;
-    else if (s == "h") src = c->h, have = R * H * 4;
     else if (s == "y") src = c->y, have = R * H * 4;
     else if (s == "qkv") src = c->qkv, have = R * c->qkv_max * 4;
     else if (s == "q") src = c->q, have = R * std::max(c->cfg.n_heads * c->cfg.head_dim, c->cfg.d_heads * c->cfg.d_head_dim) * 4;
-    else if (s == "o") src = c->o, have = R * std::max(c->cfg.n_heads * c->cfg.head_dim, c->cfg.d_heads * c->cfg.d_head_dim) * 4;
     else if (s == "x_d") src = c->x_d, have = R * H * 4;
     else return fail(c, DFL_E_INVALID_ARG, "unknown buffer " + s);
     if (bytes > have) return fail(c, DFL_E_INVALID_ARG, "read past the buffer");
@@ -1316,18 +1339,29 @@ int dfl_q41_pack(const void *src, int K, int N, void *img, void *stream) {
                            static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
 }
 
-// scratch = arrival counters (N/32 ints, at offset 0, rounded up to 256 bytes), then the partial sums
+int64_t dfl_act_bytes(int M, int K) {
+    if (M < 1 || M > kMaxRows || K < 16 || K % 16) return -1;
+    return (int64_t)(act_words(K) * 4 + act_sums(K) * 4);
+}
+
+int dfl_act_pack(const float *x, int M, int K, void *act, void *stream) {
+    if (!x || !act || dfl_act_bytes(M, K) < 0) return DFL_E_INVALID_ARG;
+    uint32_t *f = static_cast<uint32_t *>(act);
+    float *sums = reinterpret_cast<float *>(f + act_words(K));
+    return launch_act_pack(x, M, K, f, sums, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+}
+
+// scratch = arrival counters (N/32 ints, at offset 0, rounded up to 256 bytes), then the segment partials
 int64_t dfl_q41_gemm_scratch_bytes(int K, int N, int M) {
     if (K < 32 || K % 32 || N < 32 || N % 32 || M < 1 || M > kMaxRows) return -1;
     const int C = padded_k(K) / 64;
-    const int S = gemm_splits(C, N, W_Q41);
-    return (int64_t)((size_t)(N / 32 * 4 + 255) / 256 * 256 + gemm_scratch_floats(S, M, N) * 4);
+    return (int64_t)((size_t)(N / 32 * 4 + 255) / 256 * 256 + gemm_scratch_floats(C, N) * 4);
 }
 
-int dfl_q41_gemm(const void *img, int K, int N, const void *x, int M, float *y, void *scratch, size_t scratch_bytes,
+int dfl_q41_gemm(const void *img, int K, int N, const void *act, int M, float *y, void *scratch, size_t scratch_bytes,
                  void *stream) {
     const int64_t need = dfl_q41_gemm_scratch_bytes(K, N, M);
-    if (need < 0 || !img || !x || !y || !scratch || (int64_t)scratch_bytes < need) return DFL_E_INVALID_ARG;
+    if (need < 0 || !img || !act || !y || !scratch || (int64_t)scratch_bytes < need) return DFL_E_INVALID_ARG;
     const int C = padded_k(K) / 64;
     GemmArgs a{};
     a.img = static_cast<const uint8_t *>(img);
@@ -1335,15 +1369,15 @@ int dfl_q41_gemm(const void *img, int K, int N, const void *x, int M, float *y, 
     a.C = C;
     a.N = N;
     a.M = M;
-    a.S = gemm_splits(C, N, W_Q41);
-    a.x = static_cast<const uint16_t *>(x);
-    a.ldx = K;
+    a.xf = static_cast<const uint32_t *>(act);
+    a.xs = reinterpret_cast<const float *>(static_cast<const uint32_t *>(act) + act_words(K));
     a.y = y;
     a.ldy = N;
+    a.maxseg = gemm_maxseg(C, N);
     const size_t cbytes = (size_t)(N / 32 * 4 + 255) / 256 * 256;
     a.cnt = static_cast<int *>(scratch);
     a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + cbytes);
-    return launch_gemm(W_Q41, EPI_F32, X_BF16, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+    return launch_gemm(W_Q41, EPI_F32, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
 }
 
 }  // extern "C"

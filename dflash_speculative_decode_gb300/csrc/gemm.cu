@@ -6,23 +6,30 @@
 // (model card "Nemotron-3.5-Bolt-E4B-DFlash-NPU2", spec table: "5 bits per weight with scales and
 // minimums") except fc and the head, which are bf16.
 //
-// Layout. A weight matrix of K inputs x N outputs is cut into tiles of 16 output columns x 64 inputs.
-// Tile (nt, c) of a matrix with C = ceil(K/64) chunks sits at offset (nt*C + c) * tile_bytes, so one
-// column strip's whole K range is contiguous. Inside a tile the data is ordered by the lane of the
-// warp that consumes it as the A operand of mma.m16n8k16 (rows = output columns, columns = inputs):
+// Weight layout. A matrix of K inputs x N outputs is cut into tiles of 16 output columns x 64 inputs;
+// tile (nt, c) of a matrix with C = ceil(K/64) chunks sits at (nt*C + c) * tile_bytes. Inside a tile
+// the data is ordered by the lane that consumes it as the A operand of mma.m16n8k16 (rows = output
+// columns, columns = inputs):
 //   Q4_1 (640 B): lane L = 4g + t holds 16 B of codes at 16L: word s (k-step s, inputs 16s..16s+15)
 //     packs, low to high nibble, q(g,2t) q(g+8,2t) q(g,2t+8) q(g+8,2t+8) q(g,2t+1) q(g+8,2t+1)
 //     q(g,2t+9) q(g+8,2t+9), so shifting by 0/4/8/12 and masking 0x000F000F gives the four A registers.
 //     Bytes 512..639: for g = 0..7, 16 B of (d, m) fp16 pairs for columns g, g+8 of the tile's two
 //     32-input blocks.
 //   bf16 (2048 B): k-step s at 512*s, lane L's 16 B = its four A registers.
-// Q4_1 product per 32-block b: y += d_b * sum_k x_k q_k + m_b * sum_k x_k, with q entering the
-// tensor core exactly (integers 0..15 are exact in bf16) and the per-block scale applied in fp32.
+// Activations arrive in the operand format of common.cuh (bf16 hi + lo fragments in lane order and
+// per-16 sums), so a warp loads its B fragment of a k-step with one 16-byte load.
 //
-// Split K: the K chunks are cut into S equal ranges (S depends on K and N only); each warp computes
-// two tiles over one range; the last warp to finish a column pair (arrival counter) adds the S
-// partial sums in the fixed order 0..S-1 and applies the epilogue. So a row's result never depends on
-// how many rows the pass carries: a batched pass equals single-row passes bit for bit.
+// Q4_1 product per 32-block b: y += d_b * sum_k x_k q_k + m_b * sum_k x_k, with q entering the tensor
+// core exactly (integers 0..15 are exact in bf16) and the per-block scale applied in fp32.
+//
+// Work split (stream-K). Units = (quad of four 32-column groups, 64-input chunk). A persistent grid
+// of one wave takes equal contiguous unit ranges; the four warps of a CTA take the four column groups
+// of a quad, so they read the same activation chunks. A column group whose chunks span several CTAs
+// gets one partial sum per CTA ("segment"); the last segment to finish (arrival counter) adds them in
+// segment order and applies the epilogue. Segments depend on K, N and the grid only, so a row's
+// result never depends on how many rows the pass carries.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dfl {
@@ -102,108 +109,60 @@ cudaError_t launch_pack_bf16(const uint16_t *src, int K, int N, uint8_t *img, cu
     return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------------------------------------------
-// shared pieces of the product kernels
-// ---------------------------------------------------------------------------------------------------
-
-// Activations enter the tensor cores as bf16 B fragments. An fp32 activation x is split into
-// hi = bf16(x) and lo = bf16(x - hi) (x - hi is exact in fp32), so hi + lo = x to 2^-17 relative and
-// the product runs as two MMAs into the same accumulator. bf16 activations (XIN = 0) take one MMA.
-//
-// Staged layout, per chunk cc, token tile tt, k-step ks and lane L (token 8tt + L/4, t = L%4):
-//   XIN 0: 8 bytes  {x[k0+2t], x[k0+2t+1]}, {x[k0+2t+8], x[k0+2t+9]}
-//   XIN 1: 16 bytes {hi pair, hi pair+8, lo pair, lo pair+8}
-// at index ((cc*MT + tt)*4 + ks)*32 + L, so a warp reads one k-step's fragments in one conflict-free
-// shared load.
-__device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo, uint16_t hi) { return uint32_t(lo) | (uint32_t(hi) << 16); }
-
-// Copy the raw activation slice rows [0, M) x inputs [64*c0, 64*(c0+nch)) into shared memory with
-// 16-byte asynchronous copies (one round trip), zero beyond K.
-template <int XIN>
-__device__ __forceinline__ void stage_raw(uint8_t *raw, const GemmArgs &a, int row0, int c0, int nch) {
-    constexpr int E = XIN ? 4 : 2;                     // bytes per element
-    const int rowbytes = nch * 64 * E;
-    const int k0 = 64 * c0;
-    const int kend = min(a.K, 64 * (c0 + nch));
-    const int live = (kend - k0) * E;                  // bytes of a row inside K (multiple of 64)
-    const int per_row = rowbytes / 16;
-    for (int e = threadIdx.x; e < a.M * per_row; e += blockDim.x) {
-        const int m = e / per_row, off = (e % per_row) * 16;
-        uint8_t *dst = raw + m * rowbytes + off;
-        if (off < live)
-            cp_async16(dst, reinterpret_cast<const uint8_t *>(a.x) + ((long)(row0 + m) * a.ldx + k0) * E + off);
-        else
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    cp_async_wait_all();
+// fp32 rows -> operand format (the standalone product's input)
+__global__ void k_act_pack(const float *x, int M, int K, uint32_t *f, float *sums) {
+    pdl_wait();
+    pdl_trigger();
+    const int m = blockIdx.y;
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;   // blockDim 256: a 16-group is one half warp
+    const bool in = k < K && m < M;
+    const float v = in ? x[(long)m * K + k] : 0.f;
+    if (in) act_store(f, K, m, k, v);
+    const float s = half_warp_sum(v);
+    if (in && (k & 15) == 0) sums[(k / 16) * kMaxRows + m] = s;
 }
 
-template <int XIN>
-__device__ __forceinline__ float raw_at(const uint8_t *raw, int rowbytes, int m, int k) {
-    if (XIN) return reinterpret_cast<const float *>(raw + m * rowbytes)[k];
-    return bf16_to_f32(reinterpret_cast<const uint16_t *>(raw + m * rowbytes)[k]);
+cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *sums, cudaStream_t s) {
+    return launch_pdl(k_act_pack, dim3((K + 255) / 256, M), dim3(256), 0, s, x, M, K, f, sums);
 }
 
-// Fragments and per-32-block sums from the raw slice (after a barrier).
-template <int MT, int XIN>
-__device__ __forceinline__ void stage_frags(uint32_t *xs, float *sums, const uint8_t *raw, const GemmArgs &a, int nch,
-                                            bool want_sums) {
-    constexpr int W = XIN ? 4 : 2;
-    const int rowbytes = nch * 64 * (XIN ? 4 : 2);
-    for (int e = threadIdx.x; e < nch * MT * 4 * 32; e += blockDim.x) {
-        const int L = e & 31, ks = (e >> 5) & 3, tt = (e >> 7) % MT, cc = (e >> 7) / MT;
-        const int tok = 8 * tt + (L >> 2), tq = L & 3;
-        const int k = 64 * cc + 16 * ks + 2 * tq;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (tok < a.M) {
+// ---------------------------------------------------------------------------------------------------
+// one unit of work: a 64-input chunk of two 16-column tiles
+// ---------------------------------------------------------------------------------------------------
+template <int MT>
+__device__ __forceinline__ void load_frags(uint4 (&b)[MT][4], const GemmArgs &a, int c, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const int K16 = a.K / 16;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float v0 = raw_at<XIN>(raw, rowbytes, tok, k + 8 * hh);
-                const float v1 = raw_at<XIN>(raw, rowbytes, tok, k + 8 * hh + 1);
-                const uint16_t h0 = f32_to_bf16(v0), h1 = f32_to_bf16(v1);
-                w[hh] = pack_bf16x2(h0, h1);
-                if (XIN) w[2 + hh] = pack_bf16x2(f32_to_bf16(v0 - bf16_to_f32(h0)), f32_to_bf16(v1 - bf16_to_f32(h1)));
-            }
-        }
-        uint32_t *d = xs + (size_t)e * W;
-        if (XIN) *reinterpret_cast<uint4 *>(d) = make_uint4(w[0], w[1], w[2], w[3]);
-        else *reinterpret_cast<uint2 *>(d) = make_uint2(w[0], w[1]);
-    }
-    if (!want_sums) return;
-    for (int e = threadIdx.x; e < nch * 32; e += blockDim.x) {
-        const int tok = e & 15, blk = (e >> 4) & 1, cc = e >> 5;
-        float s = 0.f;
-        if (tok < a.M)
-            for (int i = 0; i < 32; ++i) s += raw_at<XIN>(raw, rowbytes, tok, 64 * cc + 32 * blk + i);
-        sums[e] = s;
+    for (int tt = 0; tt < MT; ++tt) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(a.xf) + ((long)(a.x_row0 + 8 * tt + g) * K16 + 4 * c) * 4 + t;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) b[tt][ks] = (4 * c + ks < K16) ? __ldg(p + 4 * ks) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// fragment of k-step ks, token tile tt for this lane
-template <int XIN>
-__device__ __forceinline__ uint4 frag(const uint32_t *xs, int cc, int tt, int ks, int lane, int MT) {
-    const size_t e = ((size_t)(cc * MT + tt) * 4 + ks) * 32 + lane;
-    if (XIN) return *reinterpret_cast<const uint4 *>(xs + e * 4);
-    const uint2 v = *reinterpret_cast<const uint2 *>(xs + e * 2);
-    return make_uint4(v.x, v.y, 0u, 0u);
-}
-
-template <int XIN>
-__device__ __forceinline__ void mma_x(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, const uint4 &b) {
-    mma_bf16(d, a0, a1, a2, a3, b.x, b.y);
-    if (XIN) mma_bf16(d, a0, a1, a2, a3, b.z, b.w);
-}
-
-template <int MT, int XIN>
-__device__ __forceinline__ void q41_chunk(float (&acc)[2][MT][4], const uint4 (&nb)[2], const uint4 (&sc)[2],
-                                          const uint32_t *xs, const float *sums, int cc, int lane) {
+template <int MT>
+__device__ __forceinline__ void q41_unit(float (&acc)[2][MT][4], const uint4 (&nb)[2], const uint4 (&sc)[2],
+                                         const GemmArgs &a, int c, int lane) {
     const int t = lane & 3;
+    const int K16 = a.K / 16;
+    uint4 b[MT][4];
+    load_frags<MT>(b, a, c, lane);
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
         float2 S[MT];
 #pragma unroll
-        for (int tt = 0; tt < MT; ++tt)
-            S[tt] = *reinterpret_cast<const float2 *>(sums + (cc * 2 + blk) * 16 + 8 * tt + 2 * t);
+        for (int tt = 0; tt < MT; ++tt) {
+            const int k16 = 4 * c + 2 * blk;
+            const int r = a.x_row0 + 8 * tt + 2 * t;
+            if (k16 < K16) {
+                const float2 s0 = __ldg(reinterpret_cast<const float2 *>(a.xs + k16 * kMaxRows + r));
+                const float2 s1 = __ldg(reinterpret_cast<const float2 *>(a.xs + (k16 + 1) * kMaxRows + r));
+                S[tt] = make_float2(s0.x + s1.x, s0.y + s1.y);
+            } else {
+                S[tt] = make_float2(0.f, 0.f);
+            }
+        }
         float cb[2][MT][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
@@ -212,16 +171,16 @@ __device__ __forceinline__ void q41_chunk(float (&acc)[2][MT][4], const uint4 (&
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
             const int ks = 2 * blk + kk;
-            uint4 b[MT];
-#pragma unroll
-            for (int tt = 0; tt < MT; ++tt) b[tt] = frag<XIN>(xs, cc, tt, ks, lane, MT);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const uint32_t w = ks == 0 ? nb[j].x : ks == 1 ? nb[j].y : ks == 2 ? nb[j].z : nb[j].w;
                 const uint32_t a0 = nib_pair_bf16(w), a1 = nib_pair_bf16(w >> 4);
                 const uint32_t a2 = nib_pair_bf16(w >> 8), a3 = nib_pair_bf16(w >> 12);
 #pragma unroll
-                for (int tt = 0; tt < MT; ++tt) mma_x<XIN>(cb[j][tt], a0, a1, a2, a3, b[tt]);
+                for (int tt = 0; tt < MT; ++tt) {
+                    mma_bf16(cb[j][tt], a0, a1, a2, a3, b[tt][ks].x, b[tt][ks].y);
+                    mma_bf16(cb[j][tt], a0, a1, a2, a3, b[tt][ks].z, b[tt][ks].w);
+                }
             }
         }
 #pragma unroll
@@ -240,197 +199,250 @@ __device__ __forceinline__ void q41_chunk(float (&acc)[2][MT][4], const uint4 (&
     }
 }
 
-template <int MT, int XIN>
-__device__ __forceinline__ void bf16_chunk(float (&acc)[2][MT][4], const uint4 (&w)[2][4], const uint32_t *xs, int cc,
-                                           int lane) {
+template <int MT>
+__device__ __forceinline__ void bf16_unit(float (&acc)[2][MT][4], const uint4 (&w)[2][4], const GemmArgs &a, int c,
+                                          int lane) {
+    uint4 b[MT][4];
+    load_frags<MT>(b, a, c, lane);
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-        uint4 b[MT];
-#pragma unroll
-        for (int tt = 0; tt < MT; ++tt) b[tt] = frag<XIN>(xs, cc, tt, ks, lane, MT);
+    for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int tt = 0; tt < MT; ++tt) mma_x<XIN>(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt]);
-    }
+            for (int tt = 0; tt < MT; ++tt) {
+                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt][ks].x, b[tt][ks].y);
+                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt][ks].z, b[tt][ks].w);
+            }
 }
 
 // ---------------------------------------------------------------------------------------------------
-// split-K product with fused epilogue
+// epilogue: plain fp32 rows, or the operand format of the next product (with its per-16 sums)
 // ---------------------------------------------------------------------------------------------------
+// sum over the 8 lanes with the same t (the 16 columns g, g+8 of a tile for one token)
+__device__ __forceinline__ float tile_col_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    return v;
+}
+
 template <int MT, int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs &a, float (&acc)[2][MT][4], int nt0, int nt1, int ng, int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int tt = 0; tt < MT; ++tt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int tok = 8 * tt + 2 * t + (i & 1);
-            if (tok >= a.M) continue;
-            const int r = g + 8 * (i >> 1);
+        for (int h = 0; h < 2; ++h) {
+            const int tok = 8 * tt + 2 * t + h;
+            const bool live = tok < a.M;
             if (EPI == EPI_F32) {
-                float *y = reinterpret_cast<float *>(a.y) + (long)tok * a.ldy;
-                y[16 * nt0 + r] = acc[0][tt][i];
-                y[16 * nt1 + r] = acc[1][tt][i];
+                if (!live) continue;
+                float *y = a.y + (long)tok * a.ldy;
+                y[16 * nt0 + g] = acc[0][tt][h];
+                y[16 * nt0 + g + 8] = acc[0][tt][h + 2];
+                y[16 * nt1 + g] = acc[1][tt][h];
+                y[16 * nt1 + g + 8] = acc[1][tt][h + 2];
             } else if (EPI == EPI_GLU) {
-                float *y = reinterpret_cast<float *>(a.y) + (long)tok * a.ldy;
-                y[16 * ng + r] = silu_f(acc[0][tt][i]) * acc[1][tt][i];
+                const float v0 = silu_f(acc[0][tt][h]) * acc[1][tt][h];
+                const float v1 = silu_f(acc[0][tt][h + 2]) * acc[1][tt][h + 2];
+                const int K = a.N / 2;
+                if (live) {
+                    act_store(a.yf, K, tok, 16 * ng + g, v0);
+                    act_store(a.yf, K, tok, 16 * ng + g + 8, v1);
+                }
+                const float s = tile_col_sum(v0 + v1);
+                if (live && g == 0) a.ys[ng * kMaxRows + tok] = s;
             } else if (EPI == EPI_SILU_MUL) {
-                float *y = reinterpret_cast<float *>(a.y) + (long)tok * a.ldy;
-                const uint16_t *e = a.ext + (long)tok * a.lde;
-                const int n0 = 16 * nt0 + r, n1 = 16 * nt1 + r;
-                y[n0] = silu_f(acc[0][tt][i]) * bf16_to_f32(e[n0]);
-                y[n1] = silu_f(acc[1][tt][i]) * bf16_to_f32(e[n1]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int nt = j ? nt1 : nt0;
+                    float v0 = 0.f, v1 = 0.f;
+                    if (live) {
+                        const uint16_t *e = a.ext + (long)tok * a.lde;
+                        v0 = silu_f(acc[j][tt][h]) * bf16_to_f32(e[16 * nt + g]);
+                        v1 = silu_f(acc[j][tt][h + 2]) * bf16_to_f32(e[16 * nt + g + 8]);
+                        act_store(a.yf, a.N, tok, 16 * nt + g, v0);
+                        act_store(a.yf, a.N, tok, 16 * nt + g + 8, v1);
+                    }
+                    const float s = tile_col_sum(v0 + v1);
+                    if (live && g == 0) a.ys[nt * kMaxRows + tok] = s;
+                }
             }
         }
 }
 
-template <int FMT, int MT, int EPI, int XIN>
-__global__ void __launch_bounds__(128) k_gemm(GemmArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2;
-    const int s = blockIdx.y;
-    const int c0 = int((long)s * a.C / a.S), c1 = int((long)(s + 1) * a.C / a.S);
-    const int nch = c1 - c0;
-    uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
-    float *sums = reinterpret_cast<float *>(smem + (size_t)nch * MT * 4 * 32 * (XIN ? 16 : 8));
-    uint8_t *raw = reinterpret_cast<uint8_t *>(sums + nch * 32);
+// ---------------------------------------------------------------------------------------------------
+// the product kernel
+// ---------------------------------------------------------------------------------------------------
+// One CTA per SM, 16 warps: warp w takes column group gq = w % 4 of the current quad and chunk parity
+// par = w / 4, i.e. chunks c with c % 4 == par of the CTA's chunk range of that quad. At the end of a
+// range the four parities are added in shared memory (order 0..3); a quad split over several CTAs
+// leaves one partial per CTA, added by the last CTA to finish it (order of the segments).
+constexpr int kGemmWarps = 16;
 
+__device__ __forceinline__ long cta_of(long u, long U, int G) { return ((u + 1) * G - 1) / U; }
+
+template <int FMT, int MT, int EPI>
+__global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
+    __shared__ float red[4][4][kMaxRows * 32];
+    __shared__ int s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int gq = warp & 3, par = warp >> 2;
     const int ngroups = a.N / 32;
-    const int ng = blockIdx.x * kWarpsPerCta + warp;
-    const bool active = ng < ngroups;
-    const int nt0 = active ? ((EPI == EPI_GLU) ? ng : 2 * ng) : 0;
-    const int nt1 = active ? ((EPI == EPI_GLU) ? ng + ngroups : 2 * ng + 1) : 0;
-
-    // the first weight chunks are requested before the activations are staged, so the two latencies overlap
-    constexpr int PQ = 4, PB = 2;
+    const int Q = (ngroups + 3) / 4;
+    const long U = (long)Q * a.C;
+    const int G = gridDim.x;
+    const long u0 = (long)blockIdx.x * U / G, u1 = (long)(blockIdx.x + 1) * U / G;
+    constexpr int P = (FMT == W_Q41 && MT == 1) ? 4 : 2;
     constexpr int TB = FMT == W_Q41 ? 640 : 2048;
-    const uint8_t *base0 = a.img + ((size_t)nt0 * a.C + c0) * TB;
-    const uint8_t *base1 = a.img + ((size_t)nt1 * a.C + c0) * TB;
-    uint4 nb[PQ][2], sc[PQ][2];
-    uint4 w[PB][2][4];
-    if (active) {
+
+    auto tiles = [&](int q, int &nt0, int &nt1, int &ng) {
+        ng = 4 * q + gq;
+        const int ngc = ng < ngroups ? ng : ngroups - 1;   // an idle warp of the last quad reads valid memory
+        nt0 = (EPI == EPI_GLU) ? ngc : 2 * ngc;
+        nt1 = (EPI == EPI_GLU) ? ngc + ngroups : 2 * ngc + 1;
+    };
+    uint4 nb[P][2], sc[P][2];
+    uint4 w[P][2][4];
+    auto load = [&](int q, int c, int p) {
+        int nt0, nt1, ng;
+        tiles(q, nt0, nt1, ng);
+        const uint8_t *b0 = a.img + ((size_t)nt0 * a.C + c) * TB;
+        const uint8_t *b1 = a.img + ((size_t)nt1 * a.C + c) * TB;
         if (FMT == W_Q41) {
-#pragma unroll
-            for (int p = 0; p < PQ; ++p)
-                if (p < nch) {
-                    nb[p][0] = ldg_stream(base0 + p * 640 + 16 * lane);
-                    nb[p][1] = ldg_stream(base1 + p * 640 + 16 * lane);
-                    sc[p][0] = ldg_stream(base0 + p * 640 + 512 + 16 * g);
-                    sc[p][1] = ldg_stream(base1 + p * 640 + 512 + 16 * g);
-                }
+            nb[p][0] = ldg_stream(b0 + 16 * lane);
+            nb[p][1] = ldg_stream(b1 + 16 * lane);
+            sc[p][0] = ldg_stream(b0 + 512 + 16 * g);
+            sc[p][1] = ldg_stream(b1 + 512 + 16 * g);
         } else {
 #pragma unroll
-            for (int p = 0; p < PB; ++p)
-                if (p < nch)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        w[p][0][ks] = ldg_stream(base0 + p * 2048 + 512 * ks + 16 * lane);
-                        w[p][1][ks] = ldg_stream(base1 + p * 2048 + 512 * ks + 16 * lane);
-                    }
+            for (int ks = 0; ks < 4; ++ks) {
+                w[p][0][ks] = ldg_stream(b0 + 512 * ks + 16 * lane);
+                w[p][1][ks] = ldg_stream(b1 + 512 * ks + 16 * lane);
+            }
         }
-    }
-    pdl_wait();          // the activations are written by the previous kernel
+    };
+    // sub-range [qs, qe) of quad q: this warp's chunks are c0, c0 + 4, ... < ce
+    auto my_first = [&](long qs) -> int { const int ca = int(qs % a.C); return ca + ((par - ca) % 4 + 4) % 4; };
+    auto sub_end = [&](long qs) -> long {
+        const long e = (qs / a.C + 1) * a.C;
+        return e < u1 ? e : u1;
+    };
+    auto prefetch = [&](long qs) {   // the first P units of the sub-range starting at qs
+        if (qs >= u1) return;
+        const int q = int(qs / a.C);
+        const int ce = int(sub_end(qs) - (long)q * a.C);
+        const int c0 = my_first(qs);
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            if (c0 + 4 * p < ce) load(q, c0 + 4 * p, p);
+    };
+    // weights are immutable: the first loads are issued before the previous kernel has finished
+    prefetch(u0);
+    pdl_wait();
     pdl_trigger();
-    stage_raw<XIN>(raw, a, a.x_row0, c0, nch);
-    __syncthreads();
-    stage_frags<MT, XIN>(xs, sums, raw, a, nch, FMT == W_Q41);
-    __syncthreads();
-    if (!active) return;
 
     float acc[2][MT][4];
+    auto zero = [&]() {
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int tt = 0; tt < MT; ++tt) acc[j][tt][0] = acc[j][tt][1] = acc[j][tt][2] = acc[j][tt][3] = 0.f;
-
-    if (FMT == W_Q41) {
-        for (int cb = 0; cb < nch; cb += PQ) {
+            for (int tt = 0; tt < MT; ++tt) acc[j][tt][0] = acc[j][tt][1] = acc[j][tt][2] = acc[j][tt][3] = 0.f;
+    };
+    zero();
+    for (long qs = u0; qs < u1;) {
+        const int q = int(qs / a.C);
+        const long qe = sub_end(qs);
+        const int ce = int(qe - (long)q * a.C);
+        const int c0 = my_first(qs);
+        const int nmine = c0 < ce ? (ce - c0 + 3) / 4 : 0;
+        for (int ib = 0; ib < nmine; ib += P) {
 #pragma unroll
-            for (int p = 0; p < PQ; ++p) {
-                const int cc = cb + p;
-                if (cc < nch) {
-                    q41_chunk<MT, XIN>(acc, nb[p], sc[p], xs, sums, cc, lane);
-                    const int nx = cc + PQ;
-                    if (nx < nch) {
-                        nb[p][0] = ldg_stream(base0 + (size_t)nx * 640 + 16 * lane);
-                        nb[p][1] = ldg_stream(base1 + (size_t)nx * 640 + 16 * lane);
-                        sc[p][0] = ldg_stream(base0 + (size_t)nx * 640 + 512 + 16 * g);
-                        sc[p][1] = ldg_stream(base1 + (size_t)nx * 640 + 512 + 16 * g);
-                    }
+            for (int p = 0; p < P; ++p) {
+                const int i = ib + p;
+                if (i < nmine) {
+                    const int c = c0 + 4 * i;
+                    if (FMT == W_Q41) q41_unit<MT>(acc, nb[p], sc[p], a, c, lane);
+                    else bf16_unit<MT>(acc, w[p], a, c, lane);
+                    if (i + P < nmine) load(q, c + 4 * P, p);
                 }
             }
         }
-    } else {
-        for (int cb = 0; cb < nch; cb += PB) {
-#pragma unroll
-            for (int p = 0; p < PB; ++p) {
-                const int cc = cb + p;
-                if (cc < nch) {
-                    bf16_chunk<MT, XIN>(acc, w[p], xs, cc, lane);
-                    const int nx = cc + PB;
-                    if (nx < nch)
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            w[p][0][ks] = ldg_stream(base0 + (size_t)nx * 2048 + 512 * ks + 16 * lane);
-                            w[p][1][ks] = ldg_stream(base1 + (size_t)nx * 2048 + 512 * ks + 16 * lane);
-                        }
-                }
-            }
-        }
-    }
-
-    if (a.S > 1) {
-        const int t = lane & 3;
-        float *P0 = a.part + (size_t)s * a.M * a.N;
+        // the next sub-range's first weights stream while this quad is reduced
+        prefetch(qe);
+        // add the four parities
+        float *mine = red[par][gq];
 #pragma unroll
         for (int tt = 0; tt < MT; ++tt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int tok = 8 * tt + 2 * t + (i & 1);
-                if (tok >= a.M) continue;
-                const int r = g + 8 * (i >> 1);
-                P0[(long)tok * a.N + 16 * nt0 + r] = acc[0][tt][i];
-                P0[(long)tok * a.N + 16 * nt1 + r] = acc[1][tt][i];
+                const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
+                mine[tok * 32 + r] = acc[0][tt][i];
+                mine[tok * 32 + 16 + r] = acc[1][tt][i];
             }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = (atomicAdd(a.cnt + ng, 1) == a.S - 1);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (!last) return;
-        __threadfence();
+        __syncthreads();
+        const long qa = (long)q * a.C;
+        const int first = int(cta_of(qa, U, G)), last = int(cta_of(qa + a.C - 1, U, G));
+        const int nseg = last - first + 1, seg = blockIdx.x - first;
+        const int ng = 4 * q + gq;
+        if (nseg > 1) {
+            // this CTA's partial of the quad: 4 groups x 16 rows x 32 columns, summed over parities
+            for (int e = threadIdx.x; e < 4 * kMaxRows * 32; e += blockDim.x) {
+                const int gg = e / (kMaxRows * 32), rc = e % (kMaxRows * 32);
+                if (4 * q + gg < ngroups) {
+                    const float v = ((red[0][gg][rc] + red[1][gg][rc]) + red[2][gg][rc]) + red[3][gg][rc];
+                    a.part[((size_t)(4 * q + gg) * a.maxseg + seg) * (kMaxRows * 32) + rc] = v;
+                }
+            }
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) s_last = (atomicAdd(a.cnt + q, 1) == nseg - 1);
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                // every thread adds its elements over the segments, in segment order
+                for (int e = threadIdx.x; e < 4 * kMaxRows * 32; e += blockDim.x) {
+                    const int gg = e / (kMaxRows * 32), rc = e % (kMaxRows * 32);
+                    float v = 0.f;
+                    if (4 * q + gg < ngroups) {
+                        const float *pp = a.part + (size_t)(4 * q + gg) * a.maxseg * (kMaxRows * 32) + rc;
+                        float l[16];
 #pragma unroll
-        for (int tt = 0; tt < MT; ++tt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = 8 * tt + 2 * t + (i & 1);
-                if (tok >= a.M) continue;
-                const int r = g + 8 * (i >> 1);
-                float v0 = 0.f, v1 = 0.f;
-                const float *Pb = a.part + (long)tok * a.N;
-                const size_t stride = (size_t)a.M * a.N;
-                int s2 = 0;
-                for (; s2 + 8 <= a.S; s2 += 8) {
-                    float u0[8], u1[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        u0[q] = __ldcg(Pb + (s2 + q) * stride + 16 * nt0 + r);
-                        u1[q] = __ldcg(Pb + (s2 + q) * stride + 16 * nt1 + r);
+                        for (int s2 = 0; s2 < 16; ++s2) l[s2] = s2 < nseg ? __ldcg(pp + s2 * (kMaxRows * 32)) : 0.f;
+                        for (int s2 = 0; s2 < nseg && s2 < 16; ++s2) v += l[s2];
+                        for (int s2 = 16; s2 < nseg; ++s2) v += __ldcg(pp + s2 * (kMaxRows * 32));
                     }
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v0 += u0[q], v1 += u1[q];
+                    red[0][gg][rc] = v;
                 }
-                for (; s2 < a.S; ++s2) {
-                    v0 += __ldcg(Pb + s2 * stride + 16 * nt0 + r);
-                    v1 += __ldcg(Pb + s2 * stride + 16 * nt1 + r);
-                }
-                acc[0][tt][i] = v0;
-                acc[1][tt][i] = v1;
+                if (threadIdx.x == 0) a.cnt[q] = 0;
             }
-        if (lane == 0) a.cnt[ng] = 0;
+            __syncthreads();
+        } else {
+            for (int e = threadIdx.x; e < 4 * kMaxRows * 32; e += blockDim.x) {
+                const int gg = e / (kMaxRows * 32), rc = e % (kMaxRows * 32);
+                red[0][gg][rc] = ((red[0][gg][rc] + red[1][gg][rc]) + red[2][gg][rc]) + red[3][gg][rc];
+            }
+            __syncthreads();
+        }
+        const bool fin = nseg == 1 || s_last;
+        if (fin && par == 0 && ng < ngroups) {
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
+                    acc[0][tt][i] = red[0][gq][tok * 32 + r];
+                    acc[1][tt][i] = red[0][gq][tok * 32 + 16 + r];
+                }
+            int nt0, nt1, ngx;
+            tiles(q, nt0, nt1, ngx);
+            epilogue<MT, EPI>(a, acc, nt0, nt1, ng, lane);
+        }
+        __syncthreads();   // red is reused by the next quad
+        zero();
+        if (threadIdx.x == 0) s_last = 0;
+        qs = qe;
     }
-    epilogue<MT, EPI>(a, acc, nt0, nt1, ng, lane);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -439,27 +451,7 @@ __global__ void __launch_bounds__(128) k_gemm(GemmArgs a) {
 // ---------------------------------------------------------------------------------------------------
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-template <int MT>
-__device__ __forceinline__ void stage_head_x(uint32_t *xs, const GemmArgs &a) {
-    for (int e = threadIdx.x; e < a.C * MT * 4 * 32; e += blockDim.x) {
-        const int L = e & 31, ks = (e >> 5) & 3, tt = (e >> 7) % MT, cc = (e >> 7) / MT;
-        const int tok = 8 * tt + (L >> 2), tq = L & 3;
-        const int k = 64 * cc + 16 * ks + 2 * tq;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (tok < a.M) {
-            const float *xr = reinterpret_cast<const float *>(a.x) + (long)(a.x_row0 + tok) * a.ldx;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int kk = k + 8 * hh;
-                const float2 v = kk < a.K ? *reinterpret_cast<const float2 *>(xr + kk) : make_float2(0.f, 0.f);
-                const uint16_t h0 = f32_to_bf16(v.x), h1 = f32_to_bf16(v.y);
-                w[hh] = pack_bf16x2(h0, h1);
-                w[2 + hh] = pack_bf16x2(f32_to_bf16(v.x - bf16_to_f32(h0)), f32_to_bf16(v.y - bf16_to_f32(h1)));
-            }
-        }
-        *reinterpret_cast<uint4 *>(xs + (size_t)e * 4) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
+constexpr int kHeadPad = 64;   // bytes added per staged row: conflict-free 16-byte fragment reads
 
 template <int MT>
 __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
@@ -468,7 +460,8 @@ __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
     __shared__ int widx[kWarpsPerCta][kMaxRows];
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
+    const int rowb = a.K * 4 + kHeadPad;
+    const int K16 = a.K / 16;
 
     const int ntiles = a.N / 16;
     const int gw = blockIdx.x * kWarpsPerCta + warp, nw = gridDim.x * kWarpsPerCta;
@@ -498,11 +491,20 @@ __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
 #pragma unroll
     for (int p = 0; p < P; ++p)
         if (p < units) load(p, w[p]);
-    // the activations are staged while the first weight chunks are in flight
     pdl_wait();
     pdl_trigger();
-    stage_head_x<MT>(xs, a);
+    // stage the activation fragments of all rows (one asynchronous copy round trip)
+    for (int e = threadIdx.x; e < MT * 8 * K16 * 4; e += blockDim.x) {
+        const int tok = e / (K16 * 4), rest = e % (K16 * 4);
+        uint8_t *dst = smem + tok * rowb + rest * 16;
+        if (tok < a.M)
+            cp_async16(dst, reinterpret_cast<const uint8_t *>(a.xf) + ((long)(a.x_row0 + tok) * K16 * 4 + rest) * 16);
+        else
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_wait_all();
     __syncthreads();
+
     float acc[2][MT][4];
     for (int ub = 0; ub < units; ub += P) {
 #pragma unroll
@@ -516,7 +518,21 @@ __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
 #pragma unroll
                         for (int tt = 0; tt < MT; ++tt) acc[j][tt][0] = acc[j][tt][1] = acc[j][tt][2] = acc[j][tt][3] = 0.f;
                 }
-                bf16_chunk<MT, 1>(acc, w[p], xs, c, lane);
+                const uint4 (&wv)[2][4] = w[p];
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    uint4 b[MT];
+#pragma unroll
+                    for (int tt = 0; tt < MT; ++tt)
+                        b[tt] = *reinterpret_cast<const uint4 *>(smem + (8 * tt + g) * rowb + ((4 * c + ks) * 4 + t) * 16);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int tt = 0; tt < MT; ++tt) {
+                            mma_bf16(acc[j][tt], wv[j][ks].x, wv[j][ks].y, wv[j][ks].z, wv[j][ks].w, b[tt].x, b[tt].y);
+                            mma_bf16(acc[j][tt], wv[j][ks].x, wv[j][ks].y, wv[j][ks].z, wv[j][ks].w, b[tt].z, b[tt].w);
+                        }
+                }
                 if (u + P < units) load(u + P, w[p]);
                 if (c == a.C - 1) {
 #pragma unroll
@@ -597,60 +613,42 @@ __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
 // ---------------------------------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------------------------------
-int gemm_splits(int C, int N, int fmt) {
-    (void)fmt;
-    const int ngroups = N / 32;
-    int S = (kSplitTargetWarps + ngroups - 1) / ngroups;
-    const int smin = (C + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit;   // bound shared memory
-    const int smax = C / 4 > 0 ? C / 4 : 1;                                // at least 4 chunks a warp
-    if (S > smax) S = smax;
-    if (S < smin) S = smin;
-    if (S < 1) S = 1;
-    if (S > C) S = C;
-    return S;
+// Grid of a product: one CTA per SM at most, and at least four units (chunks of a quad) per CTA.
+int gemm_grid(int C, int N) {
+    const long Q = (N / 32 + 3) / 4;
+    const long U = Q * C;
+    long G = 152;
+    if (G > U / 4) G = U / 4;
+    return int(G < 1 ? 1 : G);
 }
 
-size_t gemm_scratch_floats(int S, int M, int N) { return S > 1 ? (size_t)S * M * N : 0; }
-
-size_t gemm_smem(int C, int S, int MT, int XIN, int fmt, int M) {
-    (void)fmt;
-    const int maxch = (C + S - 1) / S;
-    return (size_t)maxch * MT * 4 * 32 * (XIN ? 16 : 8) + (size_t)maxch * 128 + (size_t)M * maxch * 64 * (XIN ? 4 : 2);
+int gemm_maxseg(int C, int N) {
+    const int G = gemm_grid(C, N);
+    const long Q = (N / 32 + 3) / 4;
+    const long U = Q * C;
+    int mx = 1;
+    for (long q = 0; q < Q; ++q) {
+        const long a0 = ((q * C + 1) * G - 1) / U, a1 = ((q * C + C) * G - 1) / U;
+        mx = std::max(mx, int(a1 - a0 + 1));
+    }
+    return mx;
 }
 
-template <int FMT, int MT, int EPI, int XIN>
+size_t gemm_scratch_floats(int C, int N) {
+    const int ms = gemm_maxseg(C, N);
+    return ms > 1 ? (size_t)(N / 32) * ms * kMaxRows * 32 : 0;
+}
+
+template <int FMT, int MT, int EPI>
 static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    const size_t smem = gemm_smem(a.C, a.S, MT, XIN, FMT, a.M);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm<FMT, MT, EPI, XIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    const int ngroups = a.N / 32;
-    dim3 grid((ngroups + kWarpsPerCta - 1) / kWarpsPerCta, a.S);
-    return launch_pdl(k_gemm<FMT, MT, EPI, XIN>, grid, dim3(128), smem, s, a);
+    return launch_pdl(k_gemm<FMT, MT, EPI>, dim3(gemm_grid(a.C, a.N)), dim3(kGemmWarps * 32), 0, s, a);
 }
 
-template <int MT>
-static cudaError_t run_head(const GemmArgs &a, cudaStream_t s) {
-    const size_t smem = (size_t)a.C * MT * 2048;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_head<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    const int per_sm = smem <= 48 * 1024 ? 4 : (smem <= 100 * 1024 ? 2 : 1);
-    int grid = 152 * per_sm;
-    const int ntiles = a.N / 16;
-    if (grid * kWarpsPerCta > ntiles) grid = (ntiles + kWarpsPerCta - 1) / kWarpsPerCta;
-    return launch_pdl(k_head<MT>, dim3(grid), dim3(128), smem, s, a);
-}
+size_t head_smem(int K, int MT) { return (size_t)MT * 8 * (K * 4 + kHeadPad); }
 
 int head_grid(int C, int M, int N) {
     const int MT = M > 8 ? 2 : 1;
-    const size_t smem = (size_t)C * MT * 2048;
+    const size_t smem = head_smem(C * 64, MT);
     const int per_sm = smem <= 48 * 1024 ? 4 : (smem <= 100 * 1024 ? 2 : 1);
     int grid = 152 * per_sm;
     const int ntiles = N / 16;
@@ -658,16 +656,27 @@ int head_grid(int C, int M, int N) {
     return grid;
 }
 
-cudaError_t launch_gemm(int fmt, int epi, int xin, const GemmArgs &a, cudaStream_t s) {
+template <int MT>
+static cudaError_t run_head(const GemmArgs &a, cudaStream_t s) {
+    const size_t smem = head_smem(a.K, MT);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_head<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    return launch_pdl(k_head<MT>, dim3(head_grid(a.C, a.M, a.N)), dim3(128), smem, s, a);
+}
+
+cudaError_t launch_gemm(int fmt, int epi, const GemmArgs &a, cudaStream_t s) {
     const bool two = a.M > 8;
     if (epi == EPI_ARGMAX) return two ? run_head<2>(a, s) : run_head<1>(a, s);
-#define DFL_GEMM_CASE(F, E, X)                                                      \
-    if (fmt == F && epi == E && xin == X) return two ? run_gemm<F, 2, E, X>(a, s) : run_gemm<F, 1, E, X>(a, s);
-    DFL_GEMM_CASE(W_Q41, EPI_F32, 1)
-    DFL_GEMM_CASE(W_Q41, EPI_GLU, 1)
-    DFL_GEMM_CASE(W_Q41, EPI_SILU_MUL, 1)
-    DFL_GEMM_CASE(W_BF16, EPI_F32, 1)
-    DFL_GEMM_CASE(W_Q41, EPI_F32, 0)
+#define DFL_GEMM_CASE(F, E) \
+    if (fmt == F && epi == E) return two ? run_gemm<F, 2, E>(a, s) : run_gemm<F, 1, E>(a, s);
+    DFL_GEMM_CASE(W_Q41, EPI_F32)
+    DFL_GEMM_CASE(W_Q41, EPI_GLU)
+    DFL_GEMM_CASE(W_Q41, EPI_SILU_MUL)
+    DFL_GEMM_CASE(W_BF16, EPI_F32)
 #undef DFL_GEMM_CASE
     return cudaErrorInvalidValue;
 }

@@ -126,8 +126,7 @@ __global__ void __launch_bounds__(kRowThreads) k_rows(RowArgs a) {
             if (i < per && h < a.H) tp[h] = xv[i];
         }
     }
-    if (a.out) {
-        float *o = a.out + (long)m * a.ld_out;
+    if (a.outf) {
         float r = 1.f;
         if (a.w_next) {
             float ss = 0.f;
@@ -135,26 +134,30 @@ __global__ void __launch_bounds__(kRowThreads) k_rows(RowArgs a) {
             for (int i = 0; i < kRowMaxPer; ++i) ss += xv[i] * xv[i];
             r = 1.0f / sqrtf(block_sum(ss, red) / a.H + a.eps);
         }
+        const int row = a.out_row0 + m;
 #pragma unroll
         for (int i = 0; i < kRowMaxPer; ++i) {
+            if (i >= per) break;
             const int h = threadIdx.x + i * kRowThreads;
-            if (i < per && h < a.H) {
-                const float v = a.w_next ? (xv[i] * r) * bf16_to_f32(a.w_next[h]) : xv[i];
-                o[h] = live ? v : 0.f;
-            }
+            float v = 0.f;
+            if (h < a.H && live) v = a.w_next ? (xv[i] * r) * bf16_to_f32(a.w_next[h]) : xv[i];
+            if (h < a.H) act_store(a.outf, a.H, row, h, v);
+            const float sg = half_warp_sum(v);
+            if (h < a.H && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = sg;
         }
     }
 }
 
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
-    if (a.H > kRowThreads * kRowMaxPer) return cudaErrorInvalidValue;
+    if (a.H > kRowThreads * kRowMaxPer || a.H % 16) return cudaErrorInvalidValue;
     return launch_pdl(k_rows, dim3(a.M), dim3(kRowThreads), 0, s, a);
 }
 
-// dst[m] = RMSNorm(src[m], w) for live rows (m < st->ctx_rows when live_from_ctx), zeros else.
+// dst row (row0 + m) = RMSNorm(src[m], w) for live rows (m < st->ctx_rows when live_from_ctx), zeros
+// otherwise, in operand format.
 __global__ void __launch_bounds__(kRowThreads) k_cast_rows(const float *src, int ld_src, int H, const uint16_t *w,
-                                                           float eps, float *dst, int ld_dst, const DevState *st,
-                                                           int live_from_ctx) {
+                                                           float eps, uint32_t *dstf, float *dsts, int row0,
+                                                           const DevState *st, int live_from_ctx) {
     pdl_wait();
     pdl_trigger();
     __shared__ float red[33];
@@ -172,15 +175,21 @@ __global__ void __launch_bounds__(kRowThreads) k_cast_rows(const float *src, int
     const float r = 1.0f / sqrtf(block_sum(ss, red) / H + eps);
 #pragma unroll
     for (int i = 0; i < kRowMaxPer; ++i) {
+        if (i >= per) break;
         const int h = threadIdx.x + i * kRowThreads;
-        if (i < per && h < H) dst[(long)m * ld_dst + h] = live ? (v[i] * r) * bf16_to_f32(w[h]) : 0.f;
+        const float o = (h < H && live) ? (v[i] * r) * bf16_to_f32(w[h]) : 0.f;
+        if (h < H) act_store(dstf, H, row0 + m, h, o);
+        const float sg = half_warp_sum(o);
+        if (h < H && (h & 15) == 0) dsts[(h >> 4) * kMaxRows + row0 + m] = sg;
     }
 }
 
 cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const uint16_t *w_norm, float eps,
-                             float *dst, int ld_dst, const DevState *st, int live_from_ctx, cudaStream_t s) {
-    if (H > kRowThreads * kRowMaxPer) return cudaErrorInvalidValue;
-    return launch_pdl(k_cast_rows, dim3(M), dim3(kRowThreads), 0, s, src, ld_src, H, w_norm, eps, dst, ld_dst, st, live_from_ctx);
+                             uint32_t *dstf, float *dsts, int row0, const DevState *st, int live_from_ctx,
+                             cudaStream_t s) {
+    if (H > kRowThreads * kRowMaxPer || H % 16) return cudaErrorInvalidValue;
+    return launch_pdl(k_cast_rows, dim3(M), dim3(kRowThreads), 0, s, src, ld_src, H, w_norm, eps, dstf, dsts, row0, st,
+                      live_from_ctx);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -369,7 +378,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                     den = fmaf(__ldcg(a.part_ml + b * 2 + 1), f, den);
                     num = fmaf(__ldcg(a.part_acc + b * hd + d), f, num);
                 }
-                a.out[(long)m * a.nq * hd + (long)h * hd + d] = num / den;
+                const float o = num / den;
+                const int col = h * hd + d;
+                act_store(a.outf, a.nq * hd, m, col, o);
+                const float sg = half_warp_sum(o);
+                if ((col & 15) == 0) a.outs[(col >> 4) * kMaxRows + m] = sg;
             }
             if (tid == 0) a.cnt[h] = 0;
         }
@@ -385,7 +398,7 @@ cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    if (a.hd % 32 || a.M > kMaxRows || a.nB > kAttnChunk) return cudaErrorInvalidValue;
+    if (a.hd % 32 || a.M > kMaxRows || a.nB > kAttnChunk || (a.M * a.hd) % 32) return cudaErrorInvalidValue;
     return launch_pdl(k_attn, dim3(grid), dim3(kAttnThreads), attn_smem(a.M, a.hd), s, a);
 }
 
@@ -509,20 +522,20 @@ cudaError_t launch_rope_table(float2 *tab, int max_pos, int hd, double base, cud
 
 namespace dfl {
 
-// dst[m] = taps row of position st->draft_n + m for m < st->ctx_rows, zeros for the other rows.
-__global__ void k_copy_taps(const float *taps, int ld, const DevState *st, float *dst, int ld_dst) {
+// dst row m = taps row of position st->draft_n + m for m < st->ctx_rows, zeros for the other rows, in
+// operand format (the fc product is bf16-weighted: no sums needed).
+__global__ void k_copy_taps(const float *taps, int ld, const DevState *st, uint32_t *dstf) {
     pdl_wait();
     pdl_trigger();
     const int m = blockIdx.x;
     const bool live = m < st->ctx_rows;
     const float *src = taps + (long)(st->draft_n + (live ? m : 0)) * ld;
-    float *d = dst + (long)m * ld_dst;
-    for (int i = threadIdx.x; i < ld; i += blockDim.x) d[i] = live ? src[i] : 0.f;
+    for (int i = threadIdx.x; i < ld; i += blockDim.x) act_store(dstf, ld, m, i, live ? src[i] : 0.f);
 }
 
-cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, float *dst, int ld_dst,
-                             cudaStream_t s) {
-    return launch_pdl(k_copy_taps, dim3(M), dim3(256), 0, s, taps, ld, st, dst, ld_dst);
+cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, uint32_t *dstf, cudaStream_t s) {
+    if (ld % 16) return cudaErrorInvalidValue;
+    return launch_pdl(k_copy_taps, dim3(M), dim3(256), 0, s, taps, ld, st, dstf);
 }
 
 }  // namespace dfl

@@ -189,9 +189,8 @@ int dfl_read_taps(dfl_ctx *ctx, int pos0, int rows, float *host_dst);
 int dfl_draft_append_taps(dfl_ctx *ctx, const void *dev_taps, int rows);
 
 /* Inspection: copy the first `bytes` of an internal buffer of the last pass to host memory. Names:
- * "x" [16][hidden] residual rows, "h" [16][hidden] next product input, "y" [16][hidden] last projection
- * output, "qkv" [16][width], "q" [16][heads*head_dim] (normed, rotated), "o" [16][heads*head_dim]
- * attention output, "x_d" [16][hidden] draft residual rows; all fp32. */
+ * "x" [16][hidden] residual rows, "y" [16][hidden] last projection output, "qkv" [16][width],
+ * "q" [16][heads*head_dim] (normed, rotated), "x_d" [16][hidden] draft residual rows; all fp32. */
 int dfl_debug_read(dfl_ctx *ctx, const char *name, void *host_dst, size_t bytes);
 
 /* Planted drafts (measurement workloads that control acceptance): after dfl_draft_block, replace its
@@ -217,14 +216,19 @@ void dfl_destroy(dfl_ctx *ctx);
 int64_t dfl_q41_image_bytes(int K, int N);
 /* Pack a container-layout Q4_1 matrix (DEVICE) into the tile image (DEVICE). */
 int dfl_q41_pack(const void *dev_src, int K, int N, void *dev_image, void *cuda_stream);
+/* Bytes of an activation operand buffer for up to 16 rows of K inputs (K % 16 == 0). */
+int64_t dfl_act_bytes(int M, int K);
+/* Pack fp32 rows x (DEVICE [M][K]) into an activation operand buffer (DEVICE, dfl_act_bytes): bf16
+ * hi + lo fragments in the order the tensor cores consume them, and per-16-input sums. */
+int dfl_act_pack(const float *dev_x, int M, int K, void *dev_act, void *cuda_stream);
 /* Scratch bytes dfl_q41_gemm needs for K, N, M. */
 int64_t dfl_q41_gemm_scratch_bytes(int K, int N, int M);
-/* y[m][n] = sum_k x[m][k] * w[k][n] (fp32), x bf16 DEVICE [M][K], y fp32 DEVICE [M][N], from the tile
- * image; M in 1..16; N a multiple of 32. The scratch (DEVICE, >= dfl_q41_gemm_scratch_bytes) holds
- * arrival counters (first N/32 ints) and split-K partial sums; it must be zeroed once before the first
- * call (each call leaves the counters zero). Calls on one scratch must not overlap on the GPU. The
- * result does not depend on M (fixed reduction order). */
-int dfl_q41_gemm(const void *dev_image, int K, int N, const void *dev_x, int M, float *dev_y,
+/* y[m][n] = sum_k x[m][k] * w[k][n] (fp32), x given as an activation operand buffer (DEVICE, from
+ * dfl_act_pack), y fp32 DEVICE [M][N], from the tile image; M in 1..16; N a multiple of 32. The
+ * scratch (DEVICE, >= dfl_q41_gemm_scratch_bytes) holds arrival counters (first N/32 ints) and partial
+ * sums; it must be zeroed once before the first call (each call leaves the counters zero). Calls on
+ * one scratch must not overlap on the GPU. A row's result does not depend on M. */
+int dfl_q41_gemm(const void *dev_image, int K, int N, const void *dev_act, int M, float *dev_y,
                  void *dev_scratch, size_t scratch_bytes, void *cuda_stream);
 
 #ifdef __cplusplus

@@ -23,6 +23,7 @@ def torch_cuda():
 # the Q4_1 product on its own
 # ---------------------------------------------------------------------------------------------------
 def _gemm(torch, W, x_bits, K, N):
+    """Pack W, pack the (bf16-valued) activations into the operand format, run the product."""
     from dflash_speculative_decode_gb300 import _abi
     L = _abi.lib()
     M = x_bits.shape[0]
@@ -31,11 +32,13 @@ def _gemm(torch, W, x_bits, K, N):
     img = torch.empty(L.dfl_q41_image_bytes(K, N), dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream().cuda_stream
     assert L.dfl_q41_pack(ctypes.c_void_p(src.data_ptr()), K, N, ctypes.c_void_p(img.data_ptr()), ctypes.c_void_p(st)) == 0
-    x = torch.from_numpy(x_bits.view(np.int16).copy()).to(dev)
+    x = torch.from_numpy(oracle.bf16_decode(x_bits)).to(dev)
+    act = torch.empty(L.dfl_act_bytes(M, K), dtype=torch.uint8, device=dev)
+    assert L.dfl_act_pack(ctypes.c_void_p(x.data_ptr()), M, K, ctypes.c_void_p(act.data_ptr()), ctypes.c_void_p(st)) == 0
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     sb = L.dfl_q41_gemm_scratch_bytes(K, N, M)
-    scratch = torch.zeros(sb, dtype=torch.uint8, device=dev)
-    rc = L.dfl_q41_gemm(ctypes.c_void_p(img.data_ptr()), K, N, ctypes.c_void_p(x.data_ptr()), M,
+    scratch = torch.zeros(max(sb, 256), dtype=torch.uint8, device=dev)
+    rc = L.dfl_q41_gemm(ctypes.c_void_p(img.data_ptr()), K, N, ctypes.c_void_p(act.data_ptr()), M,
                         ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(scratch.data_ptr()), sb, ctypes.c_void_p(st))
     assert rc == 0
     torch.cuda.synchronize()
