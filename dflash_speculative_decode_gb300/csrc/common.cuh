@@ -65,16 +65,14 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two 4-bit codes of a packed word -> a bf16x2 register holding the codes exactly: bits [0, 4) and
-// [16, 20) of w become the low and high bf16. 0x4300 is bf16 128.0 whose last mantissa bit is worth 1,
-// so (0x4300 | q) is 128 + q; subtracting 128 leaves q exactly.
+// Two 4-bit codes of a packed word -> a bf16x2 register holding 128 + q exactly: bits [0, 4) and
+// [16, 20) of w become the low and high bf16. 0x4300 is bf16 128.0, whose last mantissa bit is worth 1,
+// so (0x4300 | q) is 128 + q. A product over such codes carries 128 * sum(x), which the Q4_1 minimum
+// term takes back (m - 128 d).
 __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w) {
     uint32_t r;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r);
-    const __nv_bfloat162 off = __floats2bfloat162_rn(128.0f, 128.0f);
-    v = __hsub2(v, off);
-    return *reinterpret_cast<uint32_t *>(&v);
+    return r;
 }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization may start
@@ -91,6 +89,9 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most one committed group of this thread is still in flight
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // ---- activation operand format ---------------------------------------------------------------------
 // An activation matrix of up to 16 rows and K inputs (K % 16 == 0) that feeds a product is stored as
@@ -98,8 +99,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.com
 // 2^-17 relative). Row tok, 16-input group kb, lane column t = 0..3 own 16 bytes at word
 // ((tok * K/16 + kb) * 4 + t) * 4: {hi(2t, 2t+1), hi(2t+8, 2t+9), lo(2t, 2t+1), lo(2t+8, 2t+9)},
 // inputs counted within the group, the lower input in the low half. Beside it, sums[kb * 16 + tok]
-// holds the fp32 sum of the row's 16 inputs of group kb (the Q4_1 minimum term).
-// act_store writes one element and returns hi + lo.
+// holds the fp32 sum of hi + lo over the row's 16 inputs of group kb (the Q4_1 minimum term); the
+// product then computes exactly sum_k (hi_k + lo_k) w_k.
+// act_store writes one element and returns hi + lo, the value the sums add.
 __device__ __forceinline__ float act_store(uint32_t *f, int K, int tok, int k, float v) {
     const int r = k & 15, t = (r & 7) >> 1, w = r >> 3, half = r & 1;
     uint16_t *p = reinterpret_cast<uint16_t *>(f + (((long)tok * (K >> 4) + (k >> 4)) * 4 + t) * 4);
@@ -153,6 +155,7 @@ struct GemmArgs {
     const uint32_t *xf;    // activations, operand format (K inputs)
     const float *xs;       // their per-16 sums
     int x_row0;            // first activation row used
+    int slots;             // products: activation chunks staged in shared memory (set by the launcher)
     float *y;              // EPI_F32: fp32 output [M][ldy]
     int ldy;
     uint32_t *yf;          // EPI_GLU / EPI_SILU_MUL: output in operand format (N/2 or N inputs)
@@ -247,10 +250,6 @@ struct AttnArgs {
                            // 1: draft (A keys max(0,n-window)..n-1 for every row, plus all B keys)
     const DevState *st;
     float scale;
-    float *part_acc;       // [nq][max_chunks][M][hd]
-    float *part_ml;        // [nq][max_chunks][M][2]
-    int *cnt;              // [nq] arrival counters (zero between launches)
-    int max_chunks;
     uint32_t *outf;        // [M][nq*hd] in operand format
     float *outs;
 };
@@ -266,7 +265,7 @@ cudaError_t launch_set_state(DevState *st, const SetStateArgs &a, cudaStream_t s
 cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t s);
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s);
 cudaError_t launch_qk(const QkArgs &a, cudaStream_t s);
-cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s);
 cudaError_t launch_rope_table(float2 *tab, int max_pos, int hd, double base, cudaStream_t s);
 cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const uint16_t *w_norm, float eps,
@@ -292,6 +291,5 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-constexpr int kAttnChunk = 32;   // keys per attention work item
 
 }  // namespace dfl

@@ -92,6 +92,8 @@ static_assert(sizeof(SnapHeader) == 256, "header size");
 
 }  // namespace
 
+constexpr int kProfClasses = 6;
+
 struct dfl_ctx {
     dfl_config cfg{};
     cudaStream_t stream = nullptr;
@@ -108,14 +110,14 @@ struct dfl_ctx {
     int TH = 0, cap_sliding = 0, cap_draft = 0, ctx_fuse = 0;
     // workspace
     float *x = nullptr, *x_d = nullptr, *y = nullptr, *y_fc = nullptr, *qkv = nullptr, *q = nullptr;
-    float *part = nullptr, *logits = nullptr, *dlogits = nullptr, *att_acc = nullptr, *att_ml = nullptr, *am_val = nullptr;
+    float *part = nullptr, *logits = nullptr, *dlogits = nullptr, *am_val = nullptr;
     Act h, hcat, hb, o, a, z, tapbuf;
     float *kB = nullptr, *vB = nullptr;
     uint16_t *ple_rows = nullptr;
-    int *cnt = nullptr, *att_cnt = nullptr, *am_idx = nullptr, *am_cnt = nullptr, *smp_cnt = nullptr;
+    int *cnt = nullptr, *am_idx = nullptr, *am_cnt = nullptr, *smp_cnt = nullptr;
     int *counters_begin = nullptr;
     size_t counters_bytes = 0;
-    int att_max_chunks = 0, nq_max = 0, qkv_max = 0;
+    int nq_max = 0, qkv_max = 0;
     // host mirror of the state
     int n = 0, draft_n = 0, pending = 0, last_accepted = -1, draft_at = -1;
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
@@ -127,8 +129,8 @@ struct dfl_ctx {
     size_t ev_next = 0, ev_reserved = 0;          // slots [0, ev_reserved) belong to captured graphs
     struct Rec { int cls; double bytes; size_t ev; };
     std::vector<Rec> recs;                        // profiled launches not yet read
-    double prof_ms[4] = {0, 0, 0, 0}, prof_bytes[4] = {0, 0, 0, 0};
-    long long prof_n[4] = {0, 0, 0, 0};
+    double prof_ms[kProfClasses] = {}, prof_bytes[kProfClasses] = {};
+    long long prof_n[kProfClasses] = {};
     // captured passes
     bool use_graphs = true, capturing = false;
     cudaStream_t cap_stream = nullptr;
@@ -155,12 +157,16 @@ int fail(dfl_ctx *c, int code, const std::string &msg) {
         if (e_ != cudaSuccess) return fail(c, DFL_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
     } while (0)
 
-// a row/attention/control kernel launch (products count themselves)
-#define DFL_LAUNCH(call)                                                                      \
+// a kernel launch of profiling class `cls` (see prof_begin)
+#define DFL_LAUNCH_C(cls, call)                                                               \
     do {                                                                                      \
+        size_t prof_slot_ = 0;                                                                \
+        DFL_CK(prof_begin(c, &prof_slot_));                                                   \
         c->launches += 1;                                                                     \
         DFL_CK(call);                                                                         \
+        DFL_CK(prof_end(c, prof_slot_, cls, 0.0));                                            \
     } while (0)
+#define DFL_LAUNCH(call) DFL_LAUNCH_C(5, call)
 
 std::string validate(const dfl_config *g) {
     auto bad = [](const char *f) { return std::string("configuration: ") + f; };
@@ -327,9 +333,6 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     c->kB = X.take<float>((size_t)R * dkv * dhd);
     c->vB = X.take<float>((size_t)R * dkv * dhd);
     c->part = X.take<float>(std::max<size_t>(part_floats, 1));
-    c->att_max_chunks = (g.max_ctx + R + kAttnChunk - 1) / kAttnChunk + 2;
-    c->att_acc = X.take<float>((size_t)c->nq_max * c->att_max_chunks * R * hd_max);
-    c->att_ml = X.take<float>((size_t)c->nq_max * c->att_max_chunks * R * 2);
     c->am_val = X.take<float>((size_t)152 * 4 * kMaxRows);
     c->am_idx = X.take<int>((size_t)152 * 4 * kMaxRows);
     c->logits = X.take<float>((size_t)R * V);
@@ -338,7 +341,6 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     X.off = (X.off + 255) / 256 * 256;
     const size_t cbeg = X.off;
     c->cnt = X.take<int>(cnt_n);
-    c->att_cnt = X.take<int>(c->nq_max);
     c->am_cnt = X.take<int>(1);
     c->smp_cnt = X.take<int>(1);
     c->counters_begin = c->cnt;
@@ -355,9 +357,14 @@ bool is_tap(const dfl_config &g, int l, int *ti) {
 }
 
 // ---- one product -----------------------------------------------------------------------------------
-// profiled launch classes: 0 = Q4_1 products, 1 = bf16 products (fc), 2 = head
+// profiled launch classes: 0 = Q4_1 products, 1 = bf16 products (fc), 2 = head, 3 = attention,
+// 4 = q/k norm + rotation + KV store, 5 = the rest (embedding, norms, state, taps, sampling)
+// With graphs on, only launches inside captured passes are bracketed (the per-pass state kernels
+// launched between replays are not).
+constexpr size_t kNoSlot = ~size_t(0);
 cudaError_t prof_begin(dfl_ctx *c, size_t *slot) {
-    if (!c->profile) return cudaSuccess;
+    *slot = kNoSlot;
+    if (!c->profile || (c->use_graphs && !c->capturing)) return cudaSuccess;
     const size_t need = c->ev_next + 2;
     while (c->ev_pool.size() < need) {
         cudaEvent_t e;
@@ -373,7 +380,7 @@ cudaError_t prof_begin(dfl_ctx *c, size_t *slot) {
 }
 
 cudaError_t prof_end(dfl_ctx *c, size_t slot, int cls, double bytes) {
-    if (!c->profile) return cudaSuccess;
+    if (slot == kNoSlot) return cudaSuccess;
     c->recs.push_back({cls, bytes, slot});
     return c->capturing ? cudaEventRecordWithFlags(c->ev_pool[slot + 1], c->stream, cudaEventRecordExternal)
                         : cudaEventRecord(c->ev_pool[slot + 1], c->stream);
@@ -582,7 +589,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         qa.k_store = own ? L.K : nullptr;
         qa.v_store = own ? L.V : nullptr;
         qa.cap = L.cap;
-        DFL_LAUNCH(launch_qk(qa, c->stream));
+        DFL_LAUNCH_C(4, launch_qk(qa, c->stream));
         AttnArgs aa{};
         aa.M = k;
         aa.nq = nq;
@@ -596,13 +603,9 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.mode = 0;
         aa.st = c->st;
         aa.scale = 1.0f / sqrtf((float)hd);
-        aa.part_acc = c->att_acc;
-        aa.part_ml = c->att_ml;
-        aa.cnt = c->att_cnt;
-        aa.max_chunks = c->att_max_chunks;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
-        DFL_LAUNCH(launch_attn(aa, 2 * 152, c->stream));
+        DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
         DFL_CK(gemm(c, L.o, c->o, 0, k, EPI_F32, c->y, H));
         RowArgs r1 = rows(c, k, c->x);
         r1.y = c->y;
@@ -717,7 +720,7 @@ int run_ctx_only(dfl_ctx *c, int r) {
         qa.k_store = D.K;
         qa.v_store = D.V;
         qa.cap = c->cap_draft;
-        DFL_LAUNCH(launch_qk(qa, c->stream));
+        DFL_LAUNCH_C(4, launch_qk(qa, c->stream));
     }
     c->draft_n += r;
     return DFL_OK;
@@ -766,7 +769,7 @@ int draft_body(dfl_ctx *c) {
         qb.k_store = c->kB;
         qb.v_store = c->vB;
         qb.cap = 0;
-        DFL_LAUNCH(launch_qk(qb, c->stream));
+        DFL_LAUNCH_C(4, launch_qk(qb, c->stream));
         if (F > 0) {
             QkArgs qc = draft_qk(c, l);
             qc.M = F;
@@ -776,7 +779,7 @@ int draft_body(dfl_ctx *c) {
             qc.k_store = D.K;
             qc.v_store = D.V;
             qc.cap = c->cap_draft;
-            DFL_LAUNCH(launch_qk(qc, c->stream));
+            DFL_LAUNCH_C(4, launch_qk(qc, c->stream));
         }
         AttnArgs aa{};
         aa.M = B;
@@ -794,13 +797,9 @@ int draft_body(dfl_ctx *c) {
         aa.mode = 1;
         aa.st = c->st;
         aa.scale = 1.0f / sqrtf((float)dhd);
-        aa.part_acc = c->att_acc;
-        aa.part_ml = c->att_ml;
-        aa.cnt = c->att_cnt;
-        aa.max_chunks = c->att_max_chunks;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
-        DFL_LAUNCH(launch_attn(aa, 2 * 152, c->stream));
+        DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
         DFL_CK(gemm(c, D.o, c->o, 0, B, EPI_F32, c->y, H));
         RowArgs r1 = rows(c, B, c->x_d);
         r1.eps = g.d_eps;
@@ -1225,7 +1224,7 @@ int dfl_set_option(dfl_ctx *c, int option, int value) {
         c->profile = value != 0;
         c->recs.clear();
         c->ev_next = c->ev_reserved;
-        for (int i = 0; i < 4; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
+        for (int i = 0; i < kProfClasses; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
     }
     else return fail(c, DFL_E_INVALID_ARG, "unknown option");
     return DFL_OK;
@@ -1302,7 +1301,7 @@ int dfl_plant_proposals(dfl_ctx *c, const int32_t *dev_table, int table_len) {
 int64_t dfl_launch_count(const dfl_ctx *c) { return c ? c->launches : -1; }
 
 int dfl_profile_read(dfl_ctx *c, int cls, int64_t *launches, double *ms, double *bytes) {
-    if (!c || cls < 0 || cls > 2) return DFL_E_INVALID_ARG;
+    if (!c || cls < 0 || cls >= kProfClasses) return DFL_E_INVALID_ARG;
     DFL_CK(cudaStreamSynchronize(c->stream));
     DFL_CK(harvest(c, c->recs));
     c->recs.clear();

@@ -117,8 +117,7 @@ __global__ void k_act_pack(const float *x, int M, int K, uint32_t *f, float *sum
     const int k = blockIdx.x * blockDim.x + threadIdx.x;   // blockDim 256: a 16-group is one half warp
     const bool in = k < K && m < M;
     const float v = in ? x[(long)m * K + k] : 0.f;
-    if (in) act_store(f, K, m, k, v);
-    const float s = half_warp_sum(v);
+    const float s = half_warp_sum(in ? act_store(f, K, m, k, v) : 0.f);
     if (in && (k & 15) == 0) sums[(k / 16) * kMaxRows + m] = s;
 }
 
@@ -127,50 +126,87 @@ cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *su
 }
 
 // ---------------------------------------------------------------------------------------------------
-// one unit of work: a 64-input chunk of two 16-column tiles
+// activation staging: the chunks a CTA needs are copied to shared memory once (one asynchronous copy
+// round trip), so the unit loop reads its B fragments and sums from shared memory.
+// Per slot (one 64-input chunk): sums [4 groups][16 rows] fp32 (256 B), then R = 8*MT rows of 256 B
+// fragments; inside a row the four 64-byte k-steps are stored at position ks ^ (row & 1), so the two
+// rows a quarter warp reads fall on different banks.
 // ---------------------------------------------------------------------------------------------------
 template <int MT>
-__device__ __forceinline__ void load_frags(uint4 (&b)[MT][4], const GemmArgs &a, int c, int lane) {
-    const int g = lane >> 2, t = lane & 3;
+__host__ __device__ constexpr int slot_bytes() { return 256 + MT * 8 * 256; }
+template <int MT>
+__host__ __device__ constexpr int red_bytes() { return 16 * MT * 8 * 32 * 4; }   // [4 parities][4 groups][R][32]
+
+// copy the chunks of units [s0, s1) (at most `slots` distinct chunks; slot of chunk c = (c - s0 % C) mod C)
+template <int MT>
+__device__ __forceinline__ void stage_x(const GemmArgs &a, uint8_t *xs_sm, long s0, long s1) {
+    constexpr int R = MT * 8;
     const int K16 = a.K / 16;
-#pragma unroll
-    for (int tt = 0; tt < MT; ++tt) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(a.xf) + ((long)(a.x_row0 + 8 * tt + g) * K16 + 4 * c) * 4 + t;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) b[tt][ks] = (4 * c + ks < K16) ? __ldg(p + 4 * ks) : make_uint4(0u, 0u, 0u, 0u);
+    const long span = s1 - s0;
+    const int nch = int(span < a.C ? span : a.C);
+    const int cb = int(s0 % a.C);
+    const int per = 16 + R * 16;   // 16-byte pieces per slot
+    for (int e = threadIdx.x; e < nch * per; e += blockDim.x) {
+        const int slot = e / per, r = e % per;
+        const int c = (cb + slot) % a.C;
+        uint8_t *base = xs_sm + slot * slot_bytes<MT>();
+        if (r < 16) {   // sums: group 4c + r/4, rows 4*(r%4) .. +3
+            const int kb = 4 * c + (r >> 2);
+            uint8_t *dst = base + 16 * r;
+            if (kb < K16) cp_async16(dst, a.xs + kb * kMaxRows + 4 * (r & 3));
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            const int rr = r - 16, tok = rr >> 4, ks = (rr >> 2) & 3, t = rr & 3;
+            const int kb = 4 * c + ks;
+            uint8_t *dst = base + 256 + tok * 256 + ((ks ^ (tok & 1)) * 4 + t) * 16;
+            if (kb < K16)
+                cp_async16(dst, a.xf + (((long)(a.x_row0 + tok) * K16 + kb) * 4 + t) * 4);
+            else
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
+    cp_async_wait_all();
 }
 
+// B fragment (hi in .x/.y, lo in .z/.w) of k-step ks for rows 8*tt + g
+__device__ __forceinline__ uint4 frag(const uint8_t *slot, int tt, int ks, int g, int t) {
+    const int tok = 8 * tt + g;
+    return *reinterpret_cast<const uint4 *>(slot + 256 + tok * 256 + ((ks ^ (tok & 1)) * 4 + t) * 16);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// one unit of work: a 64-input chunk of two 16-column tiles
+// ---------------------------------------------------------------------------------------------------
+// Q4_1: the codes enter the tensor cores as 128 + q (exact in bf16), so per 32-block b
+//   sum_k x_k w_k = d_b sum_k x_k (128 + q_k) + (m_b - 128 d_b) sum_k x_k,
+// with sum_k x_k the staged per-16 sums of the operand (hi + lo) values.
 template <int MT>
 __device__ __forceinline__ void q41_unit(float (&acc)[2][MT][4], const uint4 (&nb)[2], const uint4 (&sc)[2],
-                                         const GemmArgs &a, int c, int lane) {
-    const int t = lane & 3;
-    const int K16 = a.K / 16;
-    uint4 b[MT][4];
-    load_frags<MT>(b, a, c, lane);
+                                         const uint8_t *slot, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const float *sums = reinterpret_cast<const float *>(slot);
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
         float2 S[MT];
 #pragma unroll
         for (int tt = 0; tt < MT; ++tt) {
-            const int k16 = 4 * c + 2 * blk;
-            const int r = a.x_row0 + 8 * tt + 2 * t;
-            if (k16 < K16) {
-                const float2 s0 = __ldg(reinterpret_cast<const float2 *>(a.xs + k16 * kMaxRows + r));
-                const float2 s1 = __ldg(reinterpret_cast<const float2 *>(a.xs + (k16 + 1) * kMaxRows + r));
-                S[tt] = make_float2(s0.x + s1.x, s0.y + s1.y);
-            } else {
-                S[tt] = make_float2(0.f, 0.f);
-            }
+            const float2 s0 = *reinterpret_cast<const float2 *>(sums + (2 * blk) * kMaxRows + 8 * tt + 2 * t);
+            const float2 s1 = *reinterpret_cast<const float2 *>(sums + (2 * blk + 1) * kMaxRows + 8 * tt + 2 * t);
+            S[tt] = make_float2(s0.x + s1.x, s0.y + s1.y);
         }
-        float cb[2][MT][4];
+        float ch[2][MT][4], cl[2][MT][4];   // hi and lo chains
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int tt = 0; tt < MT; ++tt) cb[j][tt][0] = cb[j][tt][1] = cb[j][tt][2] = cb[j][tt][3] = 0.f;
+            for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ch[j][tt][i] = cl[j][tt][i] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
             const int ks = 2 * blk + kk;
+            uint4 b[MT];
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt) b[tt] = frag(slot, tt, ks, g, t);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const uint32_t w = ks == 0 ? nb[j].x : ks == 1 ? nb[j].y : ks == 2 ? nb[j].z : nb[j].w;
@@ -178,8 +214,8 @@ __device__ __forceinline__ void q41_unit(float (&acc)[2][MT][4], const uint4 (&n
                 const uint32_t a2 = nib_pair_bf16(w >> 8), a3 = nib_pair_bf16(w >> 12);
 #pragma unroll
                 for (int tt = 0; tt < MT; ++tt) {
-                    mma_bf16(cb[j][tt], a0, a1, a2, a3, b[tt][ks].x, b[tt][ks].y);
-                    mma_bf16(cb[j][tt], a0, a1, a2, a3, b[tt][ks].z, b[tt][ks].w);
+                    mma_bf16(ch[j][tt], a0, a1, a2, a3, b[tt].x, b[tt].y);
+                    mma_bf16(cl[j][tt], a0, a1, a2, a3, b[tt].z, b[tt].w);
                 }
             }
         }
@@ -188,31 +224,34 @@ __device__ __forceinline__ void q41_unit(float (&acc)[2][MT][4], const uint4 (&n
             uint32_t dlo = blk ? sc[j].z : sc[j].x, dhi = blk ? sc[j].w : sc[j].y;
             const float2 flo = __half22float2(*reinterpret_cast<__half2 *>(&dlo));   // (d, m) of column g
             const float2 fhi = __half22float2(*reinterpret_cast<__half2 *>(&dhi));   // column g + 8
+            const float mlo = fmaf(-128.f, flo.x, flo.y), mhi = fmaf(-128.f, fhi.x, fhi.y);
 #pragma unroll
             for (int tt = 0; tt < MT; ++tt) {
-                acc[j][tt][0] = fmaf(flo.y, S[tt].x, fmaf(flo.x, cb[j][tt][0], acc[j][tt][0]));
-                acc[j][tt][1] = fmaf(flo.y, S[tt].y, fmaf(flo.x, cb[j][tt][1], acc[j][tt][1]));
-                acc[j][tt][2] = fmaf(fhi.y, S[tt].x, fmaf(fhi.x, cb[j][tt][2], acc[j][tt][2]));
-                acc[j][tt][3] = fmaf(fhi.y, S[tt].y, fmaf(fhi.x, cb[j][tt][3], acc[j][tt][3]));
+                acc[j][tt][0] = fmaf(mlo, S[tt].x, fmaf(flo.x, ch[j][tt][0] + cl[j][tt][0], acc[j][tt][0]));
+                acc[j][tt][1] = fmaf(mlo, S[tt].y, fmaf(flo.x, ch[j][tt][1] + cl[j][tt][1], acc[j][tt][1]));
+                acc[j][tt][2] = fmaf(mhi, S[tt].x, fmaf(fhi.x, ch[j][tt][2] + cl[j][tt][2], acc[j][tt][2]));
+                acc[j][tt][3] = fmaf(mhi, S[tt].y, fmaf(fhi.x, ch[j][tt][3] + cl[j][tt][3], acc[j][tt][3]));
             }
         }
     }
 }
 
 template <int MT>
-__device__ __forceinline__ void bf16_unit(float (&acc)[2][MT][4], const uint4 (&w)[2][4], const GemmArgs &a, int c,
-                                          int lane) {
-    uint4 b[MT][4];
-    load_frags<MT>(b, a, c, lane);
+__device__ __forceinline__ void bf16_unit(float (&acc)[2][MT][4], const uint4 (&w)[2][4], const uint8_t *slot, int lane) {
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
+    for (int ks = 0; ks < 4; ++ks) {
+        uint4 b[MT];
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt) b[tt] = frag(slot, tt, ks, g, t);
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int tt = 0; tt < MT; ++tt) {
-                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt][ks].x, b[tt][ks].y);
-                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt][ks].z, b[tt][ks].w);
+                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt].x, b[tt].y);
+                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt].z, b[tt].w);
             }
+    }
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -246,25 +285,22 @@ __device__ __forceinline__ void epilogue(const GemmArgs &a, float (&acc)[2][MT][
                 const float v0 = silu_f(acc[0][tt][h]) * acc[1][tt][h];
                 const float v1 = silu_f(acc[0][tt][h + 2]) * acc[1][tt][h + 2];
                 const int K = a.N / 2;
-                if (live) {
-                    act_store(a.yf, K, tok, 16 * ng + g, v0);
-                    act_store(a.yf, K, tok, 16 * ng + g + 8, v1);
-                }
-                const float s = tile_col_sum(v0 + v1);
+                float hl = 0.f;
+                if (live) hl = act_store(a.yf, K, tok, 16 * ng + g, v0) + act_store(a.yf, K, tok, 16 * ng + g + 8, v1);
+                const float s = tile_col_sum(hl);
                 if (live && g == 0) a.ys[ng * kMaxRows + tok] = s;
             } else if (EPI == EPI_SILU_MUL) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int nt = j ? nt1 : nt0;
-                    float v0 = 0.f, v1 = 0.f;
+                    float hl = 0.f;
                     if (live) {
                         const uint16_t *e = a.ext + (long)tok * a.lde;
-                        v0 = silu_f(acc[j][tt][h]) * bf16_to_f32(e[16 * nt + g]);
-                        v1 = silu_f(acc[j][tt][h + 2]) * bf16_to_f32(e[16 * nt + g + 8]);
-                        act_store(a.yf, a.N, tok, 16 * nt + g, v0);
-                        act_store(a.yf, a.N, tok, 16 * nt + g + 8, v1);
+                        const float v0 = silu_f(acc[j][tt][h]) * bf16_to_f32(e[16 * nt + g]);
+                        const float v1 = silu_f(acc[j][tt][h + 2]) * bf16_to_f32(e[16 * nt + g + 8]);
+                        hl = act_store(a.yf, a.N, tok, 16 * nt + g, v0) + act_store(a.yf, a.N, tok, 16 * nt + g + 8, v1);
                     }
-                    const float s = tile_col_sum(v0 + v1);
+                    const float s = tile_col_sum(hl);
                     if (live && g == 0) a.ys[nt * kMaxRows + tok] = s;
                 }
             }
@@ -278,14 +314,20 @@ __device__ __forceinline__ void epilogue(const GemmArgs &a, float (&acc)[2][MT][
 // par = w / 4, i.e. chunks c with c % 4 == par of the CTA's chunk range of that quad. At the end of a
 // range the four parities are added in shared memory (order 0..3); a quad split over several CTAs
 // leaves one partial per CTA, added by the last CTA to finish it (order of the segments).
+// The CTA's unit range [u0, u1) is cut into stages of at most a.slots distinct chunks (one stage
+// unless the range is long); each stage's activations are staged in shared memory, and the loop walks
+// the pieces (quad sub-range x stage) in order.
 constexpr int kGemmWarps = 16;
 
 __device__ __forceinline__ long cta_of(long u, long U, int G) { return ((u + 1) * G - 1) / U; }
 
 template <int FMT, int MT, int EPI>
 __global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
-    __shared__ float red[4][4][kMaxRows * 32];
+    extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_last;
+    constexpr int R = MT * 8;
+    float *red = reinterpret_cast<float *>(smem);               // [4 par][4 gq][R][32]
+    uint8_t *xs_sm = smem + red_bytes<MT>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int gq = warp & 3, par = warp >> 2;
     const int ngroups = a.N / 32;
@@ -295,6 +337,18 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
     const long u0 = (long)blockIdx.x * U / G, u1 = (long)(blockIdx.x + 1) * U / G;
     constexpr int P = (FMT == W_Q41 && MT == 1) ? 4 : 2;
     constexpr int TB = FMT == W_Q41 ? 640 : 2048;
+    // stage length in units: the whole range when its distinct chunks fit
+    const long span = u1 - u0;
+    const long L = (span < a.C ? span : a.C) <= a.slots ? span : a.slots;
+    auto stage_end = [&](long x) -> long {
+        const long e = u0 + ((x - u0) / L + 1) * L;
+        return e < u1 ? e : u1;
+    };
+    auto piece_end = [&](long x) -> long {
+        const long qe = (x / a.C + 1) * a.C;
+        const long se = stage_end(x);
+        return qe < se ? qe : se;
+    };
 
     auto tiles = [&](int q, int &nt0, int &nt1, int &ng) {
         ng = 4 * q + gq;
@@ -322,17 +376,13 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
             }
         }
     };
-    // sub-range [qs, qe) of quad q: this warp's chunks are c0, c0 + 4, ... < ce
-    auto my_first = [&](long qs) -> int { const int ca = int(qs % a.C); return ca + ((par - ca) % 4 + 4) % 4; };
-    auto sub_end = [&](long qs) -> long {
-        const long e = (qs / a.C + 1) * a.C;
-        return e < u1 ? e : u1;
-    };
-    auto prefetch = [&](long qs) {   // the first P units of the sub-range starting at qs
-        if (qs >= u1) return;
-        const int q = int(qs / a.C);
-        const int ce = int(sub_end(qs) - (long)q * a.C);
-        const int c0 = my_first(qs);
+    // this warp's first chunk of a piece starting at unit ps (chunks c % 4 == par)
+    auto my_first = [&](long ps) -> int { const int ca = int(ps % a.C); return ca + ((par - ca) % 4 + 4) % 4; };
+    auto prefetch = [&](long ps) {   // the first P units of the piece starting at ps
+        if (ps >= u1) return;
+        const int q = int(ps / a.C);
+        const int ce = int(piece_end(ps) - (long)q * a.C);
+        const int c0 = my_first(ps);
 #pragma unroll
         for (int p = 0; p < P; ++p)
             if (c0 + 4 * p < ce) load(q, c0 + 4 * p, p);
@@ -342,6 +392,10 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
     pdl_wait();
     pdl_trigger();
 
+    long s0 = u0, s1 = stage_end(u0);
+    stage_x<MT>(a, xs_sm, s0, s1);
+    __syncthreads();
+
     float acc[2][MT][4];
     auto zero = [&]() {
 #pragma unroll
@@ -350,11 +404,13 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
             for (int tt = 0; tt < MT; ++tt) acc[j][tt][0] = acc[j][tt][1] = acc[j][tt][2] = acc[j][tt][3] = 0.f;
     };
     zero();
-    for (long qs = u0; qs < u1;) {
-        const int q = int(qs / a.C);
-        const long qe = sub_end(qs);
-        const int ce = int(qe - (long)q * a.C);
-        const int c0 = my_first(qs);
+    for (long ps = u0; ps < u1;) {
+        const int q = int(ps / a.C);
+        const long pe = piece_end(ps);
+        const long qend = ((long)q + 1) * a.C < u1 ? ((long)q + 1) * a.C : u1;
+        const int ce = int(pe - (long)q * a.C);
+        const int c0 = my_first(ps);
+        const int cbase = int(s0 % a.C);
         const int nmine = c0 < ce ? (ce - c0 + 3) / 4 : 0;
         for (int ib = 0; ib < nmine; ib += P) {
 #pragma unroll
@@ -362,86 +418,102 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
                 const int i = ib + p;
                 if (i < nmine) {
                     const int c = c0 + 4 * i;
-                    if (FMT == W_Q41) q41_unit<MT>(acc, nb[p], sc[p], a, c, lane);
-                    else bf16_unit<MT>(acc, w[p], a, c, lane);
+                    const uint8_t *slot = xs_sm + ((c - cbase + a.C) % a.C) * slot_bytes<MT>();
+                    if (FMT == W_Q41) q41_unit<MT>(acc, nb[p], sc[p], slot, lane);
+                    else bf16_unit<MT>(acc, w[p], slot, lane);
                     if (i + P < nmine) load(q, c + 4 * P, p);
                 }
             }
         }
-        // the next sub-range's first weights stream while this quad is reduced
-        prefetch(qe);
-        // add the four parities
-        float *mine = red[par][gq];
-#pragma unroll
-        for (int tt = 0; tt < MT; ++tt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
-                mine[tok * 32 + r] = acc[0][tt][i];
-                mine[tok * 32 + 16 + r] = acc[1][tt][i];
-            }
-        __syncthreads();
-        const long qa = (long)q * a.C;
-        const int first = int(cta_of(qa, U, G)), last = int(cta_of(qa + a.C - 1, U, G));
-        const int nseg = last - first + 1, seg = blockIdx.x - first;
-        const int ng = 4 * q + gq;
-        if (nseg > 1) {
-            // this CTA's partial of the quad: 4 groups x 16 rows x 32 columns, summed over parities
-            for (int e = threadIdx.x; e < 4 * kMaxRows * 32; e += blockDim.x) {
-                const int gg = e / (kMaxRows * 32), rc = e % (kMaxRows * 32);
-                if (4 * q + gg < ngroups) {
-                    const float v = ((red[0][gg][rc] + red[1][gg][rc]) + red[2][gg][rc]) + red[3][gg][rc];
-                    a.part[((size_t)(4 * q + gg) * a.maxseg + seg) * (kMaxRows * 32) + rc] = v;
-                }
-            }
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) s_last = (atomicAdd(a.cnt + q, 1) == nseg - 1);
-            __syncthreads();
-            if (s_last) {
-                __threadfence();
-                // every thread adds its elements over the segments, in segment order
-                for (int e = threadIdx.x; e < 4 * kMaxRows * 32; e += blockDim.x) {
-                    const int gg = e / (kMaxRows * 32), rc = e % (kMaxRows * 32);
-                    float v = 0.f;
-                    if (4 * q + gg < ngroups) {
-                        const float *pp = a.part + (size_t)(4 * q + gg) * a.maxseg * (kMaxRows * 32) + rc;
-                        float l[16];
-#pragma unroll
-                        for (int s2 = 0; s2 < 16; ++s2) l[s2] = s2 < nseg ? __ldcg(pp + s2 * (kMaxRows * 32)) : 0.f;
-                        for (int s2 = 0; s2 < nseg && s2 < 16; ++s2) v += l[s2];
-                        for (int s2 = 16; s2 < nseg; ++s2) v += __ldcg(pp + s2 * (kMaxRows * 32));
-                    }
-                    red[0][gg][rc] = v;
-                }
-                if (threadIdx.x == 0) a.cnt[q] = 0;
-            }
-            __syncthreads();
-        } else {
-            for (int e = threadIdx.x; e < 4 * kMaxRows * 32; e += blockDim.x) {
-                const int gg = e / (kMaxRows * 32), rc = e % (kMaxRows * 32);
-                red[0][gg][rc] = ((red[0][gg][rc] + red[1][gg][rc]) + red[2][gg][rc]) + red[3][gg][rc];
-            }
-            __syncthreads();
-        }
-        const bool fin = nseg == 1 || s_last;
-        if (fin && par == 0 && ng < ngroups) {
+        // the next piece's first weights stream while this one is reduced or restaged
+        prefetch(pe);
+        if (pe == qend) {
+            // add the four parities
+            float *mine = red + (par * 4 + gq) * (R * 32);
 #pragma unroll
             for (int tt = 0; tt < MT; ++tt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
-                    acc[0][tt][i] = red[0][gq][tok * 32 + r];
-                    acc[1][tt][i] = red[0][gq][tok * 32 + 16 + r];
+                    mine[tok * 32 + r] = acc[0][tt][i];
+                    mine[tok * 32 + 16 + r] = acc[1][tt][i];
                 }
-            int nt0, nt1, ngx;
-            tiles(q, nt0, nt1, ngx);
-            epilogue<MT, EPI>(a, acc, nt0, nt1, ng, lane);
+            __syncthreads();
+            const long qa = (long)q * a.C;
+            const int first = int(cta_of(qa, U, G)), last = int(cta_of(qa + a.C - 1, U, G));
+            const int nseg = last - first + 1, seg = blockIdx.x - first;
+            const int ng = 4 * q + gq;
+            constexpr int GR = R * 32;   // one group's elements
+            auto red_at = [&](int pp, int gg, int rc) -> float & { return red[(pp * 4 + gg) * GR + rc]; };
+            if (nseg > 1) {
+                // this CTA's partial of the quad: 4 groups x R rows x 32 columns, summed over parities
+                for (int e = threadIdx.x; e < 4 * GR; e += blockDim.x) {
+                    const int gg = e / GR, rc = e % GR;
+                    if (4 * q + gg < ngroups) {
+                        const float v = ((red_at(0, gg, rc) + red_at(1, gg, rc)) + red_at(2, gg, rc)) + red_at(3, gg, rc);
+                        a.part[((size_t)(4 * q + gg) * a.maxseg + seg) * (kMaxRows * 32) + rc] = v;
+                    }
+                }
+                // one thread publishes the CTA's partial (barrier, then fence and ticket)
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    const int last_one = atomicAdd(a.cnt + q, 1) == nseg - 1;
+                    if (last_one) __threadfence();
+                    s_last = last_one;
+                }
+                __syncthreads();
+                if (s_last) {
+                    // every thread adds its elements over the segments, in segment order
+                    for (int e = threadIdx.x; e < 4 * GR; e += blockDim.x) {
+                        const int gg = e / GR, rc = e % GR;
+                        float v = 0.f;
+                        if (4 * q + gg < ngroups) {
+                            const float *pp = a.part + (size_t)(4 * q + gg) * a.maxseg * (kMaxRows * 32) + rc;
+                            float l[16];
+#pragma unroll
+                            for (int s2 = 0; s2 < 16; ++s2) l[s2] = s2 < nseg ? __ldcg(pp + s2 * (kMaxRows * 32)) : 0.f;
+                            for (int s2 = 0; s2 < nseg && s2 < 16; ++s2) v += l[s2];
+                            for (int s2 = 16; s2 < nseg; ++s2) v += __ldcg(pp + s2 * (kMaxRows * 32));
+                        }
+                        red_at(0, gg, rc) = v;
+                    }
+                    if (threadIdx.x == 0) a.cnt[q] = 0;
+                }
+                __syncthreads();
+            } else {
+                for (int e = threadIdx.x; e < 4 * GR; e += blockDim.x) {
+                    const int gg = e / GR, rc = e % GR;
+                    red_at(0, gg, rc) = ((red_at(0, gg, rc) + red_at(1, gg, rc)) + red_at(2, gg, rc)) + red_at(3, gg, rc);
+                }
+                __syncthreads();
+            }
+            const bool fin = nseg == 1 || s_last;
+            if (fin && par == 0 && ng < ngroups) {
+#pragma unroll
+                for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
+                        acc[0][tt][i] = red_at(0, gq, tok * 32 + r);
+                        acc[1][tt][i] = red_at(0, gq, tok * 32 + 16 + r);
+                    }
+                int nt0, nt1, ngx;
+                tiles(q, nt0, nt1, ngx);
+                epilogue<MT, EPI>(a, acc, nt0, nt1, ng, lane);
+            }
+            __syncthreads();   // red is reused by the next quad
+            zero();
+            if (threadIdx.x == 0) s_last = 0;
         }
-        __syncthreads();   // red is reused by the next quad
-        zero();
-        if (threadIdx.x == 0) s_last = 0;
-        qs = qe;
+        if (pe == s1 && pe < u1) {   // next stage
+            __syncthreads();         // every warp is done with the staged activations
+            s0 = s1;
+            s1 = stage_end(s0);
+            stage_x<MT>(a, xs_sm, s0, s1);
+            __syncthreads();
+        }
+        ps = pe;
     }
 }
 
@@ -639,9 +711,27 @@ size_t gemm_scratch_floats(int C, int N) {
     return ms > 1 ? (size_t)(N / 32) * ms * kMaxRows * 32 : 0;
 }
 
+// dynamic shared memory of a product: the parity reduction buffer and the activation slots
+constexpr int kGemmSmemBudget = 224 * 1024;
+
 template <int FMT, int MT, int EPI>
-static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    return launch_pdl(k_gemm<FMT, MT, EPI>, dim3(gemm_grid(a.C, a.N)), dim3(kGemmWarps * 32), 0, s, a);
+static cudaError_t run_gemm(const GemmArgs &a0, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm<FMT, MT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kGemmSmemBudget);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    GemmArgs a = a0;
+    const int G = gemm_grid(a.C, a.N);
+    const long U = (long)((a.N / 32 + 3) / 4) * a.C;
+    const long per_cta = (U + G - 1) / G;
+    const int most = (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<MT>();
+    const long need = per_cta < a.C ? per_cta : a.C;
+    a.slots = int(need < most ? need : most);
+    const size_t smem = (size_t)red_bytes<MT>() + (size_t)a.slots * slot_bytes<MT>();
+    return launch_pdl(k_gemm<FMT, MT, EPI>, dim3(G), dim3(kGemmWarps * 32), smem, s, a);
 }
 
 size_t head_smem(int K, int MT) { return (size_t)MT * 8 * (K * 4 + kHeadPad); }

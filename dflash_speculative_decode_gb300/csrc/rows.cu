@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kRowThreads) k_rows(RowArgs a) {
             const int h = threadIdx.x + i * kRowThreads;
             float v = 0.f;
             if (h < a.H && live) v = a.w_next ? (xv[i] * r) * bf16_to_f32(a.w_next[h]) : xv[i];
-            if (h < a.H) act_store(a.outf, a.H, row, h, v);
-            const float sg = half_warp_sum(v);
+            const float hl = h < a.H ? act_store(a.outf, a.H, row, h, v) : 0.f;
+            const float sg = half_warp_sum(hl);
             if (h < a.H && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = sg;
         }
     }
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(kRowThreads) k_cast_rows(const float *src, int
         if (i >= per) break;
         const int h = threadIdx.x + i * kRowThreads;
         const float o = (h < H && live) ? (v[i] * r) * bf16_to_f32(w[h]) : 0.f;
-        if (h < H) act_store(dstf, H, row0 + m, h, o);
-        const float sg = half_warp_sum(o);
+        const float hl = h < H ? act_store(dstf, H, row0 + m, h, o) : 0.f;
+        const float sg = half_warp_sum(hl);
         if (h < H && (h & 15) == 0) dsts[(h >> 4) * kMaxRows + row0 + m] = sg;
     }
 }
@@ -240,166 +240,289 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Attention. Work item = (query head, chunk of kAttnChunk keys). The chunks cover, for the target
-// (mode 0), positions lo..n+M-1 of the head's plane with lo = max(0, n-window+1) on sliding layers, each
-// row m at position n+m seeing keys max(0, n+m-window+1)..n+m (all of 0..n+m on full layers); for the
-// draft (mode 1), context positions max(0, n-window)..n-1 for every row plus one chunk of the block's
-// own keys, all visible. Each item writes its softmax partial (max, sum, sum of p*v); the last item of
-// a head (arrival counter) combines the chunks in chunk order and writes bf16 outputs.
-constexpr int kAttnThreads = 128;
+// Attention. One thread-block cluster of kAttnCluster CTAs per query head. Keys are cut into blocks of
+// kAttnKeys ABSOLUTE positions (block b = positions 32b .. 32b+31); CTA r of the cluster takes the
+// blocks b with b % kAttnCluster == r, in ascending order, and folds each into a running softmax state
+// per row (max, sum, sum of p*v). The states of the cluster's CTAs are then merged in rank order through
+// distributed shared memory. A row's result depends only on its own visible keys and their absolute
+// positions (a block with no visible key leaves the state exactly unchanged), so it does not depend on
+// how many rows the pass carries or where the pass starts.
+// Target (mode 0): row m at position p = n+m sees plane positions max(0, p-window+1)..p (0..p on full
+// layers). Draft (mode 1): every row sees context positions max(0, n-window)..n-1, plus all nB keys of
+// the block's own store as one extra block after the context blocks.
+// ---------------------------------------------------------------------------------------------------
+constexpr int kAttnThreads = 256;
+constexpr int kAttnKeys = 32;
+constexpr int kAttnCluster = 8;
 
-__device__ __forceinline__ void attn_range(const AttnArgs &a, int n, int &lo, int &nA, int &nchunks) {
-    if (a.mode == 0) {
-        lo = a.window > 0 ? max(0, n - a.window + 1) : 0;
-        nA = n + a.M - lo;
-        nchunks = (nA + kAttnChunk - 1) / kAttnChunk;
-    } else {
-        lo = a.window > 0 ? max(0, n - a.window) : 0;
-        nA = n - lo;
-        nchunks = (nA + kAttnChunk - 1) / kAttnChunk + 1;
-    }
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// load a float from the shared memory of CTA `rank` of this cluster, at the offset of `p` in ours
+__device__ __forceinline__ float ld_cluster(const float *p, unsigned rank) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    unsigned ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+size_t attn_smem(int hd) {
+    return ((size_t)kMaxRows * hd + 4 * (size_t)kAttnKeys * (hd + 4) + (size_t)kMaxRows * kAttnKeys + 3 * kMaxRows) * 4;
 }
 
 __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const int hd = a.hd, ldk = hd + 4, hd4 = hd / 4;
+    float *Qs = sm;                                 // [16][hd] this head's query rows
+    float *Kb = Qs + kMaxRows * hd;                 // [2][32][ldk] double-buffered key block
+    float *Vb = Kb + 2 * kAttnKeys * ldk;           // [2][32][ldk]
+    float *Ps = Vb + 2 * kAttnKeys * ldk;           // [16][32] probabilities of the current block
+    float *Sc = Ps + kMaxRows * kAttnKeys;          // [16] rescale of the running sums
+    float *Mx = Sc + kMaxRows;                      // [16] running max
+    float *Ls = Mx + kMaxRows;                      // [16] running sum
+    float *Os = Kb;                                 // [16][hd] final state (after the last block)
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x / kAttnCluster;
+    const unsigned rank = cluster_rank();
+    const int g = h / (a.nq / a.nkv);
     pdl_wait();
     pdl_trigger();
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ int s_last;
-    const int hd = a.hd, ks = hd + 1;   // key row stride in floats (odd: conflict-free column reads)
-    float *Ks = reinterpret_cast<float *>(smem);
-    float *Vs = Ks + kAttnChunk * ks;
-    float *qs = Vs + kAttnChunk * ks;     // [M][hd]
-    float *ps = qs + a.M * hd;            // [M][kAttnChunk]
     const int n = a.st->n;
-    int lo, nA, nchunks;
-    attn_range(a, n, lo, nA, nchunks);
-    const int grp = a.nq / a.nkv;
-    const int items = a.nq * nchunks;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NW = kAttnThreads / 32;
+    const int M = a.M;
+    int lo, hi;   // inclusive range of plane positions any row may see
+    if (a.mode == 0) {
+        lo = a.window > 0 ? max(0, n - a.window + 1) : 0;
+        hi = n + M - 1;
+    } else {
+        lo = a.window > 0 ? max(0, n - a.window) : 0;
+        hi = n - 1;
+    }
+    const bool anyA = hi >= lo;
+    const int bA0 = anyA ? lo / kAttnKeys : 0, bA1 = anyA ? hi / kAttnKeys : -1;
+    const int bV = (a.mode == 1 && a.nB > 0) ? (anyA ? bA1 + 1 : 0) : -1;   // the draft block's own keys
+    // this CTA's blocks: b0, b0 + 8, ... <= bA1, then bV when it is ours
+    const int b0 = bA0 + int((rank - unsigned(bA0 % kAttnCluster) + kAttnCluster) % kAttnCluster);
+    const int nAmine = b0 <= bA1 ? (bA1 - b0) / kAttnCluster + 1 : 0;
+    const int nmine = nAmine + ((bV >= 0 && bV % kAttnCluster == (int)rank) ? 1 : 0);
 
-    for (int it = blockIdx.x; it < items; it += gridDim.x) {
-        const int h = it / nchunks, c = it % nchunks, g = h / grp;
-        const bool blockchunk = (a.mode == 1 && c == nchunks - 1);
-        const int j0 = blockchunk ? 0 : lo + c * kAttnChunk;
-        const int nk = blockchunk ? a.nB : min(kAttnChunk, lo + nA - j0);
-        __syncthreads();
-        // keys and values of the chunk, and the queries of this head
-        for (int e = tid; e < nk * hd; e += kAttnThreads) {
-            const int jj = e / hd, d = e % hd;
-            long off;
-            const float *kb, *vb;
-            if (blockchunk) {
-                off = ((long)jj * a.nkv + g) * hd;
-                kb = a.kB;
-                vb = a.vB;
+    auto load_block = [&](int i, int buf) {
+        float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
+        const bool virt = i >= nAmine;
+        const int b = virt ? bV : b0 + kAttnCluster * i;
+        for (int e = tid; e < kAttnKeys * hd4; e += kAttnThreads) {
+            const int j = e / hd4, d4 = e % hd4;
+            const float *ksrc = nullptr, *vsrc = nullptr;
+            if (virt) {
+                if (j < a.nB) {
+                    const long off = ((long)j * a.nkv + g) * hd + 4 * d4;
+                    ksrc = a.kB + off;
+                    vsrc = a.vB + off;
+                }
             } else {
-                const long slot = (j0 + jj) % a.capA;
-                off = (slot * a.nkv + g) * hd;
-                kb = a.kA;
-                vb = a.vA;
+                const int pos = kAttnKeys * b + j;
+                if (pos >= lo && pos <= hi) {
+                    const long off = ((long)(pos % a.capA) * a.nkv + g) * hd + 4 * d4;
+                    ksrc = a.kA + off;
+                    vsrc = a.vA + off;
+                }
             }
-            Ks[jj * ks + d] = kb[off + d];
-            Vs[jj * ks + d] = vb[off + d];
+            float *kd = K + j * ldk + 4 * d4, *vd = V + j * ldk + 4 * d4;
+            if (ksrc) {
+                cp_async16(kd, ksrc);
+                cp_async16(vd, vsrc);
+            } else {   // keys outside every row's range: zeros (they are masked; 0 * v must stay 0)
+                *reinterpret_cast<float4 *>(kd) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(vd) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-        for (int e = tid; e < a.M * hd; e += kAttnThreads) {
-            const int m = e / hd, d = e % hd;
-            qs[e] = a.q[((long)m * a.nq + h) * hd + d];
+        cp_async_commit();
+    };
+
+    if (nmine > 0) load_block(0, 0);
+    for (int e = tid; e < kMaxRows * hd4; e += kAttnThreads) {
+        const int m = e / hd4, d4 = e % hd4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < M) v = *reinterpret_cast<const float4 *>(a.q + ((long)m * a.nq + h) * hd + 4 * d4);
+        *reinterpret_cast<float4 *>(Qs + m * hd + 4 * d4) = v;
+    }
+    if (tid < kMaxRows) Mx[tid] = -INFINITY, Ls[tid] = 0.f;
+
+    // p.V ownership: thread -> float4 column c4 of rows rg, rg + RG, ...
+    const int RG = kAttnThreads / hd4;
+    const int c4 = tid % hd4, rg = tid / hd4;
+    const bool pv_on = rg < RG;
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int i = 0; i < nmine; ++i) {
+        const int buf = i & 1;
+        if (i + 1 < nmine) {
+            load_block(i + 1, buf ^ 1);
+            cp_async_wait_group1();
+        } else {
+            cp_async_wait_all();
         }
         __syncthreads();
-        // scores: thread -> key jj = lane, rows warp, warp + NW, ...
+        const float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
+        const bool virt = i >= nAmine;
+        const int b = virt ? bV : b0 + kAttnCluster * i;
+        // scores: warp -> rows warp, warp + 8; lane -> key
         {
-            const int jj = lane;
-            float sc[kMaxRows / NW];
+            const int j = lane;
+            float s[2] = {0.f, 0.f};
+            const float4 *kr = reinterpret_cast<const float4 *>(K + j * ldk);
+            const float4 *q0 = reinterpret_cast<const float4 *>(Qs + warp * hd);
+            const float4 *q1 = reinterpret_cast<const float4 *>(Qs + (warp + 8) * hd);
+            for (int d4 = 0; d4 < hd4; ++d4) {
+                const float4 k = kr[d4], x0 = q0[d4], x1 = q1[d4];
+                s[0] = fmaf(x0.x, k.x, s[0]);
+                s[0] = fmaf(x0.y, k.y, s[0]);
+                s[0] = fmaf(x0.z, k.z, s[0]);
+                s[0] = fmaf(x0.w, k.w, s[0]);
+                s[1] = fmaf(x1.x, k.x, s[1]);
+                s[1] = fmaf(x1.y, k.y, s[1]);
+                s[1] = fmaf(x1.z, k.z, s[1]);
+                s[1] = fmaf(x1.w, k.w, s[1]);
+            }
 #pragma unroll
-            for (int r = 0; r < kMaxRows / NW; ++r) sc[r] = 0.f;
-            if (jj < nk) {
-                for (int d = 0; d < hd; ++d) {
-                    const float kv = Ks[jj * ks + d];
+            for (int r = 0; r < 2; ++r) {
+                const int m = warp + 8 * r;
+                bool vis = m < M;
+                if (virt) {
+                    vis = vis && j < a.nB;
+                } else {
+                    const int pos = kAttnKeys * b + j;
+                    if (a.mode == 0) {
+                        const int p = n + m;
+                        vis = vis && pos <= p && (a.window <= 0 || pos > p - a.window) && pos >= 0;
+                    } else {
+                        vis = vis && pos >= lo && pos <= hi;
+                    }
+                }
+                const float sv = vis ? s[r] * a.scale : -INFINITY;
+                float bm = sv;
 #pragma unroll
-                    for (int r = 0; r < kMaxRows / NW; ++r) {
-                        const int m = warp + r * NW;
-                        if (m < a.M) sc[r] = fmaf(qs[m * hd + d], kv, sc[r]);
+                for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+                const float mo = Mx[m];
+                const float mn = fmaxf(mo, bm);
+                const float pj = vis ? expf(sv - mn) : 0.f;
+                float ps = pj;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+                const float sc = mo == -INFINITY ? 0.f : expf(mo - mn);
+                Ps[m * kAttnKeys + j] = pj;
+                __syncwarp();
+                if (lane == 0) {
+                    Sc[m] = sc;
+                    Mx[m] = mn;
+                    Ls[m] = fmaf(Ls[m], sc, ps);
+                }
+            }
+        }
+        __syncthreads();
+        // running p.V, keys in ascending order
+        if (pv_on) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int m = rg + RG * r;
+                if (m < kMaxRows) {
+                    const float sc = Sc[m];
+                    acc[r].x *= sc, acc[r].y *= sc, acc[r].z *= sc, acc[r].w *= sc;
+                }
+            }
+            for (int j = 0; j < kAttnKeys; ++j) {
+                const float4 v = *reinterpret_cast<const float4 *>(V + j * ldk + 4 * c4);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int m = rg + RG * r;
+                    if (m < kMaxRows) {
+                        const float p = Ps[m * kAttnKeys + j];
+                        acc[r].x = fmaf(p, v.x, acc[r].x);
+                        acc[r].y = fmaf(p, v.y, acc[r].y);
+                        acc[r].z = fmaf(p, v.z, acc[r].z);
+                        acc[r].w = fmaf(p, v.w, acc[r].w);
                     }
                 }
             }
-#pragma unroll
-            for (int r = 0; r < kMaxRows / NW; ++r) {
-                const int m = warp + r * NW;
-                if (m >= a.M) continue;
-                bool vis = jj < nk;
-                if (vis && a.mode == 0) {
-                    const int j = j0 + jj, p = n + m;
-                    vis = j <= p && (a.window <= 0 || j > p - a.window);
-                }
-                ps[m * kAttnChunk + jj] = vis ? sc[r] * a.scale : -INFINITY;
-            }
         }
-        __syncthreads();
-        // softmax partial per row: warp w takes rows w, w + NW, ...
-        float *pml = a.part_ml + ((long)h * a.max_chunks + c) * a.M * 2;
-        for (int m = warp; m < a.M; m += NW) {
-            const float v = ps[m * kAttnChunk + lane];
-            float mx = v;
+        __syncthreads();   // the buffer is refilled two blocks later
+    }
+    // publish this CTA's state, then merge the cluster's states in rank order
+    if (pv_on) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float p = mx == -INFINITY ? 0.f : expf(v - mx);
-            float sm = p;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-            ps[m * kAttnChunk + lane] = p;
-            if (lane == 0) pml[m * 2] = mx, pml[m * 2 + 1] = sm;
-        }
-        __syncthreads();
-        // p . V, keys in ascending order
-        float *pacc = a.part_acc + ((long)h * a.max_chunks + c) * a.M * hd;
-        for (int e = tid; e < a.M * hd; e += kAttnThreads) {
-            const int m = e / hd, d = e % hd;
-            float acc = 0.f;
-            for (int jj = 0; jj < nk; ++jj) acc = fmaf(ps[m * kAttnChunk + jj], Vs[jj * ks + d], acc);
-            pacc[e] = acc;
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_last = (atomicAdd(a.cnt + h, 1) == nchunks - 1);
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            for (int e = tid; e < a.M * hd; e += kAttnThreads) {
-                const int m = e / hd, d = e % hd;
-                float mt = -INFINITY;
-                for (int c2 = 0; c2 < nchunks; ++c2)
-                    mt = fmaxf(mt, __ldcg(a.part_ml + (((long)h * a.max_chunks + c2) * a.M + m) * 2));
-                float num = 0.f, den = 0.f;
-                for (int c2 = 0; c2 < nchunks; ++c2) {
-                    const long b = ((long)h * a.max_chunks + c2) * a.M + m;
-                    const float mc = __ldcg(a.part_ml + b * 2);
-                    const float f = mc == -INFINITY ? 0.f : expf(mc - mt);
-                    den = fmaf(__ldcg(a.part_ml + b * 2 + 1), f, den);
-                    num = fmaf(__ldcg(a.part_acc + b * hd + d), f, num);
-                }
-                const float o = num / den;
-                const int col = h * hd + d;
-                act_store(a.outf, a.nq * hd, m, col, o);
-                const float sg = half_warp_sum(o);
-                if ((col & 15) == 0) a.outs[(col >> 4) * kMaxRows + m] = sg;
-            }
-            if (tid == 0) a.cnt[h] = 0;
+        for (int r = 0; r < 4; ++r) {
+            const int m = rg + RG * r;
+            if (m < kMaxRows) *reinterpret_cast<float4 *>(Os + m * hd + 4 * c4) = acc[r];
         }
     }
+    cluster_sync_all();
+    const int ng16 = hd / 16;
+    const int items = M * ng16;
+    const int hw = tid >> 4;   // half warp: one (row, 16-column group) item per round
+    for (int base = 0; base < items; base += kAttnCluster * (kAttnThreads / 16)) {
+        const int it = base + int(rank) + kAttnCluster * hw;
+        const bool on = it < items;
+        float hl = 0.f;
+        int m = 0, col = 0;
+        if (on) {
+            m = it / ng16;
+            const int d = 16 * (it % ng16) + (tid & 15);
+            float mt = -INFINITY;
+            float mr[kAttnCluster];
+#pragma unroll
+            for (int r = 0; r < kAttnCluster; ++r) {
+                mr[r] = ld_cluster(Mx + m, r);
+                mt = fmaxf(mt, mr[r]);
+            }
+            float num = 0.f, den = 0.f;
+#pragma unroll
+            for (int r = 0; r < kAttnCluster; ++r) {
+                const float f = mr[r] == -INFINITY ? 0.f : expf(mr[r] - mt);
+                den = fmaf(ld_cluster(Ls + m, r), f, den);
+                num = fmaf(ld_cluster(Os + m * hd + d, r), f, num);
+            }
+            col = h * hd + d;
+            hl = act_store(a.outf, a.nq * hd, m, col, num / den);
+        }
+        const float sg = half_warp_sum(hl);   // every lane of the warp takes part
+        if (on && (tid & 15) == 0) a.outs[(col >> 4) * kMaxRows + m] = sg;
+    }
+    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
 }
 
-size_t attn_smem(int M, int hd) { return ((size_t)2 * kAttnChunk * (hd + 1) + (size_t)M * hd + (size_t)M * kAttnChunk) * 4; }
-
-cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t s) {
+cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
+    const size_t smem = attn_smem(a.hd);
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn_smem(256)));
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    if (a.hd % 32 || a.M > kMaxRows || a.nB > kAttnChunk || (a.M * a.hd) % 32) return cudaErrorInvalidValue;
-    return launch_pdl(k_attn, dim3(grid), dim3(kAttnThreads), attn_smem(a.M, a.hd), s, a);
+    if (a.hd % 16 || a.hd < 16 || a.hd > 256 || a.M < 1 || a.M > kMaxRows || a.nB > kAttnKeys || a.nq % a.nkv)
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.nq * kAttnCluster);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = kAttnCluster;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_attn, a);
 }
 
 // ---------------------------------------------------------------------------------------------------

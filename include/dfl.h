@@ -170,7 +170,7 @@ int64_t dfl_positions_held(const dfl_ctx *ctx);
  * (otherwise only the fused argmax runs); DFL_OPT_GRAPHS = 0 launches kernels one by one instead of
  * replaying captured CUDA graphs; DFL_OPT_STOP_LAYER = l >= 0 (inspection only) makes target passes
  * stop after layer l, without the head, so dfl_debug_read shows that layer's intermediates; -1 = off;
- * DFL_OPT_PROFILE = 1 brackets every product launch with CUDA events on the context's stream (read with
+ * DFL_OPT_PROFILE = 1 brackets every kernel launch with CUDA events on the context's stream (read with
  * dfl_profile_read; setting the option clears the totals). */
 enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3, DFL_OPT_PROFILE = 4 };
 int dfl_set_option(dfl_ctx *ctx, int option, int value);
@@ -202,9 +202,12 @@ int dfl_plant_proposals(dfl_ctx *ctx, const int32_t *dev_table, int table_len);
 int64_t dfl_launch_count(const dfl_ctx *ctx);
 
 /* Totals of the launches profiled while DFL_OPT_PROFILE was on, per class: 0 = Q4_1 products,
- * 1 = bf16 products (fc), 2 = the bf16 head with its fused argmax. *ms = summed event time of the
- * launches; *bytes = their algorithmic bytes (weights at 0.625 B (Q4_1) or 2 B (bf16) per weight,
- * fp32 activations in and products out). Synchronises the stream. */
+ * 1 = bf16 products (fc), 2 = the bf16 head with its fused argmax, 3 = attention, 4 = q/k norm,
+ * rotation and KV store, 5 = the other row kernels (embedding, norms, taps, sampling). With graphs on,
+ * only the launches inside draft and verify passes are bracketed. *ms = summed event time of the
+ * launches; *bytes = their algorithmic bytes for classes 0-2 (weights at 0.625 B (Q4_1) or 2 B (bf16)
+ * per weight, fp32 activations in and products out), 0 for the others. Error DFL_E_INVALID_ARG for a
+ * class outside 0..5. Synchronises the stream. */
 int dfl_profile_read(dfl_ctx *ctx, int cls, int64_t *launches, double *ms, double *bytes);
 
 const char *dfl_last_error(const dfl_ctx *ctx);
