@@ -30,6 +30,9 @@ struct DevState {
     int err;               // sticky device-side error bits
 };
 
+// DevState::err bits
+constexpr int kErrWaitTimeout = 1;   // a bounded wait in a kernel gave up
+
 struct SetStateArgs {
     int n, k, draft_n, ctx_rows, sampled, use_draft_rows, last_tok;
     float temperature;
@@ -155,7 +158,7 @@ struct GemmArgs {
     const uint32_t *xf;    // activations, operand format (K inputs)
     const float *xs;       // their per-16 sums
     int x_row0;            // first activation row used
-    int slots;             // products: activation chunks staged in shared memory (set by the launcher)
+    int *err;              // products: sticky error bits (nullable), kErrWaitTimeout
     float *y;              // EPI_F32: fp32 output [M][ldy]
     int ldy;
     uint32_t *yf;          // EPI_GLU / EPI_SILU_MUL: output in operand format (N/2 or N inputs)

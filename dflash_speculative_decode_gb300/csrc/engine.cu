@@ -410,6 +410,7 @@ cudaError_t gemm(dfl_ctx *c, const QMat &W, const Act &x, int row0, int M, int e
     a.cnt = c->cnt;
     a.ext = ext;
     a.lde = lde;
+    a.err = &c->st->err;
     c->launches += 1;
     e = launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, a, c->stream);
     if (e != cudaSuccess) return e;
@@ -844,6 +845,7 @@ int run_draft(dfl_ctx *c, int last_tok) {
 int read_state(dfl_ctx *c, DevState *out) {
     DFL_CK(cudaMemcpyAsync(out, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
     DFL_CK(cudaStreamSynchronize(c->stream));
+    if (out->err & kErrWaitTimeout) return fail(c, DFL_E_CUDA, "a kernel gave up waiting for its asynchronous copies");
     return DFL_OK;
 }
 

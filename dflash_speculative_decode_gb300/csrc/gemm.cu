@@ -34,6 +34,8 @@
 
 namespace dfl {
 
+constexpr int kGemmWarps = 16, kGemmThreads = kGemmWarps * 32;
+
 // ---------------------------------------------------------------------------------------------------
 // packing
 // ---------------------------------------------------------------------------------------------------
@@ -126,131 +128,190 @@ cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *su
 }
 
 // ---------------------------------------------------------------------------------------------------
-// activation staging: the chunks a CTA needs are copied to shared memory once (one asynchronous copy
-// round trip), so the unit loop reads its B fragments and sums from shared memory.
-// Per slot (one 64-input chunk): sums [4 groups][16 rows] fp32 (256 B), then R = 8*MT rows of 256 B
-// fragments; inside a row the four 64-byte k-steps are stored at position ks ^ (row & 1), so the two
-// rows a quarter warp reads fall on different banks.
+// shared-memory ring
+// A round is CPR consecutive chunks of one quad (CPR units; 8 for Q4_1, 4 for bf16). Its weights
+// (8*CPR tiles) and activations (R = 8*MT rows x CPR chunks, plus the chunks' per-16 sums) are brought
+// into one ring slot by bulk asynchronous copies, one per contiguous run, completing on the slot's
+// "full" mbarrier:
+//   tiles: tile (unit u, group gq, tile j) at ((2*gq + j)*CPR + u) * TB  (a group's chunks are one run)
+//   rows:  row tok at WB + tok * XR, chunk u at + 256*u (64-byte k-steps in operand order); the row
+//          pitch XR is 64 bytes past a multiple of 128 so the two rows a quarter warp reads differ in bank
+//   sums:  at WB + R * XR, 256 bytes per chunk ([4 groups][16 rows] fp32)
 // ---------------------------------------------------------------------------------------------------
-template <int MT>
-__host__ __device__ constexpr int slot_bytes() { return 256 + MT * 8 * 256; }
+template <int FMT>
+__host__ __device__ constexpr int cpr() { return FMT == W_Q41 ? 8 : 4; }
+template <int FMT>
+__host__ __device__ constexpr int xrow_bytes() { return cpr<FMT>() * 256 + 64; }
 template <int MT>
 __host__ __device__ constexpr int red_bytes() { return 16 * MT * 8 * 32 * 4; }   // [4 parities][4 groups][R][32]
-
-// copy the chunks of units [s0, s1) (at most `slots` distinct chunks; slot of chunk c = (c - s0 % C) mod C)
-template <int MT>
-__device__ __forceinline__ void stage_x(const GemmArgs &a, uint8_t *xs_sm, long s0, long s1) {
-    constexpr int R = MT * 8;
-    const int K16 = a.K / 16;
-    const long span = s1 - s0;
-    const int nch = int(span < a.C ? span : a.C);
-    const int cb = int(s0 % a.C);
-    const int per = 16 + R * 16;   // 16-byte pieces per slot
-    for (int e = threadIdx.x; e < nch * per; e += blockDim.x) {
-        const int slot = e / per, r = e % per;
-        const int c = (cb + slot) % a.C;
-        uint8_t *base = xs_sm + slot * slot_bytes<MT>();
-        if (r < 16) {   // sums: group 4c + r/4, rows 4*(r%4) .. +3
-            const int kb = 4 * c + (r >> 2);
-            uint8_t *dst = base + 16 * r;
-            if (kb < K16) cp_async16(dst, a.xs + kb * kMaxRows + 4 * (r & 3));
-            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-            const int rr = r - 16, tok = rr >> 4, ks = (rr >> 2) & 3, t = rr & 3;
-            const int kb = 4 * c + ks;
-            uint8_t *dst = base + 256 + tok * 256 + ((ks ^ (tok & 1)) * 4 + t) * 16;
-            if (kb < K16)
-                cp_async16(dst, a.xf + (((long)(a.x_row0 + tok) * K16 + kb) * 4 + t) * 4);
-            else
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-    cp_async_wait_all();
+template <int FMT>
+__host__ __device__ constexpr int tile_bytes() { return FMT == W_Q41 ? 640 : 2048; }
+template <int FMT, int MT>
+__host__ __device__ constexpr int slot_bytes() {
+    return (8 * cpr<FMT>() * tile_bytes<FMT>() + MT * 8 * xrow_bytes<FMT>() + cpr<FMT>() * 256 + 127) / 128 * 128;
+}
+constexpr int kGemmSmemBudget = 224 * 1024;
+template <int FMT, int MT>
+__host__ __device__ constexpr int ring_slots() {
+    return (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<FMT, MT>() < 6 ? (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<FMT, MT>() : 6;
 }
 
-// B fragment (hi in .x/.y, lo in .z/.w) of k-step ks for rows 8*tt + g
-__device__ __forceinline__ uint4 frag(const uint8_t *slot, int tt, int ks, int g, int t) {
-    const int tok = 8 * tt + g;
-    return *reinterpret_cast<const uint4 *>(slot + 256 + tok * 256 + ((ks ^ (tok & 1)) * 4 + t) * 16);
+__device__ __forceinline__ unsigned saddr(const void *p) { return static_cast<unsigned>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void mbar_init(uint64_t *b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+// one arrival that also announces `bytes` of asynchronous copies completing on the barrier
+__device__ __forceinline__ void mbar_expect(uint64_t *b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t *b, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false if it did not complete within the limit.
+constexpr int kWaitPolls = 1 << 18;
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity) {
+    for (int i = 0; i < kWaitPolls; ++i)
+        if (mbar_test(b, parity)) return true;
+    return false;
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16) completing on barrier b
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *b) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(saddr(dst)),
+                 "l"(src), "r"(bytes), "r"(saddr(b))
+                 : "memory");
+}
+
+// two fp32 lanes at once: d = a * b + c (each lane rounded as fmaf)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
+// mma.m16n8k16 bf16 with a zero accumulator
+__device__ __forceinline__ void mma_bf16_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                           uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 // ---------------------------------------------------------------------------------------------------
-// one unit of work: a 64-input chunk of two 16-column tiles
+// a warp's units of one round: NU chunks (u = par + 4i) of its column group, two 16-column tiles each
 // ---------------------------------------------------------------------------------------------------
 // Q4_1: the codes enter the tensor cores as 128 + q (exact in bf16), so per 32-block b
 //   sum_k x_k w_k = d_b sum_k x_k (128 + q_k) + (m_b - 128 d_b) sum_k x_k,
-// with sum_k x_k the staged per-16 sums of the operand (hi + lo) values.
-template <int MT>
-__device__ __forceinline__ void q41_unit(float (&acc)[2][MT][4], const uint4 (&nb)[2], const uint4 (&sc)[2],
-                                         const uint8_t *slot, int lane) {
+// with sum_k x_k the per-16 sums of the operand (hi + lo) values. The NU units are independent until
+// the fold, so their loads and products overlap. nblk[i]: 32-blocks of unit i inside K (0: no unit).
+template <int FMT, int MT, int NU>
+__device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t *slot, int w_off, int x_off, int s_off,
+                                          const int (&nblk)[NU], int lane) {
+    constexpr int TB = tile_bytes<FMT>(), CP = cpr<FMT>(), XR = xrow_bytes<FMT>();
     const int g = lane >> 2, t = lane & 3;
-    const float *sums = reinterpret_cast<const float *>(slot);
+    uint4 nb[NU][2], sc[NU][2];
+#pragma unroll
+    for (int i = 0; i < NU; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint8_t *w = slot + w_off + (j * CP + 4 * i) * TB;
+            nb[i][j] = *reinterpret_cast<const uint4 *>(w + 16 * lane);
+            sc[i][j] = *reinterpret_cast<const uint4 *>(w + 512 + 16 * g);
+        }
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-        float2 S[MT];
+        float c[NU][2][MT][4];
+        float2 S[NU][MT];
 #pragma unroll
-        for (int tt = 0; tt < MT; ++tt) {
-            const float2 s0 = *reinterpret_cast<const float2 *>(sums + (2 * blk) * kMaxRows + 8 * tt + 2 * t);
-            const float2 s1 = *reinterpret_cast<const float2 *>(sums + (2 * blk + 1) * kMaxRows + 8 * tt + 2 * t);
-            S[tt] = make_float2(s0.x + s1.x, s0.y + s1.y);
+        for (int i = 0; i < NU; ++i) {
+            const float *xsum = reinterpret_cast<const float *>(slot + s_off + 256 * 4 * i);
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt) {
+                const float2 s0 = *reinterpret_cast<const float2 *>(xsum + (2 * blk) * kMaxRows + 8 * tt + 2 * t);
+                const float2 s1 = *reinterpret_cast<const float2 *>(xsum + (2 * blk + 1) * kMaxRows + 8 * tt + 2 * t);
+                S[i][tt] = make_float2(s0.x + s1.x, s0.y + s1.y);
+            }
         }
-        float ch[2][MT][4], cl[2][MT][4];   // hi and lo chains
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int tt = 0; tt < MT; ++tt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) ch[j][tt][i] = cl[j][tt][i] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
             const int ks = 2 * blk + kk;
-            uint4 b[MT];
 #pragma unroll
-            for (int tt = 0; tt < MT; ++tt) b[tt] = frag(slot, tt, ks, g, t);
+            for (int i = 0; i < NU; ++i) {
+                uint4 b[MT];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint32_t w = ks == 0 ? nb[j].x : ks == 1 ? nb[j].y : ks == 2 ? nb[j].z : nb[j].w;
-                const uint32_t a0 = nib_pair_bf16(w), a1 = nib_pair_bf16(w >> 4);
-                const uint32_t a2 = nib_pair_bf16(w >> 8), a3 = nib_pair_bf16(w >> 12);
+                for (int tt = 0; tt < MT; ++tt)
+                    b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + 256 * 4 * i + tt * 8 * XR + 64 * ks);
 #pragma unroll
-                for (int tt = 0; tt < MT; ++tt) {
-                    mma_bf16(ch[j][tt], a0, a1, a2, a3, b[tt].x, b[tt].y);
-                    mma_bf16(cl[j][tt], a0, a1, a2, a3, b[tt].z, b[tt].w);
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t w = ks == 0 ? nb[i][j].x : ks == 1 ? nb[i][j].y : ks == 2 ? nb[i][j].z : nb[i][j].w;
+                    const uint32_t a0 = nib_pair_bf16(w), a1 = nib_pair_bf16(w >> 4);
+                    const uint32_t a2 = nib_pair_bf16(w >> 8), a3 = nib_pair_bf16(w >> 12);
+#pragma unroll
+                    for (int tt = 0; tt < MT; ++tt) {
+                        if (kk == 0) mma_bf16_z(c[i][j][tt], a0, a1, a2, a3, b[tt].x, b[tt].y);
+                        else mma_bf16(c[i][j][tt], a0, a1, a2, a3, b[tt].x, b[tt].y);
+                        mma_bf16(c[i][j][tt], a0, a1, a2, a3, b[tt].z, b[tt].w);
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            uint32_t dlo = blk ? sc[j].z : sc[j].x, dhi = blk ? sc[j].w : sc[j].y;
-            const float2 flo = __half22float2(*reinterpret_cast<__half2 *>(&dlo));   // (d, m) of column g
-            const float2 fhi = __half22float2(*reinterpret_cast<__half2 *>(&dhi));   // column g + 8
-            const float mlo = fmaf(-128.f, flo.x, flo.y), mhi = fmaf(-128.f, fhi.x, fhi.y);
+        for (int i = 0; i < NU; ++i) {
+            if (blk >= nblk[i]) continue;   // past K, or no unit: its registers hold nothing of use
 #pragma unroll
-            for (int tt = 0; tt < MT; ++tt) {
-                acc[j][tt][0] = fmaf(mlo, S[tt].x, fmaf(flo.x, ch[j][tt][0] + cl[j][tt][0], acc[j][tt][0]));
-                acc[j][tt][1] = fmaf(mlo, S[tt].y, fmaf(flo.x, ch[j][tt][1] + cl[j][tt][1], acc[j][tt][1]));
-                acc[j][tt][2] = fmaf(mhi, S[tt].x, fmaf(fhi.x, ch[j][tt][2] + cl[j][tt][2], acc[j][tt][2]));
-                acc[j][tt][3] = fmaf(mhi, S[tt].y, fmaf(fhi.x, ch[j][tt][3] + cl[j][tt][3], acc[j][tt][3]));
+            for (int j = 0; j < 2; ++j) {
+                uint32_t dlo = blk ? sc[i][j].z : sc[i][j].x, dhi = blk ? sc[i][j].w : sc[i][j].y;
+                const float2 flo = __half22float2(*reinterpret_cast<__half2 *>(&dlo));   // (d, m) of column g
+                const float2 fhi = __half22float2(*reinterpret_cast<__half2 *>(&dhi));   // column g + 8
+                const float mlo = fmaf(-128.f, flo.x, flo.y), mhi = fmaf(-128.f, fhi.x, fhi.y);
+#pragma unroll
+                for (int tt = 0; tt < MT; ++tt) {
+                    float2 p0 = make_float2(acc[j][tt][0], acc[j][tt][1]), p1 = make_float2(acc[j][tt][2], acc[j][tt][3]);
+                    p0 = ffma2(make_float2(flo.x, flo.x), make_float2(c[i][j][tt][0], c[i][j][tt][1]), p0);
+                    p1 = ffma2(make_float2(fhi.x, fhi.x), make_float2(c[i][j][tt][2], c[i][j][tt][3]), p1);
+                    p0 = ffma2(make_float2(mlo, mlo), S[i][tt], p0);
+                    p1 = ffma2(make_float2(mhi, mhi), S[i][tt], p1);
+                    acc[j][tt][0] = p0.x, acc[j][tt][1] = p0.y, acc[j][tt][2] = p1.x, acc[j][tt][3] = p1.y;
+                }
             }
         }
     }
 }
 
-template <int MT>
-__device__ __forceinline__ void bf16_unit(float (&acc)[2][MT][4], const uint4 (&w)[2][4], const uint8_t *slot, int lane) {
-    const int g = lane >> 2, t = lane & 3;
+// bf16 (one unit per round): nks = k-steps inside K
+template <int FMT, int MT>
+__device__ __forceinline__ void bf16_unit(float (&acc)[2][MT][4], const uint8_t *slot, int w_off, int x_off, int nks, int lane) {
+    constexpr int TB = tile_bytes<FMT>(), CP = cpr<FMT>(), XR = xrow_bytes<FMT>();
+    const uint8_t *w0 = slot + w_off, *w1 = slot + w_off + CP * TB;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
+        if (ks >= nks) break;
         uint4 b[MT];
 #pragma unroll
-        for (int tt = 0; tt < MT; ++tt) b[tt] = frag(slot, tt, ks, g, t);
+        for (int tt = 0; tt < MT; ++tt) b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + tt * 8 * XR + 64 * ks);
+        const uint4 wa = *reinterpret_cast<const uint4 *>(w0 + 512 * ks + 16 * lane);
+        const uint4 wb = *reinterpret_cast<const uint4 *>(w1 + 512 * ks + 16 * lane);
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int tt = 0; tt < MT; ++tt) {
-                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt].x, b[tt].y);
-                mma_bf16(acc[j][tt], w[j][ks].x, w[j][ks].y, w[j][ks].z, w[j][ks].w, b[tt].z, b[tt].w);
-            }
+        for (int tt = 0; tt < MT; ++tt) {
+            mma_bf16(acc[0][tt], wa.x, wa.y, wa.z, wa.w, b[tt].x, b[tt].y);
+            mma_bf16(acc[0][tt], wa.x, wa.y, wa.z, wa.w, b[tt].z, b[tt].w);
+            mma_bf16(acc[1][tt], wb.x, wb.y, wb.z, wb.w, b[tt].x, b[tt].y);
+            mma_bf16(acc[1][tt], wb.x, wb.y, wb.z, wb.w, b[tt].z, b[tt].w);
+        }
     }
 }
 
@@ -310,211 +371,250 @@ __device__ __forceinline__ void epilogue(const GemmArgs &a, float (&acc)[2][MT][
 // ---------------------------------------------------------------------------------------------------
 // the product kernel
 // ---------------------------------------------------------------------------------------------------
-// One CTA per SM, 16 warps: warp w takes column group gq = w % 4 of the current quad and chunk parity
-// par = w / 4, i.e. chunks c with c % 4 == par of the CTA's chunk range of that quad. At the end of a
-// range the four parities are added in shared memory (order 0..3); a quad split over several CTAs
-// leaves one partial per CTA, added by the last CTA to finish it (order of the segments).
-// The CTA's unit range [u0, u1) is cut into stages of at most a.slots distinct chunks (one stage
-// unless the range is long); each stage's activations are staged in shared memory, and the loop walks
-// the pieces (quad sub-range x stage) in order.
-constexpr int kGemmWarps = 16;
+// One CTA per SM: 16 compute warps and one copy warp. The CTA's unit range [u0, u1) is walked in
+// rounds; compute warp w takes column group gq = w % 4 and the round's units par, par + 4, ...
+// (par = w / 4). The copy warp fills the ring: a slot is refilled once all 16 compute warps have
+// released it ("empty" mbarrier), and the weights of the first ring_slots rounds are requested before
+// the previous kernel has finished. At the end of a quad's range the four parities are added in shared
+// memory (order 0..3); a quad split over several CTAs leaves one partial per CTA, added by the last CTA
+// to finish it (order of the segments). Every split depends on K, N and the grid only, so a row's result
+// never depends on how many rows the pass carries.
+constexpr int kGemmBlock = kGemmThreads + 32;   // + the copy warp
 
 __device__ __forceinline__ long cta_of(long u, long U, int G) { return ((u + 1) * G - 1) / U; }
+// barrier of the 16 compute warps only
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kGemmThreads) : "memory"); }
 
 template <int FMT, int MT, int EPI>
-__global__ void __launch_bounds__(kGemmWarps * 32, 1) k_gemm(GemmArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ int s_last;
+__global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[8], empty[8];
+    __shared__ int s_last, s_bad;
     constexpr int R = MT * 8;
+    constexpr int TB = tile_bytes<FMT>();
+    constexpr int CP = cpr<FMT>();
+    constexpr int NU = CP / 4;
+    constexpr int XR = xrow_bytes<FMT>();
+    constexpr int WB = 8 * CP * TB;
+    constexpr int SB = slot_bytes<FMT, MT>();
+    constexpr int S = ring_slots<FMT, MT>();
+    static_assert(S >= 2 && S <= 8, "ring");
     float *red = reinterpret_cast<float *>(smem);               // [4 par][4 gq][R][32]
-    uint8_t *xs_sm = smem + red_bytes<MT>();
+    uint8_t *ring = smem + red_bytes<MT>();                     // [S][SB]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int gq = warp & 3, par = warp >> 2;
     const int ngroups = a.N / 32;
     const int Q = (ngroups + 3) / 4;
     const long U = (long)Q * a.C;
     const int G = gridDim.x;
+    const int K16 = a.K / 16;
     const long u0 = (long)blockIdx.x * U / G, u1 = (long)(blockIdx.x + 1) * U / G;
-    constexpr int P = (FMT == W_Q41 && MT == 1) ? 4 : 2;
-    constexpr int TB = FMT == W_Q41 ? 640 : 2048;
-    // stage length in units: the whole range when its distinct chunks fit
-    const long span = u1 - u0;
-    const long L = (span < a.C ? span : a.C) <= a.slots ? span : a.slots;
-    auto stage_end = [&](long x) -> long {
-        const long e = u0 + ((x - u0) / L + 1) * L;
-        return e < u1 ? e : u1;
-    };
-    auto piece_end = [&](long x) -> long {
-        const long qe = (x / a.C + 1) * a.C;
-        const long se = stage_end(x);
-        return qe < se ? qe : se;
-    };
 
-    auto tiles = [&](int q, int &nt0, int &nt1, int &ng) {
-        ng = 4 * q + gq;
-        const int ngc = ng < ngroups ? ng : ngroups - 1;   // an idle warp of the last quad reads valid memory
-        nt0 = (EPI == EPI_GLU) ? ngc : 2 * ngc;
-        nt1 = (EPI == EPI_GLU) ? ngc + ngroups : 2 * ngc + 1;
+    // a round: chunks c .. min(c + CP, ce) - 1 of quad q
+    struct Rd {
+        int q, c, ce;
     };
-    uint4 nb[P][2], sc[P][2];
-    uint4 w[P][2][4];
-    auto load = [&](int q, int c, int p) {
-        int nt0, nt1, ng;
-        tiles(q, nt0, nt1, ng);
-        const uint8_t *b0 = a.img + ((size_t)nt0 * a.C + c) * TB;
-        const uint8_t *b1 = a.img + ((size_t)nt1 * a.C + c) * TB;
-        if (FMT == W_Q41) {
-            nb[p][0] = ldg_stream(b0 + 16 * lane);
-            nb[p][1] = ldg_stream(b1 + 16 * lane);
-            sc[p][0] = ldg_stream(b0 + 512 + 16 * g);
-            sc[p][1] = ldg_stream(b1 + 512 + 16 * g);
-        } else {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                w[p][0][ks] = ldg_stream(b0 + 512 * ks + 16 * lane);
-                w[p][1][ks] = ldg_stream(b1 + 512 * ks + 16 * lane);
-            }
+    auto rd_at_quad = [&](Rd &r, int q, int c) {
+        r.q = q;
+        r.c = c;
+        const long e = u1 - (long)q * a.C;
+        r.ce = int(e < a.C ? e : a.C);
+    };
+    auto rd_valid = [&](const Rd &r) { return (long)r.q * a.C + r.c < u1; };
+    auto rd_next = [&](Rd &r) {
+        if (r.c + CP < r.ce) r.c += CP;
+        else rd_at_quad(r, r.q + 1, 0);
+    };
+    auto tile_of = [&](int ng, int j) { return EPI == EPI_GLU ? (j ? ng + ngroups : ng) : 2 * ng + j; };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 2);            // weights arrival + activations arrival (+ their bytes)
+            mbar_init(&empty[i], kGemmWarps);  // one arrival per compute warp
         }
-    };
-    // this warp's first chunk of a piece starting at unit ps (chunks c % 4 == par)
-    auto my_first = [&](long ps) -> int { const int ca = int(ps % a.C); return ca + ((par - ca) % 4 + 4) % 4; };
-    auto prefetch = [&](long ps) {   // the first P units of the piece starting at ps
-        if (ps >= u1) return;
-        const int q = int(ps / a.C);
-        const int ce = int(piece_end(ps) - (long)q * a.C);
-        const int c0 = my_first(ps);
-#pragma unroll
-        for (int p = 0; p < P; ++p)
-            if (c0 + 4 * p < ce) load(q, c0 + 4 * p, p);
-    };
-    // weights are immutable: the first loads are issued before the previous kernel has finished
-    prefetch(u0);
-    pdl_wait();
-    pdl_trigger();
-
-    long s0 = u0, s1 = stage_end(u0);
-    stage_x<MT>(a, xs_sm, s0, s1);
+        s_bad = 0;
+        s_last = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     __syncthreads();
 
-    float acc[2][MT][4];
-    auto zero = [&]() {
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int tt = 0; tt < MT; ++tt) acc[j][tt][0] = acc[j][tt][1] = acc[j][tt][2] = acc[j][tt][3] = 0.f;
-    };
-    zero();
-    for (long ps = u0; ps < u1;) {
-        const int q = int(ps / a.C);
-        const long pe = piece_end(ps);
-        const long qend = ((long)q + 1) * a.C < u1 ? ((long)q + 1) * a.C : u1;
-        const int ce = int(pe - (long)q * a.C);
-        const int c0 = my_first(ps);
-        const int cbase = int(s0 % a.C);
-        const int nmine = c0 < ce ? (ce - c0 + 3) / 4 : 0;
-        for (int ib = 0; ib < nmine; ib += P) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const int i = ib + p;
-                if (i < nmine) {
-                    const int c = c0 + 4 * i;
-                    const uint8_t *slot = xs_sm + ((c - cbase + a.C) % a.C) * slot_bytes<MT>();
-                    if (FMT == W_Q41) q41_unit<MT>(acc, nb[p], sc[p], slot, lane);
-                    else bf16_unit<MT>(acc, w[p], slot, lane);
-                    if (i + P < nmine) load(q, c + 4 * P, p);
-                }
+    if (warp == kGemmWarps) {
+        // ---- copy warp ----
+        auto issue_w = [&](const Rd &r, int sl) {   // the weights of round r into slot sl
+            const int nc = r.ce - r.c < CP ? r.ce - r.c : CP;
+            const int live = ngroups - 4 * r.q < 4 ? ngroups - 4 * r.q : 4;
+            if (lane == 0) mbar_expect(&full[sl], unsigned(2 * live * nc * TB));
+            __syncwarp();
+            if (lane < 2 * live) {
+                const int gg = lane >> 1, j = lane & 1;
+                bulk_g2s(ring + sl * SB + (2 * gg + j) * CP * TB,
+                         a.img + ((size_t)tile_of(4 * r.q + gg, j) * a.C + r.c) * TB, unsigned(nc * TB), &full[sl]);
             }
+        };
+        auto issue_x = [&](const Rd &r, int sl) {   // the activations of round r (valid k-steps only)
+            const int nc = r.ce - r.c < CP ? r.ce - r.c : CP;
+            const int kb = K16 - 4 * r.c;
+            const unsigned xb = 64u * unsigned(kb < 4 * nc ? kb : 4 * nc);
+            if (lane == 0) mbar_expect(&full[sl], (R + 1) * xb);
+            __syncwarp();
+            uint8_t *base = ring + sl * SB + WB;
+            if (lane < R)
+                bulk_g2s(base + lane * XR, a.xf + ((size_t)(a.x_row0 + lane) * K16 + 4 * r.c) * 16, xb, &full[sl]);
+            else if (lane == R)
+                bulk_g2s(base + R * XR, a.xs + (size_t)(4 * r.c) * kMaxRows, xb, &full[sl]);
+        };
+        Rd r;
+        rd_at_quad(r, int(u0 / a.C), int(u0 % a.C));
+        const Rd r0 = r;
+        // weights are immutable: the first rounds' weights go out before the previous kernel ends
+        int k = 0;
+        for (; k < S && rd_valid(r); ++k, rd_next(r)) issue_w(r, k);
+        pdl_wait();
+        pdl_trigger();
+        Rd rx = r0;
+        for (int k2 = 0; k2 < k; ++k2, rd_next(rx)) issue_x(rx, k2);
+        for (; rd_valid(r); ++k, rd_next(r)) {
+            const int sl = k % S;
+            if (!mbar_wait(&empty[sl], unsigned(k / S - 1) & 1u)) s_bad = 1;
+            issue_w(r, sl);
+            issue_x(r, sl);
         }
-        // the next piece's first weights stream while this one is reduced or restaged
-        prefetch(pe);
-        if (pe == qend) {
-            // add the four parities
-            float *mine = red + (par * 4 + gq) * (R * 32);
+    } else {
+        // ---- compute warps ----
+        const int gq = warp & 3, par = warp >> 2;
+        pdl_wait();
+        pdl_trigger();
+        float acc[2][MT][4];
+        auto zero = [&]() {
 #pragma unroll
-            for (int tt = 0; tt < MT; ++tt)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
-                    mine[tok * 32 + r] = acc[0][tt][i];
-                    mine[tok * 32 + 16 + r] = acc[1][tt][i];
-                }
-            __syncthreads();
-            const long qa = (long)q * a.C;
-            const int first = int(cta_of(qa, U, G)), last = int(cta_of(qa + a.C - 1, U, G));
-            const int nseg = last - first + 1, seg = blockIdx.x - first;
-            const int ng = 4 * q + gq;
-            constexpr int GR = R * 32;   // one group's elements
-            auto red_at = [&](int pp, int gg, int rc) -> float & { return red[(pp * 4 + gg) * GR + rc]; };
-            if (nseg > 1) {
-                // this CTA's partial of the quad: 4 groups x R rows x 32 columns, summed over parities
-                for (int e = threadIdx.x; e < 4 * GR; e += blockDim.x) {
-                    const int gg = e / GR, rc = e % GR;
-                    if (4 * q + gg < ngroups) {
-                        const float v = ((red_at(0, gg, rc) + red_at(1, gg, rc)) + red_at(2, gg, rc)) + red_at(3, gg, rc);
-                        a.part[((size_t)(4 * q + gg) * a.maxseg + seg) * (kMaxRows * 32) + rc] = v;
+                for (int tt = 0; tt < MT; ++tt) acc[j][tt][0] = acc[j][tt][1] = acc[j][tt][2] = acc[j][tt][3] = 0.f;
+        };
+        zero();
+        // per-lane offsets inside a slot (unit par; unit par + 4i is 4i chunks further)
+        const int w_off = (2 * gq * CP + par) * TB;
+        const int x_off = WB + g * XR + 256 * par + 16 * t;
+        const int s_off = WB + R * XR + 256 * par;
+        Rd cr;
+        rd_at_quad(cr, int(u0 / a.C), int(u0 % a.C));
+        for (int k = 0; rd_valid(cr); ++k) {
+            const int sl = k % S;
+            if (!mbar_wait(&full[sl], unsigned(k / S) & 1u)) s_bad = 1;
+            const int ng = 4 * cr.q + gq;
+            if (ng < ngroups) {
+                const uint8_t *slot = ring + sl * SB;
+                if (FMT == W_Q41) {
+                    int nblk[NU];
+#pragma unroll
+                    for (int i = 0; i < NU; ++i) {
+                        const int c = cr.c + par + 4 * i, kb = K16 - 4 * c;
+                        nblk[i] = c < cr.ce ? (kb < 4 ? kb / 2 : 2) : 0;
                     }
+                    q41_units<FMT, MT, NU>(acc, slot, w_off, x_off, s_off, nblk, lane);
+                } else {
+                    const int c = cr.c + par, kb = K16 - 4 * c;
+                    if (c < cr.ce) bf16_unit<FMT, MT>(acc, slot, w_off, x_off, kb < 4 ? kb : 4, lane);
                 }
-                // one thread publishes the CTA's partial (barrier, then fence and ticket)
-                __syncthreads();
-                if (threadIdx.x == 0) {
-                    __threadfence();
-                    const int last_one = atomicAdd(a.cnt + q, 1) == nseg - 1;
-                    if (last_one) __threadfence();
-                    s_last = last_one;
-                }
-                __syncthreads();
-                if (s_last) {
-                    // every thread adds its elements over the segments, in segment order
-                    for (int e = threadIdx.x; e < 4 * GR; e += blockDim.x) {
-                        const int gg = e / GR, rc = e % GR;
-                        float v = 0.f;
-                        if (4 * q + gg < ngroups) {
-                            const float *pp = a.part + (size_t)(4 * q + gg) * a.maxseg * (kMaxRows * 32) + rc;
-                            float l[16];
-#pragma unroll
-                            for (int s2 = 0; s2 < 16; ++s2) l[s2] = s2 < nseg ? __ldcg(pp + s2 * (kMaxRows * 32)) : 0.f;
-                            for (int s2 = 0; s2 < nseg && s2 < 16; ++s2) v += l[s2];
-                            for (int s2 = 16; s2 < nseg; ++s2) v += __ldcg(pp + s2 * (kMaxRows * 32));
-                        }
-                        red_at(0, gg, rc) = v;
-                    }
-                    if (threadIdx.x == 0) a.cnt[q] = 0;
-                }
-                __syncthreads();
-            } else {
-                for (int e = threadIdx.x; e < 4 * GR; e += blockDim.x) {
-                    const int gg = e / GR, rc = e % GR;
-                    red_at(0, gg, rc) = ((red_at(0, gg, rc) + red_at(1, gg, rc)) + red_at(2, gg, rc)) + red_at(3, gg, rc);
-                }
-                __syncthreads();
             }
-            const bool fin = nseg == 1 || s_last;
-            if (fin && par == 0 && ng < ngroups) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sl]);   // this warp is done with the slot
+            Rd nx = cr;
+            rd_next(nx);
+            if (nx.q != cr.q || !rd_valid(nx)) {
+                // end of the quad's range in this CTA: add the four parities
+                const int q = cr.q;
+                float *mine = red + (par * 4 + gq) * (R * 32);
 #pragma unroll
                 for (int tt = 0; tt < MT; ++tt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
-                        acc[0][tt][i] = red_at(0, gq, tok * 32 + r);
-                        acc[1][tt][i] = red_at(0, gq, tok * 32 + 16 + r);
+                        mine[tok * 32 + r] = acc[0][tt][i];
+                        mine[tok * 32 + 16 + r] = acc[1][tt][i];
                     }
-                int nt0, nt1, ngx;
-                tiles(q, nt0, nt1, ngx);
-                epilogue<MT, EPI>(a, acc, nt0, nt1, ng, lane);
+                compute_sync();
+                const long qa = (long)q * a.C;
+                const int first = int(cta_of(qa, U, G)), last = int(cta_of(qa + a.C - 1, U, G));
+                const int nseg = last - first + 1, seg = blockIdx.x - first;
+                constexpr int G4 = R * 32 / 4;   // one group's float4s
+                float4 *red4 = reinterpret_cast<float4 *>(red);
+                auto sum_par = [&](int gg, int e) {
+                    const float4 v0 = red4[(0 * 4 + gg) * G4 + e], v1 = red4[(1 * 4 + gg) * G4 + e];
+                    const float4 v2 = red4[(2 * 4 + gg) * G4 + e], v3 = red4[(3 * 4 + gg) * G4 + e];
+                    return make_float4(((v0.x + v1.x) + v2.x) + v3.x, ((v0.y + v1.y) + v2.y) + v3.y,
+                                       ((v0.z + v1.z) + v2.z) + v3.z, ((v0.w + v1.w) + v2.w) + v3.w);
+                };
+                if (nseg > 1) {
+                    // this CTA's partial of the quad: 4 groups x R rows x 32 columns, summed over parities
+                    if (threadIdx.x < 4 * G4) {
+                        const int gg = threadIdx.x / G4, e = threadIdx.x % G4;
+                        if (4 * q + gg < ngroups)
+                            reinterpret_cast<float4 *>(a.part)[((size_t)(4 * q + gg) * a.maxseg + seg) * (kMaxRows * 8) + e] =
+                                sum_par(gg, e);
+                    }
+                    // one thread publishes the CTA's partial (barrier, then fence and ticket)
+                    compute_sync();
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        const int last_one = atomicAdd(a.cnt + q, 1) == nseg - 1;
+                        if (last_one) __threadfence();
+                        s_last = last_one;
+                    }
+                    compute_sync();
+                    if (s_last) {
+                        // every thread adds its float4 over the segments, in segment order
+                        if (threadIdx.x < 4 * G4) {
+                            const int gg = threadIdx.x / G4, e = threadIdx.x % G4;
+                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (4 * q + gg < ngroups) {
+                                const float4 *pp = reinterpret_cast<const float4 *>(a.part) +
+                                                   (size_t)(4 * q + gg) * a.maxseg * (kMaxRows * 8) + e;
+                                float4 l[8];
+                                for (int s0 = 0; s0 < nseg; s0 += 8) {
+#pragma unroll
+                                    for (int s2 = 0; s2 < 8; ++s2)
+                                        l[s2] = s0 + s2 < nseg ? __ldcg(pp + (s0 + s2) * (kMaxRows * 8)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                                    for (int s2 = 0; s2 < 8; ++s2)
+                                        if (s0 + s2 < nseg) v.x += l[s2].x, v.y += l[s2].y, v.z += l[s2].z, v.w += l[s2].w;
+                                }
+                            }
+                            red4[gg * G4 + e] = v;
+                        }
+                        if (threadIdx.x == 0) a.cnt[q] = 0;
+                    }
+                    compute_sync();
+                } else {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int gg = threadIdx.x / G4, e = threadIdx.x % G4;
+                    if (threadIdx.x < 4 * G4) v = sum_par(gg, e);
+                    compute_sync();
+                    if (threadIdx.x < 4 * G4) red4[gg * G4 + e] = v;
+                    compute_sync();
+                }
+                const bool fin = nseg == 1 || s_last;
+                const int ngq = 4 * q + gq;
+                if (fin && par == 0 && ngq < ngroups) {
+#pragma unroll
+                    for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int tok = 8 * tt + 2 * t + (i & 1), r = g + 8 * (i >> 1);
+                            acc[0][tt][i] = red[gq * (R * 32) + tok * 32 + r];
+                            acc[1][tt][i] = red[gq * (R * 32) + tok * 32 + 16 + r];
+                        }
+                    epilogue<MT, EPI>(a, acc, tile_of(ngq, 0), tile_of(ngq, 1), ngq, lane);
+                }
+                compute_sync();   // red and s_last are reused by the next quad
+                zero();
+                if (threadIdx.x == 0) s_last = 0;
             }
-            __syncthreads();   // red is reused by the next quad
-            zero();
-            if (threadIdx.x == 0) s_last = 0;
+            cr = nx;
         }
-        if (pe == s1 && pe < u1) {   // next stage
-            __syncthreads();         // every warp is done with the staged activations
-            s0 = s1;
-            s1 = stage_end(s0);
-            stage_x<MT>(a, xs_sm, s0, s1);
-            __syncthreads();
-        }
-        ps = pe;
     }
+    __syncthreads();   // every copy has landed (each was waited for) and every warp is done
+    if (threadIdx.x == 0 && s_bad && a.err) atomicOr(a.err, kErrWaitTimeout);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -711,27 +811,18 @@ size_t gemm_scratch_floats(int C, int N) {
     return ms > 1 ? (size_t)(N / 32) * ms * kMaxRows * 32 : 0;
 }
 
-// dynamic shared memory of a product: the parity reduction buffer and the activation slots
-constexpr int kGemmSmemBudget = 224 * 1024;
-
+// dynamic shared memory of a product: the parity reduction buffer and the ring
 template <int FMT, int MT, int EPI>
-static cudaError_t run_gemm(const GemmArgs &a0, cudaStream_t s) {
+static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
+    constexpr int smem = red_bytes<MT>() + ring_slots<FMT, MT>() * slot_bytes<FMT, MT>();
+    static_assert(smem <= kGemmSmemBudget, "product shared memory");
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm<FMT, MT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kGemmSmemBudget);
+        cudaError_t e = cudaFuncSetAttribute(k_gemm<FMT, MT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    GemmArgs a = a0;
-    const int G = gemm_grid(a.C, a.N);
-    const long U = (long)((a.N / 32 + 3) / 4) * a.C;
-    const long per_cta = (U + G - 1) / G;
-    const int most = (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<MT>();
-    const long need = per_cta < a.C ? per_cta : a.C;
-    a.slots = int(need < most ? need : most);
-    const size_t smem = (size_t)red_bytes<MT>() + (size_t)a.slots * slot_bytes<MT>();
-    return launch_pdl(k_gemm<FMT, MT, EPI>, dim3(G), dim3(kGemmWarps * 32), smem, s, a);
+    return launch_pdl(k_gemm<FMT, MT, EPI>, dim3(gemm_grid(a.C, a.N)), dim3(kGemmBlock), (size_t)smem, s, a);
 }
 
 size_t head_smem(int K, int MT) { return (size_t)MT * 8 * (K * 4 + kHeadPad); }
