@@ -34,7 +34,8 @@
 
 namespace dfl {
 
-constexpr int kGemmWarps = 16, kGemmThreads = kGemmWarps * 32;
+// compute warps of a product CTA: four column groups x kGemmPar chunk parities
+constexpr int kGemmWarps = 8, kGemmThreads = kGemmWarps * 32, kGemmPar = kGemmWarps / 4;
 
 // ---------------------------------------------------------------------------------------------------
 // packing
@@ -143,7 +144,7 @@ __host__ __device__ constexpr int cpr() { return FMT == W_Q41 ? 8 : 4; }
 template <int FMT>
 __host__ __device__ constexpr int xrow_bytes() { return cpr<FMT>() * 256 + 64; }
 template <int MT>
-__host__ __device__ constexpr int red_bytes() { return 16 * MT * 8 * 32 * 4; }   // [4 parities][4 groups][R][32]
+__host__ __device__ constexpr int red_bytes() { return kGemmPar * 4 * MT * 8 * 32 * 4; }   // [parity][4 groups][R][32]
 template <int FMT>
 __host__ __device__ constexpr int tile_bytes() { return FMT == W_Q41 ? 640 : 2048; }
 template <int FMT, int MT>
@@ -212,7 +213,7 @@ __device__ __forceinline__ void mma_bf16_z(float (&d)[4], uint32_t a0, uint32_t 
 }
 
 // ---------------------------------------------------------------------------------------------------
-// a warp's units of one round: NU chunks (u = par + 4i) of its column group, two 16-column tiles each
+// a warp's units of one round: NU chunks (u = par + kGemmPar*i) of its column group, two 16-column tiles each
 // ---------------------------------------------------------------------------------------------------
 // Q4_1: the codes enter the tensor cores as 128 + q (exact in bf16), so per 32-block b
 //   sum_k x_k w_k = d_b sum_k x_k (128 + q_k) + (m_b - 128 d_b) sum_k x_k,
@@ -228,7 +229,7 @@ __device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t 
     for (int i = 0; i < NU; ++i)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const uint8_t *w = slot + w_off + (j * CP + 4 * i) * TB;
+            const uint8_t *w = slot + w_off + (j * CP + kGemmPar * i) * TB;
             nb[i][j] = *reinterpret_cast<const uint4 *>(w + 16 * lane);
             sc[i][j] = *reinterpret_cast<const uint4 *>(w + 512 + 16 * g);
         }
@@ -238,7 +239,7 @@ __device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t 
         float2 S[NU][MT];
 #pragma unroll
         for (int i = 0; i < NU; ++i) {
-            const float *xsum = reinterpret_cast<const float *>(slot + s_off + 256 * 4 * i);
+            const float *xsum = reinterpret_cast<const float *>(slot + s_off + 256 * kGemmPar * i);
 #pragma unroll
             for (int tt = 0; tt < MT; ++tt) {
                 const float2 s0 = *reinterpret_cast<const float2 *>(xsum + (2 * blk) * kMaxRows + 8 * tt + 2 * t);
@@ -254,7 +255,7 @@ __device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t 
                 uint4 b[MT];
 #pragma unroll
                 for (int tt = 0; tt < MT; ++tt)
-                    b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + 256 * 4 * i + tt * 8 * XR + 64 * ks);
+                    b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + 256 * kGemmPar * i + tt * 8 * XR + 64 * ks);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t w = ks == 0 ? nb[i][j].x : ks == 1 ? nb[i][j].y : ks == 2 ? nb[i][j].z : nb[i][j].w;
@@ -371,12 +372,12 @@ __device__ __forceinline__ void epilogue(const GemmArgs &a, float (&acc)[2][MT][
 // ---------------------------------------------------------------------------------------------------
 // the product kernel
 // ---------------------------------------------------------------------------------------------------
-// One CTA per SM: 16 compute warps and one copy warp. The CTA's unit range [u0, u1) is walked in
-// rounds; compute warp w takes column group gq = w % 4 and the round's units par, par + 4, ...
-// (par = w / 4). The copy warp fills the ring: a slot is refilled once all 16 compute warps have
-// released it ("empty" mbarrier), and the weights of the first ring_slots rounds are requested before
-// the previous kernel has finished. At the end of a quad's range the four parities are added in shared
-// memory (order 0..3); a quad split over several CTAs leaves one partial per CTA, added by the last CTA
+// One CTA per SM: kGemmWarps compute warps and one copy warp. The CTA's unit range [u0, u1) is walked
+// in rounds; compute warp w takes column group gq = w % 4 and the round's units par, par + kGemmPar, ...
+// (par = w / 4). The copy warp fills the ring: a slot is refilled once every compute warp has released
+// it ("empty" mbarrier), and the weights of the first ring_slots rounds are requested before the
+// previous kernel has finished. At the end of a quad's range the parities are added in shared memory
+// (in parity order); a quad split over several CTAs leaves one partial per CTA, added by the last CTA
 // to finish it (order of the segments). Every split depends on K, N and the grid only, so a row's result
 // never depends on how many rows the pass carries.
 constexpr int kGemmBlock = kGemmThreads + 32;   // + the copy warp
@@ -393,13 +394,14 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
     constexpr int R = MT * 8;
     constexpr int TB = tile_bytes<FMT>();
     constexpr int CP = cpr<FMT>();
-    constexpr int NU = CP / 4;
+    constexpr int NU = CP / kGemmPar;
+    static_assert(CP % kGemmPar == 0, "units per warp");
     constexpr int XR = xrow_bytes<FMT>();
     constexpr int WB = 8 * CP * TB;
     constexpr int SB = slot_bytes<FMT, MT>();
     constexpr int S = ring_slots<FMT, MT>();
     static_assert(S >= 2 && S <= 8, "ring");
-    float *red = reinterpret_cast<float *>(smem);               // [4 par][4 gq][R][32]
+    float *red = reinterpret_cast<float *>(smem);               // [par][4 gq][R][32]
     uint8_t *ring = smem + red_bytes<MT>();                     // [S][SB]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int ngroups = a.N / 32;
@@ -508,13 +510,18 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     int nblk[NU];
 #pragma unroll
                     for (int i = 0; i < NU; ++i) {
-                        const int c = cr.c + par + 4 * i, kb = K16 - 4 * c;
+                        const int c = cr.c + par + kGemmPar * i, kb = K16 - 4 * c;
                         nblk[i] = c < cr.ce ? (kb < 4 ? kb / 2 : 2) : 0;
                     }
                     q41_units<FMT, MT, NU>(acc, slot, w_off, x_off, s_off, nblk, lane);
                 } else {
-                    const int c = cr.c + par, kb = K16 - 4 * c;
-                    if (c < cr.ce) bf16_unit<FMT, MT>(acc, slot, w_off, x_off, kb < 4 ? kb : 4, lane);
+#pragma unroll
+                    for (int i = 0; i < NU; ++i) {
+                        const int c = cr.c + par + kGemmPar * i, kb = K16 - 4 * c;
+                        if (c < cr.ce)
+                            bf16_unit<FMT, MT>(acc, slot, w_off + kGemmPar * i * TB, x_off + 256 * kGemmPar * i,
+                                               kb < 4 ? kb : 4, lane);
+                    }
                 }
             }
             __syncwarp();
@@ -539,16 +546,19 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                 const int nseg = last - first + 1, seg = blockIdx.x - first;
                 constexpr int G4 = R * 32 / 4;   // one group's float4s
                 float4 *red4 = reinterpret_cast<float4 *>(red);
-                auto sum_par = [&](int gg, int e) {
-                    const float4 v0 = red4[(0 * 4 + gg) * G4 + e], v1 = red4[(1 * 4 + gg) * G4 + e];
-                    const float4 v2 = red4[(2 * 4 + gg) * G4 + e], v3 = red4[(3 * 4 + gg) * G4 + e];
-                    return make_float4(((v0.x + v1.x) + v2.x) + v3.x, ((v0.y + v1.y) + v2.y) + v3.y,
-                                       ((v0.z + v1.z) + v2.z) + v3.z, ((v0.w + v1.w) + v2.w) + v3.w);
+                auto sum_par = [&](int gg, int e) {   // parities added in order
+                    float4 v = red4[gg * G4 + e];
+#pragma unroll
+                    for (int pp = 1; pp < kGemmPar; ++pp) {
+                        const float4 w = red4[(pp * 4 + gg) * G4 + e];
+                        v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
+                    }
+                    return v;
                 };
                 if (nseg > 1) {
                     // this CTA's partial of the quad: 4 groups x R rows x 32 columns, summed over parities
-                    if (threadIdx.x < 4 * G4) {
-                        const int gg = threadIdx.x / G4, e = threadIdx.x % G4;
+                    for (int te = threadIdx.x; te < 4 * G4; te += kGemmThreads) {
+                        const int gg = te / G4, e = te % G4;
                         if (4 * q + gg < ngroups)
                             reinterpret_cast<float4 *>(a.part)[((size_t)(4 * q + gg) * a.maxseg + seg) * (kMaxRows * 8) + e] =
                                 sum_par(gg, e);
@@ -564,8 +574,8 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     compute_sync();
                     if (s_last) {
                         // every thread adds its float4 over the segments, in segment order
-                        if (threadIdx.x < 4 * G4) {
-                            const int gg = threadIdx.x / G4, e = threadIdx.x % G4;
+                        for (int te = threadIdx.x; te < 4 * G4; te += kGemmThreads) {
+                            const int gg = te / G4, e = te % G4;
                             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                             if (4 * q + gg < ngroups) {
                                 const float4 *pp = reinterpret_cast<const float4 *>(a.part) +
@@ -586,11 +596,19 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     }
                     compute_sync();
                 } else {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const int gg = threadIdx.x / G4, e = threadIdx.x % G4;
-                    if (threadIdx.x < 4 * G4) v = sum_par(gg, e);
+                    constexpr int PER = (4 * G4 + kGemmThreads - 1) / kGemmThreads;
+                    float4 v[PER];
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) {
+                        const int te = threadIdx.x + i * kGemmThreads;
+                        if (te < 4 * G4) v[i] = sum_par(te / G4, te % G4);
+                    }
                     compute_sync();
-                    if (threadIdx.x < 4 * G4) red4[gg * G4 + e] = v;
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) {
+                        const int te = threadIdx.x + i * kGemmThreads;
+                        if (te < 4 * G4) red4[te] = v[i];
+                    }
                     compute_sync();
                 }
                 const bool fin = nseg == 1 || s_last;
