@@ -87,6 +87,8 @@ SIGNATURES = {
     "dfl_act_pack": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
     "dfl_q41_gemm_scratch_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "dfl_q41_gemm": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]),
+    "dfl_q41_gemm_noalloc": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp]),
+    "dfl_q41_gemm_noalloc_max_scratch": (ctypes.c_int64, []),
 }
 
 _lib = None

@@ -16,6 +16,7 @@
 #include <cstring>
 #include <functional>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -1379,6 +1380,44 @@ int dfl_q41_gemm(const void *img, int K, int N, const void *act, int M, float *y
     a.cnt = static_cast<int *>(scratch);
     a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + cbytes);
     return launch_gemm(W_Q41, EPI_F32, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+}
+
+// ---- the product with library-owned scratch -------------------------------------------------------
+// One static device array holds the arrival counters and segment partials of dfl_q41_gemm_noalloc; its
+// address is looked up once per device and cached.
+}  // extern "C"
+
+namespace {
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+constexpr int kNoallocDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoallocDevices] = {};
+}  // namespace
+
+extern "C" {
+
+int64_t dfl_q41_gemm_noalloc_max_scratch(void) { return (int64_t)kNoallocScratchBytes; }
+
+int dfl_q41_gemm_noalloc(const void *img, int K, int N, const void *act, int M, float *y, void *stream) {
+    const int64_t need = dfl_q41_gemm_scratch_bytes(K, N, M);
+    if (need < 0 || !img || !act || !y) return DFL_E_INVALID_ARG;
+    if ((size_t)need > kNoallocScratchBytes) return DFL_E_CAPACITY;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocDevices) return DFL_E_CUDA;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            // the current device is `dev`: the address is this device's copy of the array
+            if (cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch) != cudaSuccess) {
+                g_noalloc_ptr[dev] = nullptr;
+                return DFL_E_CUDA;
+            }
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return dfl_q41_gemm(img, K, N, act, M, y, scratch, kNoallocScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -234,6 +234,25 @@ int64_t dfl_q41_gemm_scratch_bytes(int K, int N, int M);
 int dfl_q41_gemm(const void *dev_image, int K, int N, const void *dev_act, int M, float *dev_y,
                  void *dev_scratch, size_t scratch_bytes, void *cuda_stream);
 
+/* The same product for callers that cannot allocate device memory per call and have no scratch
+ * buffer of their own to pass: code that must keep every device allocation out of its call path (a
+ * fixed device-memory budget reserved up front), or hosts whose plug-in interface hands over only the
+ * input and output pointers. Nothing in the DFlash method corresponds to this entry point; it is a
+ * packaging of dfl_q41_gemm.
+ * Scratch: one array of dfl_q41_gemm_noalloc_max_scratch() bytes (4 MiB) in the library's static device
+ * memory. The first call on a device looks up that device's copy of the array (cudaGetSymbolAddress,
+ * with the device current) and caches its address; make that first call outside any stream capture.
+ * No call allocates or frees memory. Every call on a device uses the same array and leaves the last
+ * call's contents in it: the arrival counters at its start must be zero, which the zero-initialised
+ * array gives and every completed call restores; calls that overlap on the GPU race on it.
+ * Errors: DFL_E_INVALID_ARG for the shapes or pointers dfl_q41_gemm rejects; DFL_E_CAPACITY when
+ * dfl_q41_gemm_scratch_bytes(K, N, M) exceeds the array; DFL_E_CUDA when the address lookup or the
+ * launch fails. Arguments as for dfl_q41_gemm. */
+int dfl_q41_gemm_noalloc(const void *dev_image, int K, int N, const void *dev_act, int M, float *dev_y,
+                         void *cuda_stream);
+/* Bytes of the static scratch array behind dfl_q41_gemm_noalloc. */
+int64_t dfl_q41_gemm_noalloc_max_scratch(void);
+
 #ifdef __cplusplus
 }
 #endif
