@@ -152,6 +152,15 @@ def run_steps(eng, torch, table_dev, first_tok, snap, n0, steps, n_gen, host_row
     return tokens
 
 
+def combine_ranks(torch, ms: float, toks: float, device) -> tuple:
+    """Replicas: the job's time is the slowest rank's, its tokens the sum over ranks."""
+    t = torch.tensor([ms, toks], dtype=torch.float64, device=device)
+    mx = t.clone()
+    torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(mx[0]), float(t[1])
+
+
 def bench_cuda(args):
     import torch
     from dflash_speculative_decode_gb300 import build
@@ -196,11 +205,7 @@ def bench_cuda(args):
     ms = e0.elapsed_time(e1)
     clocks = clk.stop()
     if world > 1:
-        t = torch.tensor([ms, toks], dtype=torch.float64, device="cuda")
-        mx = t.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
-        ms, toks_all = float(mx[0]), float(t[1])
+        ms, toks_all = combine_ranks(torch, ms, toks, "cuda")
     else:
         toks_all = toks
     value = toks_all / (ms / 1e3)
