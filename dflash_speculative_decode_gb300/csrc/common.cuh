@@ -148,7 +148,9 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 
 // ---- GEMM interface ---------------------------------------------------------------------------------
 enum WFmt { W_Q41 = 0, W_BF16 = 1 };
-enum Epi { EPI_F32 = 0, EPI_GLU = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
+// EPI_PART: each CTA only writes its segment partial of every quad it touches (no fix-up); the
+// consumer adds the segments (PartView).
+enum Epi { EPI_F32 = 0, EPI_GLU = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3, EPI_PART = 4 };
 enum ArgmaxDst { AM_VERIFY = 0, AM_DRAFT = 1 };
 
 struct GemmArgs {
@@ -178,10 +180,37 @@ struct GemmArgs {
     int am_dst;            // AM_VERIFY: st->target[m] and st->accepted; AM_DRAFT: st->props[m]
 };
 
+// The segment partials a product launched with EPI_PART leaves: element (row m, column n) is the sum,
+// in segment order, of part[((n/32 * maxseg + s) * 16 + m) * 32 + n % 32] over the nseg segments of
+// quad q = n/128 (the CTAs whose unit ranges touch the quad's C chunks; the split of a grid of G CTAs
+// over U = quads * C units gives CTA b the units [b*U/G, (b+1)*U/G)).
+struct PartView {
+    const float *part;
+    int C, G, maxseg;
+    long U;
+};
+__host__ __device__ __forceinline__ long cta_of(long u, long U, int G) { return ((u + 1) * G - 1) / U; }
+__device__ __forceinline__ float part_sum(const PartView &v, int m, int n) {
+    const int grp = n >> 5, q = grp >> 2;
+    const long qa = (long)q * v.C;
+    const int nseg = int(cta_of(qa + v.C - 1, v.U, v.G) - cta_of(qa, v.U, v.G)) + 1;
+    const float *p = v.part + ((size_t)grp * v.maxseg * kMaxRows + m) * 32 + (n & 31);
+    float l[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) l[s] = s < nseg ? __ldcg(p + (size_t)s * kMaxRows * 32) : 0.f;
+    float y = 0.f;
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+        if (s < nseg) y += l[s];
+    for (int s = 16; s < nseg; ++s) y += __ldcg(p + (size_t)s * kMaxRows * 32);
+    return y;
+}
+
 // launchers (gemm.cu)
 int gemm_grid(int C, int N);
 int gemm_maxseg(int C, int N);
 size_t gemm_scratch_floats(int C, int N);
+size_t gemm_part_floats(int C, int N);   // partials of an EPI_PART launch
 cudaError_t launch_gemm(int fmt, int epi, const GemmArgs &a, cudaStream_t s);
 cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *sums, cudaStream_t s);
 inline size_t act_words(int K) { return (size_t)kMaxRows * K; }          // fragment words of a 16-row buffer
@@ -198,6 +227,8 @@ struct RowArgs {
     float *x;              // fp32 residual [M][H]
     const float *y;        // fp32 product [M][ldy] to add (nullable)
     int ldy;
+    PartView yp;           // or the product as segment partials (yp.part non-null; takes precedence)
+    float *y_out;          // the product's rows as fp32 [M][H] (nullable; for inspection)
     const uint16_t *w_post;   // RMSNorm weight applied to y before the add (nullable: plain add)
     float lambda;          // multiply x after the add (1 = none)
     float *tap;            // tap store base (nullable), row of position p at tap + p*ld_tap + tap_off

@@ -172,7 +172,7 @@ int fail(dfl_ctx *c, int code, const std::string &msg) {
 std::string validate(const dfl_config *g) {
     auto bad = [](const char *f) { return std::string("configuration: ") + f; };
     if (g->n_layers < 1 || g->n_layers > DFL_MAX_LAYERS) return bad("n_layers out of range 1..64");
-    if (g->hidden < 64 || g->hidden % 64 || g->hidden > 4096) return bad("hidden must be a multiple of 64, <= 4096");
+    if (g->hidden < 128 || g->hidden % 128 || g->hidden > 4096) return bad("hidden must be a multiple of 128, <= 4096");
     if (g->vocab < 16 || g->vocab % 16) return bad("vocab must be a multiple of 16");
     if (g->head_dim != 64 && g->head_dim != 128 && g->head_dim != 256) return bad("head_dim must be 64, 128 or 256");
     if (g->n_heads < 1 || (g->n_heads * g->head_dim) % 64) return bad("n_heads * head_dim must be a multiple of 64");
@@ -232,7 +232,7 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     auto qm = [&](QMat &m, int K, int N, bool q41) {
         m = qmat(K, N, q41);
         m.img = W.take<uint8_t>(q41 ? q41_image_bytes(K, N) : bf16_image_bytes(K, N));
-        part_floats = std::max(part_floats, gemm_scratch_floats(m.C, N));
+        part_floats = std::max(part_floats, gemm_part_floats(m.C, N));
         cnt_n = std::max(cnt_n, N / 32);
     };
     auto vec = [&](Vec &v, size_t n) {
@@ -417,6 +417,17 @@ cudaError_t gemm(dfl_ctx *c, const QMat &W, const Act &x, int row0, int M, int e
     if (e != cudaSuccess) return e;
     const double bytes = (W.q41 ? 0.625 : 2.0) * W.K * (double)W.N + 4.0 * M * W.K + 4.0 * M * W.N;
     return prof_end(c, slot, W.q41 ? 0 : 1, bytes);
+}
+
+// the segment partials an EPI_PART product of W leaves in the context's partial buffer
+PartView part_view(const dfl_ctx *c, const QMat &W) {
+    PartView v{};
+    v.part = c->part;
+    v.C = W.C;
+    v.G = gemm_grid(W.C, W.N);
+    v.maxseg = W.maxseg;
+    v.U = (long)((W.N / 32 + 3) / 4) * W.C;
+    return v;
 }
 
 cudaError_t head(dfl_ctx *c, const Act &x, int row0, int M, float *logits, int dst) {
@@ -608,33 +619,33 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
-        DFL_CK(gemm(c, L.o, c->o, 0, k, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, L.o, c->o, 0, k, EPI_PART, nullptr, 0));
         RowArgs r1 = rows(c, k, c->x);
-        r1.y = c->y;
-        r1.ldy = H;
+        r1.yp = part_view(c, L.o);
+        r1.y_out = c->y;
         r1.w_post = L.post_attn_norm.p;
         r1.w_next = L.pre_ffn_norm.p;
         r1.outf = c->h.f;
         r1.outs = c->h.s;
         DFL_LAUNCH(launch_rows(r1, c->stream));
         DFL_CK(gemm(c, L.gu, c->h, 0, k, EPI_GLU, nullptr, 0, &c->a));
-        DFL_CK(gemm(c, L.d, c->a, 0, k, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, L.d, c->a, 0, k, EPI_PART, nullptr, 0));
         const uint16_t *next = l + 1 < NL ? c->tl[l + 1].attn_norm.p : c->final_norm.p;
         int ti = 0;
         const bool tap = is_tap(g, l, &ti);
         RowArgs r2 = rows(c, k, c->x);
-        r2.y = c->y;
-        r2.ldy = H;
+        r2.yp = part_view(c, L.d);
+        r2.y_out = c->y;
         r2.w_post = L.post_ffn_norm.p;
         r2.outf = c->h.f;
         r2.outs = c->h.s;
         if (P) {
             DFL_LAUNCH(launch_rows(r2, c->stream));   // out = x: the gate's input
             DFL_CK(gemm(c, L.pg, c->h, 0, k, EPI_SILU_MUL, nullptr, 0, &c->z, c->ple_rows + (size_t)l * P, NL * P));
-            DFL_CK(gemm(c, L.pp, c->z, 0, k, EPI_F32, c->y, H));
+            DFL_CK(gemm(c, L.pp, c->z, 0, k, EPI_PART, nullptr, 0));
             r2 = rows(c, k, c->x);
-            r2.y = c->y;
-            r2.ldy = H;
+            r2.yp = part_view(c, L.pp);
+            r2.y_out = c->y;
             r2.w_post = L.ple_norm.p;
             r2.lambda = L.lambda;
             r2.outf = c->h.f;
@@ -802,21 +813,21 @@ int draft_body(dfl_ctx *c) {
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
-        DFL_CK(gemm(c, D.o, c->o, 0, B, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, D.o, c->o, 0, B, EPI_PART, nullptr, 0));
         RowArgs r1 = rows(c, B, c->x_d);
         r1.eps = g.d_eps;
-        r1.y = c->y;
-        r1.ldy = H;
+        r1.yp = part_view(c, D.o);
+        r1.y_out = c->y;
         r1.w_next = D.ffn_norm.p;
         r1.outf = c->hb.f;
         r1.outs = c->hb.s;
         DFL_LAUNCH(launch_rows(r1, c->stream));
         DFL_CK(gemm(c, D.gu, c->hb, 0, B, EPI_GLU, nullptr, 0, &c->a));
-        DFL_CK(gemm(c, D.d, c->a, 0, B, EPI_F32, c->y, H));
+        DFL_CK(gemm(c, D.d, c->a, 0, B, EPI_PART, nullptr, 0));
         RowArgs r2 = rows(c, B, c->x_d);
         r2.eps = g.d_eps;
-        r2.y = c->y;
-        r2.ldy = H;
+        r2.yp = part_view(c, D.d);
+        r2.y_out = c->y;
         r2.w_next = l + 1 < g.d_layers ? c->dl[l + 1].attn_norm.p : c->d_final_norm.p;
         const Act &nxt = l + 1 < g.d_layers ? c->hcat : c->hb;
         r2.outf = nxt.f;

@@ -382,7 +382,6 @@ __device__ __forceinline__ void epilogue(const GemmArgs &a, float (&acc)[2][MT][
 // never depends on how many rows the pass carries.
 constexpr int kGemmBlock = kGemmThreads + 32;   // + the copy warp
 
-__device__ __forceinline__ long cta_of(long u, long U, int G) { return ((u + 1) * G - 1) / U; }
 // barrier of the 16 compute warps only
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kGemmThreads) : "memory"); }
 
@@ -555,7 +554,15 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     }
                     return v;
                 };
-                if (nseg > 1) {
+                if (EPI == EPI_PART) {
+                    // the partial of every quad, the consumer adds the segments
+                    for (int te = threadIdx.x; te < 4 * G4; te += kGemmThreads) {
+                        const int gg = te / G4, e = te % G4;
+                        if (4 * q + gg < ngroups)
+                            reinterpret_cast<float4 *>(a.part)[((size_t)(4 * q + gg) * a.maxseg + seg) * (kMaxRows * 8) + e] =
+                                sum_par(gg, e);
+                    }
+                } else if (nseg > 1) {
                     // this CTA's partial of the quad: 4 groups x R rows x 32 columns, summed over parities
                     for (int te = threadIdx.x; te < 4 * G4; te += kGemmThreads) {
                         const int gg = te / G4, e = te % G4;
@@ -611,7 +618,7 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     }
                     compute_sync();
                 }
-                const bool fin = nseg == 1 || s_last;
+                const bool fin = EPI != EPI_PART && (nseg == 1 || s_last);
                 const int ngq = 4 * q + gq;
                 if (fin && par == 0 && ngq < ngroups) {
 #pragma unroll
@@ -829,6 +836,8 @@ size_t gemm_scratch_floats(int C, int N) {
     return ms > 1 ? (size_t)(N / 32) * ms * kMaxRows * 32 : 0;
 }
 
+size_t gemm_part_floats(int C, int N) { return (size_t)(N / 32) * gemm_maxseg(C, N) * kMaxRows * 32; }
+
 // dynamic shared memory of a product: the parity reduction buffer and the ring
 template <int FMT, int MT, int EPI>
 static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
@@ -873,6 +882,7 @@ cudaError_t launch_gemm(int fmt, int epi, const GemmArgs &a, cudaStream_t s) {
 #define DFL_GEMM_CASE(F, E) \
     if (fmt == F && epi == E) return two ? run_gemm<F, 2, E>(a, s) : run_gemm<F, 1, E>(a, s);
     DFL_GEMM_CASE(W_Q41, EPI_F32)
+    DFL_GEMM_CASE(W_Q41, EPI_PART)
     DFL_GEMM_CASE(W_Q41, EPI_GLU)
     DFL_GEMM_CASE(W_Q41, EPI_SILU_MUL)
     DFL_GEMM_CASE(W_BF16, EPI_F32)

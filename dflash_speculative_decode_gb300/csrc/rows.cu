@@ -69,88 +69,116 @@ cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Residual row kernel:
-//   x += RMSNorm(y, w_post) (or x += y), x *= lambda, tap = bf16(x), out = bf16(RMSNorm(x, w_next)).
-constexpr int kRowThreads = 256;
-constexpr int kRowMaxPer = 16;   // hidden <= 4096
+// thread-block cluster helpers
+// ---------------------------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// load a float from the shared memory of CTA `rank` of this cluster, at the offset of `p` in ours
+__device__ __forceinline__ float ld_cluster(const float *p, unsigned rank) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    unsigned ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
 
-__global__ void __launch_bounds__(kRowThreads) k_rows(RowArgs a) {
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int cluster, int block, size_t smem,
+                                      cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = cluster;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// Residual row kernel:
+//   x += RMSNorm(y, w_post) (or x += y), x *= lambda, tap = x, out = RMSNorm(x, w_next) in operand format.
+// One cluster of kRowCluster CTAs per row, each CTA H / kRowCluster columns with one thread per column.
+// Row sums are block sums added over the cluster in rank order (distributed shared memory), so every CTA
+// sees the same value and the result does not depend on how many rows the pass carries.
+// ---------------------------------------------------------------------------------------------------
+constexpr int kRowCluster = 8;
+constexpr int kRowThreads = 256;   // k_cast_rows
+constexpr int kRowMaxPer = 16;     // k_cast_rows: hidden <= 4096
+
+// sum of v over the cluster's threads; slot selects a shared word (one per reduction of the kernel)
+__device__ __forceinline__ float cluster_row_sum(float v, float *red, float *slots, int slot) {
+    const float b = block_sum(v, red);
+    if (threadIdx.x == 0) slots[slot] = b;
+    cluster_sync_all();
+    float t = 0.f;
+#pragma unroll
+    for (int r = 0; r < kRowCluster; ++r) t += ld_cluster(slots + slot, r);
+    return t;
+}
+
+__global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
+    __shared__ float red[33];
+    __shared__ float slots[2];
+    const int m = blockIdx.x / kRowCluster;
+    const unsigned rank = cluster_rank();
+    const int cols = a.H / kRowCluster;
+    const bool on = int(threadIdx.x) < cols;
+    const int h = int(rank) * cols + int(threadIdx.x);
     pdl_wait();
     pdl_trigger();
-    __shared__ float red[33];
-    const int m = blockIdx.x;
     const bool live = !a.rows_from_ctx || m < a.st->ctx_rows;
-    const int per = (a.H + kRowThreads - 1) / kRowThreads;
-    float xv[kRowMaxPer];
-    float *x = a.x ? a.x + (long)m * a.H : nullptr;
-#pragma unroll
-    for (int i = 0; i < kRowMaxPer; ++i) {
-        const int h = threadIdx.x + i * kRowThreads;
-        xv[i] = (i < per && h < a.H && x) ? x[h] : 0.f;
-    }
-    if (a.y) {
-        const float *y = a.y + (long)m * a.ldy;
-        float yv[kRowMaxPer];
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < kRowMaxPer; ++i) {
-            const int h = threadIdx.x + i * kRowThreads;
-            yv[i] = (i < per && h < a.H) ? y[h] : 0.f;
-            ss += yv[i] * yv[i];
-        }
-        float r = 1.f;
-        if (a.w_post) r = 1.0f / sqrtf(block_sum(ss, red) / a.H + a.eps);
-#pragma unroll
-        for (int i = 0; i < kRowMaxPer; ++i) {
-            const int h = threadIdx.x + i * kRowThreads;
-            if (i < per && h < a.H) xv[i] = a.w_post ? xv[i] + (yv[i] * r) * bf16_to_f32(a.w_post[h]) : xv[i] + yv[i];
+    float *xr = a.x ? a.x + (long)m * a.H : nullptr;
+    float x = (on && xr) ? xr[h] : 0.f;
+    const bool have_y = a.yp.part || a.y;
+    if (have_y) {
+        float y = 0.f;
+        if (on) y = a.yp.part ? part_sum(a.yp, m, h) : a.y[(long)m * a.ldy + h];
+        if (on && a.y_out) a.y_out[(long)m * a.H + h] = y;
+        if (a.w_post) {
+            const float r = 1.0f / sqrtf(cluster_row_sum(y * y, red, slots, 0) / a.H + a.eps);
+            if (on) x += (y * r) * bf16_to_f32(a.w_post[h]);
+        } else {
+            x += y;
         }
     }
-    if (a.lambda != 1.0f) {
-#pragma unroll
-        for (int i = 0; i < kRowMaxPer; ++i) xv[i] *= a.lambda;
-    }
-    if (x && (a.y || a.lambda != 1.0f)) {
-#pragma unroll
-        for (int i = 0; i < kRowMaxPer; ++i) {
-            const int h = threadIdx.x + i * kRowThreads;
-            if (i < per && h < a.H) x[h] = xv[i];
-        }
-    }
-    if (a.tap && live) {
+    if (a.lambda != 1.0f) x *= a.lambda;
+    if (on && xr && (have_y || a.lambda != 1.0f)) xr[h] = x;
+    if (on && a.tap && live) {
         const int pos = (a.pos_from_ctx ? a.st->draft_n : a.st->n) + m;
-        float *tp = a.tap + (long)pos * a.ld_tap + a.tap_off;
-#pragma unroll
-        for (int i = 0; i < kRowMaxPer; ++i) {
-            const int h = threadIdx.x + i * kRowThreads;
-            if (i < per && h < a.H) tp[h] = xv[i];
-        }
+        a.tap[(long)pos * a.ld_tap + a.tap_off + h] = x;
     }
     if (a.outf) {
         float r = 1.f;
-        if (a.w_next) {
-            float ss = 0.f;
-#pragma unroll
-            for (int i = 0; i < kRowMaxPer; ++i) ss += xv[i] * xv[i];
-            r = 1.0f / sqrtf(block_sum(ss, red) / a.H + a.eps);
-        }
+        if (a.w_next) r = 1.0f / sqrtf(cluster_row_sum(x * x, red, slots, 1) / a.H + a.eps);
         const int row = a.out_row0 + m;
-#pragma unroll
-        for (int i = 0; i < kRowMaxPer; ++i) {
-            if (i >= per) break;
-            const int h = threadIdx.x + i * kRowThreads;
-            float v = 0.f;
-            if (h < a.H && live) v = a.w_next ? (xv[i] * r) * bf16_to_f32(a.w_next[h]) : xv[i];
-            const float hl = h < a.H ? act_store(a.outf, a.H, row, h, v) : 0.f;
-            const float sg = half_warp_sum(hl);
-            if (h < a.H && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = sg;
-        }
+        float v = 0.f;
+        if (on && live) v = a.w_next ? (x * r) * bf16_to_f32(a.w_next[h]) : x;
+        const float hl = on ? act_store(a.outf, a.H, row, h, v) : 0.f;
+        const float sg = half_warp_sum(hl);   // 16 consecutive columns: cols is a multiple of 16
+        if (on && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = sg;
     }
+    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
 }
 
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
-    if (a.H > kRowThreads * kRowMaxPer || a.H % 16) return cudaErrorInvalidValue;
-    return launch_pdl(k_rows, dim3(a.M), dim3(kRowThreads), 0, s, a);
+    if (a.H % (16 * kRowCluster) || a.H / kRowCluster > 1024 || a.M < 1 || a.M > kMaxRows) return cudaErrorInvalidValue;
+    const int cols = a.H / kRowCluster;
+    return launch_cluster_pdl(k_rows, a.M * kRowCluster, kRowCluster, (cols + 31) / 32 * 32, 0, s, a);
 }
 
 // dst row (row0 + m) = RMSNorm(src[m], w) for live rows (m < st->ctx_rows when live_from_ctx), zeros
@@ -254,24 +282,6 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t s) {
 constexpr int kAttnThreads = 256;
 constexpr int kAttnKeys = 32;
 constexpr int kAttnCluster = 8;
-
-__device__ __forceinline__ unsigned cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// load a float from the shared memory of CTA `rank` of this cluster, at the offset of `p` in ours
-__device__ __forceinline__ float ld_cluster(const float *p, unsigned rank) {
-    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
-    unsigned ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-    return v;
-}
 
 size_t attn_smem(int hd) {
     return ((size_t)kMaxRows * hd + 4 * (size_t)kAttnKeys * (hd + 4) + (size_t)kMaxRows * kAttnKeys + 3 * kMaxRows) * 4;
