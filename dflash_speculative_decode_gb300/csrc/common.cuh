@@ -260,6 +260,8 @@ struct QkArgs {
     int M, nq, nkv, hd;
     const float *qkv;      // fp32 [M][ldq] (q | k | v)
     int ldq;
+    PartView qp;           // or the product as segment partials (qp.part non-null; takes precedence)
+    float *qkv_out;        // the product's rows as fp32 [.][ldq] (nullable; for inspection)
     int row0;              // first row of qkv that belongs to this group of rows
     const uint16_t *q_norm, *k_norm;
     float eps;

@@ -585,13 +585,14 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         TLayer &O = c->tl[L.owner];
         const bool own = L.owner == l;
         const int nqkv = L.qkv.N;
-        DFL_CK(gemm(c, L.qkv, c->h, 0, k, EPI_F32, c->qkv, nqkv));
+        DFL_CK(gemm(c, L.qkv, c->h, 0, k, EPI_PART, nullptr, 0));
         QkArgs qa{};
         qa.M = k;
         qa.nq = nq;
         qa.nkv = L.nkv;
         qa.hd = hd;
-        qa.qkv = c->qkv;
+        qa.qp = part_view(c, L.qkv);
+        qa.qkv_out = c->qkv;
         qa.ldq = nqkv;
         qa.q_norm = L.q_norm.p;
         qa.k_norm = own ? L.k_norm.p : nullptr;
@@ -705,7 +706,8 @@ QkArgs draft_qk(dfl_ctx *c, int l) {
     qa.nq = g.d_heads;
     qa.nkv = g.d_kv_heads;
     qa.hd = g.d_head_dim;
-    qa.qkv = c->qkv;
+    qa.qp = part_view(c, c->dl[l].qkv);
+    qa.qkv_out = c->qkv;
     qa.ldq = c->dl[l].qkv.N;
     qa.q_norm = c->dl[l].q_norm.p;
     qa.k_norm = c->dl[l].k_norm.p;
@@ -724,7 +726,7 @@ int run_ctx_only(dfl_ctx *c, int r) {
     if (rc) return rc;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
-        DFL_CK(gemm(c, D.qkv, c->hcat, 0, kMaxRows, EPI_F32, c->qkv, D.qkv.N));
+        DFL_CK(gemm(c, D.qkv, c->hcat, 0, kMaxRows, EPI_PART, nullptr, 0));
         QkArgs qa = draft_qk(c, l);
         qa.M = kMaxRows;
         qa.row0 = 0;
@@ -774,7 +776,7 @@ int draft_body(dfl_ctx *c) {
     const int dq = g.d_heads, dhd = g.d_head_dim;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
-        DFL_CK(gemm(c, D.qkv, c->hcat, 0, B + F, EPI_F32, c->qkv, D.qkv.N));
+        DFL_CK(gemm(c, D.qkv, c->hcat, 0, B + F, EPI_PART, nullptr, 0));
         QkArgs qb = draft_qk(c, l);
         qb.M = B;
         qb.pos_mode = 1;

@@ -232,13 +232,19 @@ __global__ void k_qk(QkArgs a) {
     const bool live = !a.live_from_ctx || m < a.st->ctx_rows;
     if (!live) return;
     const int pos = (a.pos_mode == 2 ? a.st->draft_n : a.st->n) + m;
-    const float *row = a.qkv + (long)(a.row0 + m) * a.ldq;
+    const int rr = a.row0 + m;
+    // column c of this row of the product (plain rows or segment partials); kept for inspection
+    auto val = [&](int c) -> float {
+        const float v = a.qp.part ? part_sum(a.qp, rr, c) : a.qkv[(long)rr * a.ldq + c];
+        if (a.qkv_out) a.qkv_out[(long)rr * a.ldq + c] = v;
+        return v;
+    };
     const int nqh = a.q_out ? a.nq : 0;
     const bool is_q = h < nqh;
     const int hk = h - nqh;
-    const float *src = is_q ? row + h * a.hd : row + (a.nq + hk) * a.hd;
+    const int c0 = is_q ? h * a.hd : (a.nq + hk) * a.hd;
     const uint16_t *w = is_q ? a.q_norm : a.k_norm;
-    float u0 = src[i], u1 = src[i + half];
+    float u0 = val(c0 + i), u1 = val(c0 + i + half);
     const float r = 1.0f / sqrtf(block_sum(u0 * u0 + u1 * u1, red) / a.hd + a.eps);
     u0 = (u0 * r) * bf16_to_f32(w[i]);
     u1 = (u1 * r) * bf16_to_f32(w[i + half]);
@@ -252,11 +258,11 @@ __global__ void k_qk(QkArgs a) {
         const long slot = a.cap > 0 ? (long)(pos % a.cap) : (long)m;
         float *k = a.k_store + (slot * a.nkv + hk) * a.hd;
         float *v = a.v_store + (slot * a.nkv + hk) * a.hd;
-        const float *vs = row + (a.nq + a.nkv + hk) * a.hd;
+        const int cv = (a.nq + a.nkv + hk) * a.hd;
         k[i] = o0;
         k[i + half] = o1;
-        v[i] = vs[i];
-        v[i + half] = vs[i + half];
+        v[i] = val(cv + i);
+        v[i + half] = val(cv + i + half);
     }
 }
 
