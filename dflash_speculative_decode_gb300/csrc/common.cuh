@@ -115,6 +115,41 @@ __device__ __forceinline__ float act_store(uint32_t *f, int K, int tok, int k, f
     return bf16_to_f32(hi) + bf16_to_f32(lo);
 }
 
+// ---- mbarriers and bulk asynchronous copies ----------------------------------------------------------
+__device__ __forceinline__ unsigned saddr(const void *p) { return static_cast<unsigned>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void mbar_init(uint64_t *b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+// one arrival that also announces `bytes` of asynchronous copies completing on the barrier
+__device__ __forceinline__ void mbar_expect(uint64_t *b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t *b, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false if it did not complete within the limit.
+constexpr int kWaitPolls = 1 << 18;
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity) {
+    for (int i = 0; i < kWaitPolls; ++i)
+        if (mbar_test(b, parity)) return true;
+    return false;
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16) completing on barrier b
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *b) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(saddr(dst)),
+                 "l"(src), "r"(bytes), "r"(saddr(b))
+                 : "memory");
+}
+
 // Sum over the 16 lanes of a half warp (all 32 lanes must call).
 __device__ __forceinline__ float half_warp_sum(float v) {
 #pragma unroll
@@ -286,6 +321,7 @@ struct AttnArgs {
                            // 1: draft (A keys max(0,n-window)..n-1 for every row, plus all B keys)
     const DevState *st;
     float scale;
+    int *err;              // sticky error bits (nullable), kErrWaitTimeout
     uint32_t *outf;        // [M][nq*hd] in operand format
     float *outs;
 };

@@ -617,6 +617,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.mode = 0;
         aa.st = c->st;
         aa.scale = 1.0f / sqrtf((float)hd);
+        aa.err = &c->st->err;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
@@ -812,6 +813,7 @@ int draft_body(dfl_ctx *c) {
         aa.mode = 1;
         aa.st = c->st;
         aa.scale = 1.0f / sqrtf((float)dhd);
+        aa.err = &c->st->err;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_C(3, launch_attn(aa, c->stream));

@@ -304,6 +304,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     float *Mx = Sc + kMaxRows;                      // [16] running max
     float *Ls = Mx + kMaxRows;                      // [16] running sum
     float *Os = Kb;                                 // [16][hd] final state (after the last block)
+    __shared__ __align__(8) uint64_t kvbar[2];      // completion of the two key/value buffers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x / kAttnCluster;
     const unsigned rank = cluster_rank();
@@ -328,40 +329,46 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     const int nAmine = b0 <= bA1 ? (bA1 - b0) / kAttnCluster + 1 : 0;
     const int nmine = nAmine + ((bV >= 0 && bV % kAttnCluster == (int)rank) ? 1 : 0);
 
+    // warp 0: one bulk copy per key row of K and of V (rows outside every row's range are zeroed,
+    // they are masked and 0 * v must stay 0); completion on the buffer's mbarrier
     auto load_block = [&](int i, int buf) {
         float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
         const bool virt = i >= nAmine;
         const int b = virt ? bV : b0 + kAttnCluster * i;
-        for (int e = tid; e < kAttnKeys * hd4; e += kAttnThreads) {
-            const int j = e / hd4, d4 = e % hd4;
-            const float *ksrc = nullptr, *vsrc = nullptr;
-            if (virt) {
-                if (j < a.nB) {
-                    const long off = ((long)j * a.nkv + g) * hd + 4 * d4;
-                    ksrc = a.kB + off;
-                    vsrc = a.vB + off;
-                }
-            } else {
-                const int pos = kAttnKeys * b + j;
-                if (pos >= lo && pos <= hi) {
-                    const long off = ((long)(pos % a.capA) * a.nkv + g) * hd + 4 * d4;
-                    ksrc = a.kA + off;
-                    vsrc = a.vA + off;
-                }
-            }
-            float *kd = K + j * ldk + 4 * d4, *vd = V + j * ldk + 4 * d4;
-            if (ksrc) {
-                cp_async16(kd, ksrc);
-                cp_async16(vd, vsrc);
-            } else {   // keys outside every row's range: zeros (they are masked; 0 * v must stay 0)
-                *reinterpret_cast<float4 *>(kd) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(vd) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int j = lane;
+        long off = -1;
+        const float *kbase = a.kA, *vbase = a.vA;
+        if (virt) {
+            if (j < a.nB) off = ((long)j * a.nkv + g) * hd;
+            kbase = a.kB;
+            vbase = a.vB;
+        } else {
+            const int pos = kAttnKeys * b + j;
+            if (pos >= lo && pos <= hi) off = ((long)(pos % a.capA) * a.nkv + g) * hd;
+        }
+        const unsigned nvalid = __popc(__ballot_sync(0xffffffffu, off >= 0));
+        // the previous readers of this buffer are behind a barrier; order them before the async writes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (lane == 0) mbar_expect(&kvbar[buf], nvalid * 2u * unsigned(hd) * 4u);
+        __syncwarp();
+        if (off >= 0) {
+            bulk_g2s(K + j * ldk, kbase + off, unsigned(hd) * 4u, &kvbar[buf]);
+            bulk_g2s(V + j * ldk, vbase + off, unsigned(hd) * 4u, &kvbar[buf]);
+        } else {
+            for (int d4 = 0; d4 < hd4; ++d4) {
+                *reinterpret_cast<float4 *>(K + j * ldk + 4 * d4) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(V + j * ldk + 4 * d4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        cp_async_commit();
     };
 
-    if (nmine > 0) load_block(0, 0);
+    if (tid == 0) {
+        mbar_init(&kvbar[0], 1);
+        mbar_init(&kvbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == 0 && nmine > 0) load_block(0, 0);
     for (int e = tid; e < kMaxRows * hd4; e += kAttnThreads) {
         const int m = e / hd4, d4 = e % hd4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -370,57 +377,66 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     }
     if (tid < kMaxRows) Mx[tid] = -INFINITY, Ls[tid] = 0.f;
 
-    // p.V ownership: thread -> float4 column c4 of rows rg, rg + RG, ...
+    // p.V ownership: thread -> float4 column c4 of rows rg, rg + RG, ... (rows of the pass only)
     const int RG = kAttnThreads / hd4;
     const int c4 = tid % hd4, rg = tid / hd4;
-    const bool pv_on = rg < RG;
+    const bool pv_on = rg < RG && rg < M;
     float4 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool bad = false;
 
     for (int i = 0; i < nmine; ++i) {
         const int buf = i & 1;
-        if (i + 1 < nmine) {
-            load_block(i + 1, buf ^ 1);
-            cp_async_wait_group1();
-        } else {
-            cp_async_wait_all();
-        }
-        __syncthreads();
+        if (warp == 0 && i + 1 < nmine) load_block(i + 1, buf ^ 1);   // its buffer was released last round
+        if (!mbar_wait(&kvbar[buf], unsigned(i >> 1) & 1u)) bad = true;
+        __syncthreads();   // the zeroed rows written by warp 0 are visible too
         const float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
         const bool virt = i >= nAmine;
         const int b = virt ? bV : b0 + kAttnCluster * i;
-        // scores: warp -> rows warp, warp + 8; lane -> key
-        {
+        // scores: warp -> rows warp, warp + 8 (those the pass carries); lane -> key
+        const bool two = warp + 8 < M;
+        if (warp < M) {
             const int j = lane;
             float s[2] = {0.f, 0.f};
             const float4 *kr = reinterpret_cast<const float4 *>(K + j * ldk);
             const float4 *q0 = reinterpret_cast<const float4 *>(Qs + warp * hd);
             const float4 *q1 = reinterpret_cast<const float4 *>(Qs + (warp + 8) * hd);
-            for (int d4 = 0; d4 < hd4; ++d4) {
-                const float4 k = kr[d4], x0 = q0[d4], x1 = q1[d4];
-                s[0] = fmaf(x0.x, k.x, s[0]);
-                s[0] = fmaf(x0.y, k.y, s[0]);
-                s[0] = fmaf(x0.z, k.z, s[0]);
-                s[0] = fmaf(x0.w, k.w, s[0]);
-                s[1] = fmaf(x1.x, k.x, s[1]);
-                s[1] = fmaf(x1.y, k.y, s[1]);
-                s[1] = fmaf(x1.z, k.z, s[1]);
-                s[1] = fmaf(x1.w, k.w, s[1]);
+            if (two) {
+                for (int d4 = 0; d4 < hd4; ++d4) {
+                    const float4 k = kr[d4], x0 = q0[d4], x1 = q1[d4];
+                    s[0] = fmaf(x0.x, k.x, s[0]);
+                    s[0] = fmaf(x0.y, k.y, s[0]);
+                    s[0] = fmaf(x0.z, k.z, s[0]);
+                    s[0] = fmaf(x0.w, k.w, s[0]);
+                    s[1] = fmaf(x1.x, k.x, s[1]);
+                    s[1] = fmaf(x1.y, k.y, s[1]);
+                    s[1] = fmaf(x1.z, k.z, s[1]);
+                    s[1] = fmaf(x1.w, k.w, s[1]);
+                }
+            } else {
+                for (int d4 = 0; d4 < hd4; ++d4) {
+                    const float4 k = kr[d4], x0 = q0[d4];
+                    s[0] = fmaf(x0.x, k.x, s[0]);
+                    s[0] = fmaf(x0.y, k.y, s[0]);
+                    s[0] = fmaf(x0.z, k.z, s[0]);
+                    s[0] = fmaf(x0.w, k.w, s[0]);
+                }
             }
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int m = warp + 8 * r;
-                bool vis = m < M;
+                if (m >= M) break;
+                bool vis;
                 if (virt) {
-                    vis = vis && j < a.nB;
+                    vis = j < a.nB;
                 } else {
                     const int pos = kAttnKeys * b + j;
                     if (a.mode == 0) {
                         const int p = n + m;
-                        vis = vis && pos <= p && (a.window <= 0 || pos > p - a.window) && pos >= 0;
+                        vis = pos <= p && (a.window <= 0 || pos > p - a.window) && pos >= 0;
                     } else {
-                        vis = vis && pos >= lo && pos <= hi;
+                        vis = pos >= lo && pos <= hi;
                     }
                 }
                 const float sv = vis ? s[r] * a.scale : -INFINITY;
@@ -449,7 +465,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int m = rg + RG * r;
-                if (m < kMaxRows) {
+                if (m < M) {
                     const float sc = Sc[m];
                     acc[r].x *= sc, acc[r].y *= sc, acc[r].z *= sc, acc[r].w *= sc;
                 }
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int m = rg + RG * r;
-                    if (m < kMaxRows) {
+                    if (m < M) {
                         const float p = Ps[m * kAttnKeys + j];
                         acc[r].x = fmaf(p, v.x, acc[r].x);
                         acc[r].y = fmaf(p, v.y, acc[r].y);
@@ -469,14 +485,15 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                 }
             }
         }
-        __syncthreads();   // the buffer is refilled two blocks later
+        __syncthreads();   // the buffer is refilled in the next round
     }
+    if (bad && a.err) atomicOr(a.err, kErrWaitTimeout);
     // publish this CTA's state, then merge the cluster's states in rank order
     if (pv_on) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int m = rg + RG * r;
-            if (m < kMaxRows) *reinterpret_cast<float4 *>(Os + m * hd + 4 * c4) = acc[r];
+            if (m < M) *reinterpret_cast<float4 *>(Os + m * hd + 4 * c4) = acc[r];
         }
     }
     cluster_sync_all();
