@@ -290,21 +290,20 @@ constexpr int kAttnKeys = 32;
 constexpr int kAttnCluster = 8;
 
 size_t attn_smem(int hd) {
-    return ((size_t)kMaxRows * hd + 4 * (size_t)kAttnKeys * (hd + 4) + (size_t)kMaxRows * kAttnKeys + 3 * kMaxRows) * 4;
+    return ((size_t)kMaxRows * (hd + 4) + 4 * (size_t)kAttnKeys * (hd + 4) + (size_t)kMaxRows * kAttnKeys + 3 * kMaxRows) * 4;
 }
 
 __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int hd = a.hd, ldk = hd + 4, hd4 = hd / 4;
-    float *Qs = sm;                                 // [16][hd] this head's query rows
-    float *Kb = Qs + kMaxRows * hd;                 // [2][32][ldk] double-buffered key block
+    float *Qs = sm;                                 // [16][ldk] this head's query rows
+    float *Kb = Qs + kMaxRows * ldk;                // [2][32][ldk] double-buffered key block
     float *Vb = Kb + 2 * kAttnKeys * ldk;           // [2][32][ldk]
-    float *Ps = Vb + 2 * kAttnKeys * ldk;           // [16][32] probabilities of the current block
+    float *Ps = Vb + 2 * kAttnKeys * ldk;           // [16][32] scores, then probabilities, of the current block
     float *Sc = Ps + kMaxRows * kAttnKeys;          // [16] rescale of the running sums
     float *Mx = Sc + kMaxRows;                      // [16] running max
     float *Ls = Mx + kMaxRows;                      // [16] running sum
     float *Os = Kb;                                 // [16][hd] final state (after the last block)
-    __shared__ __align__(8) uint64_t kvbar[2];      // completion of the two key/value buffers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x / kAttnCluster;
     const unsigned rank = cluster_rank();
@@ -329,51 +328,50 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     const int nAmine = b0 <= bA1 ? (bA1 - b0) / kAttnCluster + 1 : 0;
     const int nmine = nAmine + ((bV >= 0 && bV % kAttnCluster == (int)rank) ? 1 : 0);
 
-    // warp 0: one bulk copy per key row of K and of V (rows outside every row's range are zeroed,
-    // they are masked and 0 * v must stay 0); completion on the buffer's mbarrier
+    // every warp: keys 4w..4w+3 of the block, 16-byte asynchronous copies by the lanes (rows outside
+    // every row's range are zeroed: they are masked, and 0 * v must stay 0); one commit group per block
     auto load_block = [&](int i, int buf) {
         float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
         const bool virt = i >= nAmine;
         const int b = virt ? bV : b0 + kAttnCluster * i;
-        const int j = lane;
-        long off = -1;
-        const float *kbase = a.kA, *vbase = a.vA;
-        if (virt) {
-            if (j < a.nB) off = ((long)j * a.nkv + g) * hd;
-            kbase = a.kB;
-            vbase = a.vB;
-        } else {
-            const int pos = kAttnKeys * b + j;
-            if (pos >= lo && pos <= hi) off = ((long)(pos % a.capA) * a.nkv + g) * hd;
-        }
-        const unsigned nvalid = __popc(__ballot_sync(0xffffffffu, off >= 0));
-        // the previous readers of this buffer are behind a barrier; order them before the async writes
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (lane == 0) mbar_expect(&kvbar[buf], nvalid * 2u * unsigned(hd) * 4u);
-        __syncwarp();
-        if (off >= 0) {
-            bulk_g2s(K + j * ldk, kbase + off, unsigned(hd) * 4u, &kvbar[buf]);
-            bulk_g2s(V + j * ldk, vbase + off, unsigned(hd) * 4u, &kvbar[buf]);
-        } else {
-            for (int d4 = 0; d4 < hd4; ++d4) {
-                *reinterpret_cast<float4 *>(K + j * ldk + 4 * d4) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(V + j * ldk + 4 * d4) = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < kAttnKeys / (kAttnThreads / 32); ++kk) {
+            const int j = warp * (kAttnKeys / (kAttnThreads / 32)) + kk;
+            const float *ks = nullptr, *vs = nullptr;
+            if (virt) {
+                if (j < a.nB) {
+                    const long off = ((long)j * a.nkv + g) * hd;
+                    ks = a.kB + off;
+                    vs = a.vB + off;
+                }
+            } else {
+                const int pos = kAttnKeys * b + j;
+                if (pos >= lo && pos <= hi) {
+                    const long off = ((long)(pos % a.capA) * a.nkv + g) * hd;
+                    ks = a.kA + off;
+                    vs = a.vA + off;
+                }
+            }
+            for (int d4 = lane; d4 < hd4; d4 += 32) {
+                float *kd = K + j * ldk + 4 * d4, *vd = V + j * ldk + 4 * d4;
+                if (ks) {
+                    cp_async16(kd, ks + 4 * d4);
+                    cp_async16(vd, vs + 4 * d4);
+                } else {
+                    *reinterpret_cast<float4 *>(kd) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *reinterpret_cast<float4 *>(vd) = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
         }
+        cp_async_commit();
     };
 
-    if (tid == 0) {
-        mbar_init(&kvbar[0], 1);
-        mbar_init(&kvbar[1], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    if (warp == 0 && nmine > 0) load_block(0, 0);
+    if (nmine > 0) load_block(0, 0);
     for (int e = tid; e < kMaxRows * hd4; e += kAttnThreads) {
         const int m = e / hd4, d4 = e % hd4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (m < M) v = *reinterpret_cast<const float4 *>(a.q + ((long)m * a.nq + h) * hd + 4 * d4);
-        *reinterpret_cast<float4 *>(Qs + m * hd + 4 * d4) = v;
+        *reinterpret_cast<float4 *>(Qs + m * ldk + 4 * d4) = v;
     }
     if (tid < kMaxRows) Mx[tid] = -INFINITY, Ls[tid] = 0.f;
 
@@ -384,79 +382,78 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     float4 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    bool bad = false;
 
     for (int i = 0; i < nmine; ++i) {
         const int buf = i & 1;
-        if (warp == 0 && i + 1 < nmine) load_block(i + 1, buf ^ 1);   // its buffer was released last round
-        if (!mbar_wait(&kvbar[buf], unsigned(i >> 1) & 1u)) bad = true;
-        __syncthreads();   // the zeroed rows written by warp 0 are visible too
+        if (i + 1 < nmine) {
+            load_block(i + 1, buf ^ 1);   // its buffer was released at the end of the last round
+            cp_async_wait_group1();
+        } else {
+            cp_async_wait_all();
+        }
+        __syncthreads();
         const float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
         const bool virt = i >= nAmine;
         const int b = virt ? bV : b0 + kAttnCluster * i;
-        // scores: warp -> rows warp, warp + 8 (those the pass carries); lane -> key
-        const bool two = warp + 8 < M;
-        if (warp < M) {
-            const int j = lane;
-            float s[2] = {0.f, 0.f};
+        // raw scores: warp w -> keys 4w..4w+3 (lane / 8), lane % 8 -> rows lane % 8 and + 8; each key row
+        // is read once per warp, four independent partial sums per dot product
+        {
+            const int j = (kAttnKeys / (kAttnThreads / 32)) * warp + (lane >> 3);
             const float4 *kr = reinterpret_cast<const float4 *>(K + j * ldk);
-            const float4 *q0 = reinterpret_cast<const float4 *>(Qs + warp * hd);
-            const float4 *q1 = reinterpret_cast<const float4 *>(Qs + (warp + 8) * hd);
-            if (two) {
-                for (int d4 = 0; d4 < hd4; ++d4) {
-                    const float4 k = kr[d4], x0 = q0[d4], x1 = q1[d4];
-                    s[0] = fmaf(x0.x, k.x, s[0]);
-                    s[0] = fmaf(x0.y, k.y, s[0]);
-                    s[0] = fmaf(x0.z, k.z, s[0]);
-                    s[0] = fmaf(x0.w, k.w, s[0]);
-                    s[1] = fmaf(x1.x, k.x, s[1]);
-                    s[1] = fmaf(x1.y, k.y, s[1]);
-                    s[1] = fmaf(x1.z, k.z, s[1]);
-                    s[1] = fmaf(x1.w, k.w, s[1]);
-                }
-            } else {
-                for (int d4 = 0; d4 < hd4; ++d4) {
-                    const float4 k = kr[d4], x0 = q0[d4];
-                    s[0] = fmaf(x0.x, k.x, s[0]);
-                    s[0] = fmaf(x0.y, k.y, s[0]);
-                    s[0] = fmaf(x0.z, k.z, s[0]);
-                    s[0] = fmaf(x0.w, k.w, s[0]);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int m = (lane & 7) + 8 * rr;
+                if (m < M) {
+                    const float4 *qr = reinterpret_cast<const float4 *>(Qs + m * ldk);
+                    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (int d4 = 0; d4 < hd4; ++d4) {
+                        const float4 k = kr[d4], x = qr[d4];
+                        t.x = fmaf(x.x, k.x, t.x);
+                        t.y = fmaf(x.y, k.y, t.y);
+                        t.z = fmaf(x.z, k.z, t.z);
+                        t.w = fmaf(x.w, k.w, t.w);
+                    }
+                    Ps[m * kAttnKeys + j] = (t.x + t.y) + (t.z + t.w);
                 }
             }
+        }
+        __syncthreads();
+        // softmax update: warp -> rows warp, warp + 8; lane -> key
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int m = warp + 8 * r;
-                if (m >= M) break;
-                bool vis;
-                if (virt) {
-                    vis = j < a.nB;
+        for (int r = 0; r < 2; ++r) {
+            const int m = warp + 8 * r;
+            if (m >= M) break;
+            const int j = lane;
+            bool vis;
+            if (virt) {
+                vis = j < a.nB;
+            } else {
+                const int pos = kAttnKeys * b + j;
+                if (a.mode == 0) {
+                    const int p = n + m;
+                    vis = pos <= p && (a.window <= 0 || pos > p - a.window) && pos >= 0;
                 } else {
-                    const int pos = kAttnKeys * b + j;
-                    if (a.mode == 0) {
-                        const int p = n + m;
-                        vis = pos <= p && (a.window <= 0 || pos > p - a.window) && pos >= 0;
-                    } else {
-                        vis = pos >= lo && pos <= hi;
-                    }
+                    vis = pos >= lo && pos <= hi;
                 }
-                const float sv = vis ? s[r] * a.scale : -INFINITY;
-                float bm = sv;
+            }
+            const float sv = vis ? Ps[m * kAttnKeys + j] * a.scale : -INFINITY;
+            float bm = sv;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-                const float mo = Mx[m];
-                const float mn = fmaxf(mo, bm);
-                const float pj = vis ? expf(sv - mn) : 0.f;
-                float ps = pj;
+            for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+            const float mo = Mx[m];
+            const float mn = fmaxf(mo, bm);
+            const float pj = vis ? expf(sv - mn) : 0.f;
+            float ps = pj;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-                const float sc = mo == -INFINITY ? 0.f : expf(mo - mn);
-                Ps[m * kAttnKeys + j] = pj;
-                __syncwarp();
-                if (lane == 0) {
-                    Sc[m] = sc;
-                    Mx[m] = mn;
-                    Ls[m] = fmaf(Ls[m], sc, ps);
-                }
+            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            const float sc = mo == -INFINITY ? 0.f : expf(mo - mn);
+            Ps[m * kAttnKeys + j] = pj;
+            __syncwarp();
+            if (lane == 0) {
+                Sc[m] = sc;
+                Mx[m] = mn;
+                Ls[m] = fmaf(Ls[m], sc, ps);
             }
         }
         __syncthreads();
@@ -487,7 +484,6 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         }
         __syncthreads();   // the buffer is refilled in the next round
     }
-    if (bad && a.err) atomicOr(a.err, kErrWaitTimeout);
     // publish this CTA's state, then merge the cluster's states in rank order
     if (pv_on) {
 #pragma unroll
