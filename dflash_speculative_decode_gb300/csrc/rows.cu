@@ -289,22 +289,44 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnKeys = 32;
 constexpr int kAttnCluster = 8;
 
+// Both products of a block run on the tensor cores (mma.m16n8k16, bf16 in, fp32 accumulate) with every
+// fp32 operand split into bf16 hi + lo and the three products hi*hi + hi*lo + lo*hi added (the lo*lo
+// term is below fp32 rounding): scores S = Q K^T (16 rows x 32 keys) and O += P V.
+//   Scores: warp w takes keys 8*(w%4) .. +7 and half w/4 of the head dimension; the two halves'
+//   partial scores are added in the softmax step (half 0 first).
+//   p.V: warp w takes head-dimension columns 8*(w + 8t) .. +7 for t < hd/64, all 16 rows, all 32 keys.
+// Row pitches (fp32 words): queries and keys hd+8 (fragment loads of 8 rows x 4 column pairs hit 32
+// banks), values hd+4 (fragment loads of 4 row pairs x 8 columns hit 32 banks).
+constexpr int kAttnKS = 8;   // k-steps of 16 per half of the head dimension (hd <= 256)
+constexpr int kAttnNT = 4;   // 8-column tiles per warp in p.V (hd <= 256)
+constexpr int kAttnSP = 40;  // pitch of the score and probability rows (32 keys + 8)
+
 size_t attn_smem(int hd) {
-    return ((size_t)kMaxRows * (hd + 4) + 4 * (size_t)kAttnKeys * (hd + 4) + (size_t)kMaxRows * kAttnKeys + 3 * kMaxRows) * 4;
+    return ((size_t)kMaxRows * (hd + 8) + 2 * (size_t)kAttnKeys * (hd + 8) + 2 * (size_t)kAttnKeys * (hd + 4) +
+            3 * (size_t)kMaxRows * kAttnSP + 3 * kMaxRows) * 4;
+}
+
+// fp32 pair -> bf16x2 hi and lo (x = hi + lo to 2^-17 relative), lower element in the low half
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const uint16_t h0 = f32_to_bf16(x0), h1 = f32_to_bf16(x1);
+    const uint16_t l0 = f32_to_bf16(x0 - bf16_to_f32(h0)), l1 = f32_to_bf16(x1 - bf16_to_f32(h1));
+    hi = uint32_t(h0) | (uint32_t(h1) << 16);
+    lo = uint32_t(l0) | (uint32_t(l1) << 16);
 }
 
 __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     extern __shared__ __align__(16) float sm[];
-    const int hd = a.hd, ldk = hd + 4, hd4 = hd / 4;
-    float *Qs = sm;                                 // [16][ldk] this head's query rows
-    float *Kb = Qs + kMaxRows * ldk;                // [2][32][ldk] double-buffered key block
-    float *Vb = Kb + 2 * kAttnKeys * ldk;           // [2][32][ldk]
-    float *Ps = Vb + 2 * kAttnKeys * ldk;           // [16][32] scores, then probabilities, of the current block
-    float *Sc = Ps + kMaxRows * kAttnKeys;          // [16] rescale of the running sums
+    const int hd = a.hd, ldq = hd + 8, ldv = hd + 4, hd4 = hd / 4;
+    float *Qs = sm;                                 // [16][ldq] this head's query rows
+    float *Kb = Qs + kMaxRows * ldq;                // [2][32][ldq] double-buffered key block
+    float *Vb = Kb + 2 * kAttnKeys * ldq;           // [2][32][ldv]
+    float *Sp = Vb + 2 * kAttnKeys * ldv;           // [2][16][kAttnSP] partial scores per half
+    float *Ps = Sp + 2 * kMaxRows * kAttnSP;        // [16][kAttnSP] probabilities of the current block
+    float *Sc = Ps + kMaxRows * kAttnSP;            // [16] rescale of the running sums
     float *Mx = Sc + kMaxRows;                      // [16] running max
     float *Ls = Mx + kMaxRows;                      // [16] running sum
     float *Os = Kb;                                 // [16][hd] final state (after the last block)
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
     const int h = blockIdx.x / kAttnCluster;
     const unsigned rank = cluster_rank();
     const int g = h / (a.nq / a.nkv);
@@ -331,7 +353,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     // every warp: keys 4w..4w+3 of the block, 16-byte asynchronous copies by the lanes (rows outside
     // every row's range are zeroed: they are masked, and 0 * v must stay 0); one commit group per block
     auto load_block = [&](int i, int buf) {
-        float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
+        float *K = Kb + buf * kAttnKeys * ldq, *V = Vb + buf * kAttnKeys * ldv;
         const bool virt = i >= nAmine;
         const int b = virt ? bV : b0 + kAttnCluster * i;
 #pragma unroll
@@ -353,7 +375,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                 }
             }
             for (int d4 = lane; d4 < hd4; d4 += 32) {
-                float *kd = K + j * ldk + 4 * d4, *vd = V + j * ldk + 4 * d4;
+                float *kd = K + j * ldq + 4 * d4, *vd = V + j * ldv + 4 * d4;
                 if (ks) {
                     cp_async16(kd, ks + 4 * d4);
                     cp_async16(vd, vs + 4 * d4);
@@ -371,17 +393,34 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         const int m = e / hd4, d4 = e % hd4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (m < M) v = *reinterpret_cast<const float4 *>(a.q + ((long)m * a.nq + h) * hd + 4 * d4);
-        *reinterpret_cast<float4 *>(Qs + m * ldk + 4 * d4) = v;
+        *reinterpret_cast<float4 *>(Qs + m * ldq + 4 * d4) = v;
     }
     if (tid < kMaxRows) Mx[tid] = -INFINITY, Ls[tid] = 0.f;
+    __syncthreads();
 
-    // p.V ownership: thread -> float4 column c4 of rows rg, rg + RG, ... (rows of the pass only)
-    const int RG = kAttnThreads / hd4;
-    const int c4 = tid % hd4, rg = tid / hd4;
-    const bool pv_on = rg < RG && rg < M;
-    float4 acc[4];
+    // this warp's query fragments (A operand, rows 0..15, its half of the head dimension), hi and lo
+    const int kg = warp & 3, kh = warp >> 2;
+    const int ksn = hd / 32;                       // k-steps per half
+    uint32_t qh[kAttnKS][4], ql[kAttnKS][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < kAttnKS; ++s) {
+        if (s < ksn) {
+            const int c = 16 * (kh * ksn + s) + 2 * tq;
+            const float2 x0 = *reinterpret_cast<const float2 *>(Qs + gq * ldq + c);
+            const float2 x1 = *reinterpret_cast<const float2 *>(Qs + (gq + 8) * ldq + c);
+            const float2 x2 = *reinterpret_cast<const float2 *>(Qs + gq * ldq + c + 8);
+            const float2 x3 = *reinterpret_cast<const float2 *>(Qs + (gq + 8) * ldq + c + 8);
+            split2(x0.x, x0.y, qh[s][0], ql[s][0]);
+            split2(x1.x, x1.y, qh[s][1], ql[s][1]);
+            split2(x2.x, x2.y, qh[s][2], ql[s][2]);
+            split2(x3.x, x3.y, qh[s][3], ql[s][3]);
+        }
+    }
+    // p.V accumulators: tiles nt = warp + 8t (columns 8nt .. 8nt+7), C fragment layout
+    const int ntn = hd / 64;
+    float o[kAttnNT][4];
+#pragma unroll
+    for (int t = 0; t < kAttnNT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
 
     for (int i = 0; i < nmine; ++i) {
         const int buf = i & 1;
@@ -392,31 +431,30 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
             cp_async_wait_all();
         }
         __syncthreads();
-        const float *K = Kb + buf * kAttnKeys * ldk, *V = Vb + buf * kAttnKeys * ldk;
+        const float *K = Kb + buf * kAttnKeys * ldq, *V = Vb + buf * kAttnKeys * ldv;
         const bool virt = i >= nAmine;
         const int b = virt ? bV : b0 + kAttnCluster * i;
-        // raw scores: warp w -> keys 4w..4w+3 (lane / 8), lane % 8 -> rows lane % 8 and + 8; each key row
-        // is read once per warp, four independent partial sums per dot product
+        // partial scores of this warp's 8 keys over its half of the head dimension
         {
-            const int j = (kAttnKeys / (kAttnThreads / 32)) * warp + (lane >> 3);
-            const float4 *kr = reinterpret_cast<const float4 *>(K + j * ldk);
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            const float *kr = K + (8 * kg + gq) * ldq;
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int m = (lane & 7) + 8 * rr;
-                if (m < M) {
-                    const float4 *qr = reinterpret_cast<const float4 *>(Qs + m * ldk);
-                    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                    for (int d4 = 0; d4 < hd4; ++d4) {
-                        const float4 k = kr[d4], x = qr[d4];
-                        t.x = fmaf(x.x, k.x, t.x);
-                        t.y = fmaf(x.y, k.y, t.y);
-                        t.z = fmaf(x.z, k.z, t.z);
-                        t.w = fmaf(x.w, k.w, t.w);
-                    }
-                    Ps[m * kAttnKeys + j] = (t.x + t.y) + (t.z + t.w);
+            for (int s = 0; s < kAttnKS; ++s) {
+                if (s < ksn) {
+                    const int col = 16 * (kh * ksn + s) + 2 * tq;
+                    const float2 k0 = *reinterpret_cast<const float2 *>(kr + col);
+                    const float2 k1 = *reinterpret_cast<const float2 *>(kr + col + 8);
+                    uint32_t bh0, bl0, bh1, bl1;
+                    split2(k0.x, k0.y, bh0, bl0);
+                    split2(k1.x, k1.y, bh1, bl1);
+                    mma_bf16(c, qh[s][0], qh[s][1], qh[s][2], qh[s][3], bh0, bh1);
+                    mma_bf16(c, qh[s][0], qh[s][1], qh[s][2], qh[s][3], bl0, bl1);
+                    mma_bf16(c, ql[s][0], ql[s][1], ql[s][2], ql[s][3], bh0, bh1);
                 }
             }
+            float *sp = Sp + kh * kMaxRows * kAttnSP;
+            *reinterpret_cast<float2 *>(sp + gq * kAttnSP + 8 * kg + 2 * tq) = make_float2(c[0], c[1]);
+            *reinterpret_cast<float2 *>(sp + (gq + 8) * kAttnSP + 8 * kg + 2 * tq) = make_float2(c[2], c[3]);
         }
         __syncthreads();
         // softmax update: warp -> rows warp, warp + 8; lane -> key
@@ -437,18 +475,19 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                     vis = pos >= lo && pos <= hi;
                 }
             }
-            const float sv = vis ? Ps[m * kAttnKeys + j] * a.scale : -INFINITY;
+            const float sraw = Sp[m * kAttnSP + j] + Sp[(kMaxRows + m) * kAttnSP + j];
+            const float sv = vis ? sraw * a.scale : -INFINITY;
             float bm = sv;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+            for (int oo = 16; oo > 0; oo >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, oo));
             const float mo = Mx[m];
             const float mn = fmaxf(mo, bm);
             const float pj = vis ? expf(sv - mn) : 0.f;
             float ps = pj;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            for (int oo = 16; oo > 0; oo >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, oo);
             const float sc = mo == -INFINITY ? 0.f : expf(mo - mn);
-            Ps[m * kAttnKeys + j] = pj;
+            Ps[m * kAttnSP + j] = pj;
             __syncwarp();
             if (lane == 0) {
                 Sc[m] = sc;
@@ -456,28 +495,40 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                 Ls[m] = fmaf(Ls[m], sc, ps);
             }
         }
+        for (int e = tid; e < (kMaxRows - M) * kAttnKeys; e += kAttnThreads)   // rows the pass does not carry
+            Ps[(M + e / kAttnKeys) * kAttnSP + e % kAttnKeys] = 0.f;
+        if (tid >= M && tid < kMaxRows) Sc[tid] = 0.f;
         __syncthreads();
-        // running p.V, keys in ascending order
-        if (pv_on) {
+        // running p.V over the block's 32 keys (two k-steps of 16)
+        {
+            const float s0 = Sc[gq], s1 = Sc[gq + 8];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int m = rg + RG * r;
-                if (m < M) {
-                    const float sc = Sc[m];
-                    acc[r].x *= sc, acc[r].y *= sc, acc[r].z *= sc, acc[r].w *= sc;
-                }
+            for (int t = 0; t < kAttnNT; ++t) {
+                o[t][0] *= s0, o[t][1] *= s0, o[t][2] *= s1, o[t][3] *= s1;
             }
-            for (int j = 0; j < kAttnKeys; ++j) {
-                const float4 v = *reinterpret_cast<const float4 *>(V + j * ldk + 4 * c4);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int m = rg + RG * r;
-                    if (m < M) {
-                        const float p = Ps[m * kAttnKeys + j];
-                        acc[r].x = fmaf(p, v.x, acc[r].x);
-                        acc[r].y = fmaf(p, v.y, acc[r].y);
-                        acc[r].z = fmaf(p, v.z, acc[r].z);
-                        acc[r].w = fmaf(p, v.w, acc[r].w);
+            for (int ks = 0; ks < 2; ++ks) {
+                const int kc = 16 * ks + 2 * tq;
+                const float2 p0 = *reinterpret_cast<const float2 *>(Ps + gq * kAttnSP + kc);
+                const float2 p1 = *reinterpret_cast<const float2 *>(Ps + (gq + 8) * kAttnSP + kc);
+                const float2 p2 = *reinterpret_cast<const float2 *>(Ps + gq * kAttnSP + kc + 8);
+                const float2 p3 = *reinterpret_cast<const float2 *>(Ps + (gq + 8) * kAttnSP + kc + 8);
+                uint32_t ah[4], al[4];
+                split2(p0.x, p0.y, ah[0], al[0]);
+                split2(p1.x, p1.y, ah[1], al[1]);
+                split2(p2.x, p2.y, ah[2], al[2]);
+                split2(p3.x, p3.y, ah[3], al[3]);
+#pragma unroll
+                for (int t = 0; t < kAttnNT; ++t) {
+                    if (t < ntn) {
+                        const int col = 8 * (warp + 8 * t) + gq;
+                        const float *vr = V + kc * ldv + col;
+                        uint32_t bh0, bl0, bh1, bl1;
+                        split2(vr[0], vr[ldv], bh0, bl0);
+                        split2(vr[8 * ldv], vr[9 * ldv], bh1, bl1);
+                        mma_bf16(o[t], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
+                        mma_bf16(o[t], ah[0], ah[1], ah[2], ah[3], bl0, bl1);
+                        mma_bf16(o[t], al[0], al[1], al[2], al[3], bh0, bh1);
                     }
                 }
             }
@@ -485,11 +536,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         __syncthreads();   // the buffer is refilled in the next round
     }
     // publish this CTA's state, then merge the cluster's states in rank order
-    if (pv_on) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int m = rg + RG * r;
-            if (m < M) *reinterpret_cast<float4 *>(Os + m * hd + 4 * c4) = acc[r];
+    for (int t = 0; t < kAttnNT; ++t) {
+        if (t < ntn) {
+            const int col = 8 * (warp + 8 * t) + 2 * tq;
+            if (gq < M) *reinterpret_cast<float2 *>(Os + gq * hd + col) = make_float2(o[t][0], o[t][1]);
+            if (gq + 8 < M) *reinterpret_cast<float2 *>(Os + (gq + 8) * hd + col) = make_float2(o[t][2], o[t][3]);
         }
     }
     cluster_sync_all();
@@ -535,7 +587,7 @@ cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    if (a.hd % 16 || a.hd < 16 || a.hd > 256 || a.M < 1 || a.M > kMaxRows || a.nB > kAttnKeys || a.nq % a.nkv)
+    if (a.hd % 64 || a.hd < 64 || a.hd > 256 || a.M < 1 || a.M > kMaxRows || a.nB > kAttnKeys || a.nq % a.nkv)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.nq * kAttnCluster);
