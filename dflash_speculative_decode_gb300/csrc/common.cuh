@@ -95,6 +95,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.com
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // wait until at most one committed group of this thread is still in flight
 __device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_group2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 
 // ---- activation operand format ---------------------------------------------------------------------
 // An activation matrix of up to 16 rows and K inputs (K % 16 == 0) that feeds a product is stored as

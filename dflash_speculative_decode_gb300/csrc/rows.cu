@@ -300,27 +300,30 @@ constexpr int kAttnCluster = 8;
 constexpr int kAttnKS = 8;   // k-steps of 16 per half of the head dimension (hd <= 256)
 constexpr int kAttnNT = 4;   // 8-column tiles per warp in p.V (hd <= 256)
 constexpr int kAttnSP = 40;  // pitch of the score and probability rows (32 keys + 8)
+constexpr int kAttnBuf = 3;  // key/value blocks in flight
 
 size_t attn_smem(int hd) {
-    return ((size_t)kMaxRows * (hd + 8) + 2 * (size_t)kAttnKeys * (hd + 8) + 2 * (size_t)kAttnKeys * (hd + 4) +
-            3 * (size_t)kMaxRows * kAttnSP + 3 * kMaxRows) * 4;
+    return ((size_t)kMaxRows * (hd + 8) + kAttnBuf * (size_t)kAttnKeys * (hd + 8) +
+            kAttnBuf * (size_t)kAttnKeys * (hd + 4) + 3 * (size_t)kMaxRows * kAttnSP + 3 * kMaxRows) * 4;
 }
 
-// fp32 pair -> bf16x2 hi and lo (x = hi + lo to 2^-17 relative), lower element in the low half
+// fp32 pair -> bf16x2 hi and lo (x = hi + lo to 2^-17 relative), lower element in the low half; the
+// roundings are the hardware's paired round-to-nearest-even conversion
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const uint16_t h0 = f32_to_bf16(x0), h1 = f32_to_bf16(x1);
-    const uint16_t l0 = f32_to_bf16(x0 - bf16_to_f32(h0)), l1 = f32_to_bf16(x1 - bf16_to_f32(h1));
-    hi = uint32_t(h0) | (uint32_t(h1) << 16);
-    lo = uint32_t(l0) | (uint32_t(l1) << 16);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int hd = a.hd, ldq = hd + 8, ldv = hd + 4, hd4 = hd / 4;
     float *Qs = sm;                                 // [16][ldq] this head's query rows
-    float *Kb = Qs + kMaxRows * ldq;                // [2][32][ldq] double-buffered key block
-    float *Vb = Kb + 2 * kAttnKeys * ldq;           // [2][32][ldv]
-    float *Sp = Vb + 2 * kAttnKeys * ldv;           // [2][16][kAttnSP] partial scores per half
+    float *Kb = Qs + kMaxRows * ldq;                // [kAttnBuf][32][ldq] key blocks in flight
+    float *Vb = Kb + kAttnBuf * kAttnKeys * ldq;    // [kAttnBuf][32][ldv]
+    float *Sp = Vb + kAttnBuf * kAttnKeys * ldv;    // [2][16][kAttnSP] partial scores per half
     float *Ps = Sp + 2 * kMaxRows * kAttnSP;        // [16][kAttnSP] probabilities of the current block
     float *Sc = Ps + kMaxRows * kAttnSP;            // [16] rescale of the running sums
     float *Mx = Sc + kMaxRows;                      // [16] running max
@@ -330,8 +333,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     const int h = blockIdx.x / kAttnCluster;
     const unsigned rank = cluster_rank();
     const int g = h / (a.nq / a.nkv);
-    pdl_wait();
-    pdl_trigger();
+    // st->n was set before the pass began (every kernel of the pass waits for its predecessor), so it
+    // may be read before this kernel's own dependency wait
     const int n = a.st->n;
     const int M = a.M;
     int lo, hi;   // inclusive range of plane positions any row may see
@@ -388,7 +391,22 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         cp_async_commit();
     };
 
-    if (nmine > 0) load_block(0, 0);
+    // blocks whose positions all precede the pass were written by earlier passes: they are immutable
+    // here and are requested before the dependency wait (the pass's own rows come from the kernel
+    // before this one)
+    auto early = [&](int i) { return a.mode == 0 && i < nAmine && kAttnKeys * (b0 + kAttnCluster * i) + kAttnKeys <= n; };
+    int issued = 0;
+    while (issued < kAttnBuf - 1 && issued < nmine && early(issued)) {
+        load_block(issued, issued);
+        ++issued;
+    }
+    pdl_wait();
+    pdl_trigger();
+    while (issued < kAttnBuf - 1 && issued < nmine) {
+        load_block(issued, issued);
+        ++issued;
+    }
+    for (int k = issued; k < kAttnBuf - 1; ++k) cp_async_commit();   // the prologue is kAttnBuf - 1 groups
     for (int e = tid; e < kMaxRows * hd4; e += kAttnThreads) {
         const int m = e / hd4, d4 = e % hd4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -423,13 +441,18 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     for (int t = 0; t < kAttnNT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
 
     for (int i = 0; i < nmine; ++i) {
-        const int buf = i & 1;
-        if (i + 1 < nmine) {
-            load_block(i + 1, buf ^ 1);   // its buffer was released at the end of the last round
-            cp_async_wait_group1();
+        const int buf = i % kAttnBuf;
+        // keep kAttnBuf - 1 blocks requested ahead (the refilled buffer was released last round). Group
+        // j holds block j: the prologue committed kAttnBuf - 1 groups and every round commits one
+        // (empty past the end), so block i has landed once at most kAttnBuf - 1 newer groups are pending
+        if (issued < nmine) {
+            load_block(issued, issued % kAttnBuf);
+            ++issued;
         } else {
-            cp_async_wait_all();
+            cp_async_commit();
         }
+        static_assert(kAttnBuf == 3, "wait depth");
+        cp_async_wait_group2();
         __syncthreads();
         const float *K = Kb + buf * kAttnKeys * ldq, *V = Vb + buf * kAttnKeys * ldv;
         const bool virt = i >= nAmine;
