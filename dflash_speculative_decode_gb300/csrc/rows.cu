@@ -112,73 +112,119 @@ inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int cl
 // ---------------------------------------------------------------------------------------------------
 // Residual row kernel:
 //   x += RMSNorm(y, w_post) (or x += y), x *= lambda, tap = x, out = RMSNorm(x, w_next) in operand format.
-// One cluster of kRowCluster CTAs per row, each CTA H / kRowCluster columns with one thread per column.
-// Row sums are block sums added over the cluster in rank order (distributed shared memory), so every CTA
-// sees the same value and the result does not depend on how many rows the pass carries.
+// One CTA per row, H/4 threads, each four consecutive columns (128-bit loads and stores). The row sums
+// are block sums in a fixed order, so the result does not depend on how many rows the pass carries.
 // ---------------------------------------------------------------------------------------------------
-constexpr int kRowCluster = 8;
 constexpr int kRowThreads = 256;   // k_cast_rows
 constexpr int kRowMaxPer = 16;     // k_cast_rows: hidden <= 4096
 
-// sum of v over the cluster's threads; slot selects a shared word (one per reduction of the kernel)
-__device__ __forceinline__ float cluster_row_sum(float v, float *red, float *slots, int slot) {
-    const float b = block_sum(v, red);
-    if (threadIdx.x == 0) slots[slot] = b;
-    cluster_sync_all();
-    float t = 0.f;
+__device__ __forceinline__ float4 bf16x4(const uint16_t *w) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(w);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// four consecutive inputs k..k+3 (k % 4 == 0) of row `tok` into the operand format; returns their hi+lo sum
+__device__ __forceinline__ float act_store4(uint32_t *f, int K, int tok, int k, float4 v) {
+    const float e[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hw[2], lw[2];
+    float s = 0.f;
 #pragma unroll
-    for (int r = 0; r < kRowCluster; ++r) t += ld_cluster(slots + slot, r);
-    return t;
+    for (int p = 0; p < 2; ++p) {
+        const uint16_t h0 = f32_to_bf16(e[2 * p]), h1 = f32_to_bf16(e[2 * p + 1]);
+        const uint16_t l0 = f32_to_bf16(e[2 * p] - bf16_to_f32(h0)), l1 = f32_to_bf16(e[2 * p + 1] - bf16_to_f32(h1));
+        hw[p] = uint32_t(h0) | (uint32_t(h1) << 16);
+        lw[p] = uint32_t(l0) | (uint32_t(l1) << 16);
+        s += (bf16_to_f32(h0) + bf16_to_f32(l0)) + (bf16_to_f32(h1) + bf16_to_f32(l1));
+    }
+    // inputs r = k%16 .. r+3: pairs (r, r+1) and (r+2, r+3) sit in lane columns t = (r&7)/2 and t+1 of
+    // word w = r/8 (hi) and w+2 (lo)
+    const int r = k & 15, t = (r & 7) >> 1, w = r >> 3;
+    uint32_t *base = f + ((long)tok * (K >> 4) + (k >> 4)) * 16;
+    base[t * 4 + w] = hw[0];
+    base[t * 4 + w + 2] = lw[0];
+    base[(t + 1) * 4 + w] = hw[1];
+    base[(t + 1) * 4 + w + 2] = lw[1];
+    return s;
+}
+
+// the four consecutive columns n..n+3 of row m of an EPI_PART product
+__device__ __forceinline__ float4 part_sum4(const PartView &v, int m, int n) {
+    const int grp = n >> 5, q = grp >> 2;
+    const long qa = (long)q * v.C;
+    const int nseg = int(cta_of(qa + v.C - 1, v.U, v.G) - cta_of(qa, v.U, v.G)) + 1;
+    const float4 *p = reinterpret_cast<const float4 *>(v.part + ((size_t)grp * v.maxseg * kMaxRows + m) * 32 + (n & 31));
+    const size_t st = (size_t)kMaxRows * 32 / 4;
+    float4 l[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) l[s] = s < nseg ? __ldcg(p + s * st) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+        if (s < nseg) y.x += l[s].x, y.y += l[s].y, y.z += l[s].z, y.w += l[s].w;
+    for (int s = 16; s < nseg; ++s) {
+        const float4 e = __ldcg(p + s * st);
+        y.x += e.x, y.y += e.y, y.z += e.z, y.w += e.w;
+    }
+    return y;
 }
 
 __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
     __shared__ float red[33];
-    __shared__ float slots[2];
-    const int m = blockIdx.x / kRowCluster;
-    const unsigned rank = cluster_rank();
-    const int cols = a.H / kRowCluster;
-    const bool on = int(threadIdx.x) < cols;
-    const int h = int(rank) * cols + int(threadIdx.x);
+    const int m = blockIdx.x;
+    const int h = 4 * int(threadIdx.x);
+    const bool on = h < a.H;
     pdl_wait();
     pdl_trigger();
     const bool live = !a.rows_from_ctx || m < a.st->ctx_rows;
     float *xr = a.x ? a.x + (long)m * a.H : nullptr;
-    float x = (on && xr) ? xr[h] : 0.f;
+    float4 x = (on && xr) ? *reinterpret_cast<const float4 *>(xr + h) : make_float4(0.f, 0.f, 0.f, 0.f);
     const bool have_y = a.yp.part || a.y;
     if (have_y) {
-        float y = 0.f;
-        if (on) y = a.yp.part ? part_sum(a.yp, m, h) : a.y[(long)m * a.ldy + h];
-        if (on && a.y_out) a.y_out[(long)m * a.H + h] = y;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (on) y = a.yp.part ? part_sum4(a.yp, m, h) : *reinterpret_cast<const float4 *>(a.y + (long)m * a.ldy + h);
+        if (on && a.y_out) *reinterpret_cast<float4 *>(a.y_out + (long)m * a.H + h) = y;
         if (a.w_post) {
-            const float r = 1.0f / sqrtf(cluster_row_sum(y * y, red, slots, 0) / a.H + a.eps);
-            if (on) x += (y * r) * bf16_to_f32(a.w_post[h]);
+            const float ss = (y.x * y.x + y.y * y.y) + (y.z * y.z + y.w * y.w);
+            const float r = 1.0f / sqrtf(block_sum(ss, red) / a.H + a.eps);
+            if (on) {
+                const float4 w = bf16x4(a.w_post + h);
+                x.x += (y.x * r) * w.x, x.y += (y.y * r) * w.y, x.z += (y.z * r) * w.z, x.w += (y.w * r) * w.w;
+            }
         } else {
-            x += y;
+            x.x += y.x, x.y += y.y, x.z += y.z, x.w += y.w;
         }
     }
-    if (a.lambda != 1.0f) x *= a.lambda;
-    if (on && xr && (have_y || a.lambda != 1.0f)) xr[h] = x;
+    if (a.lambda != 1.0f) x.x *= a.lambda, x.y *= a.lambda, x.z *= a.lambda, x.w *= a.lambda;
+    if (on && xr && (have_y || a.lambda != 1.0f)) *reinterpret_cast<float4 *>(xr + h) = x;
     if (on && a.tap && live) {
         const int pos = (a.pos_from_ctx ? a.st->draft_n : a.st->n) + m;
-        a.tap[(long)pos * a.ld_tap + a.tap_off + h] = x;
+        *reinterpret_cast<float4 *>(a.tap + (long)pos * a.ld_tap + a.tap_off + h) = x;
     }
     if (a.outf) {
         float r = 1.f;
-        if (a.w_next) r = 1.0f / sqrtf(cluster_row_sum(x * x, red, slots, 1) / a.H + a.eps);
+        if (a.w_next) r = 1.0f / sqrtf(block_sum((x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w), red) / a.H + a.eps);
         const int row = a.out_row0 + m;
-        float v = 0.f;
-        if (on && live) v = a.w_next ? (x * r) * bf16_to_f32(a.w_next[h]) : x;
-        const float hl = on ? act_store(a.outf, a.H, row, h, v) : 0.f;
-        const float sg = half_warp_sum(hl);   // 16 consecutive columns: cols is a multiple of 16
-        if (on && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = sg;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (on && live) {
+            if (a.w_next) {
+                const float4 w = bf16x4(a.w_next + h);
+                v = make_float4((x.x * r) * w.x, (x.y * r) * w.y, (x.z * r) * w.z, (x.w * r) * w.w);
+            } else {
+                v = x;
+            }
+        }
+        float hl = on ? act_store4(a.outf, a.H, row, h, v) : 0.f;
+        // four threads hold a 16-input group
+        hl += __shfl_xor_sync(0xffffffffu, hl, 1);
+        hl += __shfl_xor_sync(0xffffffffu, hl, 2);
+        if (on && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = hl;
     }
-    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
 }
 
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
-    if (a.H % (16 * kRowCluster) || a.H / kRowCluster > 1024 || a.M < 1 || a.M > kMaxRows) return cudaErrorInvalidValue;
-    const int cols = a.H / kRowCluster;
-    return launch_cluster_pdl(k_rows, a.M * kRowCluster, kRowCluster, (cols + 31) / 32 * 32, 0, s, a);
+    if (a.H % 128 || a.H / 4 > 1024 || a.M < 1 || a.M > kMaxRows) return cudaErrorInvalidValue;
+    return launch_pdl(k_rows, dim3(a.M), dim3(a.H / 4), 0, s, a);
 }
 
 // dst row (row0 + m) = RMSNorm(src[m], w) for live rows (m < st->ctx_rows when live_from_ctx), zeros
