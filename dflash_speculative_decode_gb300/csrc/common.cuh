@@ -117,6 +117,8 @@ __device__ __forceinline__ float act_store(uint32_t *f, int K, int tok, int k, f
 }
 
 // ---- mbarriers and bulk asynchronous copies ----------------------------------------------------------
+constexpr unsigned kWaitHintNs = 200000;   // 0.2 ms
+constexpr int kWaitPolls = 1 << 14;        // with the hint: a few seconds at most
 __device__ __forceinline__ unsigned saddr(const void *p) { return static_cast<unsigned>(__cvta_generic_to_shared(p)); }
 __device__ __forceinline__ void mbar_init(uint64_t *b, unsigned count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
@@ -128,17 +130,19 @@ __device__ __forceinline__ void mbar_expect(uint64_t *b, unsigned bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
 }
+// test for the phase with the given parity; a waiting thread may be suspended (up to the hint, in
+// nanoseconds) until the phase completes, so the wait costs no issue slots
 __device__ __forceinline__ bool mbar_test(uint64_t *b, unsigned parity) {
     unsigned ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(saddr(b)), "r"(parity)
+        : "r"(saddr(b)), "r"(parity), "r"(kWaitHintNs)
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity; false if it did not complete within the limit.
-constexpr int kWaitPolls = 1 << 18;
+// Bounded wait for the phase with the given parity; false if it did not complete within the limit
+// (at most kWaitPolls tests of up to kWaitHintNs each).
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity) {
     for (int i = 0; i < kWaitPolls; ++i)
         if (mbar_test(b, parity)) return true;

@@ -478,7 +478,15 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                         const int c = cr.c + par + kGemmPar * i, kb = K16 - 4 * c;
                         nblk[i] = c < cr.ce ? (kb < 4 ? kb / 2 : 2) : 0;
                     }
-                    q41_units<FMT, MT, NU>(acc, slot, w_off, x_off, s_off, nblk, lane);
+                    // units in pairs; live units are a prefix, so a pair past them is skipped whole
+                    static_assert(NU % 2 == 0, "pairs of units");
+#pragma unroll
+                    for (int i0 = 0; i0 < NU; i0 += 2) {
+                        const int np[2] = {nblk[i0], nblk[i0 + 1]};
+                        if (np[0] > 0)
+                            q41_units<FMT, MT, 2>(acc, slot, w_off + kGemmPar * i0 * TB, x_off + 256 * kGemmPar * i0,
+                                                  s_off + 256 * kGemmPar * i0, np, lane);
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < NU; ++i) {
