@@ -100,15 +100,20 @@ __device__ __forceinline__ void cp_async_wait_group2() { asm volatile("cp.async.
 // ---- activation operand format ---------------------------------------------------------------------
 // An activation matrix of up to 16 rows and K inputs (K % 16 == 0) that feeds a product is stored as
 // the B fragments of mma.m16n8k16: fp32 x = hi + lo with hi = bf16(x), lo = bf16(x - hi) (exact to
-// 2^-17 relative). Row tok, 16-input group kb, lane column t = 0..3 own 16 bytes at word
-// ((tok * K/16 + kb) * 4 + t) * 4: {hi(2t, 2t+1), hi(2t+8, 2t+9), lo(2t, 2t+1), lo(2t+8, 2t+9)},
-// inputs counted within the group, the lower input in the low half. Beside it, sums[kb * 16 + tok]
-// holds the fp32 sum of hi + lo over the row's 16 inputs of group kb (the Q4_1 minimum term); the
-// product then computes exactly sum_k (hi_k + lo_k) w_k.
-// act_store writes one element and returns hi + lo, the value the sums add.
+// 2^-17 relative). Rows come in blocks of 8 (rb = tok / 8); for each 16-input group kb the block's 8
+// rows are adjacent, 64 bytes each, so a run of groups of one row block is contiguous (one copy per row
+// block for a range of inputs). Row tok, group kb, lane column t = 0..3 own 16 bytes at word
+// ((rb * K/16 + kb) * 8 + tok % 8) * 16 + t * 4: {hi(2t, 2t+1), hi(2t+8, 2t+9), lo(2t, 2t+1),
+// lo(2t+8, 2t+9)}, inputs counted within the group, the lower input in the low half. Beside it,
+// sums[kb * 16 + tok] holds the fp32 sum of hi + lo over the row's 16 inputs of group kb (the Q4_1
+// minimum term); the product then computes exactly sum_k (hi_k + lo_k) w_k.
+// act_group gives the first word of (row tok, group kb); act_store writes one element and returns hi + lo.
+__host__ __device__ __forceinline__ long act_group(int K, int tok, int kb) {
+    return (((long)(tok >> 3) * (K >> 4) + kb) * 8 + (tok & 7)) * 16;
+}
 __device__ __forceinline__ float act_store(uint32_t *f, int K, int tok, int k, float v) {
     const int r = k & 15, t = (r & 7) >> 1, w = r >> 3, half = r & 1;
-    uint16_t *p = reinterpret_cast<uint16_t *>(f + (((long)tok * (K >> 4) + (k >> 4)) * 4 + t) * 4);
+    uint16_t *p = reinterpret_cast<uint16_t *>(f + act_group(K, tok, k >> 4) + t * 4);
     const uint16_t hi = f32_to_bf16(v);
     const uint16_t lo = f32_to_bf16(v - bf16_to_f32(hi));
     p[2 * w + half] = hi;

@@ -135,21 +135,21 @@ cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *su
 // into one ring slot by bulk asynchronous copies, one per contiguous run, completing on the slot's
 // "full" mbarrier:
 //   tiles: tile (unit u, group gq, tile j) at ((2*gq + j)*CPR + u) * TB  (a group's chunks are one run)
-//   rows:  row tok at WB + tok * XR, chunk u at + 256*u (64-byte k-steps in operand order); the row
-//          pitch XR is 64 bytes past a multiple of 128 so the two rows a quarter warp reads differ in bank
-//   sums:  at WB + R * XR, 256 bytes per chunk ([4 groups][16 rows] fp32)
+//   rows:  row block rb (8 rows) at WB + rb * CP * 2048, chunk u at + 2048*u, k-step ks at + 512*ks,
+//          row tok % 8 at + 64*(tok % 8) (the operand format's own order: one copy per row block)
+//   sums:  at WB + MT * CP * 2048, 256 bytes per chunk ([4 groups][16 rows] fp32)
 // ---------------------------------------------------------------------------------------------------
 template <int FMT>
 __host__ __device__ constexpr int cpr() { return FMT == W_Q41 ? 8 : 4; }
 template <int FMT>
-__host__ __device__ constexpr int xrow_bytes() { return cpr<FMT>() * 256 + 64; }
+__host__ __device__ constexpr int xblock_bytes() { return cpr<FMT>() * 2048; }   // one row block of a round
 template <int MT>
 __host__ __device__ constexpr int red_bytes() { return kGemmPar * 4 * MT * 8 * 32 * 4; }   // [parity][4 groups][R][32]
 template <int FMT>
 __host__ __device__ constexpr int tile_bytes() { return FMT == W_Q41 ? 640 : 2048; }
 template <int FMT, int MT>
 __host__ __device__ constexpr int slot_bytes() {
-    return (8 * cpr<FMT>() * tile_bytes<FMT>() + MT * 8 * xrow_bytes<FMT>() + cpr<FMT>() * 256 + 127) / 128 * 128;
+    return (8 * cpr<FMT>() * tile_bytes<FMT>() + MT * xblock_bytes<FMT>() + cpr<FMT>() * 256 + 127) / 128 * 128;
 }
 constexpr int kGemmSmemBudget = 224 * 1024;
 template <int FMT, int MT>
@@ -188,8 +188,8 @@ __device__ __forceinline__ void mma_bf16_z(float (&d)[4], uint32_t a0, uint32_t 
 template <int FMT, int MT, int NU>
 __device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t *slot, int w_off, int x_off, int s_off,
                                           const int (&nblk)[NU], int lane) {
-    constexpr int TB = tile_bytes<FMT>(), CP = cpr<FMT>(), XR = xrow_bytes<FMT>();
-    const int g = lane >> 2, t = lane & 3;
+    constexpr int TB = tile_bytes<FMT>(), CP = cpr<FMT>(), XB = xblock_bytes<FMT>();
+    const int t = lane & 3, g = lane >> 2;
     uint4 nb[NU][2], sc[NU][2];
 #pragma unroll
     for (int i = 0; i < NU; ++i)
@@ -221,7 +221,7 @@ __device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t 
                 uint4 b[MT];
 #pragma unroll
                 for (int tt = 0; tt < MT; ++tt)
-                    b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + 256 * kGemmPar * i + tt * 8 * XR + 64 * ks);
+                    b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + 2048 * kGemmPar * i + tt * XB + 512 * ks);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t w = ks == 0 ? nb[i][j].x : ks == 1 ? nb[i][j].y : ks == 2 ? nb[i][j].z : nb[i][j].w;
@@ -262,14 +262,14 @@ __device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t 
 // bf16 (one unit per round): nks = k-steps inside K
 template <int FMT, int MT>
 __device__ __forceinline__ void bf16_unit(float (&acc)[2][MT][4], const uint8_t *slot, int w_off, int x_off, int nks, int lane) {
-    constexpr int TB = tile_bytes<FMT>(), CP = cpr<FMT>(), XR = xrow_bytes<FMT>();
+    constexpr int TB = tile_bytes<FMT>(), CP = cpr<FMT>(), XB = xblock_bytes<FMT>();
     const uint8_t *w0 = slot + w_off, *w1 = slot + w_off + CP * TB;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
         if (ks >= nks) break;
         uint4 b[MT];
 #pragma unroll
-        for (int tt = 0; tt < MT; ++tt) b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + tt * 8 * XR + 64 * ks);
+        for (int tt = 0; tt < MT; ++tt) b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + tt * XB + 512 * ks);
         const uint4 wa = *reinterpret_cast<const uint4 *>(w0 + 512 * ks + 16 * lane);
         const uint4 wb = *reinterpret_cast<const uint4 *>(w1 + 512 * ks + 16 * lane);
 #pragma unroll
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
     constexpr int CP = cpr<FMT>();
     constexpr int NU = CP / kGemmPar;
     static_assert(CP % kGemmPar == 0, "units per warp");
-    constexpr int XR = xrow_bytes<FMT>();
+    constexpr int XB = xblock_bytes<FMT>();
     constexpr int WB = 8 * CP * TB;
     constexpr int SB = slot_bytes<FMT, MT>();
     constexpr int S = ring_slots<FMT, MT>();
@@ -421,14 +421,14 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
         auto issue_x = [&](const Rd &r, int sl) {   // the activations of round r (valid k-steps only)
             const int nc = r.ce - r.c < CP ? r.ce - r.c : CP;
             const int kb = K16 - 4 * r.c;
-            const unsigned xb = 64u * unsigned(kb < 4 * nc ? kb : 4 * nc);
-            if (lane == 0) mbar_expect(&full[sl], (R + 1) * xb);
+            const unsigned ng16 = unsigned(kb < 4 * nc ? kb : 4 * nc);   // 16-input groups of the round
+            if (lane == 0) mbar_expect(&full[sl], MT * 512u * ng16 + 64u * ng16);
             __syncwarp();
             uint8_t *base = ring + sl * SB + WB;
-            if (lane < R)
-                bulk_g2s(base + lane * XR, a.xf + ((size_t)(a.x_row0 + lane) * K16 + 4 * r.c) * 16, xb, &full[sl]);
-            else if (lane == R)
-                bulk_g2s(base + R * XR, a.xs + (size_t)(4 * r.c) * kMaxRows, xb, &full[sl]);
+            if (lane < MT)   // row block `lane`: its groups are one run of the operand format
+                bulk_g2s(base + lane * XB, a.xf + act_group(a.K, a.x_row0 + 8 * lane, 4 * r.c), 512u * ng16, &full[sl]);
+            else if (lane == MT)
+                bulk_g2s(base + MT * XB, a.xs + (size_t)(4 * r.c) * kMaxRows, 64u * ng16, &full[sl]);
         };
         Rd r;
         rd_at_quad(r, int(u0 / a.C), int(u0 % a.C));
@@ -461,8 +461,8 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
         zero();
         // per-lane offsets inside a slot (unit par; unit par + 4i is 4i chunks further)
         const int w_off = (2 * gq * CP + par) * TB;
-        const int x_off = WB + g * XR + 256 * par + 16 * t;
-        const int s_off = WB + R * XR + 256 * par;
+        const int x_off = WB + 2048 * par + 64 * g + 16 * t;
+        const int s_off = WB + MT * XB + 256 * par;
         Rd cr;
         rd_at_quad(cr, int(u0 / a.C), int(u0 % a.C));
         for (int k = 0; rd_valid(cr); ++k) {
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     for (int i0 = 0; i0 < NU; i0 += 2) {
                         const int np[2] = {nblk[i0], nblk[i0 + 1]};
                         if (np[0] > 0)
-                            q41_units<FMT, MT, 2>(acc, slot, w_off + kGemmPar * i0 * TB, x_off + 256 * kGemmPar * i0,
+                            q41_units<FMT, MT, 2>(acc, slot, w_off + kGemmPar * i0 * TB, x_off + 2048 * kGemmPar * i0,
                                                   s_off + 256 * kGemmPar * i0, np, lane);
                     }
                 } else {
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     for (int i = 0; i < NU; ++i) {
                         const int c = cr.c + par + kGemmPar * i, kb = K16 - 4 * c;
                         if (c < cr.ce)
-                            bf16_unit<FMT, MT>(acc, slot, w_off + kGemmPar * i * TB, x_off + 256 * kGemmPar * i,
+                            bf16_unit<FMT, MT>(acc, slot, w_off + kGemmPar * i * TB, x_off + 2048 * kGemmPar * i,
                                                kb < 4 ? kb : 4, lane);
                     }
                 }
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(128) k_head(GemmArgs a) {
         const int tok = e / (K16 * 4), rest = e % (K16 * 4);
         uint8_t *dst = smem + tok * rowb + rest * 16;
         if (tok < a.M)
-            cp_async16(dst, reinterpret_cast<const uint8_t *>(a.xf) + ((long)(a.x_row0 + tok) * K16 * 4 + rest) * 16);
+            cp_async16(dst, a.xf + act_group(a.K, a.x_row0 + tok, rest >> 2) + (rest & 3) * 4);
         else
             *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -815,6 +815,7 @@ size_t gemm_part_floats(int C, int N) { return (size_t)(N / 32) * gemm_maxseg(C,
 // dynamic shared memory of a product: the parity reduction buffer and the ring
 template <int FMT, int MT, int EPI>
 static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
+    if (a.x_row0 % 8) return cudaErrorInvalidValue;   // products read whole row blocks
     constexpr int smem = red_bytes<MT>() + ring_slots<FMT, MT>() * slot_bytes<FMT, MT>();
     static_assert(smem <= kGemmSmemBudget, "product shared memory");
     static bool attr = false;

@@ -140,7 +140,7 @@ __device__ __forceinline__ float act_store4(uint32_t *f, int K, int tok, int k, 
     // inputs r = k%16 .. r+3: pairs (r, r+1) and (r+2, r+3) sit in lane columns t = (r&7)/2 and t+1 of
     // word w = r/8 (hi) and w+2 (lo)
     const int r = k & 15, t = (r & 7) >> 1, w = r >> 3;
-    uint32_t *base = f + ((long)tok * (K >> 4) + (k >> 4)) * 16;
+    uint32_t *base = f + act_group(K, tok, k >> 4);
     base[t * 4 + w] = hw[0];
     base[t * 4 + w + 2] = lw[0];
     base[(t + 1) * 4 + w] = hw[1];
