@@ -9,7 +9,7 @@
 namespace dfl {
 
 constexpr int kMaxRows = 16;           // rows of one pass (R_max)
-constexpr int kWarpsPerCta = 4;        // GEMM CTA: 4 warps, each two 16-column tiles
+constexpr int kWarpsPerCta = 8;        // head CTA: 8 warps, each a range of 16-column tiles
 
 // Device-resident counters of the current pass. The host writes them with k_set_state before each
 // pass so a captured graph replays at any position.

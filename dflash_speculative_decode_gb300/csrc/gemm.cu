@@ -625,7 +625,7 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) { retur
 constexpr int kHeadPad = 64;   // bytes added per staged row: conflict-free 16-byte fragment reads
 
 template <int MT>
-__global__ void __launch_bounds__(128) k_head(GemmArgs a) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32) k_head(GemmArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float wval[kWarpsPerCta][kMaxRows];
     __shared__ int widx[kWarpsPerCta][kMaxRows];
@@ -848,7 +848,7 @@ static cudaError_t run_head(const GemmArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_pdl(k_head<MT>, dim3(head_grid(a.C, a.M, a.N)), dim3(128), smem, s, a);
+    return launch_pdl(k_head<MT>, dim3(head_grid(a.C, a.M, a.N)), dim3(kWarpsPerCta * 32), smem, s, a);
 }
 
 cudaError_t launch_gemm(int fmt, int epi, const GemmArgs &a, cudaStream_t s) {
