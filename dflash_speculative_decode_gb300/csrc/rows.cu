@@ -331,26 +331,28 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t s) {
 // layers). Draft (mode 1): every row sees context positions max(0, n-window)..n-1, plus all nB keys of
 // the block's own store as one extra block after the context blocks.
 // ---------------------------------------------------------------------------------------------------
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 512;
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kAttnKQ = kAttnWarps / 4;   // parts of the head dimension in the score products
 constexpr int kAttnKeys = 32;
 constexpr int kAttnCluster = 8;
 
 // Both products of a block run on the tensor cores (mma.m16n8k16, bf16 in, fp32 accumulate) with every
 // fp32 operand split into bf16 hi + lo and the three products hi*hi + hi*lo + lo*hi added (the lo*lo
 // term is below fp32 rounding): scores S = Q K^T (16 rows x 32 keys) and O += P V.
-//   Scores: warp w takes keys 8*(w%4) .. +7 and half w/4 of the head dimension; the two halves'
-//   partial scores are added in the softmax step (half 0 first).
-//   p.V: warp w takes head-dimension columns 8*(w + 8t) .. +7 for t < hd/64, all 16 rows, all 32 keys.
+//   Scores: warp w takes keys 8*(w%4) .. +7 and part w/4 of kAttnKQ of the head dimension; the parts'
+//   partial scores are added in the softmax step (in part order).
+//   p.V: warp w takes head-dimension column tiles w + 16t (8 columns each) that exist, all 16 rows, all 32 keys.
 // Row pitches (fp32 words): queries and keys hd+8 (fragment loads of 8 rows x 4 column pairs hit 32
 // banks), values hd+4 (fragment loads of 4 row pairs x 8 columns hit 32 banks).
-constexpr int kAttnKS = 8;   // k-steps of 16 per half of the head dimension (hd <= 256)
-constexpr int kAttnNT = 4;   // 8-column tiles per warp in p.V (hd <= 256)
+constexpr int kAttnKS = 16 / kAttnKQ;   // k-steps of 16 per part of the head dimension (hd <= 256)
+constexpr int kAttnNT = 32 / kAttnWarps; // 8-column tiles per warp in p.V (hd <= 256)
 constexpr int kAttnSP = 40;  // pitch of the score and probability rows (32 keys + 8)
 constexpr int kAttnBuf = 3;  // key/value blocks in flight
 
 size_t attn_smem(int hd) {
     return ((size_t)kMaxRows * (hd + 8) + kAttnBuf * (size_t)kAttnKeys * (hd + 8) +
-            kAttnBuf * (size_t)kAttnKeys * (hd + 4) + 3 * (size_t)kMaxRows * kAttnSP + 3 * kMaxRows) * 4;
+            kAttnBuf * (size_t)kAttnKeys * (hd + 4) + (kAttnKQ + 1) * (size_t)kMaxRows * kAttnSP + 3 * kMaxRows) * 4;
 }
 
 // fp32 pair -> bf16x2 hi and lo (x = hi + lo to 2^-17 relative), lower element in the low half; the
@@ -369,8 +371,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     float *Qs = sm;                                 // [16][ldq] this head's query rows
     float *Kb = Qs + kMaxRows * ldq;                // [kAttnBuf][32][ldq] key blocks in flight
     float *Vb = Kb + kAttnBuf * kAttnKeys * ldq;    // [kAttnBuf][32][ldv]
-    float *Sp = Vb + kAttnBuf * kAttnKeys * ldv;    // [2][16][kAttnSP] partial scores per half
-    float *Ps = Sp + 2 * kMaxRows * kAttnSP;        // [16][kAttnSP] probabilities of the current block
+    float *Sp = Vb + kAttnBuf * kAttnKeys * ldv;    // [kAttnKQ][16][kAttnSP] partial scores per part
+    float *Ps = Sp + kAttnKQ * kMaxRows * kAttnSP;  // [16][kAttnSP] probabilities of the current block
     float *Sc = Ps + kMaxRows * kAttnSP;            // [16] rescale of the running sums
     float *Mx = Sc + kMaxRows;                      // [16] running max
     float *Ls = Mx + kMaxRows;                      // [16] running sum
@@ -406,8 +408,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         const bool virt = i >= nAmine;
         const int b = virt ? bV : b0 + kAttnCluster * i;
 #pragma unroll
-        for (int kk = 0; kk < kAttnKeys / (kAttnThreads / 32); ++kk) {
-            const int j = warp * (kAttnKeys / (kAttnThreads / 32)) + kk;
+        for (int kk = 0; kk < kAttnKeys / kAttnWarps; ++kk) {
+            const int j = warp * (kAttnKeys / kAttnWarps) + kk;
             const float *ks = nullptr, *vs = nullptr;
             if (virt) {
                 if (j < a.nB) {
@@ -464,7 +466,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
 
     // this warp's query fragments (A operand, rows 0..15, its half of the head dimension), hi and lo
     const int kg = warp & 3, kh = warp >> 2;
-    const int ksn = hd / 32;                       // k-steps per half
+    const int ksn = hd / (16 * kAttnKQ);           // k-steps per part
     uint32_t qh[kAttnKS][4], ql[kAttnKS][4];
 #pragma unroll
     for (int s = 0; s < kAttnKS; ++s) {
@@ -480,8 +482,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
             split2(x3.x, x3.y, qh[s][3], ql[s][3]);
         }
     }
-    // p.V accumulators: tiles nt = warp + 8t (columns 8nt .. 8nt+7), C fragment layout
-    const int ntn = hd / 64;
+    // p.V accumulators: tiles nt = warp + kAttnWarps*t (columns 8nt .. 8nt+7), C fragment layout
+    const int ntiles = hd / 8;                     // tile nt = warp + kAttnWarps*t exists while nt < ntiles
     float o[kAttnNT][4];
 #pragma unroll
     for (int t = 0; t < kAttnNT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
@@ -526,10 +528,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
             *reinterpret_cast<float2 *>(sp + (gq + 8) * kAttnSP + 8 * kg + 2 * tq) = make_float2(c[2], c[3]);
         }
         __syncthreads();
-        // softmax update: warp -> rows warp, warp + 8; lane -> key
+        // softmax update: warp -> rows warp, warp + kAttnWarps, ...; lane -> key
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int m = warp + 8 * r;
+        for (int r = 0; r < kMaxRows / kAttnWarps; ++r) {
+            const int m = warp + kAttnWarps * r;
             if (m >= M) break;
             const int j = lane;
             bool vis;
@@ -544,7 +546,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                     vis = pos >= lo && pos <= hi;
                 }
             }
-            const float sraw = Sp[m * kAttnSP + j] + Sp[(kMaxRows + m) * kAttnSP + j];
+            float sraw = Sp[m * kAttnSP + j];
+#pragma unroll
+            for (int part = 1; part < kAttnKQ; ++part) sraw += Sp[(part * kMaxRows + m) * kAttnSP + j];
             const float sv = vis ? sraw * a.scale : -INFINITY;
             float bm = sv;
 #pragma unroll
@@ -589,8 +593,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                 split2(p3.x, p3.y, ah[3], al[3]);
 #pragma unroll
                 for (int t = 0; t < kAttnNT; ++t) {
-                    if (t < ntn) {
-                        const int col = 8 * (warp + 8 * t) + gq;
+                    if (warp + kAttnWarps * t < ntiles) {
+                        const int col = 8 * (warp + kAttnWarps * t) + gq;
                         const float *vr = V + kc * ldv + col;
                         uint32_t bh0, bl0, bh1, bl1;
                         split2(vr[0], vr[ldv], bh0, bl0);
@@ -607,8 +611,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     // publish this CTA's state, then merge the cluster's states in rank order
 #pragma unroll
     for (int t = 0; t < kAttnNT; ++t) {
-        if (t < ntn) {
-            const int col = 8 * (warp + 8 * t) + 2 * tq;
+        if (warp + kAttnWarps * t < ntiles) {
+            const int col = 8 * (warp + kAttnWarps * t) + 2 * tq;
             if (gq < M) *reinterpret_cast<float2 *>(Os + gq * hd + col) = make_float2(o[t][0], o[t][1]);
             if (gq + 8 < M) *reinterpret_cast<float2 *>(Os + (gq + 8) * hd + col) = make_float2(o[t][2], o[t][3]);
         }
