@@ -478,14 +478,16 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                         const int c = cr.c + par + kGemmPar * i, kb = K16 - 4 * c;
                         nblk[i] = c < cr.ce ? (kb < 4 ? kb / 2 : 2) : 0;
                     }
-                    // units in pairs; live units are a prefix, so a pair past them is skipped whole
-                    static_assert(NU % 2 == 0, "pairs of units");
+                    // units in pairs (or one); live units are a prefix, so a pair past them is skipped whole
+                    constexpr int NP = NU % 2 == 0 ? 2 : 1;
 #pragma unroll
-                    for (int i0 = 0; i0 < NU; i0 += 2) {
-                        const int np[2] = {nblk[i0], nblk[i0 + 1]};
+                    for (int i0 = 0; i0 < NU; i0 += NP) {
+                        int np[NP];
+#pragma unroll
+                        for (int i = 0; i < NP; ++i) np[i] = nblk[i0 + i];
                         if (np[0] > 0)
-                            q41_units<FMT, MT, 2>(acc, slot, w_off + kGemmPar * i0 * TB, x_off + 2048 * kGemmPar * i0,
-                                                  s_off + 256 * kGemmPar * i0, np, lane);
+                            q41_units<FMT, MT, NP>(acc, slot, w_off + kGemmPar * i0 * TB, x_off + 2048 * kGemmPar * i0,
+                                                   s_off + 256 * kGemmPar * i0, np, lane);
                     }
                 } else {
 #pragma unroll
