@@ -45,9 +45,8 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_floa
 
 // Round to nearest even bf16 (finite inputs).
 __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
-    uint32_t u = __float_as_uint(f);
-    u += 0x7FFFu + ((u >> 16) & 1u);
-    return uint16_t(u >> 16);
+    const __nv_bfloat16 h = __float2bfloat16_rn(f);   // the hardware conversion (round to nearest even)
+    return *reinterpret_cast<const uint16_t *>(&h);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }

@@ -169,8 +169,25 @@ __device__ __forceinline__ float4 part_sum4(const PartView &v, int m, int n) {
     return y;
 }
 
+// block-wide sum of four values at once (fixed order, as block_sum)
+__device__ __forceinline__ float4 block_sum4(float4 v, float4 *red4) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v.x = warp_sum(v.x), v.y = warp_sum(v.y), v.z = warp_sum(v.z), v.w = warp_sum(v.w);
+    if (lane == 0) red4[w] = v;
+    __syncthreads();
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (w == 0) {
+        t = lane < nw ? red4[lane] : t;
+        t.x = warp_sum(t.x), t.y = warp_sum(t.y), t.z = warp_sum(t.z), t.w = warp_sum(t.w);
+        if (lane == 0) red4[32] = t;
+    }
+    __syncthreads();
+    return red4[32];
+}
+
 __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
     __shared__ float red[33];
+    __shared__ float4 red4[33];
     const int m = blockIdx.x;
     const int h = 4 * int(threadIdx.x);
     const bool on = h < a.H;
@@ -180,16 +197,29 @@ __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
     float *xr = a.x ? a.x + (long)m * a.H : nullptr;
     float4 x = (on && xr) ? *reinterpret_cast<const float4 *>(xr + h) : make_float4(0.f, 0.f, 0.f, 0.f);
     const bool have_y = a.yp.part || a.y;
+    // With a post-norm, the output norm's sum of squares is expanded so one block reduction gives both:
+    //   x' = lambda (x + r y w),  sum x'^2 = lambda^2 (sum x^2 + 2 r sum x y w + r^2 sum (y w)^2),
+    //   r = (sum y^2 / H + eps)^(-1/2).
+    float r_next = -1.f;   // the output norm's scale when it came out of the combined reduction
     if (have_y) {
         float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
         if (on) y = a.yp.part ? part_sum4(a.yp, m, h) : *reinterpret_cast<const float4 *>(a.y + (long)m * a.ldy + h);
         if (on && a.y_out) *reinterpret_cast<float4 *>(a.y_out + (long)m * a.H + h) = y;
         if (a.w_post) {
-            const float ss = (y.x * y.x + y.y * y.y) + (y.z * y.z + y.w * y.w);
-            const float r = 1.0f / sqrtf(block_sum(ss, red) / a.H + a.eps);
+            const float4 w = on ? bf16x4(a.w_post + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 yw = make_float4(y.x * w.x, y.y * w.y, y.z * w.z, y.w * w.w);
+            float4 v4 = make_float4((y.x * y.x + y.y * y.y) + (y.z * y.z + y.w * y.w),
+                                    (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w),
+                                    (x.x * yw.x + x.y * yw.y) + (x.z * yw.z + x.w * yw.w),
+                                    (yw.x * yw.x + yw.y * yw.y) + (yw.z * yw.z + yw.w * yw.w));
+            v4 = block_sum4(v4, red4);
+            const float r = 1.0f / sqrtf(v4.x / a.H + a.eps);
             if (on) {
-                const float4 w = bf16x4(a.w_post + h);
                 x.x += (y.x * r) * w.x, x.y += (y.y * r) * w.y, x.z += (y.z * r) * w.z, x.w += (y.w * r) * w.w;
+            }
+            if (a.w_next) {
+                const float ss = a.lambda * a.lambda * (v4.y + 2.f * r * v4.z + r * r * v4.w);
+                r_next = 1.0f / sqrtf(fmaxf(ss, 0.f) / a.H + a.eps);
             }
         } else {
             x.x += y.x, x.y += y.y, x.z += y.z, x.w += y.w;
@@ -203,7 +233,9 @@ __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
     }
     if (a.outf) {
         float r = 1.f;
-        if (a.w_next) r = 1.0f / sqrtf(block_sum((x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w), red) / a.H + a.eps);
+        if (a.w_next)
+            r = r_next >= 0.f ? r_next
+                              : 1.0f / sqrtf(block_sum((x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w), red) / a.H + a.eps);
         const int row = a.out_row0 + m;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (on && live) {
