@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libdfl.so")
 MAX_LAYERS, MAX_TAPS, MAX_ROWS = 64, 8, 16
 DFL_OK, DFL_E_INVALID_ARG, DFL_E_STATE, DFL_E_CAPACITY, DFL_E_UNSUPPORTED, DFL_E_CUDA, DFL_E_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 DFL_KEEP_ACCEPTED = -1
-DFL_OPT_KEEP_LOGITS, DFL_OPT_GRAPHS, DFL_OPT_STOP_LAYER, DFL_OPT_PROFILE = 1, 2, 3, 4
+DFL_OPT_KEEP_LOGITS, DFL_OPT_GRAPHS, DFL_OPT_STOP_LAYER, DFL_OPT_PROFILE, DFL_OPT_ATTN_CLUSTER = 1, 2, 3, 4, 5
 ERRORS = {DFL_E_INVALID_ARG: "DFL_E_INVALID_ARG", DFL_E_STATE: "DFL_E_STATE", DFL_E_CAPACITY: "DFL_E_CAPACITY",
           DFL_E_UNSUPPORTED: "DFL_E_UNSUPPORTED", DFL_E_CUDA: "DFL_E_CUDA", DFL_E_TIMEOUT: "DFL_E_TIMEOUT"}
 

@@ -331,6 +331,7 @@ struct AttnArgs {
     const DevState *st;
     float scale;
     int *err;              // sticky error bits (nullable), kErrWaitTimeout
+    int max_cluster;       // 16: clusters of 16 CTAs where they fit; 8: always 8
     uint32_t *outf;        // [M][nq*hd] in operand format
     float *outs;
 };
@@ -347,6 +348,7 @@ cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t s);
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s);
 cudaError_t launch_qk(const QkArgs &a, cudaStream_t s);
 cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s);
+cudaError_t attn_prepare(int hd);   // once per head dimension, outside stream capture
 cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s);
 cudaError_t launch_rope_table(float2 *tab, int max_pos, int hd, double base, cudaStream_t s);
 cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const uint16_t *w_norm, float eps,

@@ -124,6 +124,7 @@ struct dfl_ctx {
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
     int last_k = 0;
     int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
+    int attn_cluster = 16; // largest attention cluster: 16 (when it fits) or 8
     long long launches = 0;                       // kernels this context has launched
     bool profile = false;                         // bracket product launches with events
     std::vector<cudaEvent_t> ev_pool;
@@ -618,6 +619,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.st = c->st;
         aa.scale = 1.0f / sqrtf((float)hd);
         aa.err = &c->st->err;
+        aa.max_cluster = c->attn_cluster;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
@@ -814,6 +816,7 @@ int draft_body(dfl_ctx *c) {
         aa.st = c->st;
         aa.scale = 1.0f / sqrtf((float)dhd);
         aa.err = &c->st->err;
+        aa.max_cluster = c->attn_cluster;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
@@ -960,6 +963,8 @@ int dfl_init(const dfl_config *cfg, const dfl_buffers *buf, void *stream, dfl_ct
         (e = launch_rope_table(c->rope_f, c->rope_rows, g.head_dim, g.rope_base_full, c->stream)) != cudaSuccess ||
         (e = launch_rope_table(c->rope_d, c->rope_rows, g.d_head_dim, g.d_rope_base, c->stream)) != cudaSuccess)
         return bail(e, "rope table");
+    if ((e = attn_prepare(g.head_dim)) != cudaSuccess || (e = attn_prepare(g.d_head_dim)) != cudaSuccess)
+        return bail(e, "attention setup");
     if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) return bail(e, "sync");
     c->launches = 3;   // the rope tables
     *out = c;
@@ -1243,6 +1248,15 @@ int dfl_set_option(dfl_ctx *c, int option, int value) {
         c->recs.clear();
         c->ev_next = c->ev_reserved;
         for (int i = 0; i < kProfClasses; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
+    }
+    else if (option == DFL_OPT_ATTN_CLUSTER) {
+        if (value != 8 && value != 16) return fail(c, DFL_E_INVALID_ARG, "attention cluster must be 8 or 16");
+        if (value != c->attn_cluster) {
+            DFL_CK(cudaStreamSynchronize(c->stream));
+            for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second.exec);   // captured with the old size
+            c->graphs.clear();
+            c->attn_cluster = value;
+        }
     }
     else return fail(c, DFL_E_INVALID_ARG, "unknown option");
     return DFL_OK;

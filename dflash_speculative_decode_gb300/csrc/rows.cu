@@ -352,10 +352,12 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Attention. One thread-block cluster of kAttnCluster CTAs per query head. Keys are cut into blocks of
+// Attention. One thread-block cluster of CL CTAs per unit of HP query heads (HP = 2 when the pass has at
+// most 8 rows and a key/value group holds an even number of heads: the two heads fill the 16 rows of
+// the tensor-core tile and share every key/value block they load). Keys are cut into blocks of
 // kAttnKeys ABSOLUTE positions (block b = positions 32b .. 32b+31); CTA r of the cluster takes the
-// blocks b with b % kAttnCluster == r, in ascending order, and folds each into a running softmax state
-// per row (max, sum, sum of p*v). The states of the cluster's CTAs are then merged in rank order through
+// blocks b with b % CL == r, in ascending order, and folds each into a running softmax state per
+// tile row (max, sum, sum of p*v). The states of the cluster's CTAs are then merged in rank order through
 // distributed shared memory. A row's result depends only on its own visible keys and their absolute
 // positions (a block with no visible key leaves the state exactly unchanged), so it does not depend on
 // how many rows the pass carries or where the pass starts.
@@ -367,7 +369,6 @@ constexpr int kAttnThreads = 512;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kAttnKQ = kAttnWarps / 4;   // parts of the head dimension in the score products
 constexpr int kAttnKeys = 32;
-constexpr int kAttnCluster = 8;
 
 // Both products of a block run on the tensor cores (mma.m16n8k16, bf16 in, fp32 accumulate) with every
 // fp32 operand split into bf16 hi + lo and the three products hi*hi + hi*lo + lo*hi added (the lo*lo
@@ -397,6 +398,8 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
+// Tile row r holds pass row m = r (HP = 1) or m = r % 8 of head 2u + r / 8 (HP = 2).
+template <int CL, int HP>
 __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int hd = a.hd, ldq = hd + 8, ldv = hd + 4, hd4 = hd / 4;
@@ -410,9 +413,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     float *Ls = Mx + kMaxRows;                      // [16] running sum
     float *Os = Kb;                                 // [16][hd] final state (after the last block)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
-    const int h = blockIdx.x / kAttnCluster;
+    const int unit = blockIdx.x / CL;
     const unsigned rank = cluster_rank();
-    const int g = h / (a.nq / a.nkv);
+    const int g = unit * HP / (a.nq / a.nkv);
+    auto row_m = [](int r) { return HP == 1 ? r : (r & 7); };
+    auto row_h = [unit](int r) { return HP == 1 ? unit : 2 * unit + (r >> 3); };
     // st->n was set before the pass began (every kernel of the pass waits for its predecessor), so it
     // may be read before this kernel's own dependency wait
     const int n = a.st->n;
@@ -429,16 +434,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     const int bA0 = anyA ? lo / kAttnKeys : 0, bA1 = anyA ? hi / kAttnKeys : -1;
     const int bV = (a.mode == 1 && a.nB > 0) ? (anyA ? bA1 + 1 : 0) : -1;   // the draft block's own keys
     // this CTA's blocks: b0, b0 + 8, ... <= bA1, then bV when it is ours
-    const int b0 = bA0 + int((rank - unsigned(bA0 % kAttnCluster) + kAttnCluster) % kAttnCluster);
-    const int nAmine = b0 <= bA1 ? (bA1 - b0) / kAttnCluster + 1 : 0;
-    const int nmine = nAmine + ((bV >= 0 && bV % kAttnCluster == (int)rank) ? 1 : 0);
+    const int b0 = bA0 + int((rank - unsigned(bA0 % CL) + CL) % CL);
+    const int nAmine = b0 <= bA1 ? (bA1 - b0) / CL + 1 : 0;
+    const int nmine = nAmine + ((bV >= 0 && bV % CL == (int)rank) ? 1 : 0);
 
     // every warp: keys 4w..4w+3 of the block, 16-byte asynchronous copies by the lanes (rows outside
     // every row's range are zeroed: they are masked, and 0 * v must stay 0); one commit group per block
     auto load_block = [&](int i, int buf) {
         float *K = Kb + buf * kAttnKeys * ldq, *V = Vb + buf * kAttnKeys * ldv;
         const bool virt = i >= nAmine;
-        const int b = virt ? bV : b0 + kAttnCluster * i;
+        const int b = virt ? bV : b0 + CL * i;
 #pragma unroll
         for (int kk = 0; kk < kAttnKeys / kAttnWarps; ++kk) {
             const int j = warp * (kAttnKeys / kAttnWarps) + kk;
@@ -474,7 +479,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     // blocks whose positions all precede the pass were written by earlier passes: they are immutable
     // here and are requested before the dependency wait (the pass's own rows come from the kernel
     // before this one)
-    auto early = [&](int i) { return a.mode == 0 && i < nAmine && kAttnKeys * (b0 + kAttnCluster * i) + kAttnKeys <= n; };
+    auto early = [&](int i) { return a.mode == 0 && i < nAmine && kAttnKeys * (b0 + CL * i) + kAttnKeys <= n; };
     int issued = 0;
     while (issued < kAttnBuf - 1 && issued < nmine && early(issued)) {
         load_block(issued, issued);
@@ -488,12 +493,15 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     }
     for (int k = issued; k < kAttnBuf - 1; ++k) cp_async_commit();   // the prologue is kAttnBuf - 1 groups
     for (int e = tid; e < kMaxRows * hd4; e += kAttnThreads) {
-        const int m = e / hd4, d4 = e % hd4;
+        const int r = e / hd4, d4 = e % hd4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (m < M) v = *reinterpret_cast<const float4 *>(a.q + ((long)m * a.nq + h) * hd + 4 * d4);
-        *reinterpret_cast<float4 *>(Qs + m * ldq + 4 * d4) = v;
+        if (row_m(r) < M) v = *reinterpret_cast<const float4 *>(a.q + ((long)row_m(r) * a.nq + row_h(r)) * hd + 4 * d4);
+        *reinterpret_cast<float4 *>(Qs + r * ldq + 4 * d4) = v;
     }
-    if (tid < kMaxRows) Mx[tid] = -INFINITY, Ls[tid] = 0.f;
+    if (tid < kMaxRows) Mx[tid] = -INFINITY, Ls[tid] = 0.f, Sc[tid] = 0.f;
+    // tile rows the pass does not carry keep probability 0 and rescale 0 (the softmax step skips them)
+    for (int e = tid; e < kMaxRows * kAttnKeys; e += kAttnThreads)
+        if (row_m(e / kAttnKeys) >= M) Ps[(e / kAttnKeys) * kAttnSP + e % kAttnKeys] = 0.f;
     __syncthreads();
 
     // this warp's query fragments (A operand, rows 0..15, its half of the head dimension), hi and lo
@@ -536,7 +544,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         __syncthreads();
         const float *K = Kb + buf * kAttnKeys * ldq, *V = Vb + buf * kAttnKeys * ldv;
         const bool virt = i >= nAmine;
-        const int b = virt ? bV : b0 + kAttnCluster * i;
+        const int b = virt ? bV : b0 + CL * i;
         // partial scores of this warp's 8 keys over its half of the head dimension
         {
             float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -562,9 +570,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         __syncthreads();
         // softmax update: warp -> rows warp, warp + kAttnWarps, ...; lane -> key
 #pragma unroll
-        for (int r = 0; r < kMaxRows / kAttnWarps; ++r) {
-            const int m = warp + kAttnWarps * r;
-            if (m >= M) break;
+        for (int rr = 0; rr < kMaxRows / kAttnWarps; ++rr) {
+            const int r = warp + kAttnWarps * rr;
+            const int m = row_m(r);
+            if (m >= M) continue;
             const int j = lane;
             bool vis;
             if (virt) {
@@ -578,31 +587,28 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
                     vis = pos >= lo && pos <= hi;
                 }
             }
-            float sraw = Sp[m * kAttnSP + j];
+            float sraw = Sp[r * kAttnSP + j];
 #pragma unroll
-            for (int part = 1; part < kAttnKQ; ++part) sraw += Sp[(part * kMaxRows + m) * kAttnSP + j];
+            for (int part = 1; part < kAttnKQ; ++part) sraw += Sp[(part * kMaxRows + r) * kAttnSP + j];
             const float sv = vis ? sraw * a.scale : -INFINITY;
             float bm = sv;
 #pragma unroll
             for (int oo = 16; oo > 0; oo >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, oo));
-            const float mo = Mx[m];
+            const float mo = Mx[r];
             const float mn = fmaxf(mo, bm);
             const float pj = vis ? expf(sv - mn) : 0.f;
             float ps = pj;
 #pragma unroll
             for (int oo = 16; oo > 0; oo >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, oo);
             const float sc = mo == -INFINITY ? 0.f : expf(mo - mn);
-            Ps[m * kAttnSP + j] = pj;
+            Ps[r * kAttnSP + j] = pj;
             __syncwarp();
             if (lane == 0) {
-                Sc[m] = sc;
-                Mx[m] = mn;
-                Ls[m] = fmaf(Ls[m], sc, ps);
+                Sc[r] = sc;
+                Mx[r] = mn;
+                Ls[r] = fmaf(Ls[r], sc, ps);
             }
         }
-        for (int e = tid; e < (kMaxRows - M) * kAttnKeys; e += kAttnThreads)   // rows the pass does not carry
-            Ps[(M + e / kAttnKeys) * kAttnSP + e % kAttnKeys] = 0.f;
-        if (tid >= M && tid < kMaxRows) Sc[tid] = 0.f;
         __syncthreads();
         // running p.V over the block's 32 keys (two k-steps of 16)
         {
@@ -645,37 +651,38 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     for (int t = 0; t < kAttnNT; ++t) {
         if (warp + kAttnWarps * t < ntiles) {
             const int col = 8 * (warp + kAttnWarps * t) + 2 * tq;
-            if (gq < M) *reinterpret_cast<float2 *>(Os + gq * hd + col) = make_float2(o[t][0], o[t][1]);
-            if (gq + 8 < M) *reinterpret_cast<float2 *>(Os + (gq + 8) * hd + col) = make_float2(o[t][2], o[t][3]);
+            if (row_m(gq) < M) *reinterpret_cast<float2 *>(Os + gq * hd + col) = make_float2(o[t][0], o[t][1]);
+            if (row_m(gq + 8) < M) *reinterpret_cast<float2 *>(Os + (gq + 8) * hd + col) = make_float2(o[t][2], o[t][3]);
         }
     }
     cluster_sync_all();
     const int ng16 = hd / 16;
-    const int items = M * ng16;
-    const int hw = tid >> 4;   // half warp: one (row, 16-column group) item per round
-    for (int base = 0; base < items; base += kAttnCluster * (kAttnThreads / 16)) {
-        const int it = base + int(rank) + kAttnCluster * hw;
-        const bool on = it < items;
+    const int items = (HP == 1 ? M : kMaxRows) * ng16;   // (tile row, 16-column group)
+    const int hw = tid >> 4;   // half warp: one item per round
+    for (int base = 0; base < items; base += CL * (kAttnThreads / 16)) {
+        const int it = base + int(rank) + CL * hw;
+        const int r = it / ng16;
+        const bool on = it < items && row_m(r) < M;
         float hl = 0.f;
         int m = 0, col = 0;
         if (on) {
-            m = it / ng16;
+            m = row_m(r);
             const int d = 16 * (it % ng16) + (tid & 15);
             float mt = -INFINITY;
-            float mr[kAttnCluster];
+            float mr[CL];
 #pragma unroll
-            for (int r = 0; r < kAttnCluster; ++r) {
-                mr[r] = ld_cluster(Mx + m, r);
-                mt = fmaxf(mt, mr[r]);
+            for (int q = 0; q < CL; ++q) {
+                mr[q] = ld_cluster(Mx + r, q);
+                mt = fmaxf(mt, mr[q]);
             }
             float num = 0.f, den = 0.f;
 #pragma unroll
-            for (int r = 0; r < kAttnCluster; ++r) {
-                const float f = mr[r] == -INFINITY ? 0.f : expf(mr[r] - mt);
-                den = fmaf(ld_cluster(Ls + m, r), f, den);
-                num = fmaf(ld_cluster(Os + m * hd + d, r), f, num);
+            for (int q = 0; q < CL; ++q) {
+                const float f = mr[q] == -INFINITY ? 0.f : expf(mr[q] - mt);
+                den = fmaf(ld_cluster(Ls + r, q), f, den);
+                num = fmaf(ld_cluster(Os + r * hd + d, q), f, num);
             }
-            col = h * hd + d;
+            col = row_h(r) * hd + d;
             hl = act_store(a.outf, a.nq * hd, m, col, num / den);
         }
         const float sg = half_warp_sum(hl);   // every lane of the warp takes part
@@ -684,31 +691,68 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     cluster_sync_all();   // no CTA leaves while another still reads its shared memory
 }
 
-cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
-    const size_t smem = attn_smem(a.hd);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn_smem(256)));
-        if (e != cudaSuccess) return e;
-        attr = true;
+// Clusters of 16 (a non-portable size) are used for a layer shape when at least as many of them fit on
+// the device at once as the shape has head pairs. The fit is asked once per head-dimension class, at
+// context creation (outside any stream capture); until then every launch takes clusters of 8. The
+// cluster size depends only on the shape, never on the number of rows, so a row's result does not
+// depend on the pass it travels in.
+static int g_wide_fit[2] = {0, 0};   // 16-CTA clusters that fit at once, per class (hd <= 128, hd > 128)
+
+template <int CL, int HP>
+static cudaError_t attn_attrs() {
+    static bool done = false;
+    if (done) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(k_attn<CL, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(attn_smem(256)));
+    if (e == cudaSuccess && CL > 8)
+        e = cudaFuncSetAttribute(k_attn<CL, HP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
+cudaError_t attn_prepare(int hd) {
+    cudaError_t e;
+    if ((e = attn_attrs<8, 1>()) || (e = attn_attrs<8, 2>())) return e;
+    if (attn_attrs<16, 1>() != cudaSuccess || attn_attrs<16, 2>() != cudaSuccess) {
+        cudaGetLastError();   // no wide clusters on this device: clusters of 8 throughout
+        return cudaSuccess;
     }
-    if (a.hd % 64 || a.hd < 64 || a.hd > 256 || a.M < 1 || a.M > kMaxRows || a.nB > kAttnKeys || a.nq % a.nkv)
-        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.nq * kAttnCluster);
+    cfg.gridDim = dim3(16);
     cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attrs[2];
-    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[0].val.programmaticStreamSerializationAllowed = 1;
-    attrs[1].id = cudaLaunchAttributeClusterDimension;
-    attrs[1].val.clusterDim.x = kAttnCluster;
-    attrs[1].val.clusterDim.y = 1;
-    attrs[1].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_attn, a);
+    cfg.dynamicSmemBytes = attn_smem(hd);
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 16;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_attn<16, 2>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    g_wide_fit[hd > 128] = n;
+    return cudaSuccess;
+}
+
+template <int CL, int HP>
+static cudaError_t launch_attn_t(const AttnArgs &a, cudaStream_t s) {
+    const cudaError_t e = attn_attrs<CL, HP>();
+    if (e != cudaSuccess) return e;
+    return launch_cluster_pdl(k_attn<CL, HP>, a.nq / HP * CL, CL, kAttnThreads, attn_smem(a.hd), s, a);
+}
+
+cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
+    if (a.hd % 64 || a.hd < 64 || a.hd > 256 || a.M < 1 || a.M > kMaxRows || a.nB > kAttnKeys || a.nkv < 1 ||
+        a.nq % a.nkv)
+        return cudaErrorInvalidValue;
+    const bool pairs = (a.nq / a.nkv) % 2 == 0;   // two heads of one key/value group per CTA possible
+    const bool wide = pairs && a.max_cluster >= 16 && g_wide_fit[a.hd > 128] >= a.nq / 2;
+    const bool hp2 = pairs && a.M <= 8;
+    if (wide) return hp2 ? launch_attn_t<16, 2>(a, s) : launch_attn_t<16, 1>(a, s);
+    return hp2 ? launch_attn_t<8, 2>(a, s) : launch_attn_t<8, 1>(a, s);
 }
 
 // ---------------------------------------------------------------------------------------------------

@@ -131,6 +131,25 @@ def test_spec_decode_lockstep_sampled(pair):
         assert res.tokens == [int(t) for t in plain.tokens]
 
 
+@pytest.mark.parametrize("temperature,cluster", [(None, 16), (0.8, 16), (None, 8)])
+def test_spec_decode_long_context(pair, temperature, cluster):
+    """A 2000-token prompt: the sliding rings wrap many times over, full layers read dozens of key
+    blocks, and the draft catches up on the whole context. Lockstep with the oracle as above, with
+    attention clusters of 16 (where they fit) and of 8."""
+    import dataclasses
+    from dflash_speculative_decode_gb300._abi import DFL_OPT_ATTN_CLUSTER
+    from gpu_harness import engine, lockstep
+    pc, W = pair
+    pc = dataclasses.replace(pc, max_ctx=2304)
+    eng = engine(pc, W)
+    eng.dfl_set_option(DFL_OPT_ATTN_CLUSTER, cluster)
+    res, plain = lockstep(pc, W, gen.prompt(pc.target.vocab, 2000, request=7), 24, p=0.3,
+                          temperature=temperature, seed=11, eng=eng)
+    if res.near_ties == 0:
+        assert res.tokens == [int(t) for t in plain.tokens]
+    assert res.max_rel_l1 < 1e-3
+
+
 def test_gpu_batched_equals_sequential(pair):
     """k rows in one pass give bit-identical logits to k one-row passes on the GPU."""
     from dflash_speculative_decode_gb300 import DFL_OPT_KEEP_LOGITS
