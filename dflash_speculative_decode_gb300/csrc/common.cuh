@@ -331,7 +331,7 @@ struct AttnArgs {
     const DevState *st;
     float scale;
     int *err;              // sticky error bits (nullable), kErrWaitTimeout
-    int max_cluster;       // 16: clusters of 16 CTAs where they fit; 8: always 8
+    int max_cluster;       // largest cluster size allowed (16, 8 or 4); the largest that fits is taken
     uint32_t *outf;        // [M][nq*hd] in operand format
     float *outs;
 };

@@ -124,7 +124,7 @@ struct dfl_ctx {
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
     int last_k = 0;
     int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
-    int attn_cluster = 16; // largest attention cluster: 16 (when it fits) or 8
+    int attn_cluster = 16; // largest attention cluster size allowed: 16, 8 or 4
     long long launches = 0;                       // kernels this context has launched
     bool profile = false;                         // bracket product launches with events
     std::vector<cudaEvent_t> ev_pool;
@@ -1250,7 +1250,8 @@ int dfl_set_option(dfl_ctx *c, int option, int value) {
         for (int i = 0; i < kProfClasses; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
     }
     else if (option == DFL_OPT_ATTN_CLUSTER) {
-        if (value != 8 && value != 16) return fail(c, DFL_E_INVALID_ARG, "attention cluster must be 8 or 16");
+        if (value != 4 && value != 8 && value != 16)
+            return fail(c, DFL_E_INVALID_ARG, "attention cluster must be 4, 8 or 16");
         if (value != c->attn_cluster) {
             DFL_CK(cudaStreamSynchronize(c->stream));
             for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second.exec);   // captured with the old size

@@ -79,6 +79,12 @@ __device__ __forceinline__ unsigned cluster_rank() {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // load a float from the shared memory of CTA `rank` of this cluster, at the offset of `p` in ours
 __device__ __forceinline__ float ld_cluster(const float *p, unsigned rank) {
     const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
@@ -658,46 +664,60 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     cluster_sync_all();
     const int ng16 = hd / 16;
     const int items = (HP == 1 ? M : kMaxRows) * ng16;   // (tile row, 16-column group)
-    const int hw = tid >> 4;   // half warp: one item per round
-    for (int base = 0; base < items; base += CL * (kAttnThreads / 16)) {
-        const int it = base + int(rank) + CL * hw;
+    const int hw = tid >> 4;                               // half warp: one item per round
+    constexpr int kStride = CL * (kAttnThreads / 16);
+    constexpr int kRounds = (kMaxRows * 16 + kStride - 1) / kStride;   // hd <= 256
+    float res[kRounds];
+    int res_m[kRounds], res_col[kRounds];
+    bool res_on[kRounds];
+    // every rank's (max, sum, partial output) is requested at once, then combined in rank order
+#pragma unroll
+    for (int k = 0; k < kRounds; ++k) {
+        const int it = k * kStride + int(rank) + CL * hw;
         const int r = it / ng16;
-        const bool on = it < items && row_m(r) < M;
-        float hl = 0.f;
-        int m = 0, col = 0;
-        if (on) {
-            m = row_m(r);
+        res_on[k] = it < items && row_m(r) < M;
+        res[k] = 0.f;
+        res_m[k] = res_col[k] = 0;
+        if (res_on[k]) {
             const int d = 16 * (it % ng16) + (tid & 15);
-            float mt = -INFINITY;
-            float mr[CL];
+            float mr[CL], lr[CL], orr[CL];
 #pragma unroll
             for (int q = 0; q < CL; ++q) {
                 mr[q] = ld_cluster(Mx + r, q);
-                mt = fmaxf(mt, mr[q]);
+                lr[q] = ld_cluster(Ls + r, q);
+                orr[q] = ld_cluster(Os + r * hd + d, q);
             }
+            float mt = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < CL; ++q) mt = fmaxf(mt, mr[q]);
             float num = 0.f, den = 0.f;
 #pragma unroll
             for (int q = 0; q < CL; ++q) {
                 const float f = mr[q] == -INFINITY ? 0.f : expf(mr[q] - mt);
-                den = fmaf(ld_cluster(Ls + r, q), f, den);
-                num = fmaf(ld_cluster(Os + r * hd + d, q), f, num);
+                den = fmaf(lr[q], f, den);
+                num = fmaf(orr[q], f, num);
             }
-            col = row_h(r) * hd + d;
-            hl = act_store(a.outf, a.nq * hd, m, col, num / den);
+            res[k] = num / den;
+            res_m[k] = row_m(r);
+            res_col[k] = row_h(r) * hd + d;
         }
-        const float sg = half_warp_sum(hl);   // every lane of the warp takes part
-        if (on && (tid & 15) == 0) a.outs[(col >> 4) * kMaxRows + m] = sg;
     }
-    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+    cluster_arrive();   // no reads of other CTAs' shared memory from here on
+#pragma unroll
+    for (int k = 0; k < kRounds; ++k) {
+        const float hl = res_on[k] ? act_store(a.outf, a.nq * hd, res_m[k], res_col[k], res[k]) : 0.f;
+        const float sg = half_warp_sum(hl);   // every lane of the warp takes part
+        if (res_on[k] && (tid & 15) == 0) a.outs[(res_col[k] >> 4) * kMaxRows + res_m[k]] = sg;
+    }
+    cluster_wait();     // no CTA leaves while another still reads its shared memory
 }
 
-// Clusters of 16 (a non-portable size) are used for a layer shape when at least as many of them fit on
-// the device at once as the shape has head pairs. The fit is asked once per head-dimension class, at
-// context creation (outside any stream capture); until then every launch takes clusters of 8. The
-// cluster size depends only on the shape, never on the number of rows, so a row's result does not
-// depend on the pass it travels in.
-static int g_wide_fit[2] = {0, 0};   // 16-CTA clusters that fit at once, per class (hd <= 128, hd > 128)
-
+// Cluster size per layer shape: the largest of 16 (a non-portable size), 8 and 4 such that all of the
+// shape's clusters fit on the device at once (one wave; a second wave would double the launch). The
+// fit is asked once per head-dimension class at context creation, outside any stream capture; until
+// then every launch takes clusters of 8. The size depends only on the shape, never on the number of
+// rows, so a row's result does not depend on the pass it travels in.
+static int g_fit[2][2] = {{0, 1 << 20}, {0, 1 << 20}};   // [hd > 128][16, 8]: clusters that fit at once
 template <int CL, int HP>
 static cudaError_t attn_attrs() {
     static bool done = false;
@@ -710,30 +730,38 @@ static cudaError_t attn_attrs() {
     return e;
 }
 
-cudaError_t attn_prepare(int hd) {
-    cudaError_t e;
-    if ((e = attn_attrs<8, 1>()) || (e = attn_attrs<8, 2>())) return e;
-    if (attn_attrs<16, 1>() != cudaSuccess || attn_attrs<16, 2>() != cudaSuccess) {
-        cudaGetLastError();   // no wide clusters on this device: clusters of 8 throughout
-        return cudaSuccess;
-    }
+template <int CL>
+static int clusters_that_fit(int hd) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16);
+    cfg.gridDim = dim3(CL);
     cfg.blockDim = dim3(kAttnThreads);
     cfg.dynamicSmemBytes = attn_smem(hd);
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 16;
+    at[0].val.clusterDim.x = CL;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_attn<16, 2>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
+    if (cudaOccupancyMaxActiveClusters(&n, k_attn<CL, 2>, &cfg) != cudaSuccess) {
+        cudaGetLastError();   // a refused query leaves no sticky error
         n = 0;
     }
-    g_wide_fit[hd > 128] = n;
+    return n;
+}
+
+cudaError_t attn_prepare(int hd) {
+    cudaError_t e;
+    if ((e = attn_attrs<8, 1>()) || (e = attn_attrs<8, 2>()) || (e = attn_attrs<4, 1>()) || (e = attn_attrs<4, 2>()))
+        return e;
+    g_fit[hd > 128][1] = clusters_that_fit<8>(hd);
+    if (attn_attrs<16, 1>() != cudaSuccess || attn_attrs<16, 2>() != cudaSuccess) {
+        cudaGetLastError();   // no wide clusters on this device
+        g_fit[hd > 128][0] = 0;
+    } else {
+        g_fit[hd > 128][0] = clusters_that_fit<16>(hd);
+    }
     return cudaSuccess;
 }
 
@@ -749,10 +777,13 @@ cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
         a.nq % a.nkv)
         return cudaErrorInvalidValue;
     const bool pairs = (a.nq / a.nkv) % 2 == 0;   // two heads of one key/value group per CTA possible
-    const bool wide = pairs && a.max_cluster >= 16 && g_wide_fit[a.hd > 128] >= a.nq / 2;
+    const int units = pairs ? a.nq / 2 : a.nq;    // clusters of a pass of up to 8 rows
+    const int *fit = g_fit[a.hd > 128];
+    const int cl = (a.max_cluster >= 16 && fit[0] >= units) ? 16 : (a.max_cluster >= 8 && fit[1] >= units) ? 8 : 4;
     const bool hp2 = pairs && a.M <= 8;
-    if (wide) return hp2 ? launch_attn_t<16, 2>(a, s) : launch_attn_t<16, 1>(a, s);
-    return hp2 ? launch_attn_t<8, 2>(a, s) : launch_attn_t<8, 1>(a, s);
+    if (cl == 16) return hp2 ? launch_attn_t<16, 2>(a, s) : launch_attn_t<16, 1>(a, s);
+    if (cl == 8) return hp2 ? launch_attn_t<8, 2>(a, s) : launch_attn_t<8, 1>(a, s);
+    return hp2 ? launch_attn_t<4, 2>(a, s) : launch_attn_t<4, 1>(a, s);
 }
 
 // ---------------------------------------------------------------------------------------------------

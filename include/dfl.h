@@ -171,11 +171,11 @@ int64_t dfl_positions_held(const dfl_ctx *ctx);
  * replaying captured CUDA graphs; DFL_OPT_STOP_LAYER = l >= 0 (inspection only) makes target passes
  * stop after layer l, without the head, so dfl_debug_read shows that layer's intermediates; -1 = off;
  * DFL_OPT_PROFILE = 1 brackets every kernel launch with CUDA events on the context's stream (read with
- * dfl_profile_read; setting the option clears the totals); DFL_OPT_ATTN_CLUSTER = 16 (default) lets
- * attention spread each pair of query heads over a cluster of 16 CTAs where the device fits enough of
- * them at once, 8 keeps clusters of 8 (the two differ in the order in which the clusters' partial
- * softmax states are added, so logits may differ in the last bits); other values are DFL_E_INVALID_ARG.
- * Changing it drops the captured graphs. */
+ * dfl_profile_read; setting the option clears the totals); DFL_OPT_ATTN_CLUSTER = 16 (default), 8 or 4
+ * caps the number of CTAs over which attention spreads one pair of query heads (the largest size up to
+ * the cap whose clusters all fit on the device at once is taken; sizes differ in the order in which
+ * the partial softmax states are added, so logits may differ in the last bits); other values are
+ * DFL_E_INVALID_ARG. Changing it drops the captured graphs. */
 enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3, DFL_OPT_PROFILE = 4,
        DFL_OPT_ATTN_CLUSTER = 5 };
 int dfl_set_option(dfl_ctx *ctx, int option, int value);

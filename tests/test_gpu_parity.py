@@ -131,11 +131,11 @@ def test_spec_decode_lockstep_sampled(pair):
         assert res.tokens == [int(t) for t in plain.tokens]
 
 
-@pytest.mark.parametrize("temperature,cluster", [(None, 16), (0.8, 16), (None, 8)])
+@pytest.mark.parametrize("temperature,cluster", [(None, 16), (0.8, 16), (None, 8), (None, 4)])
 def test_spec_decode_long_context(pair, temperature, cluster):
     """A 2000-token prompt: the sliding rings wrap many times over, full layers read dozens of key
     blocks, and the draft catches up on the whole context. Lockstep with the oracle as above, with
-    attention clusters of 16 (where they fit) and of 8."""
+    attention clusters of up to 16, 8 and 4 CTAs."""
     import dataclasses
     from dflash_speculative_decode_gb300._abi import DFL_OPT_ATTN_CLUSTER
     from gpu_harness import engine, lockstep
