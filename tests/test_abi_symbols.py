@@ -68,3 +68,18 @@ def test_q41_sizes():
     assert L.dfl_q41_image_bytes(32, 64) == 64 * 64 * 5 // 8      # K padded to 64
     assert L.dfl_q41_image_bytes(30, 64) == -1
     assert L.dfl_q41_gemm_scratch_bytes(2560, 4096, 17) == -1
+
+
+def test_binding_constants_match_header():
+    """Every enum constant of include/dfl.h that the binding names has the header's value."""
+    from dflash_speculative_decode_gb300 import _abi
+    src = open(os.path.join(ROOT, "include", "dfl.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    header = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", src, flags=re.S):
+        for name, val in re.findall(r"\b(DFL_[A-Z0-9_]+)\s*=\s*(-?\d+)", body):
+            header[name] = int(val)
+    assert {"DFL_OPT_KEEP_LOGITS", "DFL_OPT_PROFILE", "DFL_OPT_ATTN_CLUSTER", "DFL_E_INVALID_ARG"} <= set(header)
+    named = {n: getattr(_abi, n) for n in header if hasattr(_abi, n)}
+    assert len(named) >= 8
+    assert all(named[n] == header[n] for n in named), {n: (named[n], header[n]) for n in named if named[n] != header[n]}
