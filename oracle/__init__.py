@@ -8,7 +8,8 @@ module both sides use is the seeded input generator `gen`, which holds none of t
 """
 from . import _native
 from ._native import bf16r, bf16_decode, half_decode, linear_bf16, linear_q41, q41_dequant, sample, uniform
-from .model import Draft, Target, attend, keep_positions, kv_widths, positions_held, rmsnorm, rope, silu
+from .model import (Draft, Target, attend, keep_positions, kv_widths, ple_tail, positions_held, rmsnorm, rope, silu,
+                    swiglu)
 from .spec import Pair, Run, Sampler, accept_length, plain_decode, spec_decode
 
 

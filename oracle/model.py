@@ -59,8 +59,28 @@ def rope(v: np.ndarray, pos: int, base: float) -> np.ndarray:
 
 
 def silu(g: np.ndarray) -> np.ndarray:
+    """SiLU (the "swish" gate of SwiGLU): g * sigmoid(g) = g / (1 + exp(-g))."""
     gd = np.asarray(g, F64)
     return gd / (1.0 + np.exp(-gd))
+
+
+def swiglu(gu: np.ndarray, F: int) -> np.ndarray:
+    """SwiGLU of a fused gate|up product: silu(gate) * up, the gate being the first F columns and up the
+    next F (the fused matrix is named "gate|up", gate first)."""
+    return (silu(gu[..., :F]) * np.asarray(gu[..., F:2 * F], F64)).astype(F32)
+
+
+def ple_tail(x: np.ndarray, p_l: np.ndarray, Wg: np.ndarray, Wp: np.ndarray, w_norm: np.ndarray, lam: float,
+             eps: float) -> np.ndarray:
+    """Per-layer-embedding tail of one target layer (1bit engine PR "npu forward: Gemma4 verifies a draft
+    in one batched pass", "What changes": the PLE gate and projection as M-row GEMMs, then the layer
+    scalar). The gate reads the residual stream x itself; z = silu(x . Wg) * p_l (the token's row of the
+    per-layer table); y = z . Wp is normed and added to x, and the sum is multiplied by lambda."""
+    t = nat.linear_q41(x, Wg)
+    z = (silu(t) * np.asarray(p_l, F64)).astype(F32)
+    y = nat.linear_q41(z, Wp)
+    xs = add(x, rmsnorm(y, w_norm, eps))
+    return (np.asarray(xs, F64) * F64(np.float32(lam))).astype(F32)
 
 
 def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
@@ -107,7 +127,18 @@ def positions_held(planes: Dict[int, np.ndarray], widths: List[int]) -> int:
 
 # ---- target -----------------------------------------------------------------------------------------
 class Target:
-    def __init__(self, cfg, W: dict, tap_layers=(), width_mutant: Optional[int] = None):
+    """The target model with one KV plane per layer that holds its own (linear storage: position j is row
+    j). Options that model other storage, for the tests that show which ones the pins reject:
+      ring_capacity: sliding layers also keep their rows in a ring of that many slots (slot = position mod
+        capacity), as a fixed-size device arena would, and attention reads them from the ring. A ring of
+        W + R_max - 1 slots holds every key any row of a pass of up to R_max rows still needs; a ring of W
+        slots does not (a pass overwrites keys its own first rows, or the rows kept after a rollback, need).
+      width_mutant: count every layer that holds a plane at this one width (the pages' single-width defect).
+      shared_appends: a KV-shared layer also appends its owner's new rows to a plane of its own (a
+        defect: such a layer must hold nothing)."""
+
+    def __init__(self, cfg, W: dict, tap_layers=(), width_mutant: Optional[int] = None,
+                 ring_capacity: Optional[int] = None, shared_appends: bool = False):
         self.cfg = cfg
         self.W = W
         self.tap_layers = tuple(tap_layers)
@@ -118,6 +149,18 @@ class Target:
         # a mutant that counts every layer at one width, to show the tests catch it
         self.widths = [width_mutant if (width_mutant and w[l]) else w[l] for l in range(cfg.n_layers)]
         self.planes: Dict[int, np.ndarray] = {l: np.zeros(0, F32) for l in range(cfg.n_layers) if cfg.is_owner(l)}
+        self.shared_appends = shared_appends
+        if shared_appends:
+            for l in range(cfg.n_layers):
+                if not cfg.is_owner(l):
+                    self.planes[l] = np.zeros(0, F32)
+                    self.widths[l] = w[cfg.kv_owner[l]]
+        self.ring_capacity = ring_capacity
+        self.rings: Dict[int, np.ndarray] = {}
+        if ring_capacity:
+            for l in range(cfg.n_layers):
+                if cfg.is_owner(l) and cfg.layer_type[l] == 0:
+                    self.rings[l] = np.zeros((ring_capacity, w[l]), F32)
         self.record = None               # optional dict: per-layer intermediates of the last forward
         self.n = 0                       # committed positions
         self.pending = 0                 # rows of the last forward not yet committed
@@ -143,17 +186,17 @@ class Target:
     def snapshot(self):
         if self.pending:
             raise RuntimeError("snapshot needs a committed state")
-        return copy.deepcopy((self.n, self.planes, self.taps))
+        return copy.deepcopy((self.n, self.planes, self.taps, self.rings))
 
     def restore(self, snap) -> None:
-        n, planes, taps = copy.deepcopy(snap)
-        self.n, self.planes, self.taps, self.pending = n, planes, taps, 0
+        n, planes, taps, rings = copy.deepcopy(snap)
+        self.n, self.planes, self.taps, self.rings, self.pending = n, planes, taps, rings, 0
 
     # one batched pass
-    def forward(self, tokens) -> np.ndarray:
+    def forward(self, tokens, head_rows: Optional[int] = None) -> np.ndarray:
         """Run rows `tokens` at positions n, n+1, ... through every layer (layer by layer, each row on
-        its own); append their keys and values; return fp32 logits [k][vocab]. The rows stay pending
-        until commit()."""
+        its own); append their keys and values; return fp32 logits [k][vocab] (or of the last head_rows
+        rows only). The rows stay pending until commit()."""
         if self.pending:
             raise RuntimeError("a verify is pending")
         c, W = self.cfg, self.W
@@ -178,6 +221,13 @@ class Target:
                 kk = np.stack([rope(rmsnorm(kk[i], self.norm[p + "k_norm"], c.eps), pos[i], base) for i in range(k)])
                 rows = np.concatenate([kk.reshape(k, -1), vv], axis=1).astype(F32)
                 self.planes[l] = np.concatenate([self.planes[l], rows.reshape(-1)])
+                if l in self.rings:
+                    for i in range(k):
+                        self.rings[l][pos[i] % self.ring_capacity] = rows[i]
+            elif self.shared_appends:
+                # the defect: the owner's new rows appended again to a plane of this layer's own
+                w_own = 2 * nkv * hd
+                self.planes[l] = np.concatenate([self.planes[l], self.planes[own][-k * w_own:]])
             width = self.widths[own]
             plane = self.planes[own].reshape(-1, width) if width == 2 * nkv * hd else None
             if plane is None:   # only the width mutant gets here: read the plane at its true row length
@@ -188,10 +238,14 @@ class Target:
             for i in range(k):
                 hi = pos[i] + 1
                 lo = max(0, hi - c.window) if c.layer_type[l] == 0 else 0
+                if own in self.rings:   # keys and values as the ring holds them now
+                    rows_i = self.rings[own][np.arange(lo, hi) % self.ring_capacity]
+                else:
+                    rows_i = plane[lo:hi]
                 for hq in range(nq):
                     g = hq // grp
-                    Kj = plane[lo:hi, g * hd:(g + 1) * hd]
-                    Vj = plane[lo:hi, (nkv + g) * hd:(nkv + g + 1) * hd]
+                    Kj = rows_i[:, g * hd:(g + 1) * hd]
+                    Vj = rows_i[:, (nkv + g) * hd:(nkv + g + 1) * hd]
                     o[i, hq] = attend(q[i, hq], Kj, Vj, 1.0 / np.sqrt(hd))
             if self.record is not None:
                 self.record[l] = {"h": h.copy(), "qkv": y.copy(), "q": q.reshape(k, -1).copy(),
@@ -199,18 +253,13 @@ class Target:
             y = nat.linear_q41(o.reshape(k, nq * hd), W[p + "wo"])
             x = add(x, rmsnorm(y, self.norm[p + "post_attn_norm"], c.eps))
             b = rmsnorm(x, self.norm[p + "pre_ffn_norm"], c.eps)
-            gu = nat.linear_q41(b, W[p + "wgu"])
-            F = c.ffn[l]
-            a = (silu(gu[:, :F]) * np.asarray(gu[:, F:], F64)).astype(F32)
+            a = swiglu(nat.linear_q41(b, W[p + "wgu"]), c.ffn[l])
             y = nat.linear_q41(a, W[p + "wd"])
             x = add(x, rmsnorm(y, self.norm[p + "post_ffn_norm"], c.eps))
             if c.ple_dim:
                 P = c.ple_dim
-                t = nat.linear_q41(x, W[p + "wple_g"])
-                z = (silu(t) * np.asarray(ple[:, l * P:(l + 1) * P], F64)).astype(F32)
-                y = nat.linear_q41(z, W[p + "wple_p"])
-                x = add(x, rmsnorm(y, self.norm[p + "ple_norm"], c.eps))
-                x = (np.asarray(x, F64) * F64(np.float32(self.lam[l]))).astype(F32)
+                x = ple_tail(x, ple[:, l * P:(l + 1) * P], W[p + "wple_g"], W[p + "wple_p"],
+                             self.norm[p + "ple_norm"], self.lam[l], c.eps)
             if l in self.tap_layers:
                 ti = self.tap_layers.index(l)
                 taps[:, ti * H:(ti + 1) * H] = x
@@ -219,7 +268,7 @@ class Target:
         self.last_hidden = x
         self.pending = k
         self.taps = np.concatenate([self.taps, taps])
-        return self.head(x)
+        return self.head(x if head_rows is None else x[k - head_rows:])
 
     def head(self, x: np.ndarray) -> np.ndarray:
         return nat.linear_bf16(rmsnorm(x, self.norm["final_norm"], self.cfg.eps), self.W["head"])
@@ -309,8 +358,7 @@ class Draft:
                                       1.0 / np.sqrt(hd))
             x = add(x, nat.linear_q41(o.reshape(B, -1), W[p + "wo"]))
             b = rmsnorm(x, self.norm[p + "ffn_norm"], d.eps)
-            gu = nat.linear_q41(b, W[p + "wgu"])
-            a = (silu(gu[:, : d.ffn]) * np.asarray(gu[:, d.ffn:], F64)).astype(F32)
+            a = swiglu(nat.linear_q41(b, W[p + "wgu"]), d.ffn)
             x = add(x, nat.linear_q41(a, W[p + "wd"]))
         self.last_hidden = x
         logits = nat.linear_bf16(rmsnorm(x[1:], self.norm["d.final_norm"], d.eps), head)

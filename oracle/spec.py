@@ -64,9 +64,9 @@ class Run:
 class Pair:
     """Target + draft with the draft's context kept up to date with committed rows."""
 
-    def __init__(self, pc, W, width_mutant=None, with_draft=True):
+    def __init__(self, pc, W, width_mutant=None, with_draft=True, **target_options):
         self.pc = pc
-        self.target = Target(pc.target, W, tap_layers=pc.draft.taps, width_mutant=width_mutant)
+        self.target = Target(pc.target, W, tap_layers=pc.draft.taps, width_mutant=width_mutant, **target_options)
         self.draft = Draft(pc.draft, W, pc.target) if with_draft else None
         self.W = W
 
@@ -82,7 +82,7 @@ class Pair:
         logits = None
         for i in range(0, len(prompt), step):
             rows = prompt[i:i + step]
-            logits = self.target.forward(rows)
+            logits = self.target.forward(rows, head_rows=1)
             self.target.commit(len(rows))
         self.sync_draft()
         return sampler.pick(logits[-1], self.target.n)

@@ -74,12 +74,10 @@ def test_width_mutant_fails_rollback():
     assert not np.array_equal(a2.target.forward([5])[0], b.target.forward([5])[0])
 
 
-def test_shared_planes_stay_empty():
-    """P6: KV-shared layers hold no plane through verify, rollback, snapshot and restore; the held count
-    ignores them; owners grow by exactly their width per row."""
-    pc = gen.tiny_shared_pair()
-    W = gen.generate(pc)
-    pair = _prefilled(pc, W, P=10)
+def _check_shared_planes_empty(pair):
+    """The empty-plane checks: shared layers hold no plane through verify, rollback, snapshot and
+    restore; owners grow by exactly their width per row; the held count ignores shared layers."""
+    pc = pair.pc
     tg = pair.target
     shared = [l for l in range(pc.target.n_layers) if not pc.target.is_owner(l)]
     assert shared == [4, 5]
@@ -93,6 +91,51 @@ def test_shared_planes_stay_empty():
     assert all(tg.plane(l) is None for l in shared) and tg.positions_held() == 12
     pair.restore(snap)
     assert all(tg.plane(l) is None for l in shared) and tg.positions_held() == 10
+
+
+def test_shared_planes_stay_empty():
+    """P6 on tiny-shared (layers 4 and 5 read the planes of layers 3 and 2)."""
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    _check_shared_planes_empty(_prefilled(pc, W, P=10))
+
+
+def test_shared_append_mutant_fails_empty_plane_check():
+    """A KV-shared layer that appends (its owner's rows, to a plane of its own) must fail P6."""
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    pair = oracle.Pair(pc, W, shared_appends=True)
+    pair.prefill(gen.prompt(pc.target.vocab, 10), oracle.Sampler())
+    # the logits are those of the correct model: only the bookkeeping differs, so only P6 sees it
+    ok = _prefilled(pc, W, P=10)
+    np.testing.assert_array_equal(pair.target.forward([7])[0], ok.target.forward([7])[0])
+    pair.target.commit(0)
+    with pytest.raises(AssertionError):
+        _check_shared_planes_empty(pair)
+
+
+def _rollback_logits(pc, W, P, **opts):
+    """(verify 8 rows, commit 3, next 4 rows) on a pair with the given storage options."""
+    rows = [int(t) for t in gen.prompt(pc.target.vocab, 8, request=6)]
+    nxt = [int(t) for t in gen.prompt(pc.target.vocab, 4, request=7)]
+    a = oracle.Pair(pc, W, **opts)
+    a.prefill(gen.prompt(pc.target.vocab, P), oracle.Sampler(), chunk=16)   # passes of at most 16 rows
+    a.target.forward(rows)
+    a.target.commit(3)
+    return a.target.forward(nxt)
+
+
+def test_ring_capacity_reading():
+    """P5 with ring storage: a sliding ring of W + 15 slots (what the device arena holds) gives the
+    logits of linear storage exactly at a context where the ring has wrapped; a ring of exactly W slots
+    fails (the pass overwrites keys its own first rows and the rows kept after the rollback need)."""
+    pc = gen.tiny_pair()                       # window 64, passes of up to 16 rows
+    W = gen.generate(pc)
+    P, Wn = 150, pc.target.window              # 150 + 11 positions: the rings wrap twice
+    lin = _rollback_logits(pc, W, P)
+    np.testing.assert_array_equal(_rollback_logits(pc, W, P, ring_capacity=Wn + 15), lin)
+    bad = _rollback_logits(pc, W, P, ring_capacity=Wn)
+    assert np.abs(bad.astype(np.float64) - lin).max() > 1e-3
 
 
 def test_shared_layer_reads_owner_plane():
@@ -182,3 +225,112 @@ def test_draft_context_window_and_bidirectional_block():
     _, l2 = d.block(5, W["emb"], W["head"])
     assert not np.array_equal(l0, l2)
     d.restore(snap)
+
+
+# ---- the draft's context path and block (model card "Nemotron-3.5-Bolt-E4B-DFlash-NPU2", spec table:
+# fc fuses the zero-based outputs of the tapped target layers; block of [token, mask, ...]) ----------
+def test_taps_are_layer_outputs_in_ascending_order():
+    """Tap slice i of a row is the residual stream after target layer taps[i] (PLE and lambda included)."""
+    pc = gen.tiny_shared_pair()                # taps (1, 3, 5)
+    W = gen.generate(pc)
+    tg = om.Target(pc.target, W, tap_layers=pc.draft.taps)
+    tg.record = {}
+    tg.forward(gen.prompt(pc.target.vocab, 5))
+    H = pc.target.hidden
+    for i, l in enumerate(pc.draft.taps):
+        np.testing.assert_array_equal(tg.taps[:, i * H:(i + 1) * H], tg.record[l]["x"])
+
+
+def test_fc_orientation_one_nonzero_entry():
+    """fc [hidden out][taps*hidden in] with one nonzero entry (output 3, input H + 40): every context
+    row is nonzero only at element 3 and follows element 40 of tap 1 alone (a transposed fc or another
+    concatenation order would move or lose it)."""
+    pc = gen.tiny_shared_pair()
+    W = dict(gen.generate(pc))
+    H, T = pc.target.hidden, len(pc.draft.taps)
+    fc = np.zeros((H, T * H), np.float32)
+    fc[3, H + 40] = 1.0
+    W["d.fc"] = gen.bf16_bits(fc)
+    d = om.Draft(pc.draft, W, pc.target)
+    taps = np.random.default_rng(14).standard_normal((4, T * H)).astype(np.float32)
+    c = d.context_rows(taps)
+    assert (np.count_nonzero(c, axis=1) == 1).all() and (c[:, 3] != 0).all()
+    t2 = taps.copy()
+    t2[:, 40] *= -3.0                          # element 40 of tap 0: no effect
+    t2[:, 2 * H + 40] *= -3.0                  # element 40 of tap 2: no effect
+    t2[:, H + 3] *= -3.0                       # element 3 of tap 1: no effect
+    np.testing.assert_array_equal(d.context_rows(t2), c)
+    t3 = taps.copy()
+    t3[:, H + 40] *= -1.0                      # element 40 of tap 1: the sign follows it
+    np.testing.assert_array_equal(d.context_rows(t3), -c)
+
+
+def test_draft_context_keys_rotated_at_their_positions():
+    """Context row j's key is rotated at absolute position j: the same taps row made context at
+    positions 0 and 1 gives k_1 = rope(k_0, 1) exactly (rope at position 0 is the identity)."""
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    d = om.Draft(pc.draft, W, pc.target)
+    row = np.random.default_rng(15).standard_normal((1, len(pc.draft.taps) * pc.target.hidden)).astype(np.float32)
+    d.append_ctx(np.concatenate([row, row]))
+    hd = pc.draft.head_dim
+    for l in range(pc.draft.n_layers):
+        for g in range(pc.draft.n_kv_heads):
+            k0 = d.ctx_k[l][0, g * hd:(g + 1) * hd]
+            np.testing.assert_array_equal(d.ctx_k[l][1, g * hd:(g + 1) * hd], oracle.rope(k0, 1, pc.draft.rope_base))
+        np.testing.assert_array_equal(d.ctx_v[l][0], d.ctx_v[l][1])   # values are not rotated
+
+
+def test_draft_block_is_bidirectional():
+    """Row 0 of the block (the last token) sees the mask rows after it: its hidden state changes with
+    the mask token. A causal block would leave row 0 unchanged."""
+    import dataclasses
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    pair = _prefilled(pc, W, P=30)
+    d0 = pair.draft
+    d0.block(5, W["emb"], W["head"])
+    h0 = d0.last_hidden.copy()
+    d1 = om.Draft(dataclasses.replace(pc.draft, mask_token=pc.draft.mask_token - 1), W, pc.target)
+    d1.restore(d0.snapshot())
+    d1.block(5, W["emb"], W["head"])
+    assert np.abs(d1.last_hidden[0].astype(np.float64) - h0[0]).max() > 1e-4
+
+
+def test_draft_block_rotary_relative_positions():
+    """The block's rows sit at positions n..n+B-1 and context keys at their own positions: shifting the
+    whole context by 4 positions (with the window hiding the extra rows) leaves the proposals and, up
+    to rounding of the rotations, the logits unchanged; rows rotated at fixed positions would not."""
+    pc = gen.tiny_shared_pair()                # draft window 24
+    W = gen.generate(pc)
+    T = np.random.default_rng(16).standard_normal((40, len(pc.draft.taps) * pc.target.hidden)).astype(np.float32)
+    a = om.Draft(pc.draft, W, pc.target)
+    a.append_ctx(T)
+    pa, la = a.block(9, W["emb"], W["head"])
+    b = om.Draft(pc.draft, W, pc.target)
+    b.append_ctx(np.concatenate([np.zeros((4, T.shape[1]), np.float32), T]))
+    pb, lb = b.block(9, W["emb"], W["head"])
+    assert list(pa) == list(pb)
+    np.testing.assert_allclose(lb, la, rtol=0, atol=2e-4)
+    # the same 24 visible rows one position further from the block (a row dropped at the window's far
+    # end, a zero row added next to the block) change the logits: relative positions matter
+    c = om.Draft(pc.draft, W, pc.target)
+    c.append_ctx(np.concatenate([T[:39], np.zeros((1, T.shape[1]), np.float32)]))
+    _, lc = c.block(9, W["emb"], W["head"])
+    assert np.abs(lc.astype(np.float64) - la).max() > 1e-3
+
+
+def test_ple_model_with_silent_tail_equals_ple_free_model():
+    """lambda = 1 and a zero PLE projection give exactly the same logits as the model without PLE."""
+    import dataclasses
+    pc = gen.tiny_shared_pair()
+    W = dict(gen.generate(pc))
+    t = pc.target
+    for l in range(t.n_layers):
+        W[f"t{l}.wple_p"] = gen.pack_q41(np.zeros((t.hidden, t.ple_dim), np.float32))
+        W[f"t{l}.lambda"] = gen.bf16_bits(np.ones(1, np.float32))
+    t0 = dataclasses.replace(t, ple_dim=0)
+    toks = gen.prompt(t.vocab, 6)
+    la = om.Target(t, W).forward(toks)
+    lb = om.Target(t0, W).forward(toks)
+    np.testing.assert_array_equal(la, lb)

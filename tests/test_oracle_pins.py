@@ -314,3 +314,62 @@ def test_planted_walk_expected_tokens_per_step(p, expect):
         passes += 1
         toks += a + 1
     assert toks / passes == pytest.approx(expect, rel=0.02)
+
+
+# ---- SwiGLU gate and the per-layer-embedding tail --------------------------------------------------
+def test_silu_closed_forms():
+    """silu(x) = x * sigmoid(x): silu(0) = 0, silu(1) = e / (1 + e), silu(x) - x -> 0 as x -> +inf,
+    silu(x) -> 0 as x -> -inf, silu(-x) = silu(x) - x, slope 1/2 at 0. A plain sigmoid, a tanh gate or
+    a sign slip fails one of them."""
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    assert oracle.silu(np.array([1.0]))[0] == pytest.approx(np.e / (1.0 + np.e), rel=1e-15)
+    big = oracle.silu(np.array([40.0, -40.0]))
+    assert abs(big[0] - 40.0) < 1e-12 and abs(big[1]) < 1e-12
+    x = np.random.default_rng(12).standard_normal(1000) * 5.0
+    np.testing.assert_allclose(oracle.silu(-x), oracle.silu(x) - x, rtol=0, atol=1e-13)
+    h = 1e-6
+    assert (oracle.silu(np.array([h]))[0] - oracle.silu(np.array([-h]))[0]) / (2 * h) == pytest.approx(0.5, abs=1e-9)
+
+
+def test_swiglu_gate_is_the_first_half():
+    """gate|up: the gate is the first F columns. With gate -20 and up 3 the unit is shut (about -1e-7);
+    the halves swapped would give silu(3) * -20 = -57.1. With gate 30 and up 2 it passes 2 * 30."""
+    gu = np.array([[-20.0, 3.0], [30.0, 2.0]], np.float32)
+    a = oracle.swiglu(gu, 1)
+    assert abs(a[0, 0]) < 1e-6
+    assert a[1, 0] == pytest.approx(60.0, rel=1e-6)
+    assert abs(oracle.swiglu(gu[:, ::-1].copy(), 1)[0, 0] + 57.1) < 0.1   # the swap is visible
+
+
+def _ple_fixture(seed=13, H=64, P=32):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((3, H)) * 2.0).astype(np.float32)
+    p_l = rng.standard_normal((3, P)).astype(np.float32)
+    Wg = gen.pack_q41((rng.standard_normal((P, H)) * 0.3).astype(np.float32))
+    Wp = gen.pack_q41((rng.standard_normal((H, P)) * 0.3).astype(np.float32))
+    w = oracle.bf16_decode(gen.bf16_bits(rng.uniform(0.75, 1.25, H).astype(np.float32)))
+    return x, p_l, Wg, Wp, w
+
+
+def test_ple_tail_order():
+    """The PLE tail: gate on the residual stream itself, projection normed BEFORE the add, layer scalar
+    AFTER it (1bit engine PR "npu forward: Gemma4 verifies a draft in one batched pass", "What changes":
+    PLE gate and projection, then the layer scalar)."""
+    x, p_l, Wg, Wp, w = _ple_fixture()
+    lam, eps = 0.625, 1e-6
+    lam_x = (x.astype(np.float64) * np.float64(np.float32(lam))).astype(np.float32)
+    # a zero projection contributes exactly nothing: x * lambda
+    Wp0 = gen.pack_q41(np.zeros((x.shape[1], p_l.shape[1]), np.float32))
+    np.testing.assert_array_equal(oracle.ple_tail(x, p_l, Wg, Wp0, w, lam, eps), lam_x)
+    # a zero norm weight also gives x * lambda: the norm applies to the projection before the add
+    # (a norm after the add would give zero)
+    np.testing.assert_array_equal(oracle.ple_tail(x, p_l, Wg, Wp, np.zeros_like(w), lam, eps), lam_x)
+    # lambda after the add: halving lambda halves the result exactly
+    full = oracle.ple_tail(x, p_l, Wg, Wp, w, 1.0, eps)
+    np.testing.assert_array_equal(oracle.ple_tail(x, p_l, Wg, Wp, w, 0.5, eps), (full * np.float32(0.5)))
+    # the gate reads x itself, not a normed copy: the added term changes when x is scaled
+    d1 = full.astype(np.float64) - x
+    d2 = oracle.ple_tail(2 * x, p_l, Wg, Wp, w, 1.0, eps).astype(np.float64) - 2 * x.astype(np.float64)
+    assert np.abs(d1 - d2).max() > 1e-2
+    # the token's per-layer row multiplies the gate: a zero row adds nothing
+    np.testing.assert_array_equal(oracle.ple_tail(x, np.zeros_like(p_l), Wg, Wp, w, 1.0, eps), x)
