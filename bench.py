@@ -40,10 +40,12 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """nvidia-smi samples (every 20 ms) with their host arrival times; stop() reports the samples that
+    fell inside the timed window (and all of them when fewer than three did)."""
 
     def __init__(self, index=0):
         self.index, self.samples, self.proc = index, [], None
+        self.t0 = self.t1 = None
 
     def start(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -51,10 +53,11 @@ class Clocks:
              "clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            time.sleep(0.3)   # the first samples arrive before the timed region
         except OSError:
             self.proc = None
 
@@ -62,21 +65,28 @@ class Clocks:
         for line in self.proc.stdout:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 9:
-                self.samples.append(parts)
+                self.samples.append((time.time(), parts))
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
 
     def stop(self):
+        time.sleep(0.1)
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        inside = [p for t, p in self.samples if self.t0 is not None and self.t0 <= t <= self.t1 + 0.05]
+        use = inside if len(inside) >= 3 else [p for _, p in self.samples]
+        sm = [float(s[1]) for s in use if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in use if s[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for s in use for i in range(4) if s[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "period_ms": 20}
 
 
 # ---------------------------------------------------------------------------------------------------
@@ -161,6 +171,48 @@ def combine_ranks(torch, ms: float, toks: float, device) -> tuple:
     return float(mx[0]), float(t[1])
 
 
+# In-pass durations of the Q4_1 products (device clock, dfl_profile_read) are paired with the DRAM bytes
+# ncu counted for one product launch of the same kernel source. The fraction dram/algorithmic of that
+# capture scales to the average launch of the step; it is reported only while the product kernel's
+# source still hashes to the value it had when the counters were taken.
+TRAFFIC_CAPTURE = None   # {"gemm_cu_sha16": ..., "dram_bytes": ..., "algorithmic_bytes": ..., "profile": ...}
+
+
+def _gemm_source_hash():
+    import hashlib
+    src = os.path.join(ROOT, "dflash_speculative_decode_gb300", "csrc", "gemm.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def roofline(prof, steps, ms_step, pk):
+    """The dominant kernel (the Q4_1 products) against measured HBM, from the in-pass stamps of a
+    profiled rerun of the same steps."""
+    names = ["q41_products", "bf16_products", "head", "attention", "qk_norm_rope_kv", "rows_embed_sample"]
+    (q_n, q_ms, q_bytes), (f_n, f_ms, f_bytes), (h_n, h_ms, h_bytes) = prof[:3]
+    total = sum(p[1] for p in prof)
+    breakdown = {nm: {"launches_per_step": round(p[0] / steps, 1), "ms_per_step": round(p[1] / steps, 4),
+                      "share_of_step": round(p[1] / steps / ms_step, 3) if ms_step else None}
+                 for nm, p in zip(names, prof)}
+    breakdown["untimed_rest_ms_per_step"] = round(max(ms_step - total / steps, 0.0), 4)
+    breakdown["note"] = ("in-pass device durations (earliest CTA past its dependency wait to the latest CTA done) "
+                         "of a profiled rerun of the same steps; programmatic-launch overlap kept")
+    achieved = q_bytes / (q_ms / 1e3) / 1e9 if q_ms else 0.0
+    per_launch = q_bytes / max(q_n, 1)
+    traffic = None
+    if TRAFFIC_CAPTURE and TRAFFIC_CAPTURE.get("gemm_cu_sha16") == _gemm_source_hash():
+        traffic = round(per_launch * TRAFFIC_CAPTURE["dram_bytes"] / TRAFFIC_CAPTURE["algorithmic_bytes"])
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+            "kernel": "k_gemm (the Q4_1 products of draft and verify)", "peak_source": pk["src"],
+            "frac_vs_8TBs": round(achieved / 8000.0, 4), "launches": q_n,
+            "avg_launch_us": round(q_ms * 1e3 / max(q_n, 1), 2), "bytes_per_launch": round(per_launch),
+            "traffic_capture": (TRAFFIC_CAPTURE or {}).get("profile"),
+            "head": {"achieved": round(h_bytes / (h_ms / 1e3) / 1e9, 1) if h_ms else None, "launches": h_n,
+                     "avg_launch_us": round(h_ms * 1e3 / max(h_n, 1), 2),
+                     "frac": round(h_bytes / (h_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4) if h_ms else None},
+            "breakdown": breakdown}
+
+
 def bench_cuda(args):
     import torch
     from dflash_speculative_decode_gb300 import build
@@ -190,17 +242,19 @@ def bench_cuda(args):
     eng.dfl_restore(snap)
     sys.stderr.write(f"[bench] kernel launches before the timed region: {eng.dfl_launch_count()}\n")
     # timed: device-resident loop
+    clk = Clocks(local)
+    clk.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clk = Clocks(local)
-    clk.start()
     l0 = eng.dfl_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
     e0.record(stream)
     toks = run_steps(eng, torch, table, first, snap, n0, args.steps, args.gen)
     e1.record(stream)
     torch.cuda.synchronize()
+    clk.window(t_wall0, time.time())
     launches = eng.dfl_launch_count() - l0
     ms = e0.elapsed_time(e1)
     clocks = clk.stop()
@@ -219,31 +273,14 @@ def bench_cuda(args):
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t1
 
-    # roofline: per-launch events on the products over the same steps
+    # roofline: the same steps again with every pass's launches stamped on the device
     eng.dfl_restore(snap)
     eng.dfl_set_option(DFL_OPT_PROFILE, 1)
     run_steps(eng, torch, table, first, snap, n0, args.steps, args.gen)
     prof = [eng.dfl_profile_read(i) for i in range(6)]
     eng.dfl_set_option(DFL_OPT_PROFILE, 0)
-    (q_n, q_ms, q_bytes), (f_n, f_ms, f_bytes), (h_n, h_ms, h_bytes) = prof[:3]
-    names = ["q41_products", "bf16_products", "head", "attention", "qk_norm_rope_kv", "rows_other"]
-    prof_total = sum(p[1] for p in prof)
-    breakdown = {nm: {"launches_per_step": round(p[0] / args.steps, 1), "ms_per_step": round(p[1] / args.steps, 4),
-                      "share": round(p[1] / prof_total, 3) if prof_total else None}
-                 for nm, p in zip(names, prof)}
-    breakdown["note"] = "event-bracketed launches of the profiled rerun (brackets serialise the passes)"
     pk = peaks()
-    achieved = q_bytes / (q_ms / 1e3) / 1e9 if q_ms else 0.0
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
-            "kernel": "k_gemm (Q4_1 products of draft and verify)", "peak_source": pk["src"],
-            "launches": q_n, "avg_launch_us": round(q_ms * 1e3 / max(q_n, 1), 2),
-            "bytes_per_launch": round(q_bytes / max(q_n, 1)),
-            "frac_vs_8TBs": round(achieved / 8000.0, 4),
-            "head": {"achieved": round(h_bytes / (h_ms / 1e3) / 1e9, 1) if h_ms else None, "launches": h_n,
-                     "avg_launch_us": round(h_ms * 1e3 / max(h_n, 1), 2)},
-            "products_share_of_step": round((q_ms + h_ms + f_ms) / ms, 3) if ms else None,
-            "breakdown": breakdown}
+    roof = roofline(prof, args.steps, ms / args.steps, pk)
 
     out = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -255,6 +292,10 @@ def bench_cuda(args):
                    "d2h_bytes_per_step": 4 * (pc.draft.block - 1) + 4 * pc.draft.block + 4},
            "gpu_launches": launches, "roofline": roof, "clocks": clocks,
            "setup_s": {"load": round(t_load, 1), "prefill": round(t_prefill, 2)}}
+    del eng
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_sweep:
+        out["product_sweep"] = product_sweep(torch, SWEEP_SHAPES_STEP, [1, 2, 4, 8, 16], buf_bytes=1.0e9, pk=pk)
     if want_cpu:
         out["cpu_baseline"] = cpu_baseline(pc, W, args, out["tokens_per_step"])
     if rank == 0:
@@ -263,12 +304,27 @@ def bench_cuda(args):
         torch.distributed.destroy_process_group()
 
 
+def _attention_share(pc, ctx):
+    """Multiply-adds of attention over a context of `ctx` keys as a fraction of one verify pass of 8 rows
+    (target layers; the products dominate)."""
+    t = pc.target
+    macs_attn = 0
+    for l in range(t.n_layers):
+        keys = min(ctx, t.window) if t.layer_type[l] == gen.SLIDING else ctx
+        macs_attn += 8 * t.n_heads * keys * t.head_dim * 2
+    return macs_attn
+
+
 def cpu_baseline(pc, W, args, tokens_per_step):
     """The oracle (C products, one row at a time, OpenMP over output columns) on a bounded sample of the
     same workload: one speculative pass (draft block + 8-row verify) of the E4B pair after a 4-token
-    prefix; tokens/s = the GPU run's tokens per pass / the oracle's time per pass."""
+    prefix (a 1024-token prefill costs the oracle about ten minutes); tokens/s = the GPU run's tokens per
+    pass / the oracle's time per pass. At 1024 context the oracle's pass adds the attention over 1024
+    keys, stated as `attention_share_1024`; its products are the same. Also the tiny pair's pass on one
+    thread."""
     import oracle
     oracle.build()
+    nthreads = oracle.threads()
     pair = oracle.Pair(pc, W)
     prompt = gen.prompt(pc.target.vocab, 4)
     first, _ = pair.prefill(prompt, oracle.Sampler())
@@ -277,10 +333,32 @@ def cpu_baseline(pc, W, args, tokens_per_step):
     dp, _ = pair.draft.block(first, W["emb"], W["head"])
     pair.verify([first] + [int(v) for v in dp], oracle.Sampler())
     dt = time.time() - t0
-    return {"value": round(tokens_per_step / dt, 4), "unit": "tokens/s", "cores": os.cpu_count(),
-            "kind": "oracle", "sample": "one speculative pass (draft block + 8-row verify) of the E4B pair "
-                                        "at a 4-token context, scaled by the GPU run's tokens per pass",
-            "seconds_per_pass": round(dt, 2)}
+    t = pc.target
+    weight_macs = 8 * sum(t.hidden * ((t.n_heads + (2 * t.kv_heads[l] if t.is_owner(l) else 0)) * t.head_dim)
+                          + t.n_heads * t.head_dim * t.hidden + t.hidden * 3 * t.ffn[l] + 2 * t.hidden * t.ple_dim
+                          for l in range(t.n_layers)) + 8 * t.hidden * t.vocab
+    share = _attention_share(pc, args.ctx) / weight_macs
+    # config 1 (the tiny pair), one thread
+    tiny = gen.tiny_pair()
+    Wt = gen.generate(tiny)
+    oracle.set_threads(1)
+    try:
+        tp = oracle.Pair(tiny, Wt)
+        f1, _ = tp.prefill(gen.prompt(tiny.target.vocab, 32), oracle.Sampler())
+        t1 = time.time()
+        tp.sync_draft()
+        dp1, _ = tp.draft.block(f1, Wt["emb"], Wt["head"])
+        tp.verify([f1] + [int(v) for v in dp1], oracle.Sampler())
+        dt1 = time.time() - t1
+    finally:
+        oracle.set_threads(nthreads)
+    return {"value": round(tokens_per_step / dt, 4), "unit": "tokens/s", "cores": nthreads,
+            "threads": f"{nthreads} threads of {os.cpu_count()}", "kind": "oracle",
+            "sample": "one speculative pass (draft block + 8-row verify) of the E4B pair at a 4-token context, "
+                      "scaled by the GPU run's tokens per pass",
+            "seconds_per_pass": round(dt, 2), "attention_share_1024": round(share, 4),
+            "config1_one_thread": {"seconds_per_pass": round(dt1, 3), "threads": 1,
+                                   "sample": "tiny pair, one speculative pass after a 32-token prompt"}}
 
 
 REFERENCE_BUDGET_S = 120.0   # seconds of timed oracle passes in the reference arm
@@ -288,7 +366,9 @@ REFERENCE_BUDGET_S = 120.0   # seconds of timed oracle passes in the reference a
 
 def bench_reference(args):
     """The oracle as the reference arm, on the machine's host cores: K timed speculative passes (draft block
-    + 8-row verify + commit) of the E4B pair on a bounded sample of the workload (4-token context).
+    + 8-row verify + commit) of the E4B pair on a bounded sample of the workload (4-token context: a
+    1024-token prefill alone costs the oracle about ten minutes; its passes at 1024 context add only the
+    attention over 1024 keys, `attention_share_1024` of the products' multiply-adds).
     A pass costs the oracle the same whatever the proposals, so tokens/s = the planted stream's expected
     tokens per pass at corruption p, 1 + sum_{i=1..7} (1-p)^i, over the measured time per pass."""
     rank = int(os.environ.get("RANK", "0"))
@@ -325,12 +405,14 @@ def bench_reference(args):
         timed += 1
     per_pass = 1.0 + sum((1.0 - args.p) ** i for i in range(1, pc.draft.block))
     value = per_pass * timed / t_timed
+    nthreads = oracle.threads()
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
            "steps": args.steps, "warmup": args.warmup, "steps_timed": timed, "warmup_run": warm,
            "ms_per_step": round(1e3 * t_timed / timed, 2),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp64 arithmetic, fp32 storage",
            "data": "synthetic", "config": dict(cfgdesc, sample="4-token context"),
-           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": nthreads,
+                            "threads": f"{nthreads} threads of {os.cpu_count()}", "kind": "oracle",
                             "sample": f"{timed} timed speculative passes (of {args.steps} requested; at most "
                                       f"{REFERENCE_BUDGET_S:.0f} s of passes) of the E4B pair at a 4-token context, "
                                       f"{per_pass:.3f} tokens per pass (planted p={args.p})"},
@@ -338,58 +420,68 @@ def bench_reference(args):
     print(json.dumps(out), flush=True)
 
 
-def bench_gemm(args):
-    """Isolated Q4_1 product sweep: rows M in {1,2,4,8,16}; up to 100 packed weight buffers per shape
-    cycled so the weights come from HBM (8 GB of images); activations N(0,1) rounded to bf16, packed
-    once into the operand format (resident); 100 timed launches per point."""
+# Config 2 (the isolated product sweep): K x N shapes of the step's Q4_1 products and the bf16 head.
+SWEEP_SHAPES = [("q41", 2560, 10240), ("q41", 10240, 2560), ("q41", 2560, 4096), ("q41", 2560, 20480),
+                ("q41", 20480, 2560), ("q41", 2560, 40960), ("q41", 3072, 2560), ("q41", 2560, 3584),
+                ("bf16_head", 2560, 262144)]
+SWEEP_SHAPES_STEP = [("q41", 2560, 10240), ("q41", 10240, 2560), ("q41", 2560, 4096), ("bf16_head", 2560, 262144)]
+
+
+def product_sweep(torch, shapes, rows, buf_bytes, pk, reps=100):
+    """Graph-timed back-to-back launches per (shape, M): weight images cycled so that every launch reads
+    its weights from HBM (at least buf_bytes of images, or 2 images of the head); activations N(0,1)
+    rounded to bf16, packed once (resident). GB/s = (weight bytes + M*K*4 + M*N*4) / time per launch."""
     import ctypes
-    import torch
-    from dflash_speculative_decode_gb300 import _abi, build
-    build.build()
+    from dflash_speculative_decode_gb300 import _abi
     L = _abi.lib()
-    pk = peaks()
     dev = torch.device("cuda:0")
     st = torch.cuda.current_stream()
+    vp = ctypes.c_void_p
     res = []
-    shapes = [(2560, 10240), (10240, 2560), (2560, 4096), (2560, 20480), (20480, 2560)]
-    if args.gemm_shape:
-        shapes = [tuple(int(v) for v in args.gemm_shape.split("x"))]
-    rows = [int(v) for v in args.gemm_rows.split(",")]
-    for K, N in shapes:
-        nbuf = max(8, min(args.gemm_bufs, int(8e9 // (K * N * 0.625))))
+    for kind, K, N in shapes:
+        q41 = kind == "q41"
+        wb = K * N * (0.625 if q41 else 2.0)
+        nbuf = max(2, min(100, int(buf_bytes // wb) + 1))
+        spec = gen.TensorSpec("sweep", "q41" if q41 else "bf16", (N, K), 0.02)
+        src = torch.from_numpy(gen.make_tensor(spec, seed=5).reshape(-1).view(np.uint8)).to(dev)
         imgs = []
-        src = torch.from_numpy(gen.make_tensor(gen.TensorSpec("sweep", "q41", (N, K), 0.02), seed=5).reshape(-1)).to(dev)
-        for i in range(nbuf):
-            img = torch.empty(L.dfl_q41_image_bytes(K, N), dtype=torch.uint8, device=dev)
-            L.dfl_q41_pack(ctypes.c_void_p(src.data_ptr()), K, N, ctypes.c_void_p(img.data_ptr()),
-                           ctypes.c_void_p(st.cuda_stream))
+        for _ in range(nbuf):
+            if q41:
+                img = torch.empty(L.dfl_q41_image_bytes(K, N), dtype=torch.uint8, device=dev)
+                L.dfl_q41_pack(vp(src.data_ptr()), K, N, vp(img.data_ptr()), vp(st.cuda_stream))
+            else:
+                img = torch.empty(L.dfl_bf16_image_bytes(K, N), dtype=torch.uint8, device=dev)
+                L.dfl_bf16_pack(vp(src.data_ptr()), K, N, vp(img.data_ptr()), vp(st.cuda_stream))
             imgs.append(img)
         del src
         for M in rows:
             xb = gen.activations(M, K, seed=M)
             x = torch.from_numpy((xb.astype(np.uint32) << 16).view(np.float32)).to(dev)   # bf16 values as fp32
             act = torch.empty(L.dfl_act_bytes(M, K), dtype=torch.uint8, device=dev)
-            L.dfl_act_pack(ctypes.c_void_p(x.data_ptr()), M, K, ctypes.c_void_p(act.data_ptr()),
-                           ctypes.c_void_p(st.cuda_stream))
-            y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            sb = L.dfl_q41_gemm_scratch_bytes(K, N, M)
+            L.dfl_act_pack(vp(x.data_ptr()), M, K, vp(act.data_ptr()), vp(st.cuda_stream))
+            if q41:
+                y = torch.empty((M, N), dtype=torch.float32, device=dev)
+                sb = L.dfl_q41_gemm_scratch_bytes(K, N, M)
+            else:
+                y = torch.empty(M, dtype=torch.int32, device=dev)
+                sb = L.dfl_bf16_head_scratch_bytes(K, N, M)
             scratch = torch.zeros(max(sb, 256), dtype=torch.uint8, device=dev)
 
-            def once(i):
-                L.dfl_q41_gemm(ctypes.c_void_p(imgs[i % nbuf].data_ptr()), K, N, ctypes.c_void_p(act.data_ptr()), M,
-                               ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(scratch.data_ptr()), sb,
-                               ctypes.c_void_p(st.cuda_stream))
-            for i in range(max(args.warmup, 3)):
-                once(i)
-            # 100 launches captured in one CUDA graph: the timing sees the GPU, not the Python launch rate
-            reps = 100
+            def once(i, s):
+                if q41:
+                    L.dfl_q41_gemm(vp(imgs[i % nbuf].data_ptr()), K, N, vp(act.data_ptr()), M, vp(y.data_ptr()),
+                                   vp(scratch.data_ptr()), sb, vp(s))
+                else:
+                    L.dfl_bf16_head_argmax(vp(imgs[i % nbuf].data_ptr()), K, N, vp(act.data_ptr()), M,
+                                           vp(y.data_ptr()), None, vp(scratch.data_ptr()), sb, vp(s))
+            for i in range(3):
+                once(i, st.cuda_stream)
+            n_rep = reps if q41 else 10
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                cs = torch.cuda.current_stream()
-                for i in range(reps):
-                    L.dfl_q41_gemm(ctypes.c_void_p(imgs[i % nbuf].data_ptr()), K, N, ctypes.c_void_p(act.data_ptr()),
-                                   M, ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(scratch.data_ptr()), sb,
-                                   ctypes.c_void_p(cs.cuda_stream))
+                cs = torch.cuda.current_stream().cuda_stream
+                for i in range(n_rep):
+                    once(i, cs)
             g.replay()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -397,14 +489,30 @@ def bench_gemm(args):
             g.replay()
             e1.record(st)
             torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / reps
-            by = K * N * 0.625 + M * K * 4 + M * N * 4   # weights, operand-format activations, fp32 out
+            us = e0.elapsed_time(e1) * 1e3 / n_rep
+            by = wb + M * K * 4 + M * N * 4 * (1 if q41 else 0)
             gbs = by / (us * 1e-6) / 1e9
-            res.append({"K": K, "N": N, "M": M, "us": round(us, 2), "GB/s": round(gbs, 1),
+            res.append({"kind": kind, "K": K, "N": N, "M": M, "us": round(us, 2), "GB/s": round(gbs, 1),
                         "frac_measured": round(gbs / pk["hbm_gbs"], 3), "frac_8TBs": round(gbs / 8000, 3)})
+            del g
         del imgs
         torch.cuda.empty_cache()
-    print(json.dumps({"workload": "isolated Q4_1 product sweep", "peak_gbs": pk["hbm_gbs"], "results": res}), flush=True)
+    return res
+
+
+def bench_gemm(args):
+    """Config 2 on its own: every shape of SWEEP_SHAPES (or --gemm-shape), rows --gemm-rows."""
+    import torch
+    from dflash_speculative_decode_gb300 import build
+    build.build()
+    pk = peaks()
+    shapes = SWEEP_SHAPES
+    if args.gemm_shape:
+        shapes = [("q41",) + tuple(int(v) for v in args.gemm_shape.split("x"))]
+    rows = [int(v) for v in args.gemm_rows.split(",")]
+    res = product_sweep(torch, shapes, rows, buf_bytes=args.gemm_bufs * 1e8, pk=pk)
+    print(json.dumps({"workload": "isolated Q4_1 product sweep (config 2) and the bf16 head", "peak_gbs": pk["hbm_gbs"],
+                      "results": res}), flush=True)
 
 
 def main():
@@ -417,10 +525,11 @@ def main():
     ap.add_argument("--ctx", type=int, default=1024)
     ap.add_argument("--p", type=float, default=0.3)
     ap.add_argument("--gen", type=int, default=512, help="tokens per decode before restarting from the prefix")
-    ap.add_argument("--gemm-bufs", type=int, default=100, help="weight images cycled by the product sweep")
+    ap.add_argument("--gemm-bufs", type=int, default=40, help="sweep: cycle at least this many x 100 MB of images")
     ap.add_argument("--gemm-shape", default="", help="one KxN shape for the product sweep")
     ap.add_argument("--gemm-rows", default="1,2,4,8,16", help="row counts of the product sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="leave the product sweep out of the bench line")
     args = ap.parse_args()
     if args.impl == "reference":
         return bench_reference(args)

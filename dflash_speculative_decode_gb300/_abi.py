@@ -18,6 +18,7 @@ MAX_LAYERS, MAX_TAPS, MAX_ROWS = 64, 8, 16
 DFL_OK, DFL_E_INVALID_ARG, DFL_E_STATE, DFL_E_CAPACITY, DFL_E_UNSUPPORTED, DFL_E_CUDA, DFL_E_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 DFL_KEEP_ACCEPTED = -1
 DFL_OPT_KEEP_LOGITS, DFL_OPT_GRAPHS, DFL_OPT_STOP_LAYER, DFL_OPT_PROFILE, DFL_OPT_ATTN_CLUSTER = 1, 2, 3, 4, 5
+DFL_OPT_TEST_STALL = 6
 ERRORS = {DFL_E_INVALID_ARG: "DFL_E_INVALID_ARG", DFL_E_STATE: "DFL_E_STATE", DFL_E_CAPACITY: "DFL_E_CAPACITY",
           DFL_E_UNSUPPORTED: "DFL_E_UNSUPPORTED", DFL_E_CUDA: "DFL_E_CUDA", DFL_E_TIMEOUT: "DFL_E_TIMEOUT"}
 
@@ -66,6 +67,7 @@ SIGNATURES = {
     "dfl_draft_block": (ctypes.c_int, [vp, ctypes.c_int32, i32p]),
     "dfl_verify_block": (ctypes.c_int, [vp, i32p, ctypes.c_int, P(dfl_sampling), i32p, i32p]),
     "dfl_commit_verify_rows": (ctypes.c_int, [vp, ctypes.c_int]),
+    "dfl_commit_accepted": (ctypes.c_int, [vp, ctypes.c_int, i32p]),
     "dfl_snapshot_bytes": (ctypes.c_int64, [vp]),
     "dfl_snapshot": (ctypes.c_int, [vp, vp, ctypes.c_size_t]),
     "dfl_restore": (ctypes.c_int, [vp, vp, ctypes.c_size_t]),
@@ -87,8 +89,16 @@ SIGNATURES = {
     "dfl_act_pack": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
     "dfl_q41_gemm_scratch_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "dfl_q41_gemm": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]),
+    "dfl_q41_gemm_status": (ctypes.c_int, [vp, vp]),
+    "dfl_bf16_image_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int]),
+    "dfl_bf16_pack": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
+    "dfl_bf16_head_scratch_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "dfl_bf16_head_argmax": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp,
+                                            ctypes.c_size_t, vp]),
     "dfl_q41_gemm_noalloc": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp]),
     "dfl_q41_gemm_noalloc_max_scratch": (ctypes.c_int64, []),
+    "dfl_q41_gemm_noalloc_status": (ctypes.c_int, [vp]),
+    "dfl_q41_gemm_noalloc_reset": (ctypes.c_int, [vp]),
 }
 
 _lib = None
@@ -223,6 +233,11 @@ class Engine:
 
     def dfl_commit_verify_rows(self, keep: int):
         self._check(self.L.dfl_commit_verify_rows(self.ctx, int(keep)), "dfl_commit_verify_rows")
+
+    def dfl_commit_accepted(self, max_keep: int) -> int:
+        kept = np.zeros(1, np.int32)
+        self._check(self.L.dfl_commit_accepted(self.ctx, int(max_keep), _ptr(kept)), "dfl_commit_accepted")
+        return int(kept[0])
 
     def dfl_snapshot_bytes(self) -> int:
         return int(self.L.dfl_snapshot_bytes(self.ctx))

@@ -40,6 +40,14 @@ struct SetStateArgs {
     int rows[kMaxRows];
 };
 
+// Function attributes (shared-memory size, cluster sizes) are set once per device.
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+    return d;
+}
+
 // ---- small device helpers ------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
@@ -81,7 +89,9 @@ __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w) {
 // while its predecessor is still running. Everything before pdl_wait() must touch only data no earlier
 // kernel writes (weights); pdl_wait() returns once the predecessor grid has completed and its writes are
 // visible. pdl_trigger() lets the successor be scheduled (once every CTA of this grid has triggered or
-// exited). Both are no-ops for a kernel launched without the attribute.
+// exited); it orders no memory, so the small row kernels trigger on entry, which lets the product after
+// them land on the SMs and stream its first weights while they run. Both are no-ops for a kernel
+// launched without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -95,6 +105,32 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 // wait until at most one committed group of this thread is still in flight
 __device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_group2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+
+// ---- profiling stamps ---------------------------------------------------------------------------------
+// A profiled pass gives each instrumented launch a slot. Thread 0 of every CTA lowers prof[slot] to the
+// time it passed its dependency wait and raises prof[kProfSlots + slot] to the time the CTA finished
+// (device globaltimer, ns). The launch's in-pass duration is the difference: it excludes the time its
+// CTAs spent resident before their dependency was met, so durations of consecutive launches do not
+// overlap and add up to no more than the pass. prof == nullptr (not profiling) records nothing.
+constexpr int kProfSlots = 2048;
+struct Stamp {
+    unsigned long long *prof;
+    int slot;
+};
+__device__ __forceinline__ unsigned long long globaltimer_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void stamp_ready(const Stamp &s) {
+    if (s.prof && threadIdx.x == 0) atomicMin(s.prof + s.slot, globaltimer_now());
+}
+// every thread of the CTA calls it (it synchronises the CTA first)
+__device__ __forceinline__ void stamp_done(const Stamp &s) {
+    if (!s.prof) return;
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(s.prof + kProfSlots + s.slot, globaltimer_now());
+}
 
 // ---- activation operand format ---------------------------------------------------------------------
 // An activation matrix of up to 16 rows and K inputs (K % 16 == 0) that feeds a product is stored as
@@ -121,9 +157,10 @@ __device__ __forceinline__ float act_store(uint32_t *f, int K, int tok, int k, f
 }
 
 // ---- mbarriers and bulk asynchronous copies ----------------------------------------------------------
-constexpr unsigned kWaitHintNs = 200000;   // 0.2 ms
-constexpr int kWaitPolls = 1 << 14;        // with the hint: a few seconds at most
+constexpr unsigned kWaitHintNs = 20000;              // suspend-time hint of one test (20 us)
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // a bounded wait gives up after 1 s
 __device__ __forceinline__ unsigned saddr(const void *p) { return static_cast<unsigned>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ unsigned long long globaltimer_ns() { return globaltimer_now(); }
 __device__ __forceinline__ void mbar_init(uint64_t *b, unsigned count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
 }
@@ -145,12 +182,21 @@ __device__ __forceinline__ bool mbar_test(uint64_t *b, unsigned parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity; false if it did not complete within the limit
-// (at most kWaitPolls tests of up to kWaitHintNs each).
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity) {
-    for (int i = 0; i < kWaitPolls; ++i)
+// Bounded wait for the phase with the given parity. Returns false, without waiting, once *bad is set
+// (another wait of the CTA gave up), and gives up itself (setting *bad) when the phase has not
+// completed kWaitLimitNs after the wait began.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity, volatile int *bad) {
+    if (*bad) return false;
+    if (mbar_test(b, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (*bad) return false;
         if (mbar_test(b, parity)) return true;
-    return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *bad = 1;
+            return false;
+        }
+    }
 }
 // global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16) completing on barrier b
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *b) {
@@ -195,7 +241,7 @@ enum WFmt { W_Q41 = 0, W_BF16 = 1 };
 // EPI_PART: each CTA only writes its segment partial of every quad it touches (no fix-up); the
 // consumer adds the segments (PartView).
 enum Epi { EPI_F32 = 0, EPI_GLU = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3, EPI_PART = 4 };
-enum ArgmaxDst { AM_VERIFY = 0, AM_DRAFT = 1 };
+enum ArgmaxDst { AM_VERIFY = 0, AM_DRAFT = 1, AM_OUT = 2 };
 
 struct GemmArgs {
     const uint8_t *img;    // tile image
@@ -205,6 +251,10 @@ struct GemmArgs {
     const float *xs;       // their per-16 sums
     int x_row0;            // first activation row used
     int *err;              // products: sticky error bits (nullable), kErrWaitTimeout
+    int skip_on_err;       // 1: a launch that finds *err set on entry issues no copies (the pass it
+                           // belongs to has already failed) and its results are undefined
+    int stall;             // test of the give-up path: the copy warp issues nothing, so every wait of
+                           // the compute warps gives up (kErrWaitTimeout); 0 in normal use
     float *y;              // EPI_F32: fp32 output [M][ldy]
     int ldy;
     uint32_t *yf;          // EPI_GLU / EPI_SILU_MUL: output in operand format (N/2 or N inputs)
@@ -221,7 +271,10 @@ struct GemmArgs {
     int *am_idx;
     int *am_cnt;           // CTA arrival counter (zero between launches)
     DevState *st;
-    int am_dst;            // AM_VERIFY: st->target[m] and st->accepted; AM_DRAFT: st->props[m]
+    int am_dst;            // AM_VERIFY: st->target[m] and st->accepted; AM_DRAFT: st->props[m];
+                           // AM_OUT: am_out[m] (the standalone head)
+    int *am_out;
+    Stamp ps;              // profiling stamp (ps.prof == nullptr: none)
 };
 
 // The segment partials a product launched with EPI_PART leaves: element (row m, column n) is the sum,
@@ -256,6 +309,7 @@ int gemm_maxseg(int C, int N);
 size_t gemm_scratch_floats(int C, int N);
 size_t gemm_part_floats(int C, int N);   // partials of an EPI_PART launch
 cudaError_t launch_gemm(int fmt, int epi, const GemmArgs &a, cudaStream_t s);
+int head_grid(int C, int M, int N);   // CTAs of a head launch (per-CTA maxima: head_grid * kMaxRows)
 cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *sums, cudaStream_t s);
 inline size_t act_words(int K) { return (size_t)kMaxRows * K; }          // fragment words of a 16-row buffer
 inline size_t act_sums(int K) { return (size_t)(K / 16) * kMaxRows; }     // sum floats
@@ -285,6 +339,7 @@ struct RowArgs {
     const DevState *st;
     int pos_from_ctx;      // tap positions: 0 = st->n + m, 1 = st->draft_n + m
     int rows_from_ctx;     // 1: only rows < st->ctx_rows are live (the rest are written as zeros)
+    Stamp ps;
 };
 
 struct EmbedArgs {
@@ -298,6 +353,7 @@ struct EmbedArgs {
     const uint16_t *ple;   // bf16 [vocab][ple_w] (nullable)
     int ple_w;
     uint16_t *ple_out;     // bf16 [M][ple_w]
+    Stamp ps;
 };
 
 struct QkArgs {
@@ -316,6 +372,7 @@ struct QkArgs {
     float *q_out;          // fp32 [M][nq][hd] (nullable: no query)
     float *k_store, *v_store;      // [cap][nkv][hd] (nullable: no append)
     int cap;               // ring capacity (slot = pos % cap)
+    Stamp ps;
 };
 
 struct AttnArgs {
@@ -334,6 +391,7 @@ struct AttnArgs {
     int max_cluster;       // largest cluster size allowed (16, 8 or 4); the largest that fits is taken
     uint32_t *outf;        // [M][nq*hd] in operand format
     float *outs;
+    Stamp ps;
 };
 
 struct SampleArgs {
@@ -341,6 +399,7 @@ struct SampleArgs {
     int M, V, ld;
     DevState *st;
     int *cnt;
+    Stamp ps;
 };
 
 cudaError_t launch_set_state(DevState *st, const SetStateArgs &a, cudaStream_t s);

@@ -24,7 +24,6 @@
 #include "dfl.h"
 
 namespace dfl {
-int head_grid(int C, int M, int N);
 size_t attn_smem(int M, int hd);
 }  // namespace dfl
 
@@ -121,16 +120,19 @@ struct dfl_ctx {
     int nq_max = 0, qkv_max = 0;
     // host mirror of the state
     int n = 0, draft_n = 0, pending = 0, last_accepted = -1, draft_at = -1;
+    int draft_n_ok = 0;       // draft_n as of the last call that read the device state without an error
+    bool test_stall = false;  // test of the give-up path: the products of the next passes issue no copies
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
     int last_k = 0;
     int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
     int attn_cluster = 16; // largest attention cluster size allowed: 16, 8 or 4
     long long launches = 0;                       // kernels this context has launched
-    bool profile = false;                         // bracket product launches with events
-    std::vector<cudaEvent_t> ev_pool;
-    size_t ev_next = 0, ev_reserved = 0;          // slots [0, ev_reserved) belong to captured graphs
-    struct Rec { int cls; double bytes; size_t ev; };
-    std::vector<Rec> recs;                        // profiled launches not yet read
+    bool profile = false;                         // stamp the instrumented launches of each pass
+    unsigned long long *prof = nullptr;           // device stamps [2][kProfSlots] (workspace)
+    int prof_next = 0;                            // next slot of the pass being built
+    struct Rec { int cls; double bytes; int slot; };
+    std::vector<Rec> recs;                        // profiled launches of the pass being built
+    std::vector<unsigned long long> prof_host;
     double prof_ms[kProfClasses] = {}, prof_bytes[kProfClasses] = {};
     long long prof_n[kProfClasses] = {};
     // captured passes
@@ -140,7 +142,6 @@ struct dfl_ctx {
         cudaGraphExec_t exec = nullptr;
         std::vector<Rec> recs;                    // profiled launches inside the graph
         long long launches = 0;                   // kernels per replay
-        bool pending = false;                     // replayed since its events were last read
     };
     std::map<uint64_t, Graph> graphs;
     std::string err;
@@ -159,16 +160,19 @@ int fail(dfl_ctx *c, int code, const std::string &msg) {
         if (e_ != cudaSuccess) return fail(c, DFL_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
     } while (0)
 
-// a kernel launch of profiling class `cls` (see prof_begin)
+// a kernel launch (not stamped; its time is not in any class)
 #define DFL_LAUNCH_C(cls, call)                                                               \
     do {                                                                                      \
-        size_t prof_slot_ = 0;                                                                \
-        DFL_CK(prof_begin(c, &prof_slot_));                                                   \
         c->launches += 1;                                                                     \
         DFL_CK(call);                                                                         \
-        DFL_CK(prof_end(c, prof_slot_, cls, 0.0));                                            \
     } while (0)
 #define DFL_LAUNCH(call) DFL_LAUNCH_C(5, call)
+// a stamped kernel launch of profiling class `cls`: the argument struct gets its profiling slot
+#define DFL_LAUNCH_S(cls, args, launcher)                                                     \
+    do {                                                                                      \
+        (args).ps = stamp(c, cls, 0.0);                                                       \
+        DFL_LAUNCH_C(cls, launcher(args, c->stream));                                         \
+    } while (0)
 
 std::string validate(const dfl_config *g) {
     auto bad = [](const char *f) { return std::string("configuration: ") + f; };
@@ -337,6 +341,7 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     c->part = X.take<float>(std::max<size_t>(part_floats, 1));
     c->am_val = X.take<float>((size_t)152 * 4 * kMaxRows);
     c->am_idx = X.take<int>((size_t)152 * 4 * kMaxRows);
+    c->prof = X.take<unsigned long long>(2 * (size_t)kProfSlots);
     c->logits = X.take<float>((size_t)R * V);
     c->dlogits = X.take<float>((size_t)R * V);
     // counters that must read zero between launches, contiguous so one memset clears them
@@ -360,40 +365,18 @@ bool is_tap(const dfl_config &g, int l, int *ti) {
 
 // ---- one product -----------------------------------------------------------------------------------
 // profiled launch classes: 0 = Q4_1 products, 1 = bf16 products (fc), 2 = head, 3 = attention,
-// 4 = q/k norm + rotation + KV store, 5 = the rest (embedding, norms, state, taps, sampling)
-// With graphs on, only launches inside captured passes are bracketed (the per-pass state kernels
-// launched between replays are not).
-constexpr size_t kNoSlot = ~size_t(0);
-cudaError_t prof_begin(dfl_ctx *c, size_t *slot) {
-    *slot = kNoSlot;
-    if (!c->profile || (c->use_graphs && !c->capturing)) return cudaSuccess;
-    const size_t need = c->ev_next + 2;
-    while (c->ev_pool.size() < need) {
-        cudaEvent_t e;
-        cudaError_t r = cudaEventCreate(&e);
-        if (r != cudaSuccess) return r;
-        c->ev_pool.push_back(e);
-    }
-    *slot = c->ev_next;
-    c->ev_next += 2;
-    // inside a capture the record must become a node of the graph (timestamped at every replay)
-    return c->capturing ? cudaEventRecordWithFlags(c->ev_pool[*slot], c->stream, cudaEventRecordExternal)
-                        : cudaEventRecord(c->ev_pool[*slot], c->stream);
-}
-
-cudaError_t prof_end(dfl_ctx *c, size_t slot, int cls, double bytes) {
-    if (slot == kNoSlot) return cudaSuccess;
+// 4 = q/k norm + rotation + KV store, 5 = row kernels (residual, norms, taps), embedding, sampling.
+// The small state and copy kernels are not stamped.
+Stamp stamp(dfl_ctx *c, int cls, double bytes) {
+    if (!c->profile || c->prof_next >= kProfSlots) return Stamp{nullptr, 0};
+    const int slot = c->prof_next++;
     c->recs.push_back({cls, bytes, slot});
-    return c->capturing ? cudaEventRecordWithFlags(c->ev_pool[slot + 1], c->stream, cudaEventRecordExternal)
-                        : cudaEventRecord(c->ev_pool[slot + 1], c->stream);
+    return Stamp{c->prof, slot};
 }
 
 // y = x . W for M rows; EPI_F32 writes fp32 rows to y, EPI_GLU / EPI_SILU_MUL write `out` in operand format
 cudaError_t gemm(dfl_ctx *c, const QMat &W, const Act &x, int row0, int M, int epi, float *y, int ldy,
                  const Act *out = nullptr, const uint16_t *ext = nullptr, int lde = 0) {
-    size_t slot = 0;
-    cudaError_t e = prof_begin(c, &slot);
-    if (e != cudaSuccess) return e;
     GemmArgs a{};
     a.img = W.img;
     a.K = W.K;
@@ -413,11 +396,11 @@ cudaError_t gemm(dfl_ctx *c, const QMat &W, const Act &x, int row0, int M, int e
     a.ext = ext;
     a.lde = lde;
     a.err = &c->st->err;
+    a.skip_on_err = 1;
+    a.stall = c->test_stall ? 1 : 0;
+    a.ps = stamp(c, W.q41 ? 0 : 1, (W.q41 ? 0.625 : 2.0) * W.K * (double)W.N + 4.0 * M * W.K + 4.0 * M * W.N);
     c->launches += 1;
-    e = launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, a, c->stream);
-    if (e != cudaSuccess) return e;
-    const double bytes = (W.q41 ? 0.625 : 2.0) * W.K * (double)W.N + 4.0 * M * W.K + 4.0 * M * W.N;
-    return prof_end(c, slot, W.q41 ? 0 : 1, bytes);
+    return launch_gemm(W.q41 ? W_Q41 : W_BF16, epi, a, c->stream);
 }
 
 // the segment partials an EPI_PART product of W leaves in the context's partial buffer
@@ -432,9 +415,6 @@ PartView part_view(const dfl_ctx *c, const QMat &W) {
 }
 
 cudaError_t head(dfl_ctx *c, const Act &x, int row0, int M, float *logits, int dst) {
-    size_t slot = 0;
-    cudaError_t e = prof_begin(c, &slot);
-    if (e != cudaSuccess) return e;
     GemmArgs a{};
     a.img = c->head.img;
     a.K = c->head.K;
@@ -451,43 +431,51 @@ cudaError_t head(dfl_ctx *c, const Act &x, int row0, int M, float *logits, int d
     a.am_cnt = c->am_cnt;
     a.st = c->st;
     a.am_dst = dst;
+    a.ps = stamp(c, 2, 2.0 * a.K * (double)a.N + 4.0 * M * a.K + (logits ? 4.0 * M * a.N : 0.0));
     c->launches += 1;
-    e = launch_gemm(W_BF16, EPI_ARGMAX, a, c->stream);
-    if (e != cudaSuccess) return e;
-    const double bytes = 2.0 * a.K * (double)a.N + 4.0 * M * a.K + (logits ? 4.0 * M * a.N : 0.0);
-    return prof_end(c, slot, 2, bytes);
+    return launch_gemm(W_BF16, EPI_ARGMAX, a, c->stream);
 }
 
-// fold finished profiled launches into the totals
-cudaError_t harvest(dfl_ctx *c, std::vector<dfl_ctx::Rec> &recs) {
+// Fold the stamps of one profiled pass (its records `recs`) into the totals (synchronises).
+cudaError_t harvest(dfl_ctx *c, const std::vector<dfl_ctx::Rec> &recs) {
     if (recs.empty()) return cudaSuccess;
-    cudaError_t e = cudaEventSynchronize(c->ev_pool[recs.back().ev + 1]);
+    c->prof_host.resize(2 * kProfSlots);
+    cudaError_t e = cudaMemcpyAsync(c->prof_host.data(), c->prof, 2 * kProfSlots * sizeof(unsigned long long),
+                                    cudaMemcpyDeviceToHost, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) return e;
     for (const auto &r : recs) {
-        float t = 0.f;
-        e = cudaEventElapsedTime(&t, c->ev_pool[r.ev], c->ev_pool[r.ev + 1]);
-        if (e != cudaSuccess) return e;
-        c->prof_ms[r.cls] += t;
+        const unsigned long long t0 = c->prof_host[r.slot], t1 = c->prof_host[kProfSlots + r.slot];
+        if (t1 < t0) continue;   // the launch had no CTA (nothing to do)
+        c->prof_ms[r.cls] += (t1 - t0) * 1e-6;
         c->prof_bytes[r.cls] += r.bytes;
         c->prof_n[r.cls] += 1;
     }
     return cudaSuccess;
 }
 
+// reset the stamps before a profiled pass: ready times to the maximum, done times to zero
+cudaError_t prof_reset(dfl_ctx *c) {
+    cudaError_t e = cudaMemsetAsync(c->prof, 0xFF, kProfSlots * sizeof(unsigned long long), c->stream);
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(c->prof + kProfSlots, 0, kProfSlots * sizeof(unsigned long long), c->stream);
+}
+
 // Run a pass body either directly or as a CUDA graph captured once per key (on a private stream,
-// replayed on the context's stream). The body must only enqueue kernels.
+// replayed on the context's stream). The body must only enqueue kernels. A profiled pass is followed
+// by a synchronising read of its stamps.
 int run_graph(dfl_ctx *c, uint64_t key, const std::function<int()> &body) {
+    c->prof_next = 0;
+    c->recs.clear();
     if (!c->use_graphs) {
+        if (c->profile) DFL_CK(prof_reset(c));
         const int rc = body();
         if (rc) return rc;
-        if (c->profile) {
-            DFL_CK(harvest(c, c->recs));
-            c->recs.clear();
-            c->ev_next = c->ev_reserved;
-        }
+        if (c->profile) DFL_CK(harvest(c, c->recs));
+        c->recs.clear();
         return DFL_OK;
     }
-    key = key * 2 + (c->profile ? 1 : 0);
+    key = (key * 2 + (c->profile ? 1 : 0)) * 2 + (c->test_stall ? 1 : 0);
     auto it = c->graphs.find(key);
     if (it == c->graphs.end()) {
         if (!c->cap_stream) DFL_CK(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
@@ -495,8 +483,6 @@ int run_graph(dfl_ctx *c, uint64_t key, const std::function<int()> &body) {
         c->stream = c->cap_stream;
         c->capturing = true;
         const long long l0 = c->launches;
-        c->recs.clear();
-        c->ev_next = c->ev_reserved;
         cudaError_t e = cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal);
         int rc = e == cudaSuccess ? body() : DFL_E_CUDA;
         cudaGraph_t g = nullptr;
@@ -517,17 +503,13 @@ int run_graph(dfl_ctx *c, uint64_t key, const std::function<int()> &body) {
         c->launches = l0;
         G.recs = c->recs;
         c->recs.clear();
-        c->ev_reserved = c->ev_next;
         it = c->graphs.emplace(key, G).first;
     }
     dfl_ctx::Graph &G = it->second;
-    if (G.pending) {
-        DFL_CK(harvest(c, G.recs));
-        G.pending = false;
-    }
+    if (c->profile) DFL_CK(prof_reset(c));
     DFL_CK(cudaGraphLaunch(G.exec, c->stream));
     c->launches += G.launches;
-    G.pending = c->profile && !G.recs.empty();
+    if (c->profile) DFL_CK(harvest(c, G.recs));
     return DFL_OK;
 }
 
@@ -573,12 +555,12 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
     ea.ple = P ? c->ple_table.p : nullptr;
     ea.ple_w = NL * P;
     ea.ple_out = c->ple_rows;
-    DFL_LAUNCH(launch_embed(ea, c->stream));
+    DFL_LAUNCH_S(5, ea, launch_embed);
     RowArgs r0 = rows(c, k, c->x);
     r0.w_next = c->tl[0].attn_norm.p;
     r0.outf = c->h.f;
     r0.outs = c->h.s;
-    DFL_LAUNCH(launch_rows(r0, c->stream));
+    DFL_LAUNCH_S(5, r0, launch_rows);
     const int last_layer = (c->stop_layer >= 0 && c->stop_layer < NL) ? c->stop_layer : NL - 1;
     if (last_layer < NL - 1) do_head = false;
     for (int l = 0; l <= last_layer; ++l) {
@@ -604,7 +586,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         qa.k_store = own ? L.K : nullptr;
         qa.v_store = own ? L.V : nullptr;
         qa.cap = L.cap;
-        DFL_LAUNCH_C(4, launch_qk(qa, c->stream));
+        DFL_LAUNCH_S(4, qa, launch_qk);
         AttnArgs aa{};
         aa.M = k;
         aa.nq = nq;
@@ -622,7 +604,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.max_cluster = c->attn_cluster;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
-        DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
+        DFL_LAUNCH_S(3, aa, launch_attn);
         DFL_CK(gemm(c, L.o, c->o, 0, k, EPI_PART, nullptr, 0));
         RowArgs r1 = rows(c, k, c->x);
         r1.yp = part_view(c, L.o);
@@ -631,7 +613,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         r1.w_next = L.pre_ffn_norm.p;
         r1.outf = c->h.f;
         r1.outs = c->h.s;
-        DFL_LAUNCH(launch_rows(r1, c->stream));
+        DFL_LAUNCH_S(5, r1, launch_rows);
         DFL_CK(gemm(c, L.gu, c->h, 0, k, EPI_GLU, nullptr, 0, &c->a));
         DFL_CK(gemm(c, L.d, c->a, 0, k, EPI_PART, nullptr, 0));
         const uint16_t *next = l + 1 < NL ? c->tl[l + 1].attn_norm.p : c->final_norm.p;
@@ -644,7 +626,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         r2.outf = c->h.f;
         r2.outs = c->h.s;
         if (P) {
-            DFL_LAUNCH(launch_rows(r2, c->stream));   // out = x: the gate's input
+            DFL_LAUNCH_S(5, r2, launch_rows);   // out = x: the gate's input
             DFL_CK(gemm(c, L.pg, c->h, 0, k, EPI_SILU_MUL, nullptr, 0, &c->z, c->ple_rows + (size_t)l * P, NL * P));
             DFL_CK(gemm(c, L.pp, c->z, 0, k, EPI_PART, nullptr, 0));
             r2 = rows(c, k, c->x);
@@ -661,7 +643,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
             r2.ld_tap = c->TH;
             r2.tap_off = ti * H;
         }
-        DFL_LAUNCH(launch_rows(r2, c->stream));
+        DFL_LAUNCH_S(5, r2, launch_rows);
     }
     if (do_head) {
         float *lg = (c->keep_logits || sampled) ? c->logits : nullptr;
@@ -674,7 +656,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
             sa.ld = g.vocab;
             sa.st = c->st;
             sa.cnt = c->smp_cnt;
-            DFL_LAUNCH(launch_sample(sa, c->stream));
+            DFL_LAUNCH_S(5, sa, launch_sample);
         }
     }
     return DFL_OK;
@@ -738,7 +720,7 @@ int run_ctx_only(dfl_ctx *c, int r) {
         qa.k_store = D.K;
         qa.v_store = D.V;
         qa.cap = c->cap_draft;
-        DFL_LAUNCH_C(4, launch_qk(qa, c->stream));
+        DFL_LAUNCH_S(4, qa, launch_qk);
     }
     c->draft_n += r;
     return DFL_OK;
@@ -769,13 +751,13 @@ int draft_body(dfl_ctx *c) {
     ea.use_draft = 1;
     ea.mask_token = g.mask_token;
     ea.x = c->x_d;
-    DFL_LAUNCH(launch_embed(ea, c->stream));
+    DFL_LAUNCH_S(5, ea, launch_embed);
     RowArgs r0 = rows(c, B, c->x_d);
     r0.eps = g.d_eps;
     r0.w_next = c->dl[0].attn_norm.p;
     r0.outf = c->hcat.f;
     r0.outs = c->hcat.s;
-    DFL_LAUNCH(launch_rows(r0, c->stream));
+    DFL_LAUNCH_S(5, r0, launch_rows);
     const int dq = g.d_heads, dhd = g.d_head_dim;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
@@ -787,7 +769,7 @@ int draft_body(dfl_ctx *c) {
         qb.k_store = c->kB;
         qb.v_store = c->vB;
         qb.cap = 0;
-        DFL_LAUNCH_C(4, launch_qk(qb, c->stream));
+        DFL_LAUNCH_S(4, qb, launch_qk);
         if (F > 0) {
             QkArgs qc = draft_qk(c, l);
             qc.M = F;
@@ -797,7 +779,7 @@ int draft_body(dfl_ctx *c) {
             qc.k_store = D.K;
             qc.v_store = D.V;
             qc.cap = c->cap_draft;
-            DFL_LAUNCH_C(4, launch_qk(qc, c->stream));
+            DFL_LAUNCH_S(4, qc, launch_qk);
         }
         AttnArgs aa{};
         aa.M = B;
@@ -819,7 +801,7 @@ int draft_body(dfl_ctx *c) {
         aa.max_cluster = c->attn_cluster;
         aa.outf = c->o.f;
         aa.outs = c->o.s;
-        DFL_LAUNCH_C(3, launch_attn(aa, c->stream));
+        DFL_LAUNCH_S(3, aa, launch_attn);
         DFL_CK(gemm(c, D.o, c->o, 0, B, EPI_PART, nullptr, 0));
         RowArgs r1 = rows(c, B, c->x_d);
         r1.eps = g.d_eps;
@@ -828,7 +810,7 @@ int draft_body(dfl_ctx *c) {
         r1.w_next = D.ffn_norm.p;
         r1.outf = c->hb.f;
         r1.outs = c->hb.s;
-        DFL_LAUNCH(launch_rows(r1, c->stream));
+        DFL_LAUNCH_S(5, r1, launch_rows);
         DFL_CK(gemm(c, D.gu, c->hb, 0, B, EPI_GLU, nullptr, 0, &c->a));
         DFL_CK(gemm(c, D.d, c->a, 0, B, EPI_PART, nullptr, 0));
         RowArgs r2 = rows(c, B, c->x_d);
@@ -839,7 +821,7 @@ int draft_body(dfl_ctx *c) {
         const Act &nxt = l + 1 < g.d_layers ? c->hcat : c->hb;
         r2.outf = nxt.f;
         r2.outs = nxt.s;
-        DFL_LAUNCH(launch_rows(r2, c->stream));
+        DFL_LAUNCH_S(5, r2, launch_rows);
     }
     float *lg = c->keep_logits ? c->dlogits : nullptr;
     DFL_CK(head(c, c->hb, 1, B - 1, lg, AM_DRAFT));
@@ -861,10 +843,23 @@ int run_draft(dfl_ctx *c, int last_tok) {
 
 
 
+// Read the device counters (synchronises the stream). A bounded wait that gave up in any pass since
+// the last read is reported as DFL_E_TIMEOUT: the error bits are cleared, the draft context falls back
+// to the rows confirmed by the last good read (the rows made context since then are made again by the
+// next draft block), and the caller restores its own counters. Committed planes, taps and positions
+// are untouched by a failed pass (it writes only rows past the committed positions).
 int read_state(dfl_ctx *c, DevState *out) {
     DFL_CK(cudaMemcpyAsync(out, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
     DFL_CK(cudaStreamSynchronize(c->stream));
-    if (out->err & kErrWaitTimeout) return fail(c, DFL_E_CUDA, "a kernel gave up waiting for its asynchronous copies");
+    if (out->err & kErrWaitTimeout) {
+        DFL_CK(cudaMemsetAsync(&c->st->err, 0, sizeof(int), c->stream));
+        DFL_CK(cudaStreamSynchronize(c->stream));
+        c->draft_n = std::min(c->draft_n_ok, c->n);
+        c->draft_n_ok = c->draft_n;
+        c->draft_at = -1;
+        return fail(c, DFL_E_TIMEOUT, "a kernel gave up waiting for its asynchronous copies (bounded wait)");
+    }
+    c->draft_n_ok = c->draft_n;
     return DFL_OK;
 }
 
@@ -1063,6 +1058,7 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
     if (rc) return rc;
     if ((rc = check_tokens(c, tokens, n))) return rc;
     const bool sampled = s && s->temperature > 0.f;
+    const int n_start = c->n;
     int done = 0, last_k = 0;
     while (done < n) {
         const int k = std::min(kMaxRows, n - done);
@@ -1075,7 +1071,12 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
     }
     if ((rc = catch_up(c, 0))) return rc;
     DevState hs;
-    if ((rc = read_state(c, &hs))) return rc;
+    if ((rc = read_state(c, &hs))) {
+        c->n = n_start;   // none of the chunks counts
+        c->draft_n = std::min(c->draft_n, n_start);
+        c->draft_n_ok = c->draft_n;
+        return rc;
+    }
     if (next_tok) *next_tok = hs.target[last_k - 1];
     c->last_k = last_k;
     c->draft_at = -1;
@@ -1138,6 +1139,16 @@ int dfl_commit_verify_rows(dfl_ctx *c, int keep) {
     c->pending = 0;
     c->draft_at = -1;
     return DFL_OK;
+}
+
+int dfl_commit_accepted(dfl_ctx *c, int max_keep, int32_t *kept) {
+    if (!c) return DFL_E_INVALID_ARG;
+    if (!c->pending) return fail(c, DFL_E_STATE, "no pending verify");
+    if (max_keep < 0) return fail(c, DFL_E_INVALID_ARG, "max_keep must be >= 0");
+    const int keep = std::min(std::min(c->last_accepted + 1, c->pending), max_keep);
+    const int rc = dfl_commit_verify_rows(c, keep);
+    if (rc == DFL_OK && kept) *kept = keep;
+    return rc;
 }
 
 int64_t dfl_snapshot_bytes(const dfl_ctx *c) {
@@ -1222,6 +1233,7 @@ int dfl_restore(dfl_ctx *c, const void *src, size_t bytes) {
     if (tb) DFL_CK(cudaMemcpyAsync(c->taps + (size_t)hdr.draft_n * c->TH, s + off, tb, cudaMemcpyDeviceToDevice, c->stream));
     c->n = hdr.n;
     c->draft_n = hdr.draft_n;
+    c->draft_n_ok = hdr.draft_n;
     c->draft_at = -1;
     c->draft_only = false;
     return DFL_OK;
@@ -1243,12 +1255,11 @@ int dfl_set_option(dfl_ctx *c, int option, int value) {
     else if (option == DFL_OPT_STOP_LAYER) c->stop_layer = value;
     else if (option == DFL_OPT_PROFILE) {
         DFL_CK(cudaStreamSynchronize(c->stream));
-        for (auto &kv : c->graphs) kv.second.pending = false;
         c->profile = value != 0;
         c->recs.clear();
-        c->ev_next = c->ev_reserved;
         for (int i = 0; i < kProfClasses; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
     }
+    else if (option == DFL_OPT_TEST_STALL) c->test_stall = value != 0;
     else if (option == DFL_OPT_ATTN_CLUSTER) {
         if (value != 4 && value != 8 && value != 16)
             return fail(c, DFL_E_INVALID_ARG, "attention cluster must be 4, 8 or 16");
@@ -1315,6 +1326,15 @@ int dfl_debug_read(dfl_ctx *c, const char *name, void *dst, size_t bytes) {
     else if (s == "qkv") src = c->qkv, have = R * c->qkv_max * 4;
     else if (s == "q") src = c->q, have = R * std::max(c->cfg.n_heads * c->cfg.head_dim, c->cfg.d_heads * c->cfg.d_head_dim) * 4;
     else if (s == "x_d") src = c->x_d, have = R * H * 4;
+    else if (s.size() > 1 && (s[0] == 'k' || s[0] == 'v') && isdigit((unsigned char)s[1])) {
+        size_t used = 0;
+        const int l = std::stoi(s.substr(1), &used);
+        if (used != s.size() - 1 || l < 0 || l >= c->cfg.n_layers) return fail(c, DFL_E_INVALID_ARG, "bad layer in " + s);
+        const TLayer &L = c->tl[l];
+        if (L.owner != l) return fail(c, DFL_E_INVALID_ARG, s + ": a KV-shared layer holds no plane");
+        src = s[0] == 'k' ? L.K : L.V;
+        have = (size_t)L.cap * L.nkv * c->cfg.head_dim * 4;
+    }
     else return fail(c, DFL_E_INVALID_ARG, "unknown buffer " + s);
     if (bytes > have) return fail(c, DFL_E_INVALID_ARG, "read past the buffer");
     DFL_CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, c->stream));
@@ -1336,13 +1356,6 @@ int64_t dfl_launch_count(const dfl_ctx *c) { return c ? c->launches : -1; }
 int dfl_profile_read(dfl_ctx *c, int cls, int64_t *launches, double *ms, double *bytes) {
     if (!c || cls < 0 || cls >= kProfClasses) return DFL_E_INVALID_ARG;
     DFL_CK(cudaStreamSynchronize(c->stream));
-    DFL_CK(harvest(c, c->recs));
-    c->recs.clear();
-    for (auto &kv : c->graphs)
-        if (kv.second.pending) {
-            DFL_CK(harvest(c, kv.second.recs));
-            kv.second.pending = false;
-        }
     if (launches) *launches = c->prof_n[cls];
     if (ms) *ms = c->prof_ms[cls];
     if (bytes) *bytes = c->prof_bytes[cls];
@@ -1355,7 +1368,6 @@ void dfl_destroy(dfl_ctx *c) {
     if (!c) return;
     if (c->stream) cudaStreamSynchronize(c->stream);
     for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second.exec);
-    for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     delete c;
 }
@@ -1383,17 +1395,20 @@ int dfl_act_pack(const float *x, int M, int K, void *act, void *stream) {
     return launch_act_pack(x, M, K, f, sums, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
 }
 
-// scratch = arrival counters (N/32 ints, at offset 0, rounded up to 256 bytes), then the segment partials
+// scratch = a 256-byte header (the error word at offset 0), the arrival counters (N/32 ints, rounded up
+// to 256 bytes), then the segment partials
+constexpr size_t kScratchHeader = 256;
 int64_t dfl_q41_gemm_scratch_bytes(int K, int N, int M) {
     if (K < 32 || K % 32 || N < 32 || N % 32 || M < 1 || M > kMaxRows) return -1;
     const int C = padded_k(K) / 64;
-    return (int64_t)((size_t)(N / 32 * 4 + 255) / 256 * 256 + gemm_scratch_floats(C, N) * 4);
+    return (int64_t)(kScratchHeader + (size_t)(N / 32 * 4 + 255) / 256 * 256 + gemm_scratch_floats(C, N) * 4);
 }
 
 int dfl_q41_gemm(const void *img, int K, int N, const void *act, int M, float *y, void *scratch, size_t scratch_bytes,
                  void *stream) {
     const int64_t need = dfl_q41_gemm_scratch_bytes(K, N, M);
     if (need < 0 || !img || !act || !y || !scratch || (int64_t)scratch_bytes < need) return DFL_E_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(scratch) & 255) return DFL_E_INVALID_ARG;
     const int C = padded_k(K) / 64;
     GemmArgs a{};
     a.img = static_cast<const uint8_t *>(img);
@@ -1406,23 +1421,96 @@ int dfl_q41_gemm(const void *img, int K, int N, const void *act, int M, float *y
     a.y = y;
     a.ldy = N;
     a.maxseg = gemm_maxseg(C, N);
+    uint8_t *base = static_cast<uint8_t *>(scratch);
     const size_t cbytes = (size_t)(N / 32 * 4 + 255) / 256 * 256;
-    a.cnt = static_cast<int *>(scratch);
-    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + cbytes);
+    a.err = reinterpret_cast<int *>(base);
+    a.cnt = reinterpret_cast<int *>(base + kScratchHeader);
+    a.part = reinterpret_cast<float *>(base + kScratchHeader + cbytes);
     return launch_gemm(W_Q41, EPI_F32, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
 }
 
+int dfl_q41_gemm_status(const void *scratch, void *stream) {
+    if (!scratch) return DFL_E_INVALID_ARG;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int err = 0;
+    if (cudaMemcpyAsync(&err, scratch, sizeof err, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return DFL_E_CUDA;
+    if (!(err & kErrWaitTimeout)) return DFL_OK;
+    if (cudaMemsetAsync(const_cast<void *>(scratch), 0, sizeof err, s) != cudaSuccess) return DFL_E_CUDA;
+    return DFL_E_TIMEOUT;
+}
+
+// ---- the bf16 head on its own ------------------------------------------------------------------------
+int64_t dfl_bf16_image_bytes(int K, int N) {
+    if (K < 64 || K % 64 || N < 16 || N % 16) return -1;
+    return (int64_t)bf16_image_bytes(K, N);
+}
+
+int dfl_bf16_pack(const void *src, int K, int N, void *img, void *stream) {
+    if (!src || !img || dfl_bf16_image_bytes(K, N) < 0) return DFL_E_INVALID_ARG;
+    return launch_pack_bf16(static_cast<const uint16_t *>(src), K, N, static_cast<uint8_t *>(img),
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+}
+
+// scratch: the CTA arrival counter (256-byte header), then per-CTA maxima and their indices
+int64_t dfl_bf16_head_scratch_bytes(int K, int N, int M) {
+    if (dfl_bf16_image_bytes(K, N) < 0 || M < 1 || M > kMaxRows) return -1;
+    return (int64_t)(kScratchHeader + (size_t)head_grid(K / 64, M, N) * kMaxRows * 8);
+}
+
+int dfl_bf16_head_argmax(const void *img, int K, int N, const void *act, int M, int32_t *argmax, float *logits,
+                         void *scratch, size_t scratch_bytes, void *stream) {
+    const int64_t need = dfl_bf16_head_scratch_bytes(K, N, M);
+    if (need < 0 || !img || !act || !argmax || !scratch || (int64_t)scratch_bytes < need) return DFL_E_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(scratch) & 255) return DFL_E_INVALID_ARG;
+    const int C = K / 64, G = head_grid(C, M, N);
+    uint8_t *base = static_cast<uint8_t *>(scratch);
+    GemmArgs a{};
+    a.img = static_cast<const uint8_t *>(img);
+    a.K = K;
+    a.C = C;
+    a.N = N;
+    a.M = M;
+    a.xf = static_cast<const uint32_t *>(act);
+    a.xs = reinterpret_cast<const float *>(static_cast<const uint32_t *>(act) + act_words(K));
+    a.logits = logits;
+    a.ldl = N;
+    a.am_cnt = reinterpret_cast<int *>(base);
+    a.am_val = reinterpret_cast<float *>(base + kScratchHeader);
+    a.am_idx = reinterpret_cast<int *>(base + kScratchHeader + (size_t)G * kMaxRows * 4);
+    a.am_dst = AM_OUT;
+    a.am_out = argmax;
+    return launch_gemm(W_BF16, EPI_ARGMAX, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+}
+
 // ---- the product with library-owned scratch -------------------------------------------------------
-// One static device array holds the arrival counters and segment partials of dfl_q41_gemm_noalloc; its
-// address is looked up once per device and cached.
+// One static device array holds the error word, arrival counters and segment partials of
+// dfl_q41_gemm_noalloc; its address is looked up once per device and cached (dropped again by
+// dfl_q41_gemm_noalloc_reset).
 }  // extern "C"
 
 namespace {
 constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
-constexpr int kNoallocDevices = 64;
+constexpr int kNoallocDevices = kMaxDevices;
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[kNoallocDevices] = {};
+
+// this device's copy of the array (the device must be current); nullptr on failure
+void *noalloc_scratch() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        // the current device is `dev`: the address is this device's copy of the array
+        if (cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch) != cudaSuccess) {
+            g_noalloc_ptr[dev] = nullptr;
+            return nullptr;
+        }
+    }
+    return g_noalloc_ptr[dev];
+}
 }  // namespace
 
 extern "C" {
@@ -1433,21 +1521,28 @@ int dfl_q41_gemm_noalloc(const void *img, int K, int N, const void *act, int M, 
     const int64_t need = dfl_q41_gemm_scratch_bytes(K, N, M);
     if (need < 0 || !img || !act || !y) return DFL_E_INVALID_ARG;
     if ((size_t)need > kNoallocScratchBytes) return DFL_E_CAPACITY;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocDevices) return DFL_E_CUDA;
-    void *scratch = nullptr;
+    void *scratch = noalloc_scratch();
+    if (!scratch) return DFL_E_CUDA;
+    return dfl_q41_gemm(img, K, N, act, M, y, scratch, kNoallocScratchBytes, stream);
+}
+
+int dfl_q41_gemm_noalloc_status(void *stream) {
+    void *scratch = noalloc_scratch();
+    if (!scratch) return DFL_E_CUDA;
+    return dfl_q41_gemm_status(scratch, stream);
+}
+
+int dfl_q41_gemm_noalloc_reset(void *stream) {
+    const int dev = current_device();
+    if (dev < 0) return DFL_E_CUDA;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mu);
-        if (!g_noalloc_ptr[dev]) {
-            // the current device is `dev`: the address is this device's copy of the array
-            if (cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch) != cudaSuccess) {
-                g_noalloc_ptr[dev] = nullptr;
-                return DFL_E_CUDA;
-            }
-        }
-        scratch = g_noalloc_ptr[dev];
+        g_noalloc_ptr[dev] = nullptr;   // looked up again: the context may have been recreated
     }
-    return dfl_q41_gemm(img, K, N, act, M, y, scratch, kNoallocScratchBytes, stream);
+    void *scratch = noalloc_scratch();
+    if (!scratch) return DFL_E_CUDA;
+    return cudaMemsetAsync(scratch, 0, kNoallocScratchBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DFL_OK : DFL_E_CUDA;
 }
 
 }  // extern "C"

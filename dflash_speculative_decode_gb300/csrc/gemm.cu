@@ -36,6 +36,11 @@ namespace dfl {
 
 // compute warps of a product CTA: four column groups x kGemmPar chunk parities
 constexpr int kGemmWarps = 8, kGemmThreads = kGemmWarps * 32, kGemmPar = kGemmWarps / 4;
+// Two product CTAs fit on one SM (shared memory, registers), so the next product of a chain lands on the
+// SM while the current one still computes and streams its first weights in the meantime.
+constexpr int kGemmCtasPerSm = 2;
+constexpr int kGemmMaxRegs = 112;   // 2 CTAs x 9 warps x 32 lanes x 112 registers <= 65536
+static_assert(kGemmCtasPerSm * (kGemmWarps + 1) * 32 * kGemmMaxRegs <= 65536, "two product CTAs per SM");
 
 // ---------------------------------------------------------------------------------------------------
 // packing
@@ -114,8 +119,8 @@ cudaError_t launch_pack_bf16(const uint16_t *src, int K, int N, uint8_t *img, cu
 
 // fp32 rows -> operand format (the standalone product's input)
 __global__ void k_act_pack(const float *x, int M, int K, uint32_t *f, float *sums) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     const int m = blockIdx.y;
     const int k = blockIdx.x * blockDim.x + threadIdx.x;   // blockDim 256: a 16-group is one half warp
     const bool in = k < K && m < M;
@@ -140,7 +145,7 @@ cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *su
 //   sums:  at WB + MT * CP * 2048, 256 bytes per chunk ([4 groups][16 rows] fp32)
 // ---------------------------------------------------------------------------------------------------
 template <int FMT>
-__host__ __device__ constexpr int cpr() { return FMT == W_Q41 ? 8 : 4; }
+__host__ __device__ constexpr int cpr() { return FMT == W_Q41 ? 4 : 2; }
 template <int FMT>
 __host__ __device__ constexpr int xblock_bytes() { return cpr<FMT>() * 2048; }   // one row block of a round
 template <int MT>
@@ -151,7 +156,7 @@ template <int FMT, int MT>
 __host__ __device__ constexpr int slot_bytes() {
     return (8 * cpr<FMT>() * tile_bytes<FMT>() + MT * xblock_bytes<FMT>() + cpr<FMT>() * 256 + 127) / 128 * 128;
 }
-constexpr int kGemmSmemBudget = 224 * 1024;
+constexpr int kGemmSmemBudget = 110 * 1024;   // per CTA: two CTAs and their static shared memory per SM
 template <int FMT, int MT>
 __host__ __device__ constexpr int ring_slots() {
     return (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<FMT, MT>() < 6 ? (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<FMT, MT>() : 6;
@@ -352,10 +357,11 @@ constexpr int kGemmBlock = kGemmThreads + 32;   // + the copy warp
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kGemmThreads) : "memory"); }
 
 template <int FMT, int MT, int EPI>
-__global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
+__global__ void __maxnreg__(kGemmMaxRegs) k_gemm(GemmArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[8], empty[8];
-    __shared__ int s_last, s_bad;
+    __shared__ int s_last, s_issued;
+    __shared__ volatile int s_bad;   // set by the first bounded wait that gives up
     constexpr int R = MT * 8;
     constexpr int TB = tile_bytes<FMT>();
     constexpr int CP = cpr<FMT>();
@@ -400,6 +406,7 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
         }
         s_bad = 0;
         s_last = 0;
+        s_issued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -430,27 +437,50 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
             else if (lane == MT)
                 bulk_g2s(base + MT * XB, a.xs + (size_t)(4 * r.c) * kMaxRows, 64u * ng16, &full[sl]);
         };
+        // a round whose copies are not issued (the pass failed before this launch): two plain arrivals
+        // complete its phase without data, so no wait of the compute warps runs out
+        auto arrive_only = [&](int sl, int n) {
+            if (lane == 0)
+                for (int i = 0; i < n; ++i) mbar_arrive(&full[sl]);
+            __syncwarp();
+        };
         Rd r;
         rd_at_quad(r, int(u0 / a.C), int(u0 % a.C));
         const Rd r0 = r;
-        // weights are immutable: the first rounds' weights go out before the previous kernel ends
         int k = 0;
-        for (; k < S && rd_valid(r); ++k, rd_next(r)) issue_w(r, k);
+        if (!a.stall) {
+            // weights are immutable: the first rounds' weights go out before the previous kernel ends
+            for (; k < S && rd_valid(r); ++k, rd_next(r)) issue_w(r, k);
+        }
         pdl_wait();
         pdl_trigger();
-        Rd rx = r0;
-        for (int k2 = 0; k2 < k; ++k2, rd_next(rx)) issue_x(rx, k2);
-        for (; rd_valid(r); ++k, rd_next(r)) {
-            const int sl = k % S;
-            if (!mbar_wait(&empty[sl], unsigned(k / S - 1) & 1u)) s_bad = 1;
-            issue_w(r, sl);
-            issue_x(r, sl);
+        // the pass this launch belongs to has already failed: no more copies, rounds complete empty
+        const bool skip = a.skip_on_err && a.err && *reinterpret_cast<volatile int *>(a.err) != 0;
+        if (!a.stall || skip) {
+            Rd rx = r0;
+            for (int k2 = 0; k2 < k; ++k2, rd_next(rx)) {
+                if (skip) arrive_only(k2, 1);
+                else issue_x(rx, k2);
+            }
+            for (; rd_valid(r); ++k, rd_next(r)) {
+                const int sl = k % S;
+                // once any wait of the CTA has given up, nothing more is issued
+                if (!mbar_wait(&empty[sl], unsigned(k / S - 1) & 1u, &s_bad) || s_bad) break;
+                if (skip) {
+                    arrive_only(sl, 2);
+                } else {
+                    issue_w(r, sl);
+                    issue_x(r, sl);
+                }
+            }
         }
+        if (lane == 0) s_issued = k;   // rounds whose copies went out (read after the final barrier)
     } else {
         // ---- compute warps ----
         const int gq = warp & 3, par = warp >> 2;
         pdl_wait();
         pdl_trigger();
+        stamp_ready(a.ps);
         float acc[2][MT][4];
         auto zero = [&]() {
 #pragma unroll
@@ -467,9 +497,11 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
         rd_at_quad(cr, int(u0 / a.C), int(u0 % a.C));
         for (int k = 0; rd_valid(cr); ++k) {
             const int sl = k % S;
-            if (!mbar_wait(&full[sl], unsigned(k / S) & 1u)) s_bad = 1;
+            // a round whose wait gave up is skipped (its slot may still be landing); the control flow,
+            // and so every barrier of the compute warps, stays the same
+            const bool landed = mbar_wait(&full[sl], unsigned(k / S) & 1u, &s_bad);
             const int ng = 4 * cr.q + gq;
-            if (ng < ngroups) {
+            if (landed && ng < ngroups) {
                 const uint8_t *slot = ring + sl * SB;
                 if (FMT == W_Q41) {
                     int nblk[NU];
@@ -614,8 +646,24 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
             cr = nx;
         }
     }
-    __syncthreads();   // every copy has landed (each was waited for) and every warp is done
-    if (threadIdx.x == 0 && s_bad && a.err) atomicOr(a.err, kErrWaitTimeout);
+    __syncthreads();   // every warp is done
+    if (s_bad) {
+        // A wait gave up: copies issued into a slot may still be in flight. Before the CTA exits, wait
+        // (bounded again) for the last round issued into each slot; its phase completes only once
+        // every byte of it, and of the rounds before it in that slot, has landed.
+        if (warp == kGemmWarps && lane == 0) {
+            const int issued = s_issued;
+            volatile int drain_bad = 0;
+            for (int sl = 0; sl < S && sl < issued; ++sl) {
+                const int last = sl + (issued - 1 - sl) / S * S;
+                mbar_wait(&full[sl], unsigned(last / S) & 1u, &drain_bad);
+                drain_bad = 0;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && a.err) atomicOr(a.err, kErrWaitTimeout);
+    }
+    stamp_done(a.ps);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -628,7 +676,7 @@ constexpr int kHeadPad = 64;   // bytes added per staged row: conflict-free 16-b
 
 template <int MT>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) k_head(GemmArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ float wval[kWarpsPerCta][kMaxRows];
     __shared__ int widx[kWarpsPerCta][kMaxRows];
     __shared__ int s_last;
@@ -666,6 +714,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) k_head(GemmArgs a) {
         if (p < units) load(p, w[p]);
     pdl_wait();
     pdl_trigger();
+    stamp_ready(a.ps);
     // stage the activation fragments of all rows (one asynchronous copy round trip)
     for (int e = threadIdx.x; e < MT * 8 * K16 * 4; e += blockDim.x) {
         const int tok = e / (K16 * 4), rest = e % (K16 * 4);
@@ -757,6 +806,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) k_head(GemmArgs a) {
     __syncthreads();
     if (threadIdx.x == 0) s_last = (atomicAdd(a.am_cnt, 1) == (int)gridDim.x - 1);
     __syncthreads();
+    stamp_done(a.ps);
     if (!s_last) return;
     __threadfence();
     if (threadIdx.x < a.M) {
@@ -769,7 +819,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) k_head(GemmArgs a) {
             if (better(bvv, bii, v, i)) v = bvv, i = bii;
         }
         if (a.am_dst == AM_VERIFY) a.st->target[tok] = i;
-        else a.st->props[tok] = i;
+        else if (a.am_dst == AM_DRAFT) a.st->props[tok] = i;
+        else a.am_out[tok] = i;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -781,6 +832,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) k_head(GemmArgs a) {
         }
         *a.am_cnt = 0;
     }
+    stamp_done(a.ps);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -820,11 +872,13 @@ static cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     if (a.x_row0 % 8) return cudaErrorInvalidValue;   // products read whole row blocks
     constexpr int smem = red_bytes<MT>() + ring_slots<FMT, MT>() * slot_bytes<FMT, MT>();
     static_assert(smem <= kGemmSmemBudget, "product shared memory");
-    static bool attr = false;
-    if (!attr) {
+    static bool attr[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (!attr[dev]) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm<FMT, MT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr[dev] = true;
     }
     return launch_pdl(k_gemm<FMT, MT, EPI>, dim3(gemm_grid(a.C, a.N)), dim3(kGemmBlock), (size_t)smem, s, a);
 }
@@ -844,11 +898,13 @@ int head_grid(int C, int M, int N) {
 template <int MT>
 static cudaError_t run_head(const GemmArgs &a, cudaStream_t s) {
     const size_t smem = head_smem(a.K, MT);
-    static bool attr = false;
-    if (!attr) {
+    static bool attr[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (!attr[dev]) {
         cudaError_t e = cudaFuncSetAttribute(k_head<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr[dev] = true;
     }
     return launch_pdl(k_head<MT>, dim3(head_grid(a.C, a.M, a.N)), dim3(kWarpsPerCta * 32), smem, s, a);
 }

@@ -14,8 +14,8 @@ namespace dfl {
 
 // ---------------------------------------------------------------------------------------------------
 __global__ void k_set_state(DevState *st, SetStateArgs a) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     const int i = threadIdx.x;
     int r = 0;
     if (i < kMaxRows) r = a.use_draft_rows ? (i == 0 ? st->last_tok : st->props[i - 1]) : a.rows[i];
@@ -39,8 +39,8 @@ cudaError_t launch_set_state(DevState *st, const SetStateArgs &a, cudaStream_t s
 
 // planted drafts: the proposals for positions n+1..n+count become table[n+1..n+count]
 __global__ void k_plant(DevState *st, const int32_t *table, int count) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     const int i = threadIdx.x;
     if (i < count) st->props[i] = table[st->n + 1 + i];
 }
@@ -52,8 +52,9 @@ cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStre
 // ---------------------------------------------------------------------------------------------------
 // x[m] = emb[token_m] * scale (fp32); the row's per-layer-embedding inputs are a plain table row.
 __global__ void k_embed(EmbedArgs a) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
+    stamp_ready(a.ps);
     const int m = blockIdx.x;
     const int tok = a.use_draft ? (m == 0 ? a.st->last_tok : a.mask_token) : a.st->rows[m];
     const uint16_t *e = a.emb + (long)tok * a.H;
@@ -62,6 +63,7 @@ __global__ void k_embed(EmbedArgs a) {
         const uint16_t *p = a.ple + (long)tok * a.ple_w;
         for (int h = threadIdx.x; h < a.ple_w; h += blockDim.x) a.ple_out[(long)m * a.ple_w + h] = p[h];
     }
+    stamp_done(a.ps);
 }
 
 cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t s) {
@@ -197,8 +199,9 @@ __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
     const int m = blockIdx.x;
     const int h = 4 * int(threadIdx.x);
     const bool on = h < a.H;
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
+    stamp_ready(a.ps);
     const bool live = !a.rows_from_ctx || m < a.st->ctx_rows;
     float *xr = a.x ? a.x + (long)m * a.H : nullptr;
     float4 x = (on && xr) ? *reinterpret_cast<const float4 *>(xr + h) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -258,6 +261,7 @@ __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
         hl += __shfl_xor_sync(0xffffffffu, hl, 2);
         if (on && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = hl;
     }
+    stamp_done(a.ps);
 }
 
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
@@ -270,8 +274,8 @@ cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
 __global__ void __launch_bounds__(kRowThreads) k_cast_rows(const float *src, int ld_src, int H, const uint16_t *w,
                                                            float eps, uint32_t *dstf, float *dsts, int row0,
                                                            const DevState *st, int live_from_ctx) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     __shared__ float red[33];
     const int m = blockIdx.x;
     const bool live = !live_from_ctx || m < st->ctx_rows;
@@ -309,12 +313,16 @@ cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const u
 // absolute position, from a (cos, sin) table computed in double precision. Keys and values are
 // stored into their plane slot (pos % cap), or into the block store (slot = row).
 __global__ void k_qk(QkArgs a) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     __shared__ float red[33];
+    stamp_ready(a.ps);
     const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.hd / 2;
     const bool live = !a.live_from_ctx || m < a.st->ctx_rows;
-    if (!live) return;
+    if (!live) {
+        stamp_done(a.ps);
+        return;
+    }
     const int pos = (a.pos_mode == 2 ? a.st->draft_n : a.st->n) + m;
     const int rr = a.row0 + m;
     // column c of this row of the product (plain rows or segment partials); kept for inspection
@@ -348,6 +356,7 @@ __global__ void k_qk(QkArgs a) {
         v[i] = val(cv + i);
         v[i + half] = val(cv + i + half);
     }
+    stamp_done(a.ps);
 }
 
 cudaError_t launch_qk(const QkArgs &a, cudaStream_t s) {
@@ -493,6 +502,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     }
     pdl_wait();
     pdl_trigger();
+    stamp_ready(a.ps);
     while (issued < kAttnBuf - 1 && issued < nmine) {
         load_block(issued, issued);
         ++issued;
@@ -710,6 +720,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         if (res_on[k] && (tid & 15) == 0) a.outs[(res_col[k] >> 4) * kMaxRows + res_m[k]] = sg;
     }
     cluster_wait();     // no CTA leaves while another still reads its shared memory
+    stamp_done(a.ps);
 }
 
 // Cluster size per layer shape: the largest of 16 (a non-portable size), 8 and 4 such that all of the
@@ -717,16 +728,20 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
 // fit is asked once per head-dimension class at context creation, outside any stream capture; until
 // then every launch takes clusters of 8. The size depends only on the shape, never on the number of
 // rows, so a row's result does not depend on the pass it travels in.
-static int g_fit[2][2] = {{0, 1 << 20}, {0, 1 << 20}};   // [hd > 128][16, 8]: clusters that fit at once
+// [device][hd > 128][16, 8]: clusters that fit at once (until attn_prepare: none of 16, all of 8)
+static int g_fit[kMaxDevices][2][2];
+static bool g_fit_set[kMaxDevices];
 template <int CL, int HP>
 static cudaError_t attn_attrs() {
-    static bool done = false;
-    if (done) return cudaSuccess;
+    static bool done[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (done[dev]) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k_attn<CL, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(attn_smem(256)));
     if (e == cudaSuccess && CL > 8)
         e = cudaFuncSetAttribute(k_attn<CL, HP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess) done = true;
+    if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
@@ -753,14 +768,21 @@ static int clusters_that_fit(int hd) {
 
 cudaError_t attn_prepare(int hd) {
     cudaError_t e;
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (!g_fit_set[dev]) {
+        g_fit[dev][0][0] = g_fit[dev][1][0] = 0;
+        g_fit[dev][0][1] = g_fit[dev][1][1] = 1 << 20;
+        g_fit_set[dev] = true;
+    }
     if ((e = attn_attrs<8, 1>()) || (e = attn_attrs<8, 2>()) || (e = attn_attrs<4, 1>()) || (e = attn_attrs<4, 2>()))
         return e;
-    g_fit[hd > 128][1] = clusters_that_fit<8>(hd);
+    g_fit[dev][hd > 128][1] = clusters_that_fit<8>(hd);
     if (attn_attrs<16, 1>() != cudaSuccess || attn_attrs<16, 2>() != cudaSuccess) {
         cudaGetLastError();   // no wide clusters on this device
-        g_fit[hd > 128][0] = 0;
+        g_fit[dev][hd > 128][0] = 0;
     } else {
-        g_fit[hd > 128][0] = clusters_that_fit<16>(hd);
+        g_fit[dev][hd > 128][0] = clusters_that_fit<16>(hd);
     }
     return cudaSuccess;
 }
@@ -778,7 +800,10 @@ cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const bool pairs = (a.nq / a.nkv) % 2 == 0;   // two heads of one key/value group per CTA possible
     const int units = pairs ? a.nq / 2 : a.nq;    // clusters of a pass of up to 8 rows
-    const int *fit = g_fit[a.hd > 128];
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    static const int kNoFit[2] = {0, 1 << 20};   // attn_prepare not run on this device: clusters of 8
+    const int *fit = g_fit_set[dev] ? g_fit[dev][a.hd > 128] : kNoFit;
     const int cl = (a.max_cluster >= 16 && fit[0] >= units) ? 16 : (a.max_cluster >= 8 && fit[1] >= units) ? 8 : 4;
     const bool hp2 = pairs && a.M <= 8;
     if (cl == 16) return hp2 ? launch_attn_t<16, 2>(a, s) : launch_attn_t<16, 1>(a, s);
@@ -800,11 +825,12 @@ constexpr int kSampleThreads = 1024;
 // Row m's token for position n+m+1: the smallest j whose running sum of exp((l_j - max)/T) exceeds
 // U * total (running sums in double; each thread sums a contiguous segment, then a block scan).
 __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleArgs a) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     __shared__ float redf[33];
     __shared__ double wsum[32];
     __shared__ int s_tok, s_last;
+    stamp_ready(a.ps);
     const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *l = a.logits + (long)m * a.ld;
     const float T = a.st->temperature;
@@ -877,6 +903,7 @@ __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleArgs a) {
         a.st->accepted = acc_len;
         *a.cnt = 0;
     }
+    stamp_done(a.ps);
 }
 
 cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s) {
@@ -909,8 +936,8 @@ namespace dfl {
 // dst row m = taps row of position st->draft_n + m for m < st->ctx_rows, zeros for the other rows, in
 // operand format (the fc product is bf16-weighted: no sums needed).
 __global__ void k_copy_taps(const float *taps, int ld, const DevState *st, uint32_t *dstf) {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     const int m = blockIdx.x;
     const bool live = m < st->ctx_rows;
     const float *src = taps + (long)(st->draft_n + (live ? m : 0)) * ld;

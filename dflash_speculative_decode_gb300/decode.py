@@ -54,9 +54,8 @@ def spec_decode(eng, prompt, n_gen: int, temperature=None, seed=0,
         props = np.asarray(propose(n, dp) if propose else dp, np.int32)[: B - 1]
         rows = np.concatenate([[last], props]).astype(np.int32)
         tt, a = eng.dfl_verify_block(rows, temperature=temperature, seed=seed)
-        emit = [int(v) for v in props[:a]] + [int(tt[a])]
-        emit = emit[: n_gen - len(g.tokens)]
-        eng.dfl_commit_verify_rows(len(emit))
+        kept = eng.dfl_commit_accepted(n_gen - len(g.tokens))   # accepted + 1, within the budget
+        emit = [int(v) for v in tt[:kept]]                     # the verify's tokens of the kept rows
         g.held.append(n)
         g.accepted.append(a)
         g.proposals.append(list(map(int, dp)))

@@ -50,7 +50,8 @@ enum {
     DFL_E_CAPACITY = -3,         /* positions would exceed max_ctx */
     DFL_E_UNSUPPORTED = -4,      /* e.g. k > DFL_MAX_ROWS, a shape the kernels do not take */
     DFL_E_CUDA = -5,             /* a CUDA call failed; the message names it */
-    DFL_E_TIMEOUT = -6           /* a bounded device wait gave up */
+    DFL_E_TIMEOUT = -6           /* a bounded device wait gave up (about 1 s); reported by the next call
+                                    that reads the device state, with the state of the last good call */
 };
 
 enum { DFL_SLIDING = 0, DFL_FULL = 1 };
@@ -123,61 +124,87 @@ int dfl_init(const dfl_config *cfg, const dfl_buffers *buf, void *cuda_stream, d
  * passed this call (it is read by kernels enqueued here). */
 int dfl_load_tensor(dfl_ctx *ctx, const char *name, const void *dev_src, size_t bytes);
 
-/* Prefill (extend the context): run the n tokens at positions held..held+n-1 in chunks of at most
- * DFL_MAX_ROWS rows, commit them, bring the draft context up to date, and write the target's token
- * for the next position to *next_tok (greedy or sampled). Fails with DFL_E_CAPACITY if held + n + 1
- * exceeds max_ctx. */
+/* Prefill (extend the context; 1bit engine PR "npu forward: Gemma4 verifies a draft in one batched
+ * pass; KV row width per layer", "What changes" item 1, extend_context): run the n tokens at positions
+ * held..held+n-1 in chunks of at most DFL_MAX_ROWS rows, commit them, bring the draft context up to date,
+ * and write the target's token for the next position to *next_tok (greedy or sampled). Fails with
+ * DFL_E_CAPACITY if held + n exceeds max_ctx; on any error positions held stay as they were. */
 int dfl_prefill(dfl_ctx *ctx, const int32_t *tokens, int n, const dfl_sampling *s, int32_t *next_tok);
 
-/* Draft block at positions held..held+block-1 for rows [last_tok, mask x (block-1)]: first makes the
- * committed rows not yet in the draft context into context (fc of their taps, then each draft layer's
- * key and value), then runs the block. Proposals (block-1 tokens for positions held+1..) are kept on
- * the device for dfl_verify_block(rows = NULL) and copied to `proposals` when it is not NULL. */
+/* Draft block (model card "Nemotron-3.5-Bolt-E4B-DFlash-NPU2", "How it is used"; 1bit engine PR "a
+ * Gemma4 pack stops re-reading its weights every token; tools/dflash_acceptance", item 2) at positions
+ * held..held+block-1 for rows [last_tok, mask x (block-1)]: first makes the committed rows not yet in
+ * the draft context into context (fc of their taps, then each draft layer's key and value), then runs
+ * the block. Proposals (block-1 tokens for positions held+1..) are kept on the device for
+ * dfl_verify_block(rows = NULL) and copied to `proposals` when it is not NULL (which synchronises; with
+ * NULL the call does not synchronise, and a device error surfaces at the next synchronising call). */
 int dfl_draft_block(dfl_ctx *ctx, int32_t last_tok, int32_t *proposals);
 
-/* Batched verify of k rows at positions held..held+k-1. rows = [last token, proposal 1, ..,
- * proposal k-1]; rows == NULL takes last_tok of the last draft block and its k-1 first proposals.
- * Writes the target's token for positions held+1..held+k to target_tok[0..k-1] (if not NULL) and
- * the accepted length a (longest prefix with proposal i == target token i-1) to *accepted (if not
- * NULL). The rows stay pending until dfl_commit_verify_rows. k in 1..DFL_MAX_ROWS. */
+/* Batched verify (1bit engine PR "npu forward: Gemma4 verifies a draft in one batched pass; KV row
+ * width per layer", "What changes": every projection one M-row product, a KV-shared layer reads its
+ * owner's plane and appends nothing; acceptance: model card "How it is used") of k rows at positions
+ * held..held+k-1. rows = [last token, proposal 1, .., proposal k-1]; rows == NULL takes last_tok of the
+ * last draft block and its k-1 first proposals. Writes the target's token for positions
+ * held+1..held+k to target_tok[0..k-1] (if not NULL) and the accepted length a (longest prefix with
+ * proposal i == target token i-1) to *accepted (if not NULL). The tokens the pass emits are
+ * target_tok[0..a] (the accepted proposals equal the target's tokens before them, plus the target's
+ * token after the last one). The rows stay pending until dfl_commit_verify_rows / dfl_commit_accepted.
+ * k in 1..DFL_MAX_ROWS. */
 int dfl_verify_block(dfl_ctx *ctx, const int32_t *rows, int k, const dfl_sampling *s,
                      int32_t *target_tok, int32_t *accepted);
 
-/* commit_verify_rows: keep the first `keep` rows of the pending verify (0 <= keep <= k); positions
- * held become held + keep. Pure index arithmetic: no data moves; later rows are overwritten by the
- * next pass. keep = DFL_KEEP_ACCEPTED keeps accepted + 1 rows (the accepted proposals and the row of
- * the last token) as counted by the last verify. */
+/* commit_verify_rows (1bit engine PR "npu forward: Gemma4 verifies a draft in one batched pass",
+ * "What changes" item 1 and "Proof": 3 held, commit_verify_rows(2), 5 held): keep the first `keep` rows
+ * of the pending verify (0 <= keep <= k); positions held become held + keep. Pure index arithmetic: no
+ * data moves; later rows are overwritten by the next pass. keep = DFL_KEEP_ACCEPTED keeps accepted + 1
+ * rows (the accepted proposals and the row of the last token) as counted by the last verify. */
 #define DFL_KEEP_ACCEPTED (-1)
 int dfl_commit_verify_rows(dfl_ctx *ctx, int keep);
+/* The acceptance step's commit (model card "How it is used": the longest agreeing prefix plus one
+ * target token are kept): keep min(accepted + 1, max_keep) rows of the pending verify, where max_keep
+ * caps the tokens a caller still wants (a token budget), and write that count to *kept (if not NULL).
+ * The kept rows' tokens are target_tok[0..*kept-1] of the verify. */
+int dfl_commit_accepted(dfl_ctx *ctx, int max_keep, int32_t *kept);
 
-/* Snapshot of the committed state (positions held, every owner plane, the draft context, the taps
- * of committed rows not yet in the draft context) into a DEVICE buffer of at least
- * dfl_snapshot_bytes() bytes; restore replaces the state with a snapshot taken from a context with
- * the same configuration. Both need the committed state (no pending verify). KV-shared layers have no
- * plane and contribute nothing. */
+/* Snapshot (1bit engine PR "npu forward: Gemma4 verifies a draft in one batched pass", "What changes"
+ * item 1: snapshot and restore cut each plane at its own layer's width; a KV-shared layer's plane stays
+ * empty) of the committed state (positions held, every owner plane, the draft context, the taps of
+ * committed rows not yet in the draft context) into a DEVICE buffer of at least dfl_snapshot_bytes()
+ * bytes; restore replaces the state with a snapshot taken from a context with the same configuration.
+ * Both need the committed state (no pending verify). KV-shared layers have no plane and contribute
+ * nothing. A snapshot taken once after a pinned prefix may be restored any number of times (FastFlowLM
+ * PR #899 "gemma4e-dflash-flash", "Changes": the pinned prefix must not be overwritten by a request). */
 int64_t dfl_snapshot_bytes(const dfl_ctx *ctx);
 int dfl_snapshot(dfl_ctx *ctx, void *dev_dst, size_t bytes);
 int dfl_restore(dfl_ctx *ctx, const void *dev_src, size_t bytes);
 
-/* Per-layer KV row width in floats per position: 2 * kv_heads * head_dim for a layer with its own
- * plane, 0 for a KV-shared layer. out: n_layers entries. */
+/* Per-layer KV row width in floats per position (1bit engine PR "npu forward: Gemma4 verifies a draft
+ * in one batched pass", "What changes" item 1, kv_widths(): 2 x 256 on E4B's sliding layers, 2 x 512 on
+ * its full layers): 2 * kv_heads * head_dim for a layer with its own plane, 0 for a KV-shared layer.
+ * out: n_layers entries. */
 int dfl_kv_widths(const dfl_ctx *ctx, int32_t *out);
 
-/* Positions held (committed), counted over owner planes only. -1 on a NULL context. */
+/* Positions held (committed), counted over owner planes only (same PR, "What changes" item 1: the
+ * positions-held count ignores shared layers). -1 on a NULL context. */
 int64_t dfl_positions_held(const dfl_ctx *ctx);
 
 /* Options. DFL_OPT_KEEP_LOGITS = 1 makes verify and draft passes also store their fp32 logits
  * (otherwise only the fused argmax runs); DFL_OPT_GRAPHS = 0 launches kernels one by one instead of
  * replaying captured CUDA graphs; DFL_OPT_STOP_LAYER = l >= 0 (inspection only) makes target passes
  * stop after layer l, without the head, so dfl_debug_read shows that layer's intermediates; -1 = off;
- * DFL_OPT_PROFILE = 1 brackets every kernel launch with CUDA events on the context's stream (read with
- * dfl_profile_read; setting the option clears the totals); DFL_OPT_ATTN_CLUSTER = 16 (default), 8 or 4
+ * DFL_OPT_PROFILE = 1 times the kernel launches of every pass on the device (read with
+ * dfl_profile_read; setting the option clears the totals; each profiled pass synchronises once, to read
+ * its time stamps); DFL_OPT_ATTN_CLUSTER = 16 (default), 8 or 4
  * caps the number of CTAs over which attention spreads one pair of query heads (the largest size up to
  * the cap whose clusters all fit on the device at once is taken; sizes differ in the order in which
  * the partial softmax states are added, so logits may differ in the last bits); other values are
  * DFL_E_INVALID_ARG. Changing it drops the captured graphs. */
 enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3, DFL_OPT_PROFILE = 4,
-       DFL_OPT_ATTN_CLUSTER = 5 };
+       DFL_OPT_ATTN_CLUSTER = 5, DFL_OPT_TEST_STALL = 6 };
+/* DFL_OPT_TEST_STALL = 1 (tests of the error path only): the Q4_1 products of the following passes
+ * issue no copies, so the first one's bounded waits give up after about a second and the call that reads
+ * the device state returns DFL_E_TIMEOUT with the state unchanged; set it back to 0 and the context
+ * works as before. */
 int dfl_set_option(dfl_ctx *ctx, int option, int value);
 
 /* Copy the fp32 logits of the last pass (rows x vocab, row-major) to host memory. which = 0: the
@@ -195,7 +222,10 @@ int dfl_draft_append_taps(dfl_ctx *ctx, const void *dev_taps, int rows);
 
 /* Inspection: copy the first `bytes` of an internal buffer of the last pass to host memory. Names:
  * "x" [16][hidden] residual rows, "y" [16][hidden] last projection output, "qkv" [16][width],
- * "q" [16][heads*head_dim] (normed, rotated), "x_d" [16][hidden] draft residual rows; all fp32. */
+ * "q" [16][heads*head_dim] (normed, rotated), "x_d" [16][hidden] draft residual rows; "k<l>" and "v<l>"
+ * the key and value plane of target layer l, [slots][kv_heads][head_dim] with position p in slot p
+ * (full layers) or p mod (window + 15) (sliding layers); all fp32. A KV-shared layer has no plane
+ * (DFL_E_INVALID_ARG). */
 int dfl_debug_read(dfl_ctx *ctx, const char *name, void *host_dst, size_t bytes);
 
 /* Planted drafts (measurement workloads that control acceptance): after dfl_draft_block, replace its
@@ -208,11 +238,14 @@ int64_t dfl_launch_count(const dfl_ctx *ctx);
 
 /* Totals of the launches profiled while DFL_OPT_PROFILE was on, per class: 0 = Q4_1 products,
  * 1 = bf16 products (fc), 2 = the bf16 head with its fused argmax, 3 = attention, 4 = q/k norm,
- * rotation and KV store, 5 = the other row kernels (embedding, norms, taps, sampling). With graphs on,
- * only the launches inside draft and verify passes are bracketed. *ms = summed event time of the
- * launches; *bytes = their algorithmic bytes for classes 0-2 (weights at 0.625 B (Q4_1) or 2 B (bf16)
- * per weight, fp32 activations in and products out), 0 for the others. Error DFL_E_INVALID_ARG for a
- * class outside 0..5. Synchronises the stream. */
+ * rotation and KV store, 5 = the row kernels (residual and norms, taps), embedding and sampling (the
+ * small state and copy kernels are not timed). A launch's time is its in-pass duration on the device
+ * clock: from the earliest of its CTAs past its dependency wait to the latest of its CTAs done, so the
+ * overlap of consecutive launches (programmatic dependent launch) is kept and the durations of a
+ * pass's launches add up to at most the pass. *ms = their sum; *bytes = the launches' algorithmic
+ * bytes for classes 0-2 (weights at 0.625 B (Q4_1) or 2 B (bf16) per weight, fp32 activations in and
+ * products out), 0 for the others. Error DFL_E_INVALID_ARG for a class outside 0..5. Synchronises the
+ * stream. */
 int dfl_profile_read(dfl_ctx *ctx, int cls, int64_t *launches, double *ms, double *bytes);
 
 const char *dfl_last_error(const dfl_ctx *ctx);
@@ -233,11 +266,33 @@ int dfl_act_pack(const float *dev_x, int M, int K, void *dev_act, void *cuda_str
 int64_t dfl_q41_gemm_scratch_bytes(int K, int N, int M);
 /* y[m][n] = sum_k x[m][k] * w[k][n] (fp32), x given as an activation operand buffer (DEVICE, from
  * dfl_act_pack), y fp32 DEVICE [M][N], from the tile image; M in 1..16; N a multiple of 32. The
- * scratch (DEVICE, >= dfl_q41_gemm_scratch_bytes) holds arrival counters (first N/32 ints) and partial
- * sums; it must be zeroed once before the first call (each call leaves the counters zero). Calls on
- * one scratch must not overlap on the GPU. A row's result does not depend on M. */
-int dfl_q41_gemm(const void *dev_image, int K, int N, const void *dev_act, int M, float *dev_y,
+ * scratch (DEVICE, 256-byte aligned, >= dfl_q41_gemm_scratch_bytes) holds an error word (its first 4
+ * bytes), arrival counters and partial sums; it must be zeroed once before the first call (each call
+ * leaves the counters zero). Calls on one scratch must not overlap on the GPU. A row's result does not
+ * depend on M. The call only enqueues; a bounded wait that gave up sets the error word (read it with
+ * dfl_q41_gemm_status) and leaves y undefined. */
+int dfl_q41_gemm(const void *dev_image, int K, int N, const void *act, int M, float *dev_y,
                  void *dev_scratch, size_t scratch_bytes, void *cuda_stream);
+/* Status of the products enqueued on a scratch so far: synchronises the stream, returns DFL_OK, or
+ * DFL_E_TIMEOUT (and clears the error word) when a bounded wait of one of them gave up. */
+int dfl_q41_gemm_status(const void *dev_scratch, void *cuda_stream);
+
+/* ---- the bf16 head on its own (the isolated sweep's bf16 2560 x 262144 comparison shape) ---------- */
+
+/* Bytes of the packed tile image of a bf16 K x N matrix (K a multiple of 64, N of 16). */
+int64_t dfl_bf16_image_bytes(int K, int N);
+/* Pack a bf16 matrix [N][K] (DEVICE, row n = output n) into the tile image (DEVICE). */
+int dfl_bf16_pack(const void *dev_src, int K, int N, void *dev_image, void *cuda_stream);
+/* Scratch bytes dfl_bf16_head_argmax needs. */
+int64_t dfl_bf16_head_scratch_bytes(int K, int N, int M);
+/* The head product of the step with its fused argmax (model card "Nemotron-3.5-Bolt-E4B-DFlash-NPU2",
+ * "How it is used": greedy proposals and target tokens are the first maximum of the logits):
+ * argmax[m] = the first n maximising sum_k x[m][k] * w[k][n] (DEVICE int32 [M]); logits (DEVICE fp32
+ * [M][N], nullable) receives the products themselves. Activations as for dfl_q41_gemm; the scratch
+ * (DEVICE, 256-byte aligned, zeroed once before the first call; each call leaves it reusable) must not
+ * be shared by calls that overlap on the GPU. */
+int dfl_bf16_head_argmax(const void *dev_image, int K, int N, const void *dev_act, int M, int32_t *dev_argmax,
+                         float *dev_logits, void *dev_scratch, size_t scratch_bytes, void *cuda_stream);
 
 /* The same product for callers that cannot allocate device memory per call and have no scratch
  * buffer of their own to pass: code that must keep every device allocation out of its call path (a
@@ -247,6 +302,8 @@ int dfl_q41_gemm(const void *dev_image, int K, int N, const void *dev_act, int M
  * Scratch: one array of dfl_q41_gemm_noalloc_max_scratch() bytes (4 MiB) in the library's static device
  * memory. The first call on a device looks up that device's copy of the array (cudaGetSymbolAddress,
  * with the device current) and caches its address; make that first call outside any stream capture.
+ * The cached address belongs to the device's context of that moment: after cudaDeviceReset (or any
+ * other teardown of the primary context) call dfl_q41_gemm_noalloc_reset before the next product.
  * No call allocates or frees memory. Every call on a device uses the same array and leaves the last
  * call's contents in it: the arrival counters at its start must be zero, which the zero-initialised
  * array gives and every completed call restores; calls that overlap on the GPU race on it.
@@ -257,6 +314,11 @@ int dfl_q41_gemm_noalloc(const void *dev_image, int K, int N, const void *dev_ac
                          void *cuda_stream);
 /* Bytes of the static scratch array behind dfl_q41_gemm_noalloc. */
 int64_t dfl_q41_gemm_noalloc_max_scratch(void);
+/* dfl_q41_gemm_status for the static array of the current device. */
+int dfl_q41_gemm_noalloc_status(void *cuda_stream);
+/* Look the current device's array up again and zero all of it (cudaMemsetAsync on the given stream):
+ * after a context teardown, or to start from a known state. Must not overlap a product on the GPU. */
+int dfl_q41_gemm_noalloc_reset(void *cuda_stream);
 
 #ifdef __cplusplus
 }

@@ -7,7 +7,8 @@ CPU-baseline and reference legs may import it. It shares no code with the CUDA p
 module both sides use is the seeded input generator `gen`, which holds none of the step's arithmetic.
 """
 from . import _native
-from ._native import bf16r, bf16_decode, half_decode, linear_bf16, linear_q41, q41_dequant, sample, uniform
+from ._native import (bf16r, bf16_decode, half_decode, linear_bf16, linear_q41, q41_dequant, sample, set_threads, threads,
+                      uniform)
 from .model import (Draft, Target, attend, keep_positions, kv_widths, ple_tail, positions_held, rmsnorm, rope, silu,
                     swiglu)
 from .spec import Pair, Run, Sampler, accept_length, plain_decode, spec_decode

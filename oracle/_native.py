@@ -43,6 +43,8 @@ def lib() -> ctypes.CDLL:
         L.orc_sample.argtypes = [f32p, ctypes.c_int, ctypes.c_double, ctypes.c_double,
                                  ctypes.POINTER(ctypes.c_double)]
         L.orc_sample.restype = ctypes.c_int
+        L.orc_set_threads.argtypes = [ctypes.c_int]
+        L.orc_threads.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -98,6 +100,15 @@ def linear_bf16(x, W) -> np.ndarray:
     y = np.empty((R, N), np.float32)
     lib().orc_linear_bf16(x, R, K, np.ascontiguousarray(W), N, y)
     return y
+
+
+def set_threads(n: int) -> None:
+    """Threads the products use (OpenMP over output columns; every result is the same for any count)."""
+    lib().orc_set_threads(int(n))
+
+
+def threads() -> int:
+    return int(lib().orc_threads())
 
 
 def uniform(seed: int, pos: int) -> float:

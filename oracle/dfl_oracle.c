@@ -20,6 +20,9 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ---- number formats ------------------------------------------------------------------------ */
 
@@ -164,6 +167,27 @@ static uint64_t splitmix64(uint64_t x)
 
 /* The uniform in [0, 1) drawn for the token at absolute position pos: the top 53 bits of
  * splitmix64(seed XOR (pos * golden gamma)), times 2^-53. */
+/* ---- exported: threads of the products (results do not depend on them) ----------------------- */
+
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int orc_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
 double orc_uniform(uint64_t seed, int64_t pos)
 {
     uint64_t z = splitmix64(seed ^ ((uint64_t)pos * 0x9E3779B97F4A7C15ULL));

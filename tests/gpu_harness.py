@@ -45,19 +45,25 @@ class Lockstep:
     accepted: list = field(default_factory=list)
 
 
-def lockstep(pc, W, prompt, n_gen, p=0.3, temperature=None, seed=3, eng=None, check_draft=True):
+def lockstep(pc, W, prompt, n_gen, p=0.3, temperature=None, seed=3, eng=None, check_draft=True, op=None):
     """Speculative decode on the GPU and in the oracle, pass by pass, with planted drafts at
-    corruption p (planted from the oracle's plain decode). Checks draft logits and proposals, verify
-    logits, target tokens, accepted lengths and positions held. A differing token is allowed only at a
-    near-tie; both sides then continue with the GPU's token."""
+    corruption p (planted from the oracle's plain decode of the same request). Checks draft logits and
+    proposals, verify logits, target tokens, accepted lengths and positions held. A differing token is
+    allowed only at a near-tie; both sides then continue with the GPU's token.
+    `prompt` is prefilled on top of whatever both sides already hold: a fresh pair, or (eng, op) in the
+    same state (a restored prefix snapshot)."""
     eng = eng or engine(pc, W)
     eng.dfl_set_option(DFL_OPT_KEEP_LOGITS, 1)
     sm = oracle.Sampler(temperature, seed)
-    plain = oracle.plain_decode(oracle.Pair(pc, W), prompt, n_gen, sm)
+    op = op or oracle.Pair(pc, W)
+    n0 = op.target.n
+    assert eng.dfl_positions_held() == n0
+    snap = op.snapshot()
+    plain = oracle.plain_decode(op, prompt, n_gen, sm)
+    op.restore(snap)
     G = np.zeros(pc.max_ctx + 32, np.int32)
-    G[len(prompt):len(prompt) + len(plain.tokens)] = plain.tokens
+    G[n0 + len(prompt):n0 + len(prompt) + len(plain.tokens)] = plain.tokens
     cor = gen.corruption(p, pc.target.vocab, pc.max_ctx + 32)
-    op = oracle.Pair(pc, W)
     B = pc.draft.block
     res = Lockstep()
     t_o, close = op.prefill(prompt, sm)
@@ -95,10 +101,10 @@ def lockstep(pc, W, prompt, n_gen, p=0.3, temperature=None, seed=3, eng=None, ch
                 res.near_ties += 1
         a_o = oracle.accept_length(rows[1:], list(tt_g[:-1]))
         assert a_g == a_o, f"accepted {a_g} vs {a_o} at n={n}"
-        emit = rows[1:1 + a_g] + [int(tt_g[a_g])]
-        emit = emit[: n_gen - len(tokens)]
-        eng.dfl_commit_verify_rows(len(emit))
-        op.target.commit(len(emit))
+        kept = eng.dfl_commit_accepted(n_gen - len(tokens))
+        emit = [int(v) for v in tt_g[:kept]]
+        assert kept == min(a_g + 1, n_gen - len(tokens))
+        op.target.commit(kept)
         res.passes += 1
         res.accepted.append(a_g)
         tokens += emit

@@ -68,3 +68,33 @@ def test_e4b_commit_and_next_pass(e4b):
     pair2.target.commit(3)
     lb = pair2.target.forward(nxt)
     check_logits(la, lb, "E4B next pass after commit(3)")
+
+
+def test_e4b_draft_alone_contexts(e4b):
+    """Config 3: the E4B draft on its own (5 layers, 32/8 heads of 128, window 1024, shared head of 262144)
+    over context rows made from N(0, 1) taps, at contexts of 30, 1024 and 4096 rows (the last wraps the
+    1024-slot context ring four times): draft logits and proposals against the oracle's draft."""
+    import torch
+    from gpu_harness import NEAR_TIE, check_logits
+    from dflash_speculative_decode_gb300 import DFL_OPT_KEEP_LOGITS, Engine, config_from_pair
+    import dataclasses
+    pc0, W, _ = e4b
+    pc = dataclasses.replace(pc0, max_ctx=4096 + 64)
+    eng = Engine(config_from_pair(pc))
+    eng.load(W)
+    eng.dfl_set_option(DFL_OPT_KEEP_LOGITS, 1)
+    taps = gen.fc_taps(4096, len(pc.draft.taps) * pc.target.hidden)
+    d = oracle.Draft(pc.draft, W, pc.target)
+    have = 0
+    for ctx, tok in ((30, 17), (1024, 4242), (4096, 262000)):
+        eng.dfl_draft_append_taps(torch.from_numpy(taps[have:ctx]).cuda())
+        d.append_ctx(taps[have:ctx])
+        have = ctx
+        assert eng.dfl_positions_held() == ctx == d.n_ctx
+        dp_g = eng.dfl_draft_block(tok)
+        dp_o, dl_o = d.block(tok, W["emb"], W["head"])
+        r, m = check_logits(eng.dfl_read_logits(1, 7), dl_o, f"draft alone at context {ctx}")
+        for i in range(7):
+            assert dp_g[i] == dp_o[i] or oracle.model.top2_gap(dl_o[i]) < NEAR_TIE
+        print(f"draft alone, context {ctx}: rel-L1 {r:.3g}, max-abs {m:.3g}")
+    eng.close()

@@ -270,3 +270,95 @@ def test_gpu_shared_layers_have_no_plane():
     # block makes them context, the position's taps (3 taps x 256 floats); sliding planes are rings of
     # fixed size and shared layers hold nothing
     assert b12 - b10 == 2 * (2 * 2 * 64 * 4) + 2 * (3 * 256 * 4)
+
+
+def test_bounded_wait_timeout_reports_and_recovers():
+    """The error path of the bounded waits, without a fault: with DFL_OPT_TEST_STALL the products' copy
+    warps issue nothing, the first product's waits give up after about a second, later products of the
+    pass skip their copies, and the verify returns DFL_E_TIMEOUT with positions held unchanged. With the
+    option off again the same verify gives the logits of a context that never failed."""
+    from dflash_speculative_decode_gb300 import DFL_OPT_KEEP_LOGITS, DflError
+    from dflash_speculative_decode_gb300._abi import DFL_E_TIMEOUT, DFL_OPT_TEST_STALL
+    from gpu_harness import engine
+    pc = gen.tiny_pair()
+    W = gen.generate(pc)
+    prompt = gen.prompt(pc.target.vocab, 20)
+    rows = [int(t) for t in gen.prompt(pc.target.vocab, 8, request=6)]
+    a = engine(pc, W)
+    a.dfl_set_option(DFL_OPT_KEEP_LOGITS, 1)
+    a.dfl_prefill(prompt)
+    a.dfl_set_option(DFL_OPT_TEST_STALL, 1)
+    with pytest.raises(DflError) as ei:
+        a.dfl_verify_block(rows)
+    assert ei.value.code == DFL_E_TIMEOUT
+    assert a.dfl_positions_held() == 20
+    with pytest.raises(DflError):
+        a.dfl_commit_verify_rows(1)            # nothing is pending after the failed verify
+    a.dfl_set_option(DFL_OPT_TEST_STALL, 0)
+    tt_a, acc_a = a.dfl_verify_block(rows)
+    la = a.dfl_read_logits(0, 8)
+    b = engine(pc, W)
+    b.dfl_set_option(DFL_OPT_KEEP_LOGITS, 1)
+    b.dfl_prefill(prompt)
+    tt_b, acc_b = b.dfl_verify_block(rows)
+    np.testing.assert_array_equal(la, b.dfl_read_logits(0, 8))
+    assert list(tt_a) == list(tt_b) and acc_a == acc_b
+    # the draft's context after a failed draft block is rebuilt: proposals as on the clean context
+    a.dfl_commit_verify_rows(3)
+    b.dfl_commit_verify_rows(3)
+    a.dfl_set_option(DFL_OPT_TEST_STALL, 1)
+    with pytest.raises(DflError) as ei:
+        a.dfl_draft_block(int(tt_a[2]))
+    assert ei.value.code == DFL_E_TIMEOUT
+    a.dfl_set_option(DFL_OPT_TEST_STALL, 0)
+    assert list(a.dfl_draft_block(int(tt_a[2]))) == list(b.dfl_draft_block(int(tt_b[2])))
+
+
+def test_standalone_product_status(torch_cuda):
+    """dfl_q41_gemm_status reads the scratch's error word: DFL_OK after products that completed."""
+    from dflash_speculative_decode_gb300 import _abi
+    K, N = 256, 384
+    rng = np.random.default_rng(3)
+    W = gen.pack_q41((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    x = gen.bf16_bits(rng.standard_normal((4, K)).astype(np.float32))
+    _, (img, scratch) = _gemm(torch_cuda, W, x, K, N)
+    st = ctypes.c_void_p(torch_cuda.cuda.current_stream().cuda_stream)
+    assert _abi.lib().dfl_q41_gemm_status(ctypes.c_void_p(scratch.data_ptr()), st) == _abi.DFL_OK
+
+
+@pytest.mark.parametrize("K,N,M", [(256, 2048, 7), (2560, 4096, 8), (512, 1024, 16), (2560, 262144, 8)])
+def test_bf16_head_argmax_matches_oracle(torch_cuda, K, N, M):
+    """The standalone head: logits within the fp32 bound of the exact products, and the first-maximum
+    argmax equal to the oracle's (or at a near-tie of the oracle's logits)."""
+    from dflash_speculative_decode_gb300 import _abi
+    from gpu_harness import NEAR_TIE
+    torch = torch_cuda
+    L = _abi.lib()
+    rng = np.random.default_rng(K + N + M)
+    Wb = gen.bf16_bits((rng.standard_normal((N, K)) * (2.0 / K ** 0.5)).astype(np.float32))
+    x = gen.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    dev = torch.device("cuda:0")
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    src = torch.from_numpy(Wb.reshape(-1).view(np.int16)).to(dev)
+    img = torch.empty(L.dfl_bf16_image_bytes(K, N), dtype=torch.uint8, device=dev)
+    assert L.dfl_bf16_pack(ctypes.c_void_p(src.data_ptr()), K, N, ctypes.c_void_p(img.data_ptr()), st) == 0
+    xf = torch.from_numpy(oracle.bf16_decode(x)).to(dev)
+    act = torch.empty(L.dfl_act_bytes(M, K), dtype=torch.uint8, device=dev)
+    assert L.dfl_act_pack(ctypes.c_void_p(xf.data_ptr()), M, K, ctypes.c_void_p(act.data_ptr()), st) == 0
+    sb = L.dfl_bf16_head_scratch_bytes(K, N, M)
+    scratch = torch.zeros(sb, dtype=torch.uint8, device=dev)
+    am = torch.full((M,), -1, dtype=torch.int32, device=dev)
+    lg = torch.empty((M, N), dtype=torch.float32, device=dev)
+    for _ in range(2):   # the scratch is reusable
+        assert L.dfl_bf16_head_argmax(ctypes.c_void_p(img.data_ptr()), K, N, ctypes.c_void_p(act.data_ptr()), M,
+                                      ctypes.c_void_p(am.data_ptr()), ctypes.c_void_p(lg.data_ptr()),
+                                      ctypes.c_void_p(scratch.data_ptr()), sb, st) == 0
+    torch.cuda.synchronize()
+    ref = oracle.linear_bf16(oracle.bf16_decode(x), Wb).astype(np.float64)
+    absdot = oracle.linear_bf16(np.abs(oracle.bf16_decode(x)), Wb & np.uint16(0x7FFF)).astype(np.float64)
+    bound = absdot * (K + 64) * 2.0 ** -24 + 1e-6
+    got = lg.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= bound)
+    for m, i in enumerate(am.cpu().numpy()):
+        j = int(np.argmax(ref[m]))
+        assert i == j or ref[m, j] - ref[m, i] < NEAR_TIE

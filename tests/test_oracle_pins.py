@@ -373,3 +373,18 @@ def test_ple_tail_order():
     assert np.abs(d1 - d2).max() > 1e-2
     # the token's per-layer row multiplies the gate: a zero row adds nothing
     np.testing.assert_array_equal(oracle.ple_tail(x, np.zeros_like(p_l), Wg, Wp, w, 1.0, eps), x)
+
+
+def test_products_do_not_depend_on_thread_count():
+    """The oracle's products split only independent output columns over threads: one thread and all
+    threads give the same bits (so the CPU baseline may use any count)."""
+    rng = np.random.default_rng(17)
+    W = gen.pack_q41((rng.standard_normal((96, 256)) * 0.02).astype(np.float32))
+    x = rng.standard_normal((3, 256)).astype(np.float32)
+    n = oracle.threads()
+    try:
+        oracle.set_threads(1)
+        a = oracle.linear_q41(x, W)
+    finally:
+        oracle.set_threads(n)
+    np.testing.assert_array_equal(a, oracle.linear_q41(x, W))
