@@ -36,11 +36,7 @@ namespace dfl {
 
 // compute warps of a product CTA: four column groups x kGemmPar chunk parities
 constexpr int kGemmWarps = 8, kGemmThreads = kGemmWarps * 32, kGemmPar = kGemmWarps / 4;
-// Two product CTAs fit on one SM (shared memory, registers), so the next product of a chain lands on the
-// SM while the current one still computes and streams its first weights in the meantime.
-constexpr int kGemmCtasPerSm = 2;
-constexpr int kGemmMaxRegs = 112;   // 2 CTAs x 9 warps x 32 lanes x 112 registers <= 65536
-static_assert(kGemmCtasPerSm * (kGemmWarps + 1) * 32 * kGemmMaxRegs <= 65536, "two product CTAs per SM");
+
 
 // ---------------------------------------------------------------------------------------------------
 // packing
@@ -145,7 +141,7 @@ cudaError_t launch_act_pack(const float *x, int M, int K, uint32_t *f, float *su
 //   sums:  at WB + MT * CP * 2048, 256 bytes per chunk ([4 groups][16 rows] fp32)
 // ---------------------------------------------------------------------------------------------------
 template <int FMT>
-__host__ __device__ constexpr int cpr() { return FMT == W_Q41 ? 4 : 2; }
+__host__ __device__ constexpr int cpr() { return FMT == W_Q41 ? 8 : 4; }
 template <int FMT>
 __host__ __device__ constexpr int xblock_bytes() { return cpr<FMT>() * 2048; }   // one row block of a round
 template <int MT>
@@ -156,7 +152,7 @@ template <int FMT, int MT>
 __host__ __device__ constexpr int slot_bytes() {
     return (8 * cpr<FMT>() * tile_bytes<FMT>() + MT * xblock_bytes<FMT>() + cpr<FMT>() * 256 + 127) / 128 * 128;
 }
-constexpr int kGemmSmemBudget = 110 * 1024;   // per CTA: two CTAs and their static shared memory per SM
+constexpr int kGemmSmemBudget = 224 * 1024;
 template <int FMT, int MT>
 __host__ __device__ constexpr int ring_slots() {
     return (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<FMT, MT>() < 6 ? (kGemmSmemBudget - red_bytes<MT>()) / slot_bytes<FMT, MT>() : 6;
@@ -357,7 +353,7 @@ constexpr int kGemmBlock = kGemmThreads + 32;   // + the copy warp
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kGemmThreads) : "memory"); }
 
 template <int FMT, int MT, int EPI>
-__global__ void __maxnreg__(kGemmMaxRegs) k_gemm(GemmArgs a) {
+__global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[8], empty[8];
     __shared__ int s_last, s_issued;
@@ -454,14 +450,16 @@ __global__ void __maxnreg__(kGemmMaxRegs) k_gemm(GemmArgs a) {
         }
         pdl_wait();
         pdl_trigger();
-        // the pass this launch belongs to has already failed: no more copies, rounds complete empty
-        const bool skip = a.skip_on_err && a.err && *reinterpret_cast<volatile int *>(a.err) != 0;
-        if (!a.stall || skip) {
+        // The pass this launch belongs to may have failed already: then no more copies are issued and the
+        // rounds complete empty. The flag's load is in flight while the prefetched rounds' activations go
+        // out (those copies are harmless either way).
+        const int errv = (a.skip_on_err && a.err) ? *reinterpret_cast<volatile int *>(a.err) : 0;
+        {
             Rd rx = r0;
-            for (int k2 = 0; k2 < k; ++k2, rd_next(rx)) {
-                if (skip) arrive_only(k2, 1);
-                else issue_x(rx, k2);
-            }
+            for (int k2 = 0; k2 < k; ++k2, rd_next(rx)) issue_x(rx, k2);
+        }
+        const bool skip = errv != 0;
+        if (!a.stall || skip) {
             for (; rd_valid(r); ++k, rd_next(r)) {
                 const int sl = k % S;
                 // once any wait of the CTA has given up, nothing more is issued

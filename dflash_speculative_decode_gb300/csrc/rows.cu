@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
     const int m = blockIdx.x;
     const int h = 4 * int(threadIdx.x);
     const bool on = h < a.H;
+    // the norm weights are immutable: their loads (often from HBM) go out before the dependency wait
+    const float4 wp4 = (on && a.w_post) ? bf16x4(a.w_post + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 wn4 = (on && a.w_next) ? bf16x4(a.w_next + h) : make_float4(0.f, 0.f, 0.f, 0.f);
     pdl_trigger();
     pdl_wait();
     stamp_ready(a.ps);
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
         if (on) y = a.yp.part ? part_sum4(a.yp, m, h) : *reinterpret_cast<const float4 *>(a.y + (long)m * a.ldy + h);
         if (on && a.y_out) *reinterpret_cast<float4 *>(a.y_out + (long)m * a.H + h) = y;
         if (a.w_post) {
-            const float4 w = on ? bf16x4(a.w_post + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 w = wp4;
             const float4 yw = make_float4(y.x * w.x, y.y * w.y, y.z * w.z, y.w * w.w);
             float4 v4 = make_float4((y.x * y.x + y.y * y.y) + (y.z * y.z + y.w * y.w),
                                     (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w),
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (on && live) {
             if (a.w_next) {
-                const float4 w = bf16x4(a.w_next + h);
+                const float4 w = wn4;
                 v = make_float4((x.x * r) * w.x, (x.y * r) * w.y, (x.z * r) * w.z, (x.w * r) * w.w);
             } else {
                 v = x;
@@ -313,17 +316,24 @@ cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const u
 // absolute position, from a (cos, sin) table computed in double precision. Keys and values are
 // stored into their plane slot (pos % cap), or into the block store (slot = row).
 __global__ void k_qk(QkArgs a) {
+    __shared__ float red[33];
+    const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.hd / 2;
+    // Immutable inputs go out before the dependency wait: the norm weights, and the rotation row of the
+    // row's position (the position counters were set before the pass began, and every kernel of the pass
+    // waits for its predecessor, so they are final here).
+    const int nqh0 = a.q_out ? a.nq : 0;
+    const uint16_t *w0 = h < nqh0 ? a.q_norm : a.k_norm;
+    const float wlo = bf16_to_f32(w0[i]), whi = bf16_to_f32(w0[i + half]);
+    const int pos = (a.pos_mode == 2 ? a.st->draft_n : a.st->n) + m;
+    const float2 cs = a.rope[(long)pos * half + i];
     pdl_trigger();
     pdl_wait();
-    __shared__ float red[33];
     stamp_ready(a.ps);
-    const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.hd / 2;
     const bool live = !a.live_from_ctx || m < a.st->ctx_rows;
     if (!live) {
         stamp_done(a.ps);
         return;
     }
-    const int pos = (a.pos_mode == 2 ? a.st->draft_n : a.st->n) + m;
     const int rr = a.row0 + m;
     // column c of this row of the product (plain rows or segment partials); kept for inspection
     auto val = [&](int c) -> float {
@@ -335,12 +345,10 @@ __global__ void k_qk(QkArgs a) {
     const bool is_q = h < nqh;
     const int hk = h - nqh;
     const int c0 = is_q ? h * a.hd : (a.nq + hk) * a.hd;
-    const uint16_t *w = is_q ? a.q_norm : a.k_norm;
     float u0 = val(c0 + i), u1 = val(c0 + i + half);
     const float r = 1.0f / sqrtf(block_sum(u0 * u0 + u1 * u1, red) / a.hd + a.eps);
-    u0 = (u0 * r) * bf16_to_f32(w[i]);
-    u1 = (u1 * r) * bf16_to_f32(w[i + half]);
-    const float2 cs = a.rope[(long)pos * half + i];
+    u0 = (u0 * r) * wlo;
+    u1 = (u1 * r) * whi;
     const float o0 = u0 * cs.x - u1 * cs.y, o1 = u0 * cs.y + u1 * cs.x;
     if (is_q) {
         float *q = a.q_out + ((long)m * a.nq + h) * a.hd;
