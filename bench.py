@@ -92,7 +92,22 @@ class Clocks:
 # ---------------------------------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------------------------------
+def cut_pair(max_ctx):
+    """A 12-layer cut of the E4B-shaped target (layers 8-11 KV-shared, vocabulary 32768) with the full
+    5-layer draft: the same kernels at the same per-layer shapes in about 2 GB (profiling captures)."""
+    import dataclasses
+    V = 32768
+    t = gen.e4b_target(n_layers=12, first_shared=8, vocab=V)
+    d = dataclasses.replace(gen.e4b_draft(vocab=V), taps=(1, 3, 5, 8, 11))
+    return gen.PairConfig(t, d, max_ctx=max_ctx)
+
+
 def e4b_workload(args):
+    if args.workload == "cut":
+        pc = cut_pair(args.ctx + args.gen + 64)
+        return pc, {"workload": f"e4b-cut (12 layers, vocab 32768) ctx {args.ctx} block 8 greedy, planted drafts "
+                                f"p={args.p}, {args.gen}-token decodes", "context": args.ctx,
+                    "note": "profiling workload, not the benchmark configuration"}
     pc = gen.e4b_pair(max_ctx=args.ctx + args.gen + 64)
     return pc, {"workload": f"e4b-pair ctx {args.ctx} block 8 greedy, planted drafts p={args.p}, "
                             f"{args.gen}-token decodes", "target": "42 layers hidden 2560 ffn 10240/20480 12x256 heads, "
@@ -225,7 +240,7 @@ def bench_cuda(args):
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     pc, cfgdesc = e4b_workload(args)
-    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "e4b"
     eng, W, t_load = load_engine(pc, keep=want_cpu)
     prompt = gen.prompt(pc.target.vocab, args.ctx)
     t0 = time.time()
@@ -521,7 +536,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm"])
+    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut"])
     ap.add_argument("--ctx", type=int, default=1024)
     ap.add_argument("--p", type=float, default=0.3)
     ap.add_argument("--gen", type=int, default=512, help="tokens per decode before restarting from the prefix")

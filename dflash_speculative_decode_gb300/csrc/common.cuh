@@ -66,10 +66,12 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     return r;
 }
 
-// D = A * B + D for one m16n8k16 bf16 tile, fp32 accumulate.
+// D = A * B + D for one m16n8k16 bf16 tile, fp32 accumulate. Not volatile: it has no effect beyond its
+// outputs, so the compiler may interleave independent products (callers also issue them so that
+// consecutive products feed different accumulators).
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
                  "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -236,11 +238,66 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return red[32];
 }
 
+// The segment partials a product launched with EPI_PART leaves: element (row m, column n) is the sum,
+// in segment order, of part[((n/32 * maxseg + s) * 16 + m) * 32 + n % 32] over the nseg segments of
+// quad q = n/128 (the CTAs whose unit ranges touch the quad's C chunks; the split of a grid of G CTAs
+// over U = quads * C units gives CTA b the units [b*U/G, (b+1)*U/G)).
+struct PartView {
+    const float *part;
+    int C, G, maxseg;
+    long U;
+};
+__host__ __device__ __forceinline__ long cta_of(long u, long U, int G) { return ((u + 1) * G - 1) / U; }
+
+// ---- row step arguments (row kernel, and products that finish their rows: EPI_ROWS) ------------------
+struct RowArgs {
+    int M, H;
+    float *x;              // fp32 residual [M][H]
+    const float *y;        // fp32 product [M][ldy] to add (nullable)
+    int ldy;
+    PartView yp;           // or the product as segment partials (yp.part non-null; takes precedence)
+    float *y_out;          // the product's rows as fp32 [M][H] (nullable; for inspection)
+    const uint16_t *w_post;   // RMSNorm weight applied to y before the add (nullable: plain add)
+    float lambda;          // multiply x after the add (1 = none)
+    float *tap;            // tap store base (nullable), row of position p at tap + p*ld_tap + tap_off
+    int ld_tap, tap_off;
+    const uint16_t *w_next;   // RMSNorm weight for the output (nullable: output = x)
+    uint32_t *outf;        // output rows in operand format with H inputs (nullable)
+    float *outs;           // their per-16 sums
+    int out_row0;          // first output row
+    float eps;
+    const DevState *st;
+    int pos_from_ctx;      // tap positions: 0 = st->n + m, 1 = st->draft_n + m
+    int rows_from_ctx;     // 1: only rows < st->ctx_rows are live (the rest are written as zeros)
+    Stamp ps;
+};
+
+struct QkArgs {
+    int M, nq, nkv, hd;
+    const float *qkv;      // fp32 [M][ldq] (q | k | v)
+    int ldq;
+    PartView qp;           // or the product as segment partials (qp.part non-null; takes precedence)
+    float *qkv_out;        // the product's rows as fp32 [.][ldq] (nullable; for inspection)
+    int row0;              // first row of qkv that belongs to this group of rows
+    const uint16_t *q_norm, *k_norm;
+    float eps;
+    const float2 *rope;    // (cos, sin) table [max_pos][hd/2]
+    const DevState *st;
+    int pos_mode;          // 0: st->n + m, 1: st->n + m (draft block), 2: st->draft_n + m (draft context)
+    int live_from_ctx;     // 1: only rows < st->ctx_rows are live
+    float *q_out;          // fp32 [M][nq][hd] (nullable: no query)
+    float *k_store, *v_store;      // [cap][nkv][hd] (nullable: no append)
+    int cap;               // ring capacity (slot = pos % cap)
+    Stamp ps;
+};
+
 // ---- GEMM interface ---------------------------------------------------------------------------------
 enum WFmt { W_Q41 = 0, W_BF16 = 1 };
 // EPI_PART: each CTA only writes its segment partial of every quad it touches (no fix-up); the
 // consumer adds the segments (PartView).
-enum Epi { EPI_F32 = 0, EPI_GLU = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3, EPI_PART = 4 };
+// EPI_ROWS: as EPI_PART, then the last CTAs to finish perform the row step (RowArgs) of the rows.
+// EPI_QK: as EPI_PART, then the last CTAs to finish perform the q/k steps (QkArgs) of the rows.
+enum Epi { EPI_F32 = 0, EPI_GLU = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3, EPI_PART = 4, EPI_ROWS = 5, EPI_QK = 6 };
 enum ArgmaxDst { AM_VERIFY = 0, AM_DRAFT = 1, AM_OUT = 2 };
 
 struct GemmArgs {
@@ -274,19 +331,14 @@ struct GemmArgs {
     int am_dst;            // AM_VERIFY: st->target[m] and st->accepted; AM_DRAFT: st->props[m];
                            // AM_OUT: am_out[m] (the standalone head)
     int *am_out;
+    // EPI_ROWS / EPI_QK
+    RowArgs row;           // the row step (row.yp: this launch's partials)
+    QkArgs qk[2];          // the q/k steps (qk[i].qp: this launch's partials), nqk of them
+    int nqk;
+    int *row_cnt;          // [2] arrivals and finished workers (zero between launches)
     Stamp ps;              // profiling stamp (ps.prof == nullptr: none)
 };
 
-// The segment partials a product launched with EPI_PART leaves: element (row m, column n) is the sum,
-// in segment order, of part[((n/32 * maxseg + s) * 16 + m) * 32 + n % 32] over the nseg segments of
-// quad q = n/128 (the CTAs whose unit ranges touch the quad's C chunks; the split of a grid of G CTAs
-// over U = quads * C units gives CTA b the units [b*U/G, (b+1)*U/G)).
-struct PartView {
-    const float *part;
-    int C, G, maxseg;
-    long U;
-};
-__host__ __device__ __forceinline__ long cta_of(long u, long U, int G) { return ((u + 1) * G - 1) / U; }
 __device__ __forceinline__ float part_sum(const PartView &v, int m, int n) {
     const int grp = n >> 5, q = grp >> 2;
     const long qa = (long)q * v.C;
@@ -320,27 +372,6 @@ inline size_t q41_image_bytes(int K, int N) { return size_t(N / 16) * (padded_k(
 inline size_t bf16_image_bytes(int K, int N) { return size_t(N / 16) * (padded_k(K) / 64) * 2048; }
 
 // ---- row and attention interfaces (rows.cu) ------------------------------------------------------
-struct RowArgs {
-    int M, H;
-    float *x;              // fp32 residual [M][H]
-    const float *y;        // fp32 product [M][ldy] to add (nullable)
-    int ldy;
-    PartView yp;           // or the product as segment partials (yp.part non-null; takes precedence)
-    float *y_out;          // the product's rows as fp32 [M][H] (nullable; for inspection)
-    const uint16_t *w_post;   // RMSNorm weight applied to y before the add (nullable: plain add)
-    float lambda;          // multiply x after the add (1 = none)
-    float *tap;            // tap store base (nullable), row of position p at tap + p*ld_tap + tap_off
-    int ld_tap, tap_off;
-    const uint16_t *w_next;   // RMSNorm weight for the output (nullable: output = x)
-    uint32_t *outf;        // output rows in operand format with H inputs (nullable)
-    float *outs;           // their per-16 sums
-    int out_row0;          // first output row
-    float eps;
-    const DevState *st;
-    int pos_from_ctx;      // tap positions: 0 = st->n + m, 1 = st->draft_n + m
-    int rows_from_ctx;     // 1: only rows < st->ctx_rows are live (the rest are written as zeros)
-    Stamp ps;
-};
 
 struct EmbedArgs {
     int M, H;
@@ -356,24 +387,6 @@ struct EmbedArgs {
     Stamp ps;
 };
 
-struct QkArgs {
-    int M, nq, nkv, hd;
-    const float *qkv;      // fp32 [M][ldq] (q | k | v)
-    int ldq;
-    PartView qp;           // or the product as segment partials (qp.part non-null; takes precedence)
-    float *qkv_out;        // the product's rows as fp32 [.][ldq] (nullable; for inspection)
-    int row0;              // first row of qkv that belongs to this group of rows
-    const uint16_t *q_norm, *k_norm;
-    float eps;
-    const float2 *rope;    // (cos, sin) table [max_pos][hd/2]
-    const DevState *st;
-    int pos_mode;          // 0: st->n + m, 1: st->n + m (draft block), 2: st->draft_n + m (draft context)
-    int live_from_ctx;     // 1: only rows < st->ctx_rows are live
-    float *q_out;          // fp32 [M][nq][hd] (nullable: no query)
-    float *k_store, *v_store;      // [cap][nkv][hd] (nullable: no append)
-    int cap;               // ring capacity (slot = pos % cap)
-    Stamp ps;
-};
 
 struct AttnArgs {
     int M, nq, nkv, hd;

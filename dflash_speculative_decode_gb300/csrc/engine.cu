@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "dfl.h"
+#include "rowstep.cuh"
 
 namespace dfl {
 size_t attn_smem(int M, int hd);
@@ -114,7 +115,7 @@ struct dfl_ctx {
     Act h, hcat, hb, o, a, z, tapbuf;
     float *kB = nullptr, *vB = nullptr;
     uint16_t *ple_rows = nullptr;
-    int *cnt = nullptr, *am_idx = nullptr, *am_cnt = nullptr, *smp_cnt = nullptr;
+    int *cnt = nullptr, *am_idx = nullptr, *am_cnt = nullptr, *smp_cnt = nullptr, *row_cnt = nullptr;
     int *counters_begin = nullptr;
     size_t counters_bytes = 0;
     int nq_max = 0, qkv_max = 0;
@@ -122,6 +123,7 @@ struct dfl_ctx {
     int n = 0, draft_n = 0, pending = 0, last_accepted = -1, draft_at = -1;
     int draft_n_ok = 0;       // draft_n as of the last call that read the device state without an error
     bool test_stall = false;  // test of the give-up path: the products of the next passes issue no copies
+    bool fuse_steps = false;  // the row and q/k steps run on the products' last CTAs (DFL_OPT_FUSE_STEPS)
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
     int last_k = 0;
     int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
@@ -350,6 +352,7 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     c->cnt = X.take<int>(cnt_n);
     c->am_cnt = X.take<int>(1);
     c->smp_cnt = X.take<int>(1);
+    c->row_cnt = X.take<int>(2);
     c->counters_begin = c->cnt;
     c->counters_bytes = X.off - cbeg;
 }
@@ -376,8 +379,13 @@ Stamp stamp(dfl_ctx *c, int cls, double bytes) {
 
 // y = x . W for M rows; EPI_F32 writes fp32 rows to y, EPI_GLU / EPI_SILU_MUL write `out` in operand format
 cudaError_t gemm(dfl_ctx *c, const QMat &W, const Act &x, int row0, int M, int epi, float *y, int ldy,
-                 const Act *out = nullptr, const uint16_t *ext = nullptr, int lde = 0) {
+                 const Act *out = nullptr, const uint16_t *ext = nullptr, int lde = 0, const RowArgs *row = nullptr,
+                 const QkArgs *qk0 = nullptr, const QkArgs *qk1 = nullptr) {
     GemmArgs a{};
+    if (row) a.row = *row;
+    if (qk0) a.qk[0] = *qk0, a.nqk = 1;
+    if (qk1) a.qk[1] = *qk1, a.nqk = 2;
+    a.row_cnt = c->row_cnt;
     a.img = W.img;
     a.K = W.K;
     a.C = W.C;
@@ -412,6 +420,41 @@ PartView part_view(const dfl_ctx *c, const QMat &W) {
     v.maxseg = W.maxseg;
     v.U = (long)((W.N / 32 + 3) / 4) * W.C;
     return v;
+}
+
+// a product whose last CTAs also perform the row step r of its rows (r.yp: this product's partials);
+// rows wider than the product's row step takes run the row kernel after the product instead
+cudaError_t gemm_rows(dfl_ctx *c, const QMat &W, const Act &x, int M, RowArgs r) {
+    r.yp = part_view(c, W);
+    if (c->fuse_steps && r.H <= kProductRowCols)
+        return gemm(c, W, x, 0, M, EPI_ROWS, nullptr, 0, nullptr, nullptr, 0, &r);
+    cudaError_t e = gemm(c, W, x, 0, M, EPI_PART, nullptr, 0);
+    if (e != cudaSuccess) return e;
+    r.ps = stamp(c, 5, 0.0);
+    c->launches += 1;
+    return launch_rows(r, c->stream);
+}
+
+// a q|k|v product whose last CTAs also perform the q/k steps q0 (and q1) of its rows
+cudaError_t gemm_qk(dfl_ctx *c, const QMat &W, const Act &x, int M, QkArgs q0, const QkArgs *q1 = nullptr) {
+    q0.qp = part_view(c, W);
+    QkArgs b{};
+    if (q1) {
+        b = *q1;
+        b.qp = q0.qp;
+    }
+    if (c->fuse_steps)
+        return gemm(c, W, x, 0, M, EPI_QK, nullptr, 0, nullptr, nullptr, 0, nullptr, &q0, q1 ? &b : nullptr);
+    cudaError_t e = gemm(c, W, x, 0, M, EPI_PART, nullptr, 0);
+    if (e != cudaSuccess) return e;
+    for (QkArgs *q : {&q0, q1 ? &b : nullptr}) {
+        if (!q) continue;
+        q->ps = stamp(c, 4, 0.0);
+        c->launches += 1;
+        e = launch_qk(*q, c->stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t head(dfl_ctx *c, const Act &x, int row0, int M, float *logits, int dst) {
@@ -568,7 +611,6 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         TLayer &O = c->tl[L.owner];
         const bool own = L.owner == l;
         const int nqkv = L.qkv.N;
-        DFL_CK(gemm(c, L.qkv, c->h, 0, k, EPI_PART, nullptr, 0));
         QkArgs qa{};
         qa.M = k;
         qa.nq = nq;
@@ -586,7 +628,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         qa.k_store = own ? L.K : nullptr;
         qa.v_store = own ? L.V : nullptr;
         qa.cap = L.cap;
-        DFL_LAUNCH_S(4, qa, launch_qk);
+        DFL_CK(gemm_qk(c, L.qkv, c->h, k, qa));   // its last CTAs norm, rotate and store q, k, v
         AttnArgs aa{};
         aa.M = k;
         aa.nq = nq;
@@ -605,37 +647,34 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_S(3, aa, launch_attn);
-        DFL_CK(gemm(c, L.o, c->o, 0, k, EPI_PART, nullptr, 0));
+        // each of the row steps below runs in the last CTAs of the product before it
         RowArgs r1 = rows(c, k, c->x);
-        r1.yp = part_view(c, L.o);
         r1.y_out = c->y;
         r1.w_post = L.post_attn_norm.p;
         r1.w_next = L.pre_ffn_norm.p;
         r1.outf = c->h.f;
         r1.outs = c->h.s;
-        DFL_LAUNCH_S(5, r1, launch_rows);
+        DFL_CK(gemm_rows(c, L.o, c->o, k, r1));
         DFL_CK(gemm(c, L.gu, c->h, 0, k, EPI_GLU, nullptr, 0, &c->a));
-        DFL_CK(gemm(c, L.d, c->a, 0, k, EPI_PART, nullptr, 0));
         const uint16_t *next = l + 1 < NL ? c->tl[l + 1].attn_norm.p : c->final_norm.p;
         int ti = 0;
         const bool tap = is_tap(g, l, &ti);
         RowArgs r2 = rows(c, k, c->x);
-        r2.yp = part_view(c, L.d);
         r2.y_out = c->y;
         r2.w_post = L.post_ffn_norm.p;
         r2.outf = c->h.f;
         r2.outs = c->h.s;
+        const QMat *last = &L.d;
         if (P) {
-            DFL_LAUNCH_S(5, r2, launch_rows);   // out = x: the gate's input
+            DFL_CK(gemm_rows(c, L.d, c->a, k, r2));   // out = x: the gate's input
             DFL_CK(gemm(c, L.pg, c->h, 0, k, EPI_SILU_MUL, nullptr, 0, &c->z, c->ple_rows + (size_t)l * P, NL * P));
-            DFL_CK(gemm(c, L.pp, c->z, 0, k, EPI_PART, nullptr, 0));
             r2 = rows(c, k, c->x);
-            r2.yp = part_view(c, L.pp);
             r2.y_out = c->y;
             r2.w_post = L.ple_norm.p;
             r2.lambda = L.lambda;
             r2.outf = c->h.f;
             r2.outs = c->h.s;
+            last = &L.pp;
         }
         r2.w_next = next;
         if (tap) {
@@ -643,7 +682,7 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
             r2.ld_tap = c->TH;
             r2.tap_off = ti * H;
         }
-        DFL_LAUNCH_S(5, r2, launch_rows);
+        DFL_CK(gemm_rows(c, *last, P ? c->z : c->a, k, r2));
     }
     if (do_head) {
         float *lg = (c->keep_logits || sampled) ? c->logits : nullptr;
@@ -711,7 +750,6 @@ int run_ctx_only(dfl_ctx *c, int r) {
     if (rc) return rc;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
-        DFL_CK(gemm(c, D.qkv, c->hcat, 0, kMaxRows, EPI_PART, nullptr, 0));
         QkArgs qa = draft_qk(c, l);
         qa.M = kMaxRows;
         qa.row0 = 0;
@@ -720,7 +758,7 @@ int run_ctx_only(dfl_ctx *c, int r) {
         qa.k_store = D.K;
         qa.v_store = D.V;
         qa.cap = c->cap_draft;
-        DFL_LAUNCH_S(4, qa, launch_qk);
+        DFL_CK(gemm_qk(c, D.qkv, c->hcat, kMaxRows, qa));
     }
     c->draft_n += r;
     return DFL_OK;
@@ -761,7 +799,6 @@ int draft_body(dfl_ctx *c) {
     const int dq = g.d_heads, dhd = g.d_head_dim;
     for (int l = 0; l < g.d_layers; ++l) {
         DLayer &D = c->dl[l];
-        DFL_CK(gemm(c, D.qkv, c->hcat, 0, B + F, EPI_PART, nullptr, 0));
         QkArgs qb = draft_qk(c, l);
         qb.M = B;
         qb.pos_mode = 1;
@@ -769,18 +806,15 @@ int draft_body(dfl_ctx *c) {
         qb.k_store = c->kB;
         qb.v_store = c->vB;
         qb.cap = 0;
-        DFL_LAUNCH_S(4, qb, launch_qk);
-        if (F > 0) {
-            QkArgs qc = draft_qk(c, l);
-            qc.M = F;
-            qc.row0 = B;
-            qc.pos_mode = 2;
-            qc.live_from_ctx = 1;
-            qc.k_store = D.K;
-            qc.v_store = D.V;
-            qc.cap = c->cap_draft;
-            DFL_LAUNCH_S(4, qc, launch_qk);
-        }
+        QkArgs qc = draft_qk(c, l);   // the fused context rows (after the block's rows)
+        qc.M = F;
+        qc.row0 = B;
+        qc.pos_mode = 2;
+        qc.live_from_ctx = 1;
+        qc.k_store = D.K;
+        qc.v_store = D.V;
+        qc.cap = c->cap_draft;
+        DFL_CK(gemm_qk(c, D.qkv, c->hcat, B + F, qb, F > 0 ? &qc : nullptr));
         AttnArgs aa{};
         aa.M = B;
         aa.nq = dq;
@@ -802,26 +836,22 @@ int draft_body(dfl_ctx *c) {
         aa.outf = c->o.f;
         aa.outs = c->o.s;
         DFL_LAUNCH_S(3, aa, launch_attn);
-        DFL_CK(gemm(c, D.o, c->o, 0, B, EPI_PART, nullptr, 0));
         RowArgs r1 = rows(c, B, c->x_d);
         r1.eps = g.d_eps;
-        r1.yp = part_view(c, D.o);
         r1.y_out = c->y;
         r1.w_next = D.ffn_norm.p;
         r1.outf = c->hb.f;
         r1.outs = c->hb.s;
-        DFL_LAUNCH_S(5, r1, launch_rows);
+        DFL_CK(gemm_rows(c, D.o, c->o, B, r1));
         DFL_CK(gemm(c, D.gu, c->hb, 0, B, EPI_GLU, nullptr, 0, &c->a));
-        DFL_CK(gemm(c, D.d, c->a, 0, B, EPI_PART, nullptr, 0));
         RowArgs r2 = rows(c, B, c->x_d);
         r2.eps = g.d_eps;
-        r2.yp = part_view(c, D.d);
         r2.y_out = c->y;
         r2.w_next = l + 1 < g.d_layers ? c->dl[l + 1].attn_norm.p : c->d_final_norm.p;
         const Act &nxt = l + 1 < g.d_layers ? c->hcat : c->hb;
         r2.outf = nxt.f;
         r2.outs = nxt.s;
-        DFL_LAUNCH_S(5, r2, launch_rows);
+        DFL_CK(gemm_rows(c, D.d, c->a, B, r2));
     }
     float *lg = c->keep_logits ? c->dlogits : nullptr;
     DFL_CK(head(c, c->hb, 1, B - 1, lg, AM_DRAFT));
@@ -853,6 +883,8 @@ int read_state(dfl_ctx *c, DevState *out) {
     DFL_CK(cudaStreamSynchronize(c->stream));
     if (out->err & kErrWaitTimeout) {
         DFL_CK(cudaMemsetAsync(&c->st->err, 0, sizeof(int), c->stream));
+        // a pass that gave up may leave arrival counters short of their reset: start them from zero
+        DFL_CK(cudaMemsetAsync(c->counters_begin, 0, c->counters_bytes, c->stream));
         DFL_CK(cudaStreamSynchronize(c->stream));
         c->draft_n = std::min(c->draft_n_ok, c->n);
         c->draft_n_ok = c->draft_n;
@@ -1260,6 +1292,14 @@ int dfl_set_option(dfl_ctx *c, int option, int value) {
         for (int i = 0; i < kProfClasses; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
     }
     else if (option == DFL_OPT_TEST_STALL) c->test_stall = value != 0;
+    else if (option == DFL_OPT_FUSE_STEPS) {
+        if ((value != 0) != c->fuse_steps) {
+            DFL_CK(cudaStreamSynchronize(c->stream));
+            for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second.exec);   // captured the other way
+            c->graphs.clear();
+            c->fuse_steps = value != 0;
+        }
+    }
     else if (option == DFL_OPT_ATTN_CLUSTER) {
         if (value != 4 && value != 8 && value != 16)
             return fail(c, DFL_E_INVALID_ARG, "attention cluster must be 4, 8 or 16");

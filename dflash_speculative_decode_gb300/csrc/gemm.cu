@@ -31,6 +31,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "rowstep.cuh"
 
 namespace dfl {
 
@@ -173,8 +174,7 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 // mma.m16n8k16 bf16 with a zero accumulator
 __device__ __forceinline__ void mma_bf16_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                            uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
@@ -217,25 +217,38 @@ __device__ __forceinline__ void q41_units(float (&acc)[2][MT][4], const uint8_t 
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
             const int ks = 2 * blk + kk;
+            uint4 b[NU][MT];
+            uint32_t A[NU][2][4];
 #pragma unroll
             for (int i = 0; i < NU; ++i) {
-                uint4 b[MT];
 #pragma unroll
                 for (int tt = 0; tt < MT; ++tt)
-                    b[tt] = *reinterpret_cast<const uint4 *>(slot + x_off + 2048 * kGemmPar * i + tt * XB + 512 * ks);
+                    b[i][tt] = *reinterpret_cast<const uint4 *>(slot + x_off + 2048 * kGemmPar * i + tt * XB + 512 * ks);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t w = ks == 0 ? nb[i][j].x : ks == 1 ? nb[i][j].y : ks == 2 ? nb[i][j].z : nb[i][j].w;
-                    const uint32_t a0 = nib_pair_bf16(w), a1 = nib_pair_bf16(w >> 4);
-                    const uint32_t a2 = nib_pair_bf16(w >> 8), a3 = nib_pair_bf16(w >> 12);
-#pragma unroll
-                    for (int tt = 0; tt < MT; ++tt) {
-                        if (kk == 0) mma_bf16_z(c[i][j][tt], a0, a1, a2, a3, b[tt].x, b[tt].y);
-                        else mma_bf16(c[i][j][tt], a0, a1, a2, a3, b[tt].x, b[tt].y);
-                        mma_bf16(c[i][j][tt], a0, a1, a2, a3, b[tt].z, b[tt].w);
-                    }
+                    A[i][j][0] = nib_pair_bf16(w), A[i][j][1] = nib_pair_bf16(w >> 4);
+                    A[i][j][2] = nib_pair_bf16(w >> 8), A[i][j][3] = nib_pair_bf16(w >> 12);
                 }
             }
+            // the hi products of every (unit, tile) first, then the lo products: consecutive products
+            // feed different accumulators
+#pragma unroll
+            for (int i = 0; i < NU; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int tt = 0; tt < MT; ++tt) {
+                        if (kk == 0) mma_bf16_z(c[i][j][tt], A[i][j][0], A[i][j][1], A[i][j][2], A[i][j][3], b[i][tt].x, b[i][tt].y);
+                        else mma_bf16(c[i][j][tt], A[i][j][0], A[i][j][1], A[i][j][2], A[i][j][3], b[i][tt].x, b[i][tt].y);
+                    }
+#pragma unroll
+            for (int i = 0; i < NU; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int tt = 0; tt < MT; ++tt)
+                        mma_bf16(c[i][j][tt], A[i][j][0], A[i][j][1], A[i][j][2], A[i][j][3], b[i][tt].z, b[i][tt].w);
         }
 #pragma unroll
         for (int i = 0; i < NU; ++i) {
@@ -276,8 +289,11 @@ __device__ __forceinline__ void bf16_unit(float (&acc)[2][MT][4], const uint8_t 
 #pragma unroll
         for (int tt = 0; tt < MT; ++tt) {
             mma_bf16(acc[0][tt], wa.x, wa.y, wa.z, wa.w, b[tt].x, b[tt].y);
-            mma_bf16(acc[0][tt], wa.x, wa.y, wa.z, wa.w, b[tt].z, b[tt].w);
             mma_bf16(acc[1][tt], wb.x, wb.y, wb.z, wb.w, b[tt].x, b[tt].y);
+        }
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt) {
+            mma_bf16(acc[0][tt], wa.x, wa.y, wa.z, wa.w, b[tt].z, b[tt].w);
             mma_bf16(acc[1][tt], wb.x, wb.y, wb.z, wb.w, b[tt].z, b[tt].w);
         }
     }
@@ -348,6 +364,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs &a, float (&acc)[2][MT][
 // to finish it (order of the segments). Every split depends on K, N and the grid only, so a row's result
 // never depends on how many rows the pass carries.
 constexpr int kGemmBlock = kGemmThreads + 32;   // + the copy warp
+static_assert(kGemmBlock == kProductRowThreads, "row step of the products");
 
 // barrier of the 16 compute warps only
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kGemmThreads) : "memory"); }
@@ -356,7 +373,7 @@ template <int FMT, int MT, int EPI>
 __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[8], empty[8];
-    __shared__ int s_last, s_issued;
+    __shared__ int s_last, s_issued, s_ticket;
     __shared__ volatile int s_bad;   // set by the first bounded wait that gives up
     constexpr int R = MT * 8;
     constexpr int TB = tile_bytes<FMT>();
@@ -560,8 +577,8 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     }
                     return v;
                 };
-                if (EPI == EPI_PART) {
-                    // the partial of every quad, the consumer adds the segments
+                if (EPI == EPI_PART || EPI == EPI_ROWS || EPI == EPI_QK) {
+                    // the partial of every quad, the consumer (or the row step below) adds the segments
                     for (int te = threadIdx.x; te < 4 * G4; te += kGemmThreads) {
                         const int gg = te / G4, e = te % G4;
                         if (4 * q + gg < ngroups)
@@ -624,7 +641,7 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
                     }
                     compute_sync();
                 }
-                const bool fin = EPI != EPI_PART && (nseg == 1 || s_last);
+                const bool fin = EPI != EPI_PART && EPI != EPI_ROWS && EPI != EPI_QK && (nseg == 1 || s_last);
                 const int ngq = 4 * q + gq;
                 if (fin && par == 0 && ngq < ngroups) {
 #pragma unroll
@@ -645,6 +662,64 @@ __global__ void __launch_bounds__(kGemmBlock, 1) k_gemm(GemmArgs a) {
         }
     }
     __syncthreads();   // every warp is done
+    if (EPI == EPI_ROWS || EPI == EPI_QK) {
+        // The steps that need whole rows of the product, by the last CTAs to finish: each CTA takes a
+        // ticket once its partials are out; a worker waits (bounded) until every CTA has taken one, then
+        // adds the segments it needs and applies its steps. EPI_ROWS: one row per worker (the row step);
+        // EPI_QK: one (row, head) per warp (the q/k steps). Every CTA of the grid is resident (one per
+        // SM, and no later kernel starts before all of them have), so the wait always ends.
+        __shared__ float red[33];
+        __shared__ float4 red4[33];
+        constexpr int kWarps = kGemmBlock / 32;
+        int tasks0 = 0, total = a.M;
+        if (EPI == EPI_QK) {
+            tasks0 = a.qk[0].M * qk_heads(a.qk[0]);
+            total = tasks0 + (a.nqk > 1 ? a.qk[1].M * qk_heads(a.qk[1]) : 0);
+        }
+        const int want = EPI == EPI_ROWS ? total : (total + kWarps - 1) / kWarps;
+        const int nw = G < want ? G : want;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_ticket = atomicAdd(a.row_cnt, 1);
+        __syncthreads();
+        const int w = s_ticket - (G - nw);
+        if (w >= 0) {
+            constexpr int PER = kProductRowPer;
+            float4 wp[PER], wn[PER];
+            if (EPI == EPI_ROWS) row_weights<PER>(a.row, wp, wn);   // in flight during the wait below
+            if (threadIdx.x == 0) {
+                const unsigned long long t0 = globaltimer_ns();
+                for (;;) {
+                    int seen;
+                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(a.row_cnt) : "memory");
+                    if (seen >= G) break;
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        s_bad = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            __syncthreads();
+            if (!s_bad) {
+                if (EPI == EPI_ROWS) {
+                    for (int m = w; m < a.M; m += nw) row_step<PER>(a.row, m, wp, wn, red, red4);
+                } else {
+                    for (int t = w * kWarps + warp; t < total; t += nw * kWarps) {
+                        const int which = t < tasks0 ? 0 : 1, tt = which ? t - tasks0 : t;
+                        const int heads = qk_heads(a.qk[which]);
+                        qk_task(a.qk[which], tt / heads, tt % heads, lane);
+                    }
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0 && atomicAdd(a.row_cnt + 1, 1) == nw - 1) {
+                a.row_cnt[0] = 0;   // every CTA has arrived and every worker is done
+                a.row_cnt[1] = 0;
+            }
+        }
+        __syncthreads();
+    }
     if (s_bad) {
         // A wait gave up: copies issued into a slot may still be in flight. Before the CTA exits, wait
         // (bounded again) for the last round issued into each slot; its phase completes only once
@@ -748,10 +823,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) k_head(GemmArgs a) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
 #pragma unroll
-                        for (int tt = 0; tt < MT; ++tt) {
+                        for (int tt = 0; tt < MT; ++tt)
                             mma_bf16(acc[j][tt], wv[j][ks].x, wv[j][ks].y, wv[j][ks].z, wv[j][ks].w, b[tt].x, b[tt].y);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int tt = 0; tt < MT; ++tt)
                             mma_bf16(acc[j][tt], wv[j][ks].x, wv[j][ks].y, wv[j][ks].z, wv[j][ks].w, b[tt].z, b[tt].w);
-                        }
                 }
                 if (u + P < units) load(u + P, w[p]);
                 if (c == a.C - 1) {
@@ -914,6 +992,8 @@ cudaError_t launch_gemm(int fmt, int epi, const GemmArgs &a, cudaStream_t s) {
     if (fmt == F && epi == E) return two ? run_gemm<F, 2, E>(a, s) : run_gemm<F, 1, E>(a, s);
     DFL_GEMM_CASE(W_Q41, EPI_F32)
     DFL_GEMM_CASE(W_Q41, EPI_PART)
+    DFL_GEMM_CASE(W_Q41, EPI_ROWS)
+    DFL_GEMM_CASE(W_Q41, EPI_QK)
     DFL_GEMM_CASE(W_Q41, EPI_GLU)
     DFL_GEMM_CASE(W_Q41, EPI_SILU_MUL)
     DFL_GEMM_CASE(W_BF16, EPI_F32)

@@ -9,6 +9,7 @@
 // "Nemotron-3.5-Bolt-E4B-DFlash-NPU2" (draft: Qwen3-style layers, window 1024, block of 8; "How it is
 // used": every position sampled and compared with the draft when a sampler is on).
 #include "common.cuh"
+#include "rowstep.cuh"
 
 namespace dfl {
 
@@ -126,144 +127,16 @@ inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int cl
 constexpr int kRowThreads = 256;   // k_cast_rows
 constexpr int kRowMaxPer = 16;     // k_cast_rows: hidden <= 4096
 
-__device__ __forceinline__ float4 bf16x4(const uint16_t *w) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(w);
-    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-                       __uint_as_float(u.y & 0xFFFF0000u));
-}
-
-// four consecutive inputs k..k+3 (k % 4 == 0) of row `tok` into the operand format; returns their hi+lo sum
-__device__ __forceinline__ float act_store4(uint32_t *f, int K, int tok, int k, float4 v) {
-    const float e[4] = {v.x, v.y, v.z, v.w};
-    uint32_t hw[2], lw[2];
-    float s = 0.f;
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const uint16_t h0 = f32_to_bf16(e[2 * p]), h1 = f32_to_bf16(e[2 * p + 1]);
-        const uint16_t l0 = f32_to_bf16(e[2 * p] - bf16_to_f32(h0)), l1 = f32_to_bf16(e[2 * p + 1] - bf16_to_f32(h1));
-        hw[p] = uint32_t(h0) | (uint32_t(h1) << 16);
-        lw[p] = uint32_t(l0) | (uint32_t(l1) << 16);
-        s += (bf16_to_f32(h0) + bf16_to_f32(l0)) + (bf16_to_f32(h1) + bf16_to_f32(l1));
-    }
-    // inputs r = k%16 .. r+3: pairs (r, r+1) and (r+2, r+3) sit in lane columns t = (r&7)/2 and t+1 of
-    // word w = r/8 (hi) and w+2 (lo)
-    const int r = k & 15, t = (r & 7) >> 1, w = r >> 3;
-    uint32_t *base = f + act_group(K, tok, k >> 4);
-    base[t * 4 + w] = hw[0];
-    base[t * 4 + w + 2] = lw[0];
-    base[(t + 1) * 4 + w] = hw[1];
-    base[(t + 1) * 4 + w + 2] = lw[1];
-    return s;
-}
-
-// the four consecutive columns n..n+3 of row m of an EPI_PART product
-__device__ __forceinline__ float4 part_sum4(const PartView &v, int m, int n) {
-    const int grp = n >> 5, q = grp >> 2;
-    const long qa = (long)q * v.C;
-    const int nseg = int(cta_of(qa + v.C - 1, v.U, v.G) - cta_of(qa, v.U, v.G)) + 1;
-    const float4 *p = reinterpret_cast<const float4 *>(v.part + ((size_t)grp * v.maxseg * kMaxRows + m) * 32 + (n & 31));
-    const size_t st = (size_t)kMaxRows * 32 / 4;
-    float4 l[16];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) l[s] = s < nseg ? __ldcg(p + s * st) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int s = 0; s < 16; ++s)
-        if (s < nseg) y.x += l[s].x, y.y += l[s].y, y.z += l[s].z, y.w += l[s].w;
-    for (int s = 16; s < nseg; ++s) {
-        const float4 e = __ldcg(p + s * st);
-        y.x += e.x, y.y += e.y, y.z += e.z, y.w += e.w;
-    }
-    return y;
-}
-
-// block-wide sum of four values at once (fixed order, as block_sum)
-__device__ __forceinline__ float4 block_sum4(float4 v, float4 *red4) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    v.x = warp_sum(v.x), v.y = warp_sum(v.y), v.z = warp_sum(v.z), v.w = warp_sum(v.w);
-    if (lane == 0) red4[w] = v;
-    __syncthreads();
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (w == 0) {
-        t = lane < nw ? red4[lane] : t;
-        t.x = warp_sum(t.x), t.y = warp_sum(t.y), t.z = warp_sum(t.z), t.w = warp_sum(t.w);
-        if (lane == 0) red4[32] = t;
-    }
-    __syncthreads();
-    return red4[32];
-}
-
 __global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
     __shared__ float red[33];
     __shared__ float4 red4[33];
-    const int m = blockIdx.x;
-    const int h = 4 * int(threadIdx.x);
-    const bool on = h < a.H;
     // the norm weights are immutable: their loads (often from HBM) go out before the dependency wait
-    const float4 wp4 = (on && a.w_post) ? bf16x4(a.w_post + h) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 wn4 = (on && a.w_next) ? bf16x4(a.w_next + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 wp[1], wn[1];
+    row_weights<1>(a, wp, wn);
     pdl_trigger();
     pdl_wait();
     stamp_ready(a.ps);
-    const bool live = !a.rows_from_ctx || m < a.st->ctx_rows;
-    float *xr = a.x ? a.x + (long)m * a.H : nullptr;
-    float4 x = (on && xr) ? *reinterpret_cast<const float4 *>(xr + h) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const bool have_y = a.yp.part || a.y;
-    // With a post-norm, the output norm's sum of squares is expanded so one block reduction gives both:
-    //   x' = lambda (x + r y w),  sum x'^2 = lambda^2 (sum x^2 + 2 r sum x y w + r^2 sum (y w)^2),
-    //   r = (sum y^2 / H + eps)^(-1/2).
-    float r_next = -1.f;   // the output norm's scale when it came out of the combined reduction
-    if (have_y) {
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (on) y = a.yp.part ? part_sum4(a.yp, m, h) : *reinterpret_cast<const float4 *>(a.y + (long)m * a.ldy + h);
-        if (on && a.y_out) *reinterpret_cast<float4 *>(a.y_out + (long)m * a.H + h) = y;
-        if (a.w_post) {
-            const float4 w = wp4;
-            const float4 yw = make_float4(y.x * w.x, y.y * w.y, y.z * w.z, y.w * w.w);
-            float4 v4 = make_float4((y.x * y.x + y.y * y.y) + (y.z * y.z + y.w * y.w),
-                                    (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w),
-                                    (x.x * yw.x + x.y * yw.y) + (x.z * yw.z + x.w * yw.w),
-                                    (yw.x * yw.x + yw.y * yw.y) + (yw.z * yw.z + yw.w * yw.w));
-            v4 = block_sum4(v4, red4);
-            const float r = 1.0f / sqrtf(v4.x / a.H + a.eps);
-            if (on) {
-                x.x += (y.x * r) * w.x, x.y += (y.y * r) * w.y, x.z += (y.z * r) * w.z, x.w += (y.w * r) * w.w;
-            }
-            if (a.w_next) {
-                const float ss = a.lambda * a.lambda * (v4.y + 2.f * r * v4.z + r * r * v4.w);
-                r_next = 1.0f / sqrtf(fmaxf(ss, 0.f) / a.H + a.eps);
-            }
-        } else {
-            x.x += y.x, x.y += y.y, x.z += y.z, x.w += y.w;
-        }
-    }
-    if (a.lambda != 1.0f) x.x *= a.lambda, x.y *= a.lambda, x.z *= a.lambda, x.w *= a.lambda;
-    if (on && xr && (have_y || a.lambda != 1.0f)) *reinterpret_cast<float4 *>(xr + h) = x;
-    if (on && a.tap && live) {
-        const int pos = (a.pos_from_ctx ? a.st->draft_n : a.st->n) + m;
-        *reinterpret_cast<float4 *>(a.tap + (long)pos * a.ld_tap + a.tap_off + h) = x;
-    }
-    if (a.outf) {
-        float r = 1.f;
-        if (a.w_next)
-            r = r_next >= 0.f ? r_next
-                              : 1.0f / sqrtf(block_sum((x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w), red) / a.H + a.eps);
-        const int row = a.out_row0 + m;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (on && live) {
-            if (a.w_next) {
-                const float4 w = wn4;
-                v = make_float4((x.x * r) * w.x, (x.y * r) * w.y, (x.z * r) * w.z, (x.w * r) * w.w);
-            } else {
-                v = x;
-            }
-        }
-        float hl = on ? act_store4(a.outf, a.H, row, h, v) : 0.f;
-        // four threads hold a 16-input group
-        hl += __shfl_xor_sync(0xffffffffu, hl, 1);
-        hl += __shfl_xor_sync(0xffffffffu, hl, 2);
-        if (on && (h & 15) == 0) a.outs[(h >> 4) * kMaxRows + row] = hl;
-    }
+    row_step<1>(a, blockIdx.x, wp, wn, red, red4);
     stamp_done(a.ps);
 }
 

@@ -200,7 +200,12 @@ int64_t dfl_positions_held(const dfl_ctx *ctx);
  * the partial softmax states are added, so logits may differ in the last bits); other values are
  * DFL_E_INVALID_ARG. Changing it drops the captured graphs. */
 enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3, DFL_OPT_PROFILE = 4,
-       DFL_OPT_ATTN_CLUSTER = 5, DFL_OPT_TEST_STALL = 6 };
+       DFL_OPT_ATTN_CLUSTER = 5, DFL_OPT_TEST_STALL = 6, DFL_OPT_FUSE_STEPS = 7 };
+/* DFL_OPT_FUSE_STEPS = 1 runs the row steps (residual, norms, layer scalar, taps) and the q/k steps
+ * (norm, rotation, KV store) on the last CTAs of the product that feeds them instead of as separate
+ * kernels (0, the default). Both give results within the parity tolerance of each other (the sums are
+ * taken in different orders); on the E4B-shaped pair the separate kernels are faster. Changing it drops
+ * the captured graphs. */
 /* DFL_OPT_TEST_STALL = 1 (tests of the error path only): the Q4_1 products of the following passes
  * issue no copies, so the first one's bounded waits give up after about a second and the call that reads
  * the device state returns DFL_E_TIMEOUT with the state unchanged; set it back to 0 and the context

@@ -362,3 +362,16 @@ def test_bf16_head_argmax_matches_oracle(torch_cuda, K, N, M):
     for m, i in enumerate(am.cpu().numpy()):
         j = int(np.argmax(ref[m]))
         assert i == j or ref[m, j] - ref[m, i] < NEAR_TIE
+
+
+def test_spec_decode_lockstep_fused_steps(pair):
+    """The same lockstep with the row and q/k steps run on the products' last CTAs (DFL_OPT_FUSE_STEPS)."""
+    from dflash_speculative_decode_gb300._abi import DFL_OPT_FUSE_STEPS
+    from gpu_harness import engine, lockstep
+    pc, W = pair
+    eng = engine(pc, W)
+    eng.dfl_set_option(DFL_OPT_FUSE_STEPS, 1)
+    res, plain = lockstep(pc, W, gen.prompt(pc.target.vocab, 32), 32, p=0.3, eng=eng)
+    if res.near_ties == 0:
+        assert res.tokens == [int(t) for t in plain.tokens]
+    assert res.max_rel_l1 < 1e-4
