@@ -6,7 +6,7 @@ ABI's names (`_abi`), and the decode loops a caller drives (`decode`).
 """
 from ._abi import (DFL_KEEP_ACCEPTED, DFL_OPT_GRAPHS, DFL_OPT_KEEP_LOGITS, DflError, Engine, config_from_pair,
                    dfl_config, lib)
-from .decode import Generation, plain_decode, spec_decode
+from .decode import Generation, PrefixCache, plain_decode, serve_single_turn, spec_decode
 
-__all__ = ["Engine", "DflError", "config_from_pair", "dfl_config", "lib", "plain_decode", "spec_decode", "Generation",
+__all__ = ["Engine", "DflError", "config_from_pair", "dfl_config", "lib", "plain_decode", "spec_decode", "Generation", "PrefixCache", "serve_single_turn",
            "DFL_KEEP_ACCEPTED", "DFL_OPT_KEEP_LOGITS", "DFL_OPT_GRAPHS"]

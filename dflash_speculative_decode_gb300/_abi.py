@@ -67,7 +67,7 @@ SIGNATURES = {
     "dfl_draft_block": (ctypes.c_int, [vp, ctypes.c_int32, i32p]),
     "dfl_verify_block": (ctypes.c_int, [vp, i32p, ctypes.c_int, P(dfl_sampling), i32p, i32p]),
     "dfl_commit_verify_rows": (ctypes.c_int, [vp, ctypes.c_int]),
-    "dfl_commit_accepted": (ctypes.c_int, [vp, ctypes.c_int, i32p]),
+    "dfl_commit_accepted": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int32, i32p, i32p]),
     "dfl_snapshot_bytes": (ctypes.c_int64, [vp]),
     "dfl_snapshot": (ctypes.c_int, [vp, vp, ctypes.c_size_t]),
     "dfl_restore": (ctypes.c_int, [vp, vp, ctypes.c_size_t]),
@@ -234,10 +234,13 @@ class Engine:
     def dfl_commit_verify_rows(self, keep: int):
         self._check(self.L.dfl_commit_verify_rows(self.ctx, int(keep)), "dfl_commit_verify_rows")
 
-    def dfl_commit_accepted(self, max_keep: int) -> int:
+    def dfl_commit_accepted(self, max_keep: int, stop_token: int = -1):
+        """Returns the rows kept; with a stop token, (kept, stopped)."""
         kept = np.zeros(1, np.int32)
-        self._check(self.L.dfl_commit_accepted(self.ctx, int(max_keep), _ptr(kept)), "dfl_commit_accepted")
-        return int(kept[0])
+        stopped = np.zeros(1, np.int32)
+        self._check(self.L.dfl_commit_accepted(self.ctx, int(max_keep), int(stop_token), _ptr(kept), _ptr(stopped)),
+                    "dfl_commit_accepted")
+        return int(kept[0]) if stop_token < 0 else (int(kept[0]), bool(stopped[0]))
 
     def dfl_snapshot_bytes(self) -> int:
         return int(self.L.dfl_snapshot_bytes(self.ctx))

@@ -122,6 +122,7 @@ struct dfl_ctx {
     // host mirror of the state
     int n = 0, draft_n = 0, pending = 0, last_accepted = -1, draft_at = -1;
     int draft_n_ok = 0;       // draft_n as of the last call that read the device state without an error
+    int32_t last_target[kMaxRows] = {};   // the target's tokens of the last verify
     bool test_stall = false;  // test of the give-up path: the products of the next passes issue no copies
     bool fuse_steps = false;  // the row and q/k steps run on the products' last CTAs (DFL_OPT_FUSE_STEPS)
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
@@ -1159,6 +1160,7 @@ int dfl_verify_block(dfl_ctx *c, const int32_t *rows_in, int k, const dfl_sampli
     c->pending = k;
     c->last_k = k;
     c->last_accepted = hs.accepted;
+    for (int i = 0; i < k; ++i) c->last_target[i] = hs.target[i];
     return DFL_OK;
 }
 
@@ -1173,13 +1175,24 @@ int dfl_commit_verify_rows(dfl_ctx *c, int keep) {
     return DFL_OK;
 }
 
-int dfl_commit_accepted(dfl_ctx *c, int max_keep, int32_t *kept) {
+int dfl_commit_accepted(dfl_ctx *c, int max_keep, int32_t stop_token, int32_t *kept, int32_t *stopped) {
     if (!c) return DFL_E_INVALID_ARG;
     if (!c->pending) return fail(c, DFL_E_STATE, "no pending verify");
     if (max_keep < 0) return fail(c, DFL_E_INVALID_ARG, "max_keep must be >= 0");
-    const int keep = std::min(std::min(c->last_accepted + 1, c->pending), max_keep);
+    int keep = std::min(std::min(c->last_accepted + 1, c->pending), max_keep);
+    int stop = 0;
+    if (stop_token >= 0)
+        for (int i = 0; i < keep; ++i)
+            if (c->last_target[i] == stop_token) {   // token i is emitted; the row it would feed is not kept
+                keep = i + 1;
+                stop = 1;
+                break;
+            }
     const int rc = dfl_commit_verify_rows(c, keep);
-    if (rc == DFL_OK && kept) *kept = keep;
+    if (rc == DFL_OK) {
+        if (kept) *kept = keep;
+        if (stopped) *stopped = stop;
+    }
     return rc;
 }
 

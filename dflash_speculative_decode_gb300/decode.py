@@ -62,3 +62,62 @@ def spec_decode(eng, prompt, n_gen: int, temperature=None, seed=0,
         g.targets.append(list(map(int, tt)))
         g.tokens += emit
     return g
+
+
+class PrefixCache:
+    """Pinned prefixes for single-turn serving: each is prefilled once into a context that starts empty,
+    and its committed state is kept as a device snapshot (dfl_snapshot). At most `slots` prefixes are kept;
+    the least recently used one is dropped first. Requests only ever restore a pin: nothing checkpoints
+    over it (FastFlowLM PR #899 "gemma4e-dflash-flash", "Changes": a re-checkpoint after prefill overwrote
+    the pinned system prefix, so repeated requests gave different answers)."""
+
+    def __init__(self, eng, slots: int = 1):
+        if slots < 1:
+            raise ValueError("slots must be >= 1")
+        self.eng, self.slots = eng, slots
+        self.empty = eng.dfl_snapshot()          # the context as created: no positions held
+        self.pins = {}                           # prefix tokens -> snapshot, in use order
+
+    def pin(self, prefix, temperature=None, seed=0):
+        key = tuple(int(t) for t in prefix)
+        if key in self.pins:
+            snap = self.pins.pop(key)
+        else:
+            if len(self.pins) >= self.slots:
+                self.pins.pop(next(iter(self.pins)))
+            self.eng.dfl_restore(self.empty)
+            self.eng.dfl_prefill(list(key), temperature, seed)
+            snap = self.eng.dfl_snapshot()
+        self.pins[key] = snap
+        return snap
+
+
+def serve_single_turn(eng, cache: PrefixCache, prefix, prompt, n_gen: int, stop_token=None, temperature=None,
+                      seed=0, propose: Optional[Callable[[int, np.ndarray], np.ndarray]] = None) -> Generation:
+    """One single-turn request: restore the pinned prefix, prefill the prompt, then speculative decode
+    until n_gen tokens or the stop token. The stop token is emitted but never fed back: no row of the
+    context holds it (dfl_commit_accepted with the stop token), and the request leaves no checkpoint."""
+    B = eng.cfg.block
+    stop = -1 if stop_token is None else int(stop_token)
+    eng.dfl_restore(cache.pin(prefix, temperature, seed))
+    t = eng.dfl_prefill(prompt, temperature, seed)
+    g = Generation(tokens=[t])
+    if t == stop:
+        return g
+    while len(g.tokens) < n_gen:
+        n = eng.dfl_positions_held()
+        last = g.tokens[-1]
+        dp = eng.dfl_draft_block(last)
+        props = np.asarray(propose(n, dp) if propose else dp, np.int32)[: B - 1]
+        rows = np.concatenate([[last], props]).astype(np.int32)
+        tt, a = eng.dfl_verify_block(rows, temperature=temperature, seed=seed)
+        kept, stopped = eng.dfl_commit_accepted(n_gen - len(g.tokens), stop) if stop >= 0 else \
+            (eng.dfl_commit_accepted(n_gen - len(g.tokens)), False)
+        g.held.append(n)
+        g.accepted.append(a)
+        g.proposals.append(list(map(int, dp)))
+        g.targets.append(list(map(int, tt)))
+        g.tokens += [int(v) for v in tt[:kept]]
+        if stopped:
+            break
+    return g

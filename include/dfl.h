@@ -163,8 +163,11 @@ int dfl_commit_verify_rows(dfl_ctx *ctx, int keep);
 /* The acceptance step's commit (model card "How it is used": the longest agreeing prefix plus one
  * target token are kept): keep min(accepted + 1, max_keep) rows of the pending verify, where max_keep
  * caps the tokens a caller still wants (a token budget), and write that count to *kept (if not NULL).
- * The kept rows' tokens are target_tok[0..*kept-1] of the verify. */
-int dfl_commit_accepted(dfl_ctx *ctx, int max_keep, int32_t *kept);
+ * The tokens the kept rows emit are target_tok[0..*kept-1] of the verify. With stop_token >= 0, a kept
+ * row whose token is the stop token ends the count there: that token is emitted, but no row for it is
+ * ever committed (single-turn serving, FastFlowLM PR #899 "gemma4e-dflash-flash", "Changes": no KV row
+ * for the stop token); *stopped (if not NULL) is then 1, else 0. */
+int dfl_commit_accepted(dfl_ctx *ctx, int max_keep, int32_t stop_token, int32_t *kept, int32_t *stopped);
 
 /* Snapshot (1bit engine PR "npu forward: Gemma4 verifies a draft in one batched pass", "What changes"
  * item 1: snapshot and restore cut each plane at its own layer's width; a KV-shared layer's plane stays

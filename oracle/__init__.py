@@ -11,7 +11,7 @@ from ._native import (bf16r, bf16_decode, half_decode, linear_bf16, linear_q41, 
                       uniform)
 from .model import (Draft, Target, attend, keep_positions, kv_widths, ple_tail, positions_held, rmsnorm, rope, silu,
                     swiglu)
-from .spec import Pair, Run, Sampler, accept_length, plain_decode, spec_decode
+from .spec import Pair, Run, Sampler, accept_length, plain_decode, serve_single_turn, spec_decode
 
 
 def build() -> str:

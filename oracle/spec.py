@@ -143,3 +143,37 @@ def spec_decode(pair: Pair, prompt, n_gen: int, sampler: Sampler,
         run.tokens += emit
     pair.sync_draft()
     return run
+
+
+def serve_single_turn(pair: Pair, pin, prompt, n_gen: int, sampler: Sampler, stop=None,
+                      propose: Optional[Callable[[int, List[int]], List[int]]] = None) -> Run:
+    """One single-turn request (FastFlowLM PR #899 "gemma4e-dflash-flash", "What" and "Changes"): restore
+    the pinned prefix snapshot `pin`, prefill the prompt, speculative decode until n_gen tokens or the stop
+    token. The stop token is emitted but never becomes a row of the context, and the request takes no
+    checkpoint of its own."""
+    B = pair.pc.draft.block
+    pair.restore(pin)
+    t, close = pair.prefill(prompt, sampler)
+    run = Run(tokens=[t], prefill_closeness=close)
+    if stop is not None and t == stop:
+        return run
+    while len(run.tokens) < n_gen:
+        n = pair.target.n
+        last = run.tokens[-1]
+        pair.sync_draft()
+        dp, _ = pair.draft.block(last, pair.W["emb"], pair.W["head"])
+        dprops = [int(v) for v in dp]
+        props = list(propose(n, dprops)) if propose else dprops
+        rows = [last] + props[: B - 1]
+        tt, cl, _ = pair.verify(rows, sampler)
+        a = accept_length(rows[1:], tt[:-1])
+        emit = (rows[1:1 + a] + [tt[a]])[: n_gen - len(run.tokens)]
+        if stop is not None and stop in emit:
+            emit = emit[: emit.index(stop) + 1]
+        pair.target.commit(len(emit))
+        run.steps.append(StepRecord(n, rows, tt, a, emit, cl, dprops))
+        run.tokens += emit
+        if stop is not None and emit[-1] == stop:
+            break
+    pair.sync_draft()
+    return run

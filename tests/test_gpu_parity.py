@@ -375,3 +375,63 @@ def test_spec_decode_lockstep_fused_steps(pair):
     if res.near_ties == 0:
         assert res.tokens == [int(t) for t in plain.tokens]
     assert res.max_rel_l1 < 1e-4
+
+
+def test_single_turn_serving_matches_oracle():
+    """Single-turn serving on tiny-shared (KV-shared layers with empty planes, PLE, two KV widths): a
+    prefix cache of two slots, requests P1:A, P2:B, P1:A, P1:B with a stop token, each against the
+    oracle restoring the same pinned prefix; positions held exclude the stop token's row."""
+    from dflash_speculative_decode_gb300 import PrefixCache, serve_single_turn
+    from gpu_harness import engine
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    V = pc.target.vocab
+    pre = {1: list(gen.prompt(V, 24, request=30)), 2: list(gen.prompt(V, 40, request=33))}
+    req = {"A": list(gen.prompt(V, 12, request=31)), "B": list(gen.prompt(V, 12, request=32))}
+    eng = engine(pc, W)
+    cache = PrefixCache(eng, slots=2)
+    pairs = {}
+    for p in pre:
+        pair = oracle.Pair(pc, W)
+        pair.prefill(pre[p], oracle.Sampler())
+        pairs[p] = (pair, pair.snapshot())
+    full = oracle.serve_single_turn(pairs[1][0], pairs[1][1], req["B"], 20, oracle.Sampler()).tokens
+    stop = int(full[7])
+    seen = {}
+    for p, name, st in ((1, "A", None), (2, "B", None), (1, "A", None), (1, "B", stop)):
+        got = serve_single_turn(eng, cache, pre[p], req[name], 20, stop_token=st)
+        ref = oracle.serve_single_turn(pairs[p][0], pairs[p][1], req[name], 20, oracle.Sampler(), stop=st)
+        assert got.tokens == [int(t) for t in ref.tokens], (p, name)
+        assert eng.dfl_positions_held() == pairs[p][0].target.n
+        seen.setdefault((p, name), got.tokens)
+        assert got.tokens == seen[(p, name)]
+    assert len(got.tokens) == [int(t) for t in full].index(stop) + 1
+
+
+@pytest.mark.parametrize("temperature", [None, 0.8])
+def test_pinned_prefix_requests_a_b_a_lockstep(temperature):
+    """tiny-shared (shared layers' planes empty, window 16 so the rings wrap within the prefix): the prefix
+    snapshot restored on both sides before each of requests A, B, A, then every pass of the request in
+    lockstep with the oracle (draft and verify logits, tokens, accepted lengths, positions held)."""
+    from gpu_harness import engine, lockstep
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    V = pc.target.vocab
+    prefix = gen.prompt(V, 48, request=40)
+    eng = engine(pc, W)
+    eng.dfl_prefill(prefix)
+    snap_g = eng.dfl_snapshot()
+    op = oracle.Pair(pc, W)
+    op.prefill(prefix, oracle.Sampler())
+    op.sync_draft()
+    snap_o = op.snapshot()
+    req = {"A": gen.prompt(V, 12, request=41), "B": gen.prompt(V, 12, request=42)}
+    out = []
+    for name in "ABA":
+        eng.dfl_restore(snap_g)
+        op.restore(snap_o)
+        res, plain = lockstep(pc, W, req[name], 20, p=0.3, temperature=temperature, seed=9, eng=eng, op=op)
+        if res.near_ties == 0:
+            assert res.tokens == [int(t) for t in plain.tokens]
+        out.append(res.tokens)
+    assert out[0] == out[2]

@@ -334,3 +334,55 @@ def test_ple_model_with_silent_tail_equals_ple_free_model():
     la = om.Target(t, W).forward(toks)
     lb = om.Target(t0, W).forward(toks)
     np.testing.assert_array_equal(la, lb)
+
+
+# ---- single-turn serving on a pinned prefix (FastFlowLM PR #899 "gemma4e-dflash-flash", "What" and
+# "Changes": system prompt pinned and reused; no re-checkpoint after prefill; no KV row for the stop token)
+def _pinned(pc, W, prefix):
+    pair = oracle.Pair(pc, W)
+    pair.prefill(prefix, oracle.Sampler())
+    return pair, pair.snapshot()
+
+
+def test_single_turn_requests_repeat_exactly():
+    """Requests A, B, A, B, A on one pinned prefix: every A gives the same tokens, every B too, and each
+    equals a fresh context that prefilled prefix + request. A server that re-checkpoints after each
+    request's prefill (the pages' bug) restores into a stale context and answers A differently."""
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    V = pc.target.vocab
+    prefix = list(gen.prompt(V, 24, request=30))
+    req = {"A": list(gen.prompt(V, 12, request=31)), "B": list(gen.prompt(V, 12, request=32))}
+    pair, pin = _pinned(pc, W, prefix)
+    out = {"A": [], "B": []}
+    for name in "ABABA":
+        out[name].append(oracle.serve_single_turn(pair, pin, req[name], 16, oracle.Sampler()).tokens)
+    for name in "AB":
+        assert all(o == out[name][0] for o in out[name])
+        fresh = oracle.plain_decode(oracle.Pair(pc, W), prefix + req[name], 16, oracle.Sampler())
+        assert [int(t) for t in out[name][0]] == [int(t) for t in fresh.tokens]
+    # the mutant: the pin is overwritten by each request's prefill
+    bad, pin2 = _pinned(pc, W, prefix)
+    for name in "AB":                      # each request's prefill taken as the new pin
+        bad.restore(pin2)
+        bad.prefill(req[name], oracle.Sampler())
+        pin2 = bad.snapshot()
+    bad_a = oracle.serve_single_turn(bad, pin2, req["A"], 16, oracle.Sampler()).tokens
+    assert bad_a != out["A"][0]
+
+
+def test_single_turn_stop_token_has_no_row():
+    """The stop token is emitted and ends the request; no row of the context holds it: positions held
+    = prefix + prompt + tokens before the stop token."""
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    V = pc.target.vocab
+    prefix = list(gen.prompt(V, 24, request=30))
+    prompt = list(gen.prompt(V, 12, request=31))
+    pair, pin = _pinned(pc, W, prefix)
+    full = oracle.serve_single_turn(pair, pin, prompt, 20, oracle.Sampler()).tokens
+    stop = int(full[9])
+    j = [int(t) for t in full].index(stop)
+    run = oracle.serve_single_turn(pair, pin, prompt, 20, oracle.Sampler(), stop=stop)
+    assert [int(t) for t in run.tokens] == [int(t) for t in full[: j + 1]]
+    assert pair.target.positions_held() == len(prefix) + len(prompt) + j
