@@ -190,7 +190,8 @@ def combine_ranks(torch, ms: float, toks: float, device) -> tuple:
 # ncu counted for one product launch of the same kernel source. The fraction dram/algorithmic of that
 # capture scales to the average launch of the step; it is reported only while the product kernel's
 # source still hashes to the value it had when the counters were taken.
-TRAFFIC_CAPTURE = None   # {"gemm_cu_sha16": ..., "dram_bytes": ..., "algorithmic_bytes": ..., "profile": ...}
+TRAFFIC_CAPTURE = {"gemm_cu_sha16": "89c08baea2d03c0f", "dram_bytes": 16513536, "algorithmic_bytes": 16793600,
+                   "profile": "profiles/k_gemm_q41_2560x10240_m8.md"}
 
 
 def _gemm_source_hash():
