@@ -7,7 +7,10 @@ calls (proposals copied in from host memory, proposals and target tokens copied 
 `roofline` reports the Q4_1 products (the dominant kernel) against the measured HBM copy bandwidth;
 `cpu_baseline` times the oracle on a bounded sample of the same workload.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference] [--workload e4b|gemm]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference] [--workload e4b|gemm|cut|27b]
+
+`--workload 27b` runs the same step on the 27B-class pair (62 dense layers of width 5376, 16 GB of Q4_1
+weights); `cut` is a 12-layer E4B cut for profiling captures; `gemm` the isolated product sweep.
 """
 from __future__ import annotations
 
@@ -103,6 +106,15 @@ def cut_pair(max_ctx):
 
 
 def e4b_workload(args):
+    if args.workload == "27b":
+        pc = gen.b27_pair(max_ctx=args.ctx + args.gen + 64)
+        return pc, {"workload": f"27b-pair ctx {args.ctx} block 8 greedy, planted drafts p={args.p}, "
+                                f"{args.gen}-token decodes", "target": "62 layers hidden 5376 ffn 21504 32/16x128 heads, "
+                                "5 sliding (window 1024) : 1 full, vocab 262144, Q4_1",
+                    "draft": "5 layers hidden 5376 ffn 10752 32/8x128, fc 5x5376", "context": args.ctx,
+                    "generated_per_decode": args.gen, "corruption_p": args.p,
+                    "note": "second workload (the 27B-class pair), not the benchmark configuration",
+                    "l2": "weights streamed per step (about 17 GB) exceed the 129 MB L2"}
     if args.workload == "cut":
         pc = cut_pair(args.ctx + args.gen + 64)
         return pc, {"workload": f"e4b-cut (12 layers, vocab 32768) ctx {args.ctx} block 8 greedy, planted drafts "
@@ -301,7 +313,8 @@ def bench_cuda(args):
     out = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "fp32 activations, Q4_1/bf16 weights",
-           "data": "synthetic (seeded random-init weights of the E4B-shaped pair, uniform prompt)",
+           "data": f"synthetic (seeded random-init weights of the {'27B-class' if args.workload == '27b' else 'E4B-shaped'}"
+                   " pair, uniform prompt)",
            "config": dict(cfgdesc, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
            "tokens_per_step": round(toks_all / world / args.steps, 3),
            "e2e": {"value": round(toks_e2e / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * pc.draft.block,
@@ -537,7 +550,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut"])
+    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b"])
     ap.add_argument("--ctx", type=int, default=1024)
     ap.add_argument("--p", type=float, default=0.3)
     ap.add_argument("--gen", type=int, default=512, help="tokens per decode before restarting from the prefix")

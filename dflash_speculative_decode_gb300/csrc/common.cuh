@@ -410,6 +410,7 @@ struct AttnArgs {
 struct SampleArgs {
     const float *logits;   // [M][V]
     int M, V, ld;
+    int row0;              // the pass row of logits row 0 (its token is for position n + row0 + 1)
     DevState *st;
     int *cnt;
     Stamp ps;

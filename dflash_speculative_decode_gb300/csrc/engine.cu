@@ -180,7 +180,7 @@ int fail(dfl_ctx *c, int code, const std::string &msg) {
 std::string validate(const dfl_config *g) {
     auto bad = [](const char *f) { return std::string("configuration: ") + f; };
     if (g->n_layers < 1 || g->n_layers > DFL_MAX_LAYERS) return bad("n_layers out of range 1..64");
-    if (g->hidden < 128 || g->hidden % 128 || g->hidden > 4096) return bad("hidden must be a multiple of 128, <= 4096");
+    if (g->hidden < 128 || g->hidden % 128 || g->hidden > 8192) return bad("hidden must be a multiple of 128, <= 8192");
     if (g->vocab < 16 || g->vocab % 16) return bad("vocab must be a multiple of 16");
     if (g->head_dim != 64 && g->head_dim != 128 && g->head_dim != 256) return bad("head_dim must be 64, 128 or 256");
     if (g->n_heads < 1 || (g->n_heads * g->head_dim) % 64) return bad("n_heads * head_dim must be a multiple of 64");
@@ -586,7 +586,8 @@ int set_state(dfl_ctx *c, int k, const int32_t *rows_in, bool draft_rows, int ct
 }
 
 // ---- target pass: k rows at positions n..n+k-1 ---------------------------------------------------------
-int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
+// head_last: the head (and sampling) for the last row only (a prefill chunk needs only its last token)
+int target_body(dfl_ctx *c, int k, bool do_head, bool sampled, bool head_last = false) {
     const dfl_config &g = c->cfg;
     const int H = g.hidden, NL = g.n_layers, hd = g.head_dim, nq = g.n_heads, P = g.ple_dim;
     EmbedArgs ea{};
@@ -687,11 +688,13 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
     }
     if (do_head) {
         float *lg = (c->keep_logits || sampled) ? c->logits : nullptr;
-        DFL_CK(head(c, c->h, 0, k, lg, AM_VERIFY));
+        const int hr0 = head_last ? k - 1 : 0, hm = head_last ? 1 : k;
+        DFL_CK(head(c, c->h, hr0, hm, lg, AM_VERIFY));
         if (sampled) {
             SampleArgs sa{};
             sa.logits = c->logits;
-            sa.M = k;
+            sa.M = hm;
+            sa.row0 = hr0;
             sa.V = g.vocab;
             sa.ld = g.vocab;
             sa.st = c->st;
@@ -703,11 +706,12 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled) {
 }
 
 // A target pass of k rows at positions n..n+k-1 (the device counters are set beforehand).
-int run_target(dfl_ctx *c, int k, bool do_head, bool sampled) {
+int run_target(dfl_ctx *c, int k, bool do_head, bool sampled, bool head_last = false) {
     const bool early = c->stop_layer >= 0 && c->stop_layer < c->cfg.n_layers - 1;
     const uint64_t key = (1ull << 40) | (uint64_t)k | (uint64_t)do_head << 8 | (uint64_t)sampled << 9 |
-                         (uint64_t)c->keep_logits << 10 | (uint64_t)(c->stop_layer + 1) << 12;
-    const int rc = run_graph(c, key, [&] { return target_body(c, k, do_head, sampled); });
+                         (uint64_t)c->keep_logits << 10 | (uint64_t)head_last << 11 |
+                         (uint64_t)(c->stop_layer + 1) << 12;
+    const int rc = run_graph(c, key, [&] { return target_body(c, k, do_head, sampled, head_last); });
     if (rc) return rc;
     if (do_head && !early) c->have_logits = c->keep_logits || sampled;
     return DFL_OK;
@@ -1097,7 +1101,7 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
         const int k = std::min(kMaxRows, n - done);
         const bool last = done + k == n;
         if ((rc = set_state(c, k, tokens + done, false, 0, -1, s))) return rc;
-        if ((rc = run_target(c, k, last, sampled))) return rc;
+        if ((rc = run_target(c, k, last, sampled, true))) return rc;
         c->n += k;
         done += k;
         last_k = k;
@@ -1110,8 +1114,8 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
         c->draft_n_ok = c->draft_n;
         return rc;
     }
-    if (next_tok) *next_tok = hs.target[last_k - 1];
-    c->last_k = last_k;
+    if (next_tok) *next_tok = hs.target[0];   // the head ran on the last row only
+    c->last_k = 1;                            // logits of that row
     c->draft_at = -1;
     return DFL_OK;
 }

@@ -125,24 +125,30 @@ inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int cl
 // are block sums in a fixed order, so the result does not depend on how many rows the pass carries.
 // ---------------------------------------------------------------------------------------------------
 constexpr int kRowThreads = 256;   // k_cast_rows
-constexpr int kRowMaxPer = 16;     // k_cast_rows: hidden <= 4096
+constexpr int kRowMaxPer = 32;     // k_cast_rows: hidden <= 8192
 
-__global__ void __launch_bounds__(1024) k_rows(RowArgs a) {
+// MAXT bounds the block so that PER slots a thread fit its registers without spilling
+template <int PER, int MAXT>
+__global__ void __launch_bounds__(MAXT) k_rows(RowArgs a) {
     __shared__ float red[33];
     __shared__ float4 red4[33];
     // the norm weights are immutable: their loads (often from HBM) go out before the dependency wait
-    float4 wp[1], wn[1];
-    row_weights<1>(a, wp, wn);
+    float4 wp[PER], wn[PER];
+    row_weights<PER>(a, wp, wn);
     pdl_trigger();
     pdl_wait();
     stamp_ready(a.ps);
-    row_step<1>(a, blockIdx.x, wp, wn, red, red4);
+    row_step<PER, 8 / PER>(a, blockIdx.x, wp, wn, red, red4);
     stamp_done(a.ps);
 }
 
+// One CTA per row: H/4 slots, one per thread up to hidden 4096, two up to 6144 (at most 768 threads),
+// three up to 8192 (at most 704 threads).
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
-    if (a.H % 128 || a.H / 4 > 1024 || a.M < 1 || a.M > kMaxRows) return cudaErrorInvalidValue;
-    return launch_pdl(k_rows, dim3(a.M), dim3(a.H / 4), 0, s, a);
+    if (a.H % 128 || a.H > 8192 || a.M < 1 || a.M > kMaxRows) return cudaErrorInvalidValue;
+    if (a.H <= 4096) return launch_pdl(k_rows<1, 1024>, dim3(a.M), dim3(a.H / 4), 0, s, a);
+    if (a.H <= 6144) return launch_pdl(k_rows<2, 768>, dim3(a.M), dim3((a.H / 8 + 31) / 32 * 32), 0, s, a);
+    return launch_pdl(k_rows<3, 704>, dim3(a.M), dim3((a.H / 12 + 31) / 32 * 32), 0, s, a);
 }
 
 // dst row (row0 + m) = RMSNorm(src[m], w) for live rows (m < st->ctx_rows when live_from_ctx), zeros
@@ -751,7 +757,7 @@ __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleArgs a) {
     }
     inc += before;
     const double excl = inc - s;
-    const int pos = a.st->n + m + 1;
+    const int pos = a.st->n + a.row0 + m + 1;
     const double u = (double)(splitmix64(a.st->seed ^ ((unsigned long long)pos * 0x9E3779B97F4A7C15ull)) >> 11) *
                      (1.0 / 9007199254740992.0);
     const double thr = u * total;

@@ -95,13 +95,13 @@ __device__ __forceinline__ void row_weights(const RowArgs &a, float4 (&wp)[PER],
 // the norm weights of the thread's slots (loaded by the caller, so their latency can hide behind a wait).
 // Every load of the thread's columns goes out in one batch before any is used. The row sums are block
 // sums in a fixed order: the result does not depend on how many rows the pass carries.
-template <int PER>
+// NSB: segments of each slot in the batch (more are added after it, in order).
+template <int PER, int NSB = 8>
 __device__ __forceinline__ void row_step(const RowArgs &a, int m, const float4 (&wp)[PER], const float4 (&wn)[PER],
                                          float *red, float4 *red4) {
     const bool live = !a.rows_from_ctx || m < a.st->ctx_rows;
     float *xr = a.x ? a.x + (long)m * a.H : nullptr;
     const bool have_y = a.yp.part || a.y;
-    constexpr int NSB = 8;   // segments in the batch (more are added after it, in order)
     float2 xa[PER], xb[PER], la[PER][NSB], lb[PER][NSB];
     float4 x[PER], y[PER];
     int ns[PER], ca[PER];

@@ -156,7 +156,39 @@ def e4b_pair(max_ctx: int = 2048) -> PairConfig:
     return PairConfig(e4b_target(), e4b_draft(), max_ctx=max_ctx, r_max=16)
 
 
-PAIRS = {"tiny": tiny_pair, "tiny-shared": tiny_shared_pair, "e4b": e4b_pair}
+def b27_target(n_layers: int = 62, vocab: int = 262144) -> TargetConfig:
+    """A 27B-class dense target: hidden 5376, 32 query heads of 128 over 16 key-value heads in every
+    layer, FFN 21504, five sliding layers (window 1024) to one full layer, no KV sharing and no PLE
+    (about 25.6e9 layer weights, 16 GB as Q4_1)."""
+    types = _layer_types_e4b(n_layers)
+    return TargetConfig(
+        name="27b", n_layers=n_layers, hidden=5376, vocab=vocab, n_heads=32, head_dim=128,
+        layer_type=types, kv_heads=(16,) * n_layers, kv_owner=tuple(range(n_layers)),
+        ffn=(21504,) * n_layers, window=1024)
+
+
+def b27_draft(vocab: int = 262144, taps: Tuple[int, ...] = (1, 16, 31, 46, 61)) -> DraftConfig:
+    """The draft for the 27B-class target: five layers at the target's width (32/8 heads of 128, FFN
+    twice the width), fusing five taps spread evenly over the target's depth."""
+    return DraftConfig(n_layers=5, hidden=5376, ffn=10752, n_heads=32, n_kv_heads=8, head_dim=128,
+                       window=1024, block=8, taps=taps, mask_token=vocab - 1)
+
+
+def b27_pair(max_ctx: int = 2048) -> PairConfig:
+    """The 27B-class pair: 62 dense target layers and the 5-layer draft, vocab 262144."""
+    return PairConfig(b27_target(), b27_draft(), max_ctx=max_ctx, r_max=16)
+
+
+def b27_cut(max_ctx: int = 256, n_layers: int = 6, vocab: int = 32768) -> PairConfig:
+    """Six layers of the 27B-class target (five sliding, one full) at full per-layer shapes with vocab
+    32768, and the full draft tapping layers 1..5: every product shape of the 27B pair at a size the
+    oracle runs in seconds."""
+    t = b27_target(n_layers=n_layers, vocab=vocab)
+    d = b27_draft(vocab=vocab, taps=tuple(range(1, n_layers)))
+    return PairConfig(t, d, max_ctx=max_ctx, r_max=16)
+
+
+PAIRS = {"tiny": tiny_pair, "tiny-shared": tiny_shared_pair, "e4b": e4b_pair, "27b": b27_pair}
 
 
 # ----------------------------------------------------------------------------------------------

@@ -127,7 +127,8 @@ int dfl_load_tensor(dfl_ctx *ctx, const char *name, const void *dev_src, size_t 
 /* Prefill (extend the context; 1bit engine PR "npu forward: Gemma4 verifies a draft in one batched
  * pass; KV row width per layer", "What changes" item 1, extend_context): run the n tokens at positions
  * held..held+n-1 in chunks of at most DFL_MAX_ROWS rows, commit them, bring the draft context up to date,
- * and write the target's token for the next position to *next_tok (greedy or sampled). Fails with
+ * and write the target's token for the next position to *next_tok (greedy or sampled). The output
+ * head runs on the last prompt row only: only that row's token is needed. Fails with
  * DFL_E_CAPACITY if held + n exceeds max_ctx; on any error positions held stay as they were. */
 int dfl_prefill(dfl_ctx *ctx, const int32_t *tokens, int n, const dfl_sampling *s, int32_t *next_tok);
 
@@ -216,8 +217,8 @@ enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3, DFL_
 int dfl_set_option(dfl_ctx *ctx, int option, int value);
 
 /* Copy the fp32 logits of the last pass (rows x vocab, row-major) to host memory. which = 0: the
- * last verify or prefill chunk (rows <= its k); which = 1: the last draft block (rows 1..block-1,
- * rows <= block-1). Needs DFL_OPT_KEEP_LOGITS. */
+ * last verify block (rows <= its k) or, after dfl_prefill, the last prompt row (rows = 1); which = 1:
+ * the last draft block (rows 1..block-1, rows <= block-1). Needs DFL_OPT_KEEP_LOGITS. */
 int dfl_read_logits(dfl_ctx *ctx, int which, float *host_dst, int rows);
 
 /* Copy the fp32 taps of positions pos0..pos0+rows-1 (n_taps*hidden each) to host memory. */
