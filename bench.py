@@ -529,6 +529,75 @@ def product_sweep(torch, shapes, rows, buf_bytes, pk, reps=100):
     return res
 
 
+# The Q4_1 product at many rows (prompt ingest) on the tcgen05 tensor cores: E4B and 27B-class shapes.
+PREFILL_SHAPES = [(2560, 10240), (10240, 2560), (2560, 4096), (5376, 43008), (21504, 5376)]
+
+
+def prefill_sweep(torch, shapes, rows, pk, reps=10):
+    """dfl_q41_gemm_tc per (shape, M), event-timed over `reps` back-to-back calls after 3 warm-up calls.
+    A call is three kernels: weight expansion to bf16 hi/lo, row split, the tcgen05 product. TFLOP/s
+    counts the product's 2 M N K; the tensor cores run three bf16 products for it (hi*hi, hi*lo,
+    lo*hi), reported against the measured dense bf16 peak as `tensor_frac`."""
+    import ctypes
+    from dflash_speculative_decode_gb300 import _abi
+    L = _abi.lib()
+    dev = torch.device("cuda:0")
+    st = torch.cuda.current_stream()
+    vp = ctypes.c_void_p
+    res = []
+    for K, N in shapes:
+        spec = gen.TensorSpec("sweep", "q41", (N, K), 0.02)
+        src = torch.from_numpy(gen.make_tensor(spec, seed=5).reshape(-1).view(np.uint8)).to(dev)
+        img = torch.empty(L.dfl_q41_image_bytes(K, N), dtype=torch.uint8, device=dev)
+        L.dfl_q41_pack(vp(src.data_ptr()), K, N, vp(img.data_ptr()), vp(st.cuda_stream))
+        del src
+        for M in rows:
+            x = torch.randn((M, K), generator=torch.Generator(device=dev).manual_seed(M), device=dev)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            sb = L.dfl_q41_gemm_tc_scratch_bytes(K, N, M)
+            scratch = torch.zeros(sb + 1024, dtype=torch.uint8, device=dev)
+            base = (scratch.data_ptr() + 1023) // 1024 * 1024
+
+            def once():
+                rc = L.dfl_q41_gemm_tc(vp(img.data_ptr()), K, N, vp(x.data_ptr()), M, vp(y.data_ptr()), vp(base),
+                                       sb, vp(st.cuda_stream))
+                assert rc == 0, rc
+            for _ in range(3):
+                once()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(reps):
+                once()
+            e1.record(st)
+            torch.cuda.synchronize()
+            assert L.dfl_q41_gemm_status(vp(base), vp(st.cuda_stream)) == 0
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+            res.append({"K": K, "N": N, "M": M, "us": round(us, 1), "TFLOP/s": round(tf, 1),
+                        "tensor_frac": round(3 * tf / pk["bf16_tflops"], 3),
+                        })
+            del scratch, x, y
+        del img
+        torch.cuda.empty_cache()
+    return res
+
+
+def bench_prefill(args):
+    """The large-M product on its own (prompt-ingest shapes), one JSON line."""
+    import torch
+    from dflash_speculative_decode_gb300 import build
+    build.build()
+    pk = peaks()
+    shapes = PREFILL_SHAPES
+    if args.gemm_shape:
+        shapes = [tuple(int(v) for v in args.gemm_shape.split("x"))]
+    rows = [int(v) for v in args.prefill_rows.split(",")]
+    res = prefill_sweep(torch, shapes, rows, pk)
+    print(json.dumps({"workload": "Q4_1 product at many rows (tcgen05), prompt-ingest shapes",
+                      "peak_bf16_tflops": pk["bf16_tflops"], "results": res}), flush=True)
+
+
 def bench_gemm(args):
     """Config 2 on its own: every shape of SWEEP_SHAPES (or --gemm-shape), rows --gemm-rows."""
     import torch
@@ -550,7 +619,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b"])
+    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b", "prefill"])
+    ap.add_argument("--prefill-rows", default="128,256,512,1024,2048", help="row counts of the prefill sweep")
     ap.add_argument("--ctx", type=int, default=1024)
     ap.add_argument("--p", type=float, default=0.3)
     ap.add_argument("--gen", type=int, default=512, help="tokens per decode before restarting from the prefix")
@@ -564,6 +634,8 @@ def main():
         return bench_reference(args)
     if args.workload == "gemm":
         return bench_gemm(args)
+    if args.workload == "prefill":
+        return bench_prefill(args)
     return bench_cuda(args)
 
 

@@ -90,6 +90,8 @@ SIGNATURES = {
     "dfl_q41_gemm_scratch_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "dfl_q41_gemm": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]),
     "dfl_q41_gemm_status": (ctypes.c_int, [vp, vp]),
+    "dfl_q41_gemm_tc_scratch_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "dfl_q41_gemm_tc": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]),
     "dfl_bf16_image_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int]),
     "dfl_bf16_pack": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
     "dfl_bf16_head_scratch_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),

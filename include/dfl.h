@@ -286,6 +286,27 @@ int dfl_q41_gemm(const void *dev_image, int K, int N, const void *act, int M, fl
  * DFL_E_TIMEOUT (and clears the error word) when a bounded wait of one of them gave up. */
 int dfl_q41_gemm_status(const void *dev_scratch, void *cuda_stream);
 
+/* ---- the Q4_1 product at many rows (prompt ingest) on the tcgen05 tensor cores -------------------- */
+
+/* Scratch bytes dfl_q41_gemm_tc needs for K, N, M (the weights expanded to bf16 hi + lo, N x Kp x 4
+ * bytes, and the rows split the same way, M x Kp x 4 bytes, Kp = K rounded up to 64, plus a 1 KiB
+ * header), or -1 for a shape it does not take (K and N multiples of 32 as for the tile image, M >= 1). */
+int64_t dfl_q41_gemm_tc_scratch_bytes(int K, int N, int M);
+/* y[m][n] = sum_k x[m][k] * w[k][n] for a Q4_1 tile image (DEVICE, dfl_q41_pack), fp32 rows x (DEVICE
+ * [M][K], row-major) and fp32 y (DEVICE [M][N], row-major). 1bit engine PR "npu forward: Gemma4
+ * verifies a draft in one batched pass", "What changes" item 1: a prompt goes through the layer
+ * products in chunks of rows; this is that product for chunks of hundreds of rows, where it is a
+ * dense contraction. w = d q + m is formed in fp32 and split into bf16 hi + lo, x likewise; the
+ * tensor cores add hi*hi + hi*lo + lo*hi in fp32, so y carries about the error of an fp32 dot
+ * product (it is not bit-identical to dfl_q41_gemm's). The scratch (DEVICE, 1024-byte aligned, >=
+ * dfl_q41_gemm_tc_scratch_bytes) starts with the error word of dfl_q41_gemm_status, which must be
+ * zero before the first call and reports (DFL_E_TIMEOUT) a bounded device wait that gave up, leaving
+ * y undefined. Calls on one scratch must not overlap on the GPU. The call only enqueues three kernels
+ * on the stream (weight expansion, row split, product). DFL_E_INVALID_ARG for a shape, pointer, size
+ * or alignment it rejects; DFL_E_CUDA when the tensor-map encoder is unavailable or a launch fails. */
+int dfl_q41_gemm_tc(const void *dev_image, int K, int N, const float *dev_x, int M, float *dev_y,
+                    void *dev_scratch, size_t scratch_bytes, void *cuda_stream);
+
 /* ---- the bf16 head on its own (the isolated sweep's bf16 2560 x 262144 comparison shape) ---------- */
 
 /* Bytes of the packed tile image of a bf16 K x N matrix (K a multiple of 64, N of 16). */
