@@ -37,7 +37,7 @@ class dfl_config(ctypes.Structure):
         ("block", ctypes.c_int32), ("n_taps", ctypes.c_int32), ("mask_token", ctypes.c_int32),
         ("taps", ctypes.c_int32 * MAX_TAPS),
         ("d_rope_base", ctypes.c_float), ("d_eps", ctypes.c_float), ("d_emb_scale", ctypes.c_float),
-        ("max_ctx", ctypes.c_int32),
+        ("max_ctx", ctypes.c_int32), ("prefill_rows", ctypes.c_int32),
     ]
 
 
@@ -127,8 +127,9 @@ class DflError(RuntimeError):
         self.code = code
 
 
-def config_from_pair(pc) -> dfl_config:
-    """dfl_config from a pair description (attributes as in the seeded generator's PairConfig)."""
+def config_from_pair(pc, prefill_rows: int = 0) -> dfl_config:
+    """dfl_config from a pair description (attributes as in the seeded generator's PairConfig);
+    prefill_rows > 0 lets dfl_prefill take that many prompt rows per pass on the tcgen05 products."""
     t, d = pc.target, pc.draft
     c = dfl_config()
     c.n_layers, c.hidden, c.vocab = t.n_layers, t.hidden, t.vocab
@@ -142,6 +143,7 @@ def config_from_pair(pc) -> dfl_config:
         c.taps[i] = l
     c.d_rope_base, c.d_eps, c.d_emb_scale = d.rope_base, d.eps, d.emb_scale
     c.max_ctx = pc.max_ctx
+    c.prefill_rows = prefill_rows
     return c
 
 

@@ -265,6 +265,7 @@ struct RowArgs {
     uint32_t *outf;        // output rows in operand format with H inputs (nullable)
     float *outs;           // their per-16 sums
     int out_row0;          // first output row
+    float *out32;          // or output rows as fp32 [M][H] (nullable)
     float eps;
     const DevState *st;
     int pos_from_ctx;      // tap positions: 0 = st->n + m, 1 = st->draft_n + m
@@ -378,7 +379,8 @@ struct EmbedArgs {
     const uint16_t *emb;   // bf16 [vocab][H]
     float scale;
     const DevState *st;
-    int use_draft;         // 0: tokens st->rows[m]; 1: draft block [st->last_tok, mask...]
+    int use_draft;         // 0: tokens st->rows[m] (or tokens[m]); 1: draft block [st->last_tok, mask...]
+    const int32_t *tokens; // row tokens [M] (nullable: st->rows)
     int mask_token;
     float *x;              // fp32 [M][H]
     const uint16_t *ple;   // bf16 [vocab][ple_w] (nullable)
@@ -402,8 +404,9 @@ struct AttnArgs {
     float scale;
     int *err;              // sticky error bits (nullable), kErrWaitTimeout
     int max_cluster;       // largest cluster size allowed (16, 8 or 4); the largest that fits is taken
-    uint32_t *outf;        // [M][nq*hd] in operand format
+    uint32_t *outf;        // [M][nq*hd] in operand format (M <= 16)
     float *outs;
+    float *out32;          // or fp32 [M][nq*hd]; then M may exceed 16 (tiles of 16 rows, grid y)
     Stamp ps;
 };
 
@@ -429,6 +432,14 @@ cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const u
                              cudaStream_t s);
 cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, uint32_t *dstf, cudaStream_t s);
 cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStream_t s);
+// fp32 rows of a long pass: out[m][j] = silu(y[m][j]) * y[m][F + j] (gate | up halves of a product row)
+cudaError_t launch_glu32(const float *y, int M, int F, float *out, cudaStream_t s);
+// out[m][j] = silu(y[m][j]) * e[m * lde + j] (bf16 e)
+cudaError_t launch_silu_mul32(const float *y, int M, int P, const uint16_t *e, int lde, float *out, cudaStream_t s);
+// the Q4_1 product of many fp32 rows on the tcgen05 tensor cores (tcgemm.cu); scratch 1024-byte aligned
+size_t tc_gemm_scratch_bytes(int K, int N, int M);
+cudaError_t launch_tc_gemm(const uint8_t *img, int K, int N, const float *x, int M, float *y, void *scratch,
+                           int *err, cudaStream_t s);
 
 // Launch with programmatic stream serialization (kernels begin with pdl_wait()).
 template <typename... KArgs, typename... Args>

@@ -119,6 +119,11 @@ struct dfl_ctx {
     int *counters_begin = nullptr;
     size_t counters_bytes = 0;
     int nq_max = 0, qkv_max = 0;
+    // a long prefill pass: its tokens, residual rows, two fp32 row buffers, PLE rows, product scratch
+    int32_t *pf_tok = nullptr;
+    float *pf_x = nullptr, *pf_a = nullptr, *pf_b = nullptr;
+    uint16_t *pf_ple = nullptr;
+    uint8_t *pf_scratch = nullptr;
     // host mirror of the state
     int n = 0, draft_n = 0, pending = 0, last_accepted = -1, draft_at = -1;
     int draft_n_ok = 0;       // draft_n as of the last call that read the device state without an error
@@ -211,6 +216,8 @@ std::string validate(const dfl_config *g) {
     if (g->mask_token < 0 || g->mask_token >= g->vocab) return bad("mask_token out of range");
     if (g->max_ctx < 1 || g->max_ctx > (1 << 20)) return bad("max_ctx out of range");
     if (!(g->eps > 0.f) || !(g->d_eps > 0.f)) return bad("eps must be > 0");
+    if (g->prefill_rows != 0 && (g->prefill_rows < 128 || g->prefill_rows > 8192 || g->prefill_rows % 16))
+        return bad("prefill_rows must be 0 or 128..8192, a multiple of 16");
     return {};
 }
 
@@ -230,7 +237,9 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     const int H = g.hidden, V = g.vocab, NL = g.n_layers, hd = g.head_dim, nq = g.n_heads, P = g.ple_dim;
     const int R = kMaxRows;
     c->TH = g.n_taps * H;
-    c->cap_sliding = g.window + R - 1;
+    const int PF = g.prefill_rows;
+    // a sliding ring holds the window of the first row of a pass plus the pass's own rows
+    c->cap_sliding = g.window + std::max(R, PF) - 1;
     c->cap_draft = g.d_window > 0 ? g.d_window : g.max_ctx + R;
     c->ctx_fuse = R - g.block;
     c->rope_rows = g.max_ctx + 2 * R;
@@ -347,6 +356,29 @@ void plan(dfl_ctx *c, Arena &W, Arena &S, Arena &X) {
     c->prof = X.take<unsigned long long>(2 * (size_t)kProfSlots);
     c->logits = X.take<float>((size_t)R * V);
     c->dlogits = X.take<float>((size_t)R * V);
+    // buffers of a long prefill pass (rows past 16; products on the tcgen05 tensor cores)
+    if (PF) {
+        int wmax = std::max(std::max(H, nq * hd), std::max(c->qkv_max, 2 * ffn_max));
+        wmax = std::max(wmax, P);
+        c->pf_tok = X.take<int32_t>(PF);
+        c->pf_x = X.take<float>((size_t)PF * H);
+        c->pf_a = X.take<float>((size_t)PF * wmax);
+        c->pf_b = X.take<float>((size_t)PF * wmax);
+        c->pf_ple = X.take<uint16_t>((size_t)PF * std::max(NL * P, 32));
+        size_t sb = 0;
+        for (int l = 0; l < NL; ++l) {
+            const TLayer &L = c->tl[l];
+            for (const QMat *m : {&L.qkv, &L.o, &L.gu, &L.d})
+                sb = std::max(sb, tc_gemm_scratch_bytes(m->K, m->N, PF));
+            if (P) {
+                sb = std::max(sb, tc_gemm_scratch_bytes(L.pg.K, L.pg.N, PF));
+                sb = std::max(sb, tc_gemm_scratch_bytes(L.pp.K, L.pp.N, PF));
+            }
+        }
+        uint8_t *raw = X.take<uint8_t>(sb + 1024);
+        c->pf_scratch = raw ? reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023))
+                            : nullptr;
+    }
     // counters that must read zero between launches, contiguous so one memset clears them
     X.off = (X.off + 255) / 256 * 256;
     const size_t cbeg = X.off;
@@ -701,6 +733,140 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled, bool head_last = 
             sa.cnt = c->smp_cnt;
             DFL_LAUNCH_S(5, sa, launch_sample);
         }
+    }
+    return DFL_OK;
+}
+
+// ---- a long prefill pass: k (> 16) prompt rows at positions n..n+k-1 -------------------------------------
+// Layer by layer over all k rows at once: the products on the tcgen05 tensor cores (tc_product), the
+// row steps, q/k steps and attention over fp32 rows (attention in tiles of 16 rows), the gates as
+// elementwise kernels. Sliding rings hold window + prefill_rows - 1 slots, so every row's window is
+// still in its plane while the pass's later rows are appended (also for layers that read another
+// layer's plane). The head runs on the last row only.
+cudaError_t tc_product(dfl_ctx *c, const QMat &W, const float *x, int k, float *y) {
+    c->launches += 3;   // weight expansion, row split, product
+    return launch_tc_gemm(W.img, W.K, W.N, x, k, y, c->pf_scratch, &c->st->err, c->stream);
+}
+
+int prefill_long(dfl_ctx *c, int k, bool do_head, bool sampled) {
+    const dfl_config &g = c->cfg;
+    const int H = g.hidden, NL = g.n_layers, hd = g.head_dim, nq = g.n_heads, P = g.ple_dim;
+    float *A = c->pf_a, *B = c->pf_b;   // two fp32 row buffers, alternately a step's input and output
+    EmbedArgs ea{};
+    ea.M = k;
+    ea.H = H;
+    ea.emb = c->emb.p;
+    ea.scale = g.emb_scale;
+    ea.st = c->st;
+    ea.tokens = c->pf_tok;
+    ea.x = c->pf_x;
+    ea.ple = P ? c->ple_table.p : nullptr;
+    ea.ple_w = NL * P;
+    ea.ple_out = c->pf_ple;
+    DFL_LAUNCH(launch_embed(ea, c->stream));
+    RowArgs r0 = rows(c, k, c->pf_x);
+    r0.w_next = c->tl[0].attn_norm.p;
+    r0.out32 = A;
+    DFL_LAUNCH(launch_rows(r0, c->stream));
+    for (int l = 0; l < NL; ++l) {
+        TLayer &L = c->tl[l];
+        TLayer &O = c->tl[L.owner];
+        const bool own = L.owner == l;
+        const int nqkv = L.qkv.N;
+        // attention block: A = normed rows
+        DFL_CK(tc_product(c, L.qkv, A, k, B));
+        QkArgs qa{};
+        qa.M = k;
+        qa.nq = nq;
+        qa.nkv = L.nkv;
+        qa.hd = hd;
+        qa.qkv = B;
+        qa.ldq = nqkv;
+        qa.q_norm = L.q_norm.p;
+        qa.k_norm = own ? L.k_norm.p : nullptr;
+        qa.eps = g.eps;
+        qa.rope = L.type == DFL_SLIDING ? c->rope_s : c->rope_f;
+        qa.st = c->st;
+        qa.q_out = A;
+        qa.k_store = own ? L.K : nullptr;
+        qa.v_store = own ? L.V : nullptr;
+        qa.cap = L.cap;
+        DFL_LAUNCH(launch_qk(qa, c->stream));
+        AttnArgs aa{};
+        aa.M = k;
+        aa.nq = nq;
+        aa.nkv = L.nkv;
+        aa.hd = hd;
+        aa.q = A;
+        aa.kA = O.K;
+        aa.vA = O.V;
+        aa.capA = O.cap;
+        aa.window = L.type == DFL_SLIDING ? g.window : 0;
+        aa.mode = 0;
+        aa.st = c->st;
+        aa.scale = 1.0f / sqrtf((float)hd);
+        aa.err = &c->st->err;
+        aa.max_cluster = c->attn_cluster;
+        aa.out32 = B;
+        DFL_LAUNCH(launch_attn(aa, c->stream));
+        DFL_CK(tc_product(c, L.o, B, k, A));
+        RowArgs r1 = rows(c, k, c->pf_x);
+        r1.y = A;
+        r1.ldy = H;
+        r1.w_post = L.post_attn_norm.p;
+        r1.w_next = L.pre_ffn_norm.p;
+        r1.out32 = B;
+        DFL_LAUNCH(launch_rows(r1, c->stream));
+        // FFN: B = normed rows
+        DFL_CK(tc_product(c, L.gu, B, k, A));
+        DFL_LAUNCH(launch_glu32(A, k, L.ffn, B, c->stream));
+        DFL_CK(tc_product(c, L.d, B, k, A));
+        const uint16_t *next = l + 1 < NL ? c->tl[l + 1].attn_norm.p : c->final_norm.p;
+        int ti = 0;
+        const bool tap = is_tap(g, l, &ti);
+        RowArgs r2 = rows(c, k, c->pf_x);
+        r2.y = A;
+        r2.ldy = H;
+        r2.w_post = L.post_ffn_norm.p;
+        r2.out32 = B;
+        if (P) {
+            DFL_LAUNCH(launch_rows(r2, c->stream));   // out = x: the gate's input
+            DFL_CK(tc_product(c, L.pg, B, k, A));
+            DFL_LAUNCH(launch_silu_mul32(A, k, P, c->pf_ple + (size_t)l * P, NL * P, B, c->stream));
+            DFL_CK(tc_product(c, L.pp, B, k, A));
+            r2 = rows(c, k, c->pf_x);
+            r2.y = A;
+            r2.ldy = H;
+            r2.w_post = L.ple_norm.p;
+            r2.lambda = L.lambda;
+            r2.out32 = B;
+        }
+        r2.w_next = next;
+        if (tap) {
+            r2.tap = c->taps;
+            r2.ld_tap = c->TH;
+            r2.tap_off = ti * H;
+        }
+        DFL_LAUNCH(launch_rows(r2, c->stream));
+        std::swap(A, B);   // the next layer's input (B) is A again
+    }
+    if (do_head) {
+        // the last row, final-normed, in the head's operand format
+        DFL_LAUNCH(launch_act_pack(A + (size_t)(k - 1) * H, 1, H, c->h.f, c->h.s, c->stream));
+        float *lg = (c->keep_logits || sampled) ? c->logits : nullptr;
+        DFL_CK(head(c, c->h, 0, 1, lg, AM_VERIFY));
+        if (sampled) {
+            SampleArgs sa{};
+            sa.logits = c->logits;
+            sa.M = 1;
+            sa.row0 = k - 1;
+            sa.V = g.vocab;
+            sa.ld = g.vocab;
+            sa.st = c->st;
+            sa.cnt = c->smp_cnt;
+            DFL_LAUNCH(launch_sample(sa, c->stream));
+        }
+        c->have_logits = c->keep_logits || sampled;
     }
     return DFL_OK;
 }
@@ -1096,15 +1262,24 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
     if ((rc = check_tokens(c, tokens, n))) return rc;
     const bool sampled = s && s->temperature > 0.f;
     const int n_start = c->n;
-    int done = 0, last_k = 0;
+    int done = 0;
+    const int PF = c->cfg.prefill_rows;
     while (done < n) {
-        const int k = std::min(kMaxRows, n - done);
+        // long passes while at least 128 rows remain (prefill_rows > 0), then passes of up to 16 rows
+        const bool longp = PF > 0 && n - done >= 128;
+        const int k = longp ? std::min(PF, n - done) : std::min(kMaxRows, n - done);
         const bool last = done + k == n;
         if ((rc = set_state(c, k, tokens + done, false, 0, -1, s))) return rc;
-        if ((rc = run_target(c, k, last, sampled, true))) return rc;
+        if (longp) {
+            if (cudaMemcpyAsync(c->pf_tok, tokens + done, sizeof(int32_t) * k, cudaMemcpyHostToDevice, c->stream) !=
+                cudaSuccess)
+                return fail(c, DFL_E_CUDA, "prefill token copy failed");
+            if ((rc = prefill_long(c, k, last, sampled))) return rc;
+        } else if ((rc = run_target(c, k, last, sampled, true))) {
+            return rc;
+        }
         c->n += k;
         done += k;
-        last_k = k;
     }
     if ((rc = catch_up(c, 0))) return rc;
     DevState hs;

@@ -57,7 +57,7 @@ __global__ void k_embed(EmbedArgs a) {
     pdl_wait();
     stamp_ready(a.ps);
     const int m = blockIdx.x;
-    const int tok = a.use_draft ? (m == 0 ? a.st->last_tok : a.mask_token) : a.st->rows[m];
+    const int tok = a.use_draft ? (m == 0 ? a.st->last_tok : a.mask_token) : a.tokens ? a.tokens[m] : a.st->rows[m];
     const uint16_t *e = a.emb + (long)tok * a.H;
     for (int h = threadIdx.x; h < a.H; h += blockDim.x) a.x[(long)m * a.H + h] = bf16_to_f32(e[h]) * a.scale;
     if (a.ple) {
@@ -99,10 +99,10 @@ __device__ __forceinline__ float ld_cluster(const float *p, unsigned rank) {
 }
 
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int cluster, int block, size_t smem,
+inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), dim3 grid, int cluster, int block, size_t smem,
                                       cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -145,7 +145,9 @@ __global__ void __launch_bounds__(MAXT) k_rows(RowArgs a) {
 // One CTA per row: H/4 slots, one per thread up to hidden 4096, two up to 6144 (at most 768 threads),
 // three up to 8192 (at most 704 threads).
 cudaError_t launch_rows(const RowArgs &a, cudaStream_t s) {
-    if (a.H % 128 || a.H > 8192 || a.M < 1 || a.M > kMaxRows) return cudaErrorInvalidValue;
+    // rows past 16 only with fp32 output (the operand format holds 16 rows)
+    if (a.H % 128 || a.H > 8192 || a.M < 1 || (a.M > kMaxRows && (a.outf || a.out_row0)) || a.M > 65535)
+        return cudaErrorInvalidValue;
     if (a.H <= 4096) return launch_pdl(k_rows<1, 1024>, dim3(a.M), dim3(a.H / 4), 0, s, a);
     if (a.H <= 6144) return launch_pdl(k_rows<2, 768>, dim3(a.M), dim3((a.H / 8 + 31) / 32 * 32), 0, s, a);
     return launch_pdl(k_rows<3, 704>, dim3(a.M), dim3((a.H / 12 + 31) / 32 * 32), 0, s, a);
@@ -321,9 +323,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     auto row_m = [](int r) { return HP == 1 ? r : (r & 7); };
     auto row_h = [unit](int r) { return HP == 1 ? unit : 2 * unit + (r >> 3); };
     // st->n was set before the pass began (every kernel of the pass waits for its predecessor), so it
-    // may be read before this kernel's own dependency wait
-    const int n = a.st->n;
-    const int M = a.M;
+    // may be read before this kernel's own dependency wait. A pass of more than 16 rows (fp32 output)
+    // is cut into tiles of 16 rows along grid y: tile y holds rows 16y.. at positions n + 16y + m.
+    const int n_pass = a.st->n;
+    const int row_base = kMaxRows * int(blockIdx.y);
+    const int n = n_pass + row_base;
+    const int M = min(a.M - row_base, kMaxRows);
     int lo, hi;   // inclusive range of plane positions any row may see
     if (a.mode == 0) {
         lo = a.window > 0 ? max(0, n - a.window + 1) : 0;
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     // blocks whose positions all precede the pass were written by earlier passes: they are immutable
     // here and are requested before the dependency wait (the pass's own rows come from the kernel
     // before this one)
-    auto early = [&](int i) { return a.mode == 0 && i < nAmine && kAttnKeys * (b0 + CL * i) + kAttnKeys <= n; };
+    auto early = [&](int i) { return a.mode == 0 && i < nAmine && kAttnKeys * (b0 + CL * i) + kAttnKeys <= n_pass; };
     int issued = 0;
     while (issued < kAttnBuf - 1 && issued < nmine && early(issued)) {
         load_block(issued, issued);
@@ -398,7 +403,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     for (int e = tid; e < kMaxRows * hd4; e += kAttnThreads) {
         const int r = e / hd4, d4 = e % hd4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row_m(r) < M) v = *reinterpret_cast<const float4 *>(a.q + ((long)row_m(r) * a.nq + row_h(r)) * hd + 4 * d4);
+        if (row_m(r) < M)
+            v = *reinterpret_cast<const float4 *>(a.q + ((long)(row_base + row_m(r)) * a.nq + row_h(r)) * hd + 4 * d4);
         *reinterpret_cast<float4 *>(Qs + r * ldq + 4 * d4) = v;
     }
     if (tid < kMaxRows) Mx[tid] = -INFINITY, Ls[tid] = 0.f, Sc[tid] = 0.f;
@@ -602,9 +608,13 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
     cluster_arrive();   // no reads of other CTAs' shared memory from here on
 #pragma unroll
     for (int k = 0; k < kRounds; ++k) {
-        const float hl = res_on[k] ? act_store(a.outf, a.nq * hd, res_m[k], res_col[k], res[k]) : 0.f;
-        const float sg = half_warp_sum(hl);   // every lane of the warp takes part
-        if (res_on[k] && (tid & 15) == 0) a.outs[(res_col[k] >> 4) * kMaxRows + res_m[k]] = sg;
+        if (a.out32) {
+            if (res_on[k]) a.out32[(long)(row_base + res_m[k]) * (a.nq * hd) + res_col[k]] = res[k];
+        } else {
+            const float hl = res_on[k] ? act_store(a.outf, a.nq * hd, res_m[k], res_col[k], res[k]) : 0.f;
+            const float sg = half_warp_sum(hl);   // every lane of the warp takes part
+            if (res_on[k] && (tid & 15) == 0) a.outs[(res_col[k] >> 4) * kMaxRows + res_m[k]] = sg;
+        }
     }
     cluster_wait();     // no CTA leaves while another still reads its shared memory
     stamp_done(a.ps);
@@ -678,12 +688,13 @@ template <int CL, int HP>
 static cudaError_t launch_attn_t(const AttnArgs &a, cudaStream_t s) {
     const cudaError_t e = attn_attrs<CL, HP>();
     if (e != cudaSuccess) return e;
-    return launch_cluster_pdl(k_attn<CL, HP>, a.nq / HP * CL, CL, kAttnThreads, attn_smem(a.hd), s, a);
+    const int tiles = (a.M + kMaxRows - 1) / kMaxRows;
+    return launch_cluster_pdl(k_attn<CL, HP>, dim3(a.nq / HP * CL, tiles), CL, kAttnThreads, attn_smem(a.hd), s, a);
 }
 
 cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
-    if (a.hd % 64 || a.hd < 64 || a.hd > 256 || a.M < 1 || a.M > kMaxRows || a.nB > kAttnKeys || a.nkv < 1 ||
-        a.nq % a.nkv)
+    if (a.hd % 64 || a.hd < 64 || a.hd > 256 || a.M < 1 || (a.M > kMaxRows && (!a.out32 || a.mode != 0)) ||
+        a.M > 65535 * kMaxRows || a.nB > kAttnKeys || a.nkv < 1 || a.nq % a.nkv)
         return cudaErrorInvalidValue;
     const bool pairs = (a.nq / a.nkv) % 2 == 0;   // two heads of one key/value group per CTA possible
     const int units = pairs ? a.nq / 2 : a.nq;    // clusters of a pass of up to 8 rows
@@ -696,6 +707,39 @@ cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
     if (cl == 16) return hp2 ? launch_attn_t<16, 2>(a, s) : launch_attn_t<16, 1>(a, s);
     if (cl == 8) return hp2 ? launch_attn_t<8, 2>(a, s) : launch_attn_t<8, 1>(a, s);
     return hp2 ? launch_attn_t<4, 2>(a, s) : launch_attn_t<4, 1>(a, s);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// Elementwise steps of a long pass on fp32 rows (a pass of 16 rows or fewer runs them in the products'
+// epilogues): the FFN's gate, and the per-layer-embedding gate.
+__global__ void k_glu32(const float *__restrict__ y, int M, int F, float *__restrict__ out) {
+    const long i = blockIdx.x * (long)blockDim.x + threadIdx.x;
+    if (i >= (long)M * F) return;
+    const long m = i / F;
+    const int j = int(i % F);
+    const float *r = y + m * 2 * F;
+    out[i] = silu_f(r[j]) * r[F + j];
+}
+
+__global__ void k_silu_mul32(const float *__restrict__ y, int M, int P, const uint16_t *__restrict__ e, int lde,
+                             float *__restrict__ out) {
+    const long i = blockIdx.x * (long)blockDim.x + threadIdx.x;
+    if (i >= (long)M * P) return;
+    const long m = i / P;
+    const int j = int(i % P);
+    out[i] = silu_f(y[i]) * bf16_to_f32(e[m * lde + j]);
+}
+
+cudaError_t launch_glu32(const float *y, int M, int F, float *out, cudaStream_t s) {
+    const long n = (long)M * F;
+    k_glu32<<<unsigned((n + 255) / 256), 256, 0, s>>>(y, M, F, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul32(const float *y, int M, int P, const uint16_t *e, int lde, float *out, cudaStream_t s) {
+    const long n = (long)M * P;
+    k_silu_mul32<<<unsigned((n + 255) / 256), 256, 0, s>>>(y, M, P, e, lde, out);
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------------------------------

@@ -199,7 +199,26 @@ __device__ __forceinline__ void row_step(const RowArgs &a, int m, const float4 (
         }
         xs += (x[i].x * x[i].x + x[i].y * x[i].y) + (x[i].z * x[i].z + x[i].w * x[i].w);
     }
-    if (a.outf) {
+    if (a.out32) {
+        float r = 1.f;
+        if (a.w_next) r = r_next >= 0.f ? r_next : 1.0f / sqrtf(block_sum(xs, red) / a.H + a.eps);
+        float *o = a.out32 + (long)m * a.H;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            if (!on[i]) continue;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (live) {
+                if (a.w_next) {
+                    const float4 w = wn[i];
+                    v = make_float4((x[i].x * r) * w.x, (x[i].y * r) * w.y, (x[i].z * r) * w.z, (x[i].w * r) * w.w);
+                } else {
+                    v = x[i];
+                }
+            }
+            *reinterpret_cast<float2 *>(o + ca[i]) = make_float2(v.x, v.y);
+            *reinterpret_cast<float2 *>(o + ca[i] + 8) = make_float2(v.z, v.w);
+        }
+    } else if (a.outf) {
         float r = 1.f;
         if (a.w_next) r = r_next >= 0.f ? r_next : 1.0f / sqrtf(block_sum(xs, red) / a.H + a.eps);
         const int row = a.out_row0 + m;

@@ -344,6 +344,48 @@ static bool tc_shape_ok(int K, int N, int M) {
     return K >= 32 && K % 32 == 0 && N >= 32 && N % 32 == 0 && M >= 1 && M <= (1 << 20) && (long)K * N < (1L << 31);
 }
 
+size_t tc_gemm_scratch_bytes(int K, int N, int M) { return tc_shape_ok(K, N, M) ? tc_scratch(K, N, M).total : 0; }
+
+// Expand the weights, split the rows and run the product (three launches on s). The scratch's first
+// 1024 bytes are not used here (the entry point keeps its error word there).
+cudaError_t launch_tc_gemm(const uint8_t *img, int K, int N, const float *x, int M, float *y, void *scratch,
+                           int *err, cudaStream_t s) {
+    if (!tc_shape_ok(K, N, M) || !img || !x || !y || !scratch || (reinterpret_cast<uintptr_t>(scratch) & 1023))
+        return cudaErrorInvalidValue;
+    const TcScratch ts = tc_scratch(K, N, M);
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    const int Kp = padded_k(K), C = Kp / 64;
+    uint8_t *base = static_cast<uint8_t *>(scratch);
+    uint16_t *wh = reinterpret_cast<uint16_t *>(base + 1024);
+    uint16_t *wl = reinterpret_cast<uint16_t *>(base + 1024 + ts.wbytes);
+    uint16_t *xh = reinterpret_cast<uint16_t *>(base + 1024 + 2 * ts.wbytes);
+    uint16_t *xl = reinterpret_cast<uint16_t *>(base + 1024 + 2 * ts.wbytes + ts.xbytes);
+    CUtensorMap mwh, mwl, mxh, mxl;
+    if (!bf16_map(&mwh, wh, N, Kp) || !bf16_map(&mwl, wl, N, Kp) || !bf16_map(&mxh, xh, M, Kp) ||
+        !bf16_map(&mxl, xl, M, Kp))
+        return cudaErrorInvalidValue;
+    static bool attr[kMaxDevices] = {};
+    if (!attr[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        if (e != cudaSuccess) return e;
+        attr[dev] = true;
+    }
+    const long wthreads = (long)(N / 16) * C * 32;
+    k_tc_dequant<<<unsigned((wthreads + 255) / 256), 256, 0, s>>>(img, N, C, wh, wl);
+    const long xpairs = (long)M * Kp / 2;
+    k_tc_split<<<unsigned((xpairs + 255) / 256), 256, 0, s>>>(x, M, K, Kp, xh, xl);
+    TcArgs a;
+    a.M = M;
+    a.N = N;
+    a.stages = C;
+    a.y = y;
+    a.err = err;
+    const dim3 grid((N + kTcM - 1) / kTcM, (M + kTcN - 1) / kTcN);
+    k_tc_gemm<<<grid, kTcThreads, kTcSmem, s>>>(mwh, mwl, mxh, mxl, a);
+    return cudaGetLastError();
+}
+
 }  // namespace dfl
 
 using namespace dfl;
@@ -358,40 +400,11 @@ int64_t dfl_q41_gemm_tc_scratch_bytes(int K, int N, int M) {
 int dfl_q41_gemm_tc(const void *img, int K, int N, const float *x, int M, float *y, void *scratch,
                     size_t scratch_bytes, void *stream) {
     if (!tc_shape_ok(K, N, M) || !img || !x || !y || !scratch) return DFL_E_INVALID_ARG;
-    const TcScratch ts = tc_scratch(K, N, M);
-    if (scratch_bytes < ts.total || (reinterpret_cast<uintptr_t>(scratch) & 1023)) return DFL_E_INVALID_ARG;
-    const int dev = current_device();
-    if (dev < 0) return DFL_E_CUDA;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int Kp = padded_k(K), C = Kp / 64;
-    uint8_t *base = static_cast<uint8_t *>(scratch);
-    uint16_t *wh = reinterpret_cast<uint16_t *>(base + 1024);
-    uint16_t *wl = reinterpret_cast<uint16_t *>(base + 1024 + ts.wbytes);
-    uint16_t *xh = reinterpret_cast<uint16_t *>(base + 1024 + 2 * ts.wbytes);
-    uint16_t *xl = reinterpret_cast<uint16_t *>(base + 1024 + 2 * ts.wbytes + ts.xbytes);
-    CUtensorMap mwh, mwl, mxh, mxl;
-    if (!bf16_map(&mwh, wh, N, Kp) || !bf16_map(&mwl, wl, N, Kp) || !bf16_map(&mxh, xh, M, Kp) ||
-        !bf16_map(&mxl, xl, M, Kp))
-        return DFL_E_CUDA;
-    static bool attr[kMaxDevices] = {};
-    if (!attr[dev]) {
-        if (cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
-            return DFL_E_CUDA;
-        attr[dev] = true;
-    }
-    const long wthreads = (long)(N / 16) * C * 32;
-    k_tc_dequant<<<unsigned((wthreads + 255) / 256), 256, 0, s>>>(static_cast<const uint8_t *>(img), N, C, wh, wl);
-    const long xpairs = (long)M * Kp / 2;
-    k_tc_split<<<unsigned((xpairs + 255) / 256), 256, 0, s>>>(x, M, K, Kp, xh, xl);
-    TcArgs a;
-    a.M = M;
-    a.N = N;
-    a.stages = C;
-    a.y = y;
-    a.err = reinterpret_cast<int *>(base);
-    const dim3 grid((N + kTcM - 1) / kTcM, (M + kTcN - 1) / kTcN);
-    k_tc_gemm<<<grid, kTcThreads, kTcSmem, s>>>(mwh, mwl, mxh, mxl, a);
-    return cudaGetLastError() == cudaSuccess ? DFL_OK : DFL_E_CUDA;
+    if (scratch_bytes < tc_scratch(K, N, M).total || (reinterpret_cast<uintptr_t>(scratch) & 1023))
+        return DFL_E_INVALID_ARG;
+    const cudaError_t e = launch_tc_gemm(static_cast<const uint8_t *>(img), K, N, x, M, y, scratch,
+                                         static_cast<int *>(scratch), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DFL_OK : DFL_E_CUDA;
 }
 
 }  // extern "C"

@@ -77,6 +77,10 @@ typedef struct dfl_config {
     float d_rope_base, d_eps, d_emb_scale;
     /* capacity */
     int32_t max_ctx;                       /* positions the KV arena holds */
+    int32_t prefill_rows;                  /* 0, or 128..8192 (a multiple of 16): dfl_prefill takes up to
+                                              this many prompt rows in one pass whose products run on the
+                                              tcgen05 tensor cores (the buffers of such a pass, and sliding
+                                              rings of window + prefill_rows - 1 slots, are sized in) */
 } dfl_config;
 
 typedef struct dfl_sizes {
