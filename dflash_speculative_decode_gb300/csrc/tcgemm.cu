@@ -47,14 +47,18 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) 
 
 // Weights: the tile image (16 columns x 64 inputs per 640-byte tile, codes in the lane order of
 // gemm.cu) -> wh, wl bf16 [N][Kp] (row n = output column n, Kp = K padded to 64; the padding is 0).
-// One thread per (tile, lane): its four code words give it two adjacent inputs of each of 16 pairs.
-__global__ void k_tc_dequant(const uint8_t *__restrict__ img, int N, int C, uint16_t *__restrict__ wh,
-                             uint16_t *__restrict__ wl) {
-    const long tid = blockIdx.x * (long)blockDim.x + threadIdx.x;
+// One warp per tile: each lane expands its 16 bytes of codes (two adjacent inputs of 16 column pairs)
+// into shared memory, then the warp writes the tile's 16 rows of 128 bytes (hi and lo) with 16-byte
+// stores, eight lanes per row.
+constexpr int kDqWarps = 8;
+constexpr int kDqPitch = 72;   // bf16 per staged row: 144 bytes, so the lanes' 4-byte writes hit 32 banks
+__global__ void __launch_bounds__(kDqWarps * 32) k_tc_dequant(const uint8_t *__restrict__ img, int N, int C,
+                                                              uint16_t *__restrict__ wh, uint16_t *__restrict__ wl) {
+    __shared__ __align__(16) uint16_t stage[kDqWarps][2][16 * kDqPitch];
+    const int warp = threadIdx.x >> 5, L = threadIdx.x & 31;
+    const long tile = (long)blockIdx.x * kDqWarps + warp;
     const long ntiles = (long)(N / 16) * C;
-    if (tid >= ntiles * 32) return;
-    const int L = int(tid & 31);
-    const long tile = tid >> 5;
+    if (tile >= ntiles) return;   // whole warps leave together
     const int nt = int(tile / C), c = int(tile % C);
     const int g = L >> 2, t = L & 3;
     const uint8_t *src = img + tile * 640;
@@ -62,7 +66,7 @@ __global__ void k_tc_dequant(const uint8_t *__restrict__ img, int N, int C, uint
     const uint4 dm = *reinterpret_cast<const uint4 *>(src + 512 + 16 * g);   // (n0,b0) (n1,b0) (n0,b1) (n1,b1)
     const uint32_t wv[4] = {words.x, words.y, words.z, words.w};
     const uint32_t dmv[4] = {dm.x, dm.y, dm.z, dm.w};
-    const long Kp = (long)C * 64;
+    uint16_t *sh = stage[warp][0], *sl = stage[warp][1];
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const uint32_t w = wv[s];
@@ -71,8 +75,8 @@ __global__ void k_tc_dequant(const uint8_t *__restrict__ img, int N, int C, uint
         for (int e = 0; e < 4; ++e) {
             // nibble pairs (e, e + 4) hold inputs (k, k + 1) of one column: e = 0: (g, 2t), 1: (g+8, 2t),
             // 2: (g, 2t+8), 3: (g+8, 2t+8)
-            const int n = 16 * nt + g + ((e & 1) ? 8 : 0);
-            const int k = 64 * c + 16 * s + 2 * t + ((e & 2) ? 8 : 0);
+            const int r = g + ((e & 1) ? 8 : 0);
+            const int k = 16 * s + 2 * t + ((e & 2) ? 8 : 0);
             const uint32_t pair = dmv[2 * blk + (e & 1)];
             const float d = __half2float(__ushort_as_half(uint16_t(pair & 0xFFFFu)));
             const float m = __half2float(__ushort_as_half(uint16_t(pair >> 16)));
@@ -80,10 +84,19 @@ __global__ void k_tc_dequant(const uint8_t *__restrict__ img, int N, int C, uint
             uint16_t h0, l0, h1, l1;
             split_bf16(fmaf(d, q0, m), h0, l0);
             split_bf16(fmaf(d, q1, m), h1, l1);
-            const long o = (long)n * Kp + k;
-            *reinterpret_cast<uint32_t *>(wh + o) = uint32_t(h0) | (uint32_t(h1) << 16);
-            *reinterpret_cast<uint32_t *>(wl + o) = uint32_t(l0) | (uint32_t(l1) << 16);
+            *reinterpret_cast<uint32_t *>(sh + r * kDqPitch + k) = uint32_t(h0) | (uint32_t(h1) << 16);
+            *reinterpret_cast<uint32_t *>(sl + r * kDqPitch + k) = uint32_t(l0) | (uint32_t(l1) << 16);
         }
+    }
+    __syncwarp();
+    const long Kp = (long)C * 64;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int idx = it * 32 + L;              // 0..255: (array, row, 16-byte chunk)
+        const int arr = idx >> 7, r = (idx >> 3) & 15, ch = idx & 7;
+        const uint16_t *from = stage[warp][arr] + r * kDqPitch + 8 * ch;
+        uint16_t *to = (arr ? wl : wh) + (long)(16 * nt + r) * Kp + 64 * c + 8 * ch;
+        *reinterpret_cast<uint4 *>(to) = *reinterpret_cast<const uint4 *>(from);
     }
 }
 
@@ -184,8 +197,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ volatile int s_bad;
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTcM;   // first output column of the CTA
-    const int m0 = blockIdx.y * kTcN;   // first row of the CTA
+    // row tiles vary fastest: the CTAs resident at once share few weight tiles (each read from HBM once),
+    // and the rows (much smaller than the weights) stay in L2 across the waves
+    const int m0 = blockIdx.x * kTcN;   // first row of the CTA
+    const int n0 = blockIdx.y * kTcM;   // first output column of the CTA
     const int nst = a.stages;
 
     if (threadIdx.x == 0) {
@@ -371,8 +386,8 @@ cudaError_t launch_tc_gemm(const uint8_t *img, int K, int N, const float *x, int
         if (e != cudaSuccess) return e;
         attr[dev] = true;
     }
-    const long wthreads = (long)(N / 16) * C * 32;
-    k_tc_dequant<<<unsigned((wthreads + 255) / 256), 256, 0, s>>>(img, N, C, wh, wl);
+    const long wtiles = (long)(N / 16) * C;
+    k_tc_dequant<<<unsigned((wtiles + kDqWarps - 1) / kDqWarps), kDqWarps * 32, 0, s>>>(img, N, C, wh, wl);
     const long xpairs = (long)M * Kp / 2;
     k_tc_split<<<unsigned((xpairs + 255) / 256), 256, 0, s>>>(x, M, K, Kp, xh, xl);
     TcArgs a;
@@ -381,7 +396,7 @@ cudaError_t launch_tc_gemm(const uint8_t *img, int K, int N, const float *x, int
     a.stages = C;
     a.y = y;
     a.err = err;
-    const dim3 grid((N + kTcM - 1) / kTcM, (M + kTcN - 1) / kTcN);
+    const dim3 grid((M + kTcN - 1) / kTcN, (N + kTcM - 1) / kTcM);
     k_tc_gemm<<<grid, kTcThreads, kTcSmem, s>>>(mwh, mwl, mxh, mxl, a);
     return cudaGetLastError();
 }
