@@ -285,12 +285,18 @@ constexpr int kAttnKeys = 32;
 constexpr int kAttnKS = 16 / kAttnKQ;   // k-steps of 16 per part of the head dimension (hd <= 256)
 constexpr int kAttnNT = 32 / kAttnWarps; // 8-column tiles per warp in p.V (hd <= 256)
 constexpr int kAttnSP = 40;  // pitch of the score and probability rows (32 keys + 8)
-constexpr int kAttnBuf = 3;  // key/value blocks in flight
+// key/value blocks in flight (the ring's slots): as many as shared memory holds, so a CTA's blocks are
+// requested at once (a CTA takes 1-8 blocks at the step's shapes)
+constexpr int attn_buf(int hd) { return hd > 128 ? 3 : 5; }
 
-size_t attn_smem(int hd) {
-    return ((size_t)kMaxRows * (hd + 8) + kAttnBuf * (size_t)kAttnKeys * (hd + 8) +
-            kAttnBuf * (size_t)kAttnKeys * (hd + 4) + (kAttnKQ + 1) * (size_t)kMaxRows * kAttnSP + 3 * kMaxRows) * 4;
+size_t attn_smem(int hd, int nb) {
+    return ((size_t)kMaxRows * (hd + 8) + nb * (size_t)kAttnKeys * (hd + 8) + nb * (size_t)kAttnKeys * (hd + 4) +
+            (kAttnKQ + 1) * (size_t)kMaxRows * kAttnSP + 3 * kMaxRows) * 4;
 }
+size_t attn_smem(int hd) { return attn_smem(hd, attn_buf(hd)); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_n() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // fp32 pair -> bf16x2 hi and lo (x = hi + lo to 2^-17 relative), lower element in the low half; the
 // roundings are the hardware's paired round-to-nearest-even conversion
@@ -302,9 +308,10 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// Tile row r holds pass row m = r (HP = 1) or m = r % 8 of head 2u + r / 8 (HP = 2).
-template <int CL, int HP>
+// Tile row r holds pass row m = r (HP = 1) or m = r % 8 of head 2u + r / 8 (HP = 2). NB: ring slots.
+template <int CL, int HP, int NB>
 __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
+    constexpr int kAttnBuf = NB;
     extern __shared__ __align__(16) float sm[];
     const int hd = a.hd, ldq = hd + 8, ldv = hd + 4, hd4 = hd / 4;
     float *Qs = sm;                                 // [16][ldq] this head's query rows
@@ -448,8 +455,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
         } else {
             cp_async_commit();
         }
-        static_assert(kAttnBuf == 3, "wait depth");
-        cp_async_wait_group2();
+        cp_async_wait_n<kAttnBuf - 1>();
         __syncthreads();
         const float *K = Kb + buf * kAttnKeys * ldq, *V = Vb + buf * kAttnKeys * ldv;
         const bool virt = i >= nAmine;
@@ -628,18 +634,23 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(AttnArgs a) {
 // [device][hd > 128][16, 8]: clusters that fit at once (until attn_prepare: none of 16, all of 8)
 static int g_fit[kMaxDevices][2][2];
 static bool g_fit_set[kMaxDevices];
-template <int CL, int HP>
-static cudaError_t attn_attrs() {
+template <int CL, int HP, int NB>
+static cudaError_t attn_attrs_nb() {
     static bool done[kMaxDevices] = {};
     const int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k_attn<CL, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(attn_smem(256)));
+    const int smem = int(NB == attn_buf(256) ? attn_smem(256, NB) : attn_smem(128, NB));
+    cudaError_t e = cudaFuncSetAttribute(k_attn<CL, HP, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess && CL > 8)
-        e = cudaFuncSetAttribute(k_attn<CL, HP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(k_attn<CL, HP, NB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) done[dev] = true;
     return e;
+}
+template <int CL, int HP>
+static cudaError_t attn_attrs() {
+    const cudaError_t e = attn_attrs_nb<CL, HP, attn_buf(128)>();
+    return e != cudaSuccess ? e : attn_attrs_nb<CL, HP, attn_buf(256)>();
 }
 
 template <int CL>
@@ -656,7 +667,9 @@ static int clusters_that_fit(int hd) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_attn<CL, 2>, &cfg) != cudaSuccess) {
+    const cudaError_t q = hd > 128 ? cudaOccupancyMaxActiveClusters(&n, k_attn<CL, 2, attn_buf(256)>, &cfg)
+                                   : cudaOccupancyMaxActiveClusters(&n, k_attn<CL, 2, attn_buf(128)>, &cfg);
+    if (q != cudaSuccess) {
         cudaGetLastError();   // a refused query leaves no sticky error
         n = 0;
     }
@@ -689,7 +702,10 @@ static cudaError_t launch_attn_t(const AttnArgs &a, cudaStream_t s) {
     const cudaError_t e = attn_attrs<CL, HP>();
     if (e != cudaSuccess) return e;
     const int tiles = (a.M + kMaxRows - 1) / kMaxRows;
-    return launch_cluster_pdl(k_attn<CL, HP>, dim3(a.nq / HP * CL, tiles), CL, kAttnThreads, attn_smem(a.hd), s, a);
+    const dim3 grid(a.nq / HP * CL, tiles);
+    if (a.hd > 128)
+        return launch_cluster_pdl(k_attn<CL, HP, attn_buf(256)>, grid, CL, kAttnThreads, attn_smem(a.hd), s, a);
+    return launch_cluster_pdl(k_attn<CL, HP, attn_buf(128)>, grid, CL, kAttnThreads, attn_smem(a.hd), s, a);
 }
 
 cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
