@@ -608,6 +608,36 @@ def bench_prefill(args):
                       "peak_bf16_tflops": pk["bf16_tflops"], "results": res}), flush=True)
 
 
+def bench_attn(args):
+    """Profiling workload for the attention kernel: a short E4B-shaped target (six layers, no KV sharing,
+    vocab 32768) or two 27B-class layers, each with its full 5-layer draft, a prompt of --ctx tokens
+    through long prefill passes, then two speculative steps. Prints one JSON line (not a bench line)
+    with the attention launches per pass, so a profiler can skip the prompt's."""
+    import dataclasses
+    import torch
+    from dflash_speculative_decode_gb300 import build
+    build.build()
+    if args.attn_pair == "27b":
+        pc = gen.b27_cut(max_ctx=args.ctx + 64, n_layers=2, vocab=32768)
+    else:
+        t = gen.e4b_target(n_layers=6, first_shared=6, vocab=32768)
+        d = dataclasses.replace(gen.e4b_draft(vocab=32768), taps=(1, 3, 5))
+        pc = gen.PairConfig(t, d, max_ctx=args.ctx + 64)
+    eng, _, _ = load_engine(pc, prefill_rows=1024)
+    tok = eng.dfl_prefill(gen.prompt(pc.target.vocab, args.ctx))
+    for _ in range(2):
+        props = eng.dfl_draft_block(tok)
+        tt, a = eng.dfl_verify_block([tok] + [int(v) for v in props])
+        eng.dfl_commit_verify_rows(a + 1)
+        tok = int(tt[a])
+    torch.cuda.synchronize()
+    long_passes = (args.ctx // 1024) + (1 if args.ctx % 1024 >= 128 else 0)
+    print(json.dumps({"workload": f"attention profile, {args.attn_pair} layers, prompt {args.ctx}",
+                      "positions": eng.dfl_positions_held(),
+                      "prompt_attention_launches": long_passes * pc.target.n_layers,
+                      "attention_launches_per_step": pc.target.n_layers + pc.draft.n_layers}), flush=True)
+
+
 def bench_gemm(args):
     """Config 2 on its own: every shape of SWEEP_SHAPES (or --gemm-shape), rows --gemm-rows."""
     import torch
@@ -629,7 +659,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b", "prefill"])
+    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b", "prefill", "attn"])
+    ap.add_argument("--attn-pair", default="e4b", choices=["e4b", "27b"], help="layers of --workload attn")
     ap.add_argument("--prefill-rows", type=int, default=1024,
                     help="rows per long prefill pass (tcgen05 products); 0 = passes of 16 rows")
     ap.add_argument("--sweep-rows", default="128,256,512,1024,2048", help="row counts of the prefill product sweep")
@@ -648,6 +679,8 @@ def main():
         return bench_gemm(args)
     if args.workload == "prefill":
         return bench_prefill(args)
+    if args.workload == "attn":
+        return bench_attn(args)
     return bench_cuda(args)
 
 
