@@ -11,11 +11,12 @@
 // rows are split the same way. The product adds hi*hi + hi*lo + lo*hi (the lo*lo term lies below fp32
 // rounding) in fp32 in tensor memory, so a result carries about the error of an fp32 dot product.
 //
-// Kernel (k_tc_gemm). A CTA owns 128 output columns x 128 rows. Per stage of 64 inputs the TMA loads four
-// 16 KB tiles (weight hi, weight lo, row hi, row lo), each 128 rows x 128 bytes in the 128-byte swizzle
-// the MMA's shared-memory descriptors name; three stages are in flight. Warp 0 issues the copies, warp 1
-// owns the tensor memory and one of its lanes issues the MMAs (M = 128, N = 128, K = 16; twelve per
-// stage), warps 2-5 read the accumulator (tcgen05.ld, one 32-lane quarter each) and store the fp32
+// Kernel (k_tc_gemm). A tile is 128 output columns x 128 rows; one persistent CTA per SM takes every
+// G-th tile. Per stage of 64 inputs the TMA loads four 16 KB tiles (weight hi, weight lo, row hi, row
+// lo), each 128 rows x 128 bytes in the 128-byte swizzle the MMA's shared-memory descriptors name; three
+// stages are in flight, across tile boundaries. Warp 0 issues the copies, warp 1 owns the tensor memory
+// and one of its lanes issues the MMAs (M = 128, N = 128, K = 16; twelve per stage) into one of two
+// accumulators, warps 2-5 read the other one (tcgen05.ld, one 32-lane quarter each) and store the fp32
 // result. Every wait on an mbarrier is bounded; a wait that gives up stops the CTA's issuing, drains
 // what is in flight, frees the tensor memory and sets the error word.
 #include <cuda.h>   // CUtensorMap and its enums (types only: the encoder is looked up at run time)
@@ -33,7 +34,7 @@ constexpr int kTcTile = 128 * kTcK * 2;              // bytes of one operand til
 constexpr int kTcStageBytes = 4 * kTcTile;           // weight hi, weight lo, rows hi, rows lo
 constexpr int kTcThreads = 192;                      // warp 0 copies, warp 1 MMAs, warps 2-5 epilogue
 constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024;   // + slack to align the ring to 1024 bytes
-constexpr int kTcTmemCols = kTcN;                    // fp32 accumulator: 128 lanes x 128 columns
+constexpr int kTcTmemCols = 2 * kTcN;                // two fp32 accumulators of 128 lanes x 128 columns
 
 // ---------------------------------------------------------------------------------------------------
 // operand preparation
@@ -183,24 +184,24 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 struct TcArgs {
     int M, N, stages;   // rows, output columns, stages of 64 inputs
+    int tiles_m, tiles; // 128-row tiles, tiles in all (row tiles vary fastest)
     float *y;           // [M][N] fp32
     int *err;           // sticky error bits (kErrWaitTimeout), nullable
 };
 
+// Persistent: CTA c takes tiles c, c + G, c + 2G, ... Consecutive tiles share their weight tile (row
+// tiles vary fastest), so the CTAs working at once read few weight tiles from HBM and the rows stay in
+// L2. Two accumulators in tensor memory: the epilogue drains one while the products fill the other.
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tw_hi, const __grid_constant__ CUtensorMap tw_lo,
               const __grid_constant__ CUtensorMap tx_hi, const __grid_constant__ CUtensorMap tx_lo, TcArgs a) {
     extern __shared__ uint8_t tc_smem_raw[];
-    __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], acc_bar;
+    __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], accf[2], acce[2], done;
     __shared__ uint32_t s_tmem;
     __shared__ int s_issued, s_consumed;
     __shared__ volatile int s_bad;
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // row tiles vary fastest: the CTAs resident at once share few weight tiles (each read from HBM once),
-    // and the rows (much smaller than the weights) stay in L2 across the waves
-    const int m0 = blockIdx.x * kTcN;   // first row of the CTA
-    const int n0 = blockIdx.y * kTcM;   // first output column of the CTA
     const int nst = a.stages;
 
     if (threadIdx.x == 0) {
@@ -208,13 +209,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&full[i], 1);    // the producer's arrival (with the stage's bytes)
             mbar_init(&empty[i], 1);   // the MMA thread's commit
         }
-        mbar_init(&acc_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);    // the MMA thread's commit after a tile's last stage
+            mbar_init(&acce[b], 4);    // one arrival per epilogue warp once it has read the accumulator
+        }
+        mbar_init(&done, 1);           // the MMA thread's last commit
         s_bad = 0;
         s_issued = s_consumed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 1) {   // the whole warp allocates the accumulator's columns
+    if (warp == 1) {   // the whole warp allocates both accumulators' columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&s_tmem)),
                      "r"(kTcTmemCols)
                      : "memory");
@@ -226,58 +231,84 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = s_tmem;
 
     if (warp == 0) {
-        // ---- copies ----
+        // ---- copies: every stage of every tile of this CTA, through the ring ----
         if (lane == 0) {
             int k = 0;
-            for (; k < nst; ++k) {
-                const int s = k % kTcStages;
-                if (k >= kTcStages && !mbar_wait(&empty[s], unsigned(k / kTcStages - 1) & 1u, &s_bad)) break;
-                if (s_bad) break;
-                uint8_t *st = ring + s * kTcStageBytes;
-                mbar_expect(&full[s], unsigned(kTcStageBytes));
-                tma_load_2d(st, &tw_hi, k * kTcK, n0, &full[s]);
-                tma_load_2d(st + kTcTile, &tw_lo, k * kTcK, n0, &full[s]);
-                tma_load_2d(st + 2 * kTcTile, &tx_hi, k * kTcK, m0, &full[s]);
-                tma_load_2d(st + 3 * kTcTile, &tx_lo, k * kTcK, m0, &full[s]);
+            bool stop = false;
+            for (int t = blockIdx.x; t < a.tiles && !stop; t += gridDim.x) {
+                const int m0 = (t % a.tiles_m) * kTcN, n0 = (t / a.tiles_m) * kTcM;
+                for (int st = 0; st < nst; ++st, ++k) {
+                    const int s = k % kTcStages;
+                    if (k >= kTcStages && !mbar_wait(&empty[s], unsigned(k / kTcStages - 1) & 1u, &s_bad)) {
+                        stop = true;
+                        break;
+                    }
+                    if (s_bad) {
+                        stop = true;
+                        break;
+                    }
+                    uint8_t *sp = ring + s * kTcStageBytes;
+                    mbar_expect(&full[s], unsigned(kTcStageBytes));
+                    tma_load_2d(sp, &tw_hi, st * kTcK, n0, &full[s]);
+                    tma_load_2d(sp + kTcTile, &tw_lo, st * kTcK, n0, &full[s]);
+                    tma_load_2d(sp + 2 * kTcTile, &tx_hi, st * kTcK, m0, &full[s]);
+                    tma_load_2d(sp + 3 * kTcTile, &tx_lo, st * kTcK, m0, &full[s]);
+                }
             }
             s_issued = k;
         }
     } else if (warp == 1) {
-        // ---- products ----
+        // ---- products: tile li into accumulator li % 2 ----
         if (lane == 0) {
-            int k = 0;
-            for (; k < nst; ++k) {
-                const int s = k % kTcStages;
-                if (!mbar_wait(&full[s], unsigned(k / kTcStages) & 1u, &s_bad)) break;
+            int k = 0, li = 0;
+            bool stop = false;
+            for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++li) {
+                const int b = li & 1;
+                const uint32_t d = tmem + uint32_t(b * kTcN);
+                if (li >= 2 && !mbar_wait(&acce[b], unsigned(li / 2 - 1) & 1u, &s_bad)) break;
                 tc_fence_after();
-                const uint8_t *st = ring + s * kTcStageBytes;
-                const uint64_t dwh = sw128_desc(st), dwl = sw128_desc(st + kTcTile);
-                const uint64_t dxh = sw128_desc(st + 2 * kTcTile), dxl = sw128_desc(st + 3 * kTcTile);
+                for (int st = 0; st < nst; ++st, ++k) {
+                    const int s = k % kTcStages;
+                    if (!mbar_wait(&full[s], unsigned(k / kTcStages) & 1u, &s_bad)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *sp = ring + s * kTcStageBytes;
+                    const uint64_t dwh = sw128_desc(sp), dwl = sw128_desc(sp + kTcTile);
+                    const uint64_t dxh = sw128_desc(sp + 2 * kTcTile), dxl = sw128_desc(sp + 3 * kTcTile);
 #pragma unroll
-                for (int j = 0; j < kTcK / 16; ++j) {
-                    const uint64_t o = uint64_t(2 * j);   // 32 bytes further, in 16-byte units
-                    tc_mma(tmem, dwh + o, dxh + o, (k > 0 || j > 0) ? 1u : 0u);
-                    tc_mma(tmem, dwh + o, dxl + o, 1u);
-                    tc_mma(tmem, dwl + o, dxh + o, 1u);
+                    for (int j = 0; j < kTcK / 16; ++j) {
+                        const uint64_t o = uint64_t(2 * j);   // 32 bytes further, in 16-byte units
+                        tc_mma(d, dwh + o, dxh + o, (st > 0 || j > 0) ? 1u : 0u);
+                        tc_mma(d, dwh + o, dxl + o, 1u);
+                        tc_mma(d, dwl + o, dxh + o, 1u);
+                    }
+                    tc_commit(&empty[s]);   // the stage may be refilled once these products are done
                 }
-                tc_commit(&empty[s]);   // the stage may be refilled once these products are done
+                if (stop) break;
+                tc_commit(&accf[b]);        // the tile's accumulator is complete
             }
             s_consumed = k;
-            tc_commit(&acc_bar);        // every product issued so far is done (also on the error path)
+            tc_commit(&done);               // every product issued (also on the error path)
         }
         __syncwarp();
     } else {
         // ---- epilogue: warps 2..5, lane quarter warp % 4 ----
-        const bool ok = mbar_wait(&acc_bar, 0u, &s_bad);
-        tc_fence_after();
-        // tcgen05.ld is warp-collective: the whole warp reads, or none of it
-        if (__all_sync(0xffffffffu, ok && !s_bad)) {
-            const int q = warp & 3;
+        const int q = warp & 3;
+        int li = 0;
+        for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++li) {
+            const int b = li & 1;
+            const bool ok = mbar_wait(&accf[b], unsigned(li / 2) & 1u, &s_bad);
+            tc_fence_after();
+            // tcgen05.ld is warp-collective: the whole warp reads, or none of it
+            if (!__all_sync(0xffffffffu, ok && !s_bad)) break;
+            const int m0 = (t % a.tiles_m) * kTcN, n0 = (t / a.tiles_m) * kTcM;
             const int f = n0 + 32 * q + lane;
 #pragma unroll 1
             for (int c0 = 0; c0 < kTcN; c0 += 32) {
                 uint32_t r[32];
-                tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(c0), r);
+                tc_ld32(tmem + uint32_t(b * kTcN) + (uint32_t(32 * q) << 16) + uint32_t(c0), r);
                 if (f < a.N) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -286,19 +317,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);   // accumulator b may be overwritten
         }
-        tc_fence_before();
     }
     __syncthreads();
-    if (s_bad) {
-        // a wait gave up: let every copy and product already issued land before the memory is released
-        if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {
+        // every commit lands before the memory is released; after a wait gave up, also every copy
+        // already issued
+        if (s_bad)
             for (int k = s_consumed; k < s_issued; ++k) mbar_drain(&full[k % kTcStages], unsigned(k / kTcStages) & 1u);
-            mbar_drain(&acc_bar, 0u);
-            if (a.err) atomicOr(a.err, kErrWaitTimeout);
-        }
-        __syncthreads();
+        if (!mbar_drain(&done, 0u)) s_bad = 1;
+        if (s_bad && a.err) atomicOr(a.err, kErrWaitTimeout);
     }
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols) : "memory");
@@ -390,13 +423,18 @@ cudaError_t launch_tc_gemm(const uint8_t *img, int K, int N, const float *x, int
     k_tc_dequant<<<unsigned((wtiles + kDqWarps - 1) / kDqWarps), kDqWarps * 32, 0, s>>>(img, N, C, wh, wl);
     const long xpairs = (long)M * Kp / 2;
     k_tc_split<<<unsigned((xpairs + 255) / 256), 256, 0, s>>>(x, M, K, Kp, xh, xl);
+    static int sms[kMaxDevices] = {};
+    if (!sms[dev] && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
     TcArgs a;
     a.M = M;
     a.N = N;
     a.stages = C;
+    a.tiles_m = (M + kTcN - 1) / kTcN;
+    a.tiles = a.tiles_m * ((N + kTcM - 1) / kTcM);
     a.y = y;
     a.err = err;
-    const dim3 grid((M + kTcN - 1) / kTcN, (N + kTcM - 1) / kTcM);
+    const int grid = a.tiles < sms[dev] ? a.tiles : sms[dev];   // persistent: one CTA per SM
     k_tc_gemm<<<grid, kTcThreads, kTcSmem, s>>>(mwh, mwl, mxh, mxl, a);
     return cudaGetLastError();
 }
