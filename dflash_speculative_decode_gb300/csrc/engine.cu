@@ -806,7 +806,9 @@ int prefill_long(dfl_ctx *c, int k, bool do_head, bool sampled) {
         aa.st = c->st;
         aa.scale = 1.0f / sqrtf((float)hd);
         aa.err = &c->st->err;
-        aa.max_cluster = c->attn_cluster;
+        // hundreds of 16-row tiles: the total work over all tiles, not one tile's latency, sets the time,
+        // and clusters of 4 spend less of it in the merge than clusters of 16
+        aa.max_cluster = std::min(c->attn_cluster, 4);
         aa.out32 = B;
         DFL_LAUNCH(launch_attn(aa, c->stream));
         DFL_CK(tc_product(c, L.o, B, k, A));

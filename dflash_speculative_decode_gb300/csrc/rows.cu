@@ -728,13 +728,17 @@ cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
 // ---------------------------------------------------------------------------------------------------
 // Elementwise steps of a long pass on fp32 rows (a pass of 16 rows or fewer runs them in the products'
 // epilogues): the FFN's gate, and the per-layer-embedding gate.
+// four consecutive outputs per thread (F is a multiple of 64)
 __global__ void k_glu32(const float *__restrict__ y, int M, int F, float *__restrict__ out) {
-    const long i = blockIdx.x * (long)blockDim.x + threadIdx.x;
-    if (i >= (long)M * F) return;
-    const long m = i / F;
-    const int j = int(i % F);
-    const float *r = y + m * 2 * F;
-    out[i] = silu_f(r[j]) * r[F + j];
+    const long i = blockIdx.x * (long)blockDim.x + threadIdx.x;   // index of a group of four outputs
+    const int F4 = F / 4;
+    if (i >= (long)M * F4) return;
+    const long m = i / F4;
+    const int j = int(i % F4) * 4;
+    const float4 g = *reinterpret_cast<const float4 *>(y + m * 2 * F + j);
+    const float4 u = *reinterpret_cast<const float4 *>(y + m * 2 * F + F + j);
+    *reinterpret_cast<float4 *>(out + m * F + j) =
+        make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z, silu_f(g.w) * u.w);
 }
 
 __global__ void k_silu_mul32(const float *__restrict__ y, int M, int P, const uint16_t *__restrict__ e, int lde,
@@ -747,7 +751,8 @@ __global__ void k_silu_mul32(const float *__restrict__ y, int M, int P, const ui
 }
 
 cudaError_t launch_glu32(const float *y, int M, int F, float *out, cudaStream_t s) {
-    const long n = (long)M * F;
+    if (F % 4) return cudaErrorInvalidValue;
+    const long n = (long)M * (F / 4);
     k_glu32<<<unsigned((n + 255) / 256), 256, 0, s>>>(y, M, F, out);
     return cudaGetLastError();
 }
