@@ -45,6 +45,39 @@ def test_required_bytes_without_gpu():
     assert 11.5e9 < sz.weights_bytes < 13.5e9
 
 
+def test_required_bytes_27b_and_long_prefill():
+    """The 27B-class pair fits the part (16 GB of Q4_1 layers + bf16 tables); long prefill passes add
+    their row buffers, product scratch and longer sliding rings, and bad prefill_rows are refused."""
+    import gen
+    from dflash_speculative_decode_gb300 import _abi
+    L = _abi.lib()
+    sz = _abi.dfl_sizes()
+    cfg = _abi.config_from_pair(gen.b27_pair())
+    assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == 0
+    assert 21e9 < sz.weights_bytes < 24e9
+    base = (sz.state_bytes, sz.workspace_bytes)
+    cfg = _abi.config_from_pair(gen.b27_pair(), prefill_rows=1024)
+    assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == 0
+    assert sz.state_bytes > base[0] and sz.workspace_bytes > base[1]
+    assert sz.weights_bytes + sz.state_bytes + sz.workspace_bytes < 60e9
+    for bad in (100, 130, 8208, -16):
+        cfg = _abi.config_from_pair(gen.tiny_pair(), prefill_rows=bad)
+        assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == _abi.DFL_E_INVALID_ARG, bad
+    cfg = _abi.config_from_pair(gen.tiny_pair())
+    cfg.hidden = 8320                          # past the widest row step
+    assert L.dfl_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)) == _abi.DFL_E_INVALID_ARG
+
+
+def test_tc_scratch_sizes():
+    from dflash_speculative_decode_gb300 import _abi
+    L = _abi.lib()
+    Kp = 2560
+    assert L.dfl_q41_gemm_tc_scratch_bytes(2560, 10240, 2048) == 1024 + 2 * 10240 * Kp * 2 + 2 * 2048 * Kp * 2
+    assert L.dfl_q41_gemm_tc_scratch_bytes(96, 64, 1) == 1024 + 2 * 64 * 128 * 2 + 2 * 1024   # K padded to 128
+    assert L.dfl_q41_gemm_tc_scratch_bytes(2560, 48, 128) == -1    # N not a multiple of 32
+    assert L.dfl_q41_gemm_tc_scratch_bytes(2560, 64, 0) == -1
+
+
 def test_bad_configuration_is_refused():
     import gen
     from dflash_speculative_decode_gb300 import _abi
