@@ -18,7 +18,7 @@ MAX_LAYERS, MAX_TAPS, MAX_ROWS = 64, 8, 16
 DFL_OK, DFL_E_INVALID_ARG, DFL_E_STATE, DFL_E_CAPACITY, DFL_E_UNSUPPORTED, DFL_E_CUDA, DFL_E_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 DFL_KEEP_ACCEPTED = -1
 DFL_OPT_KEEP_LOGITS, DFL_OPT_GRAPHS, DFL_OPT_STOP_LAYER, DFL_OPT_PROFILE, DFL_OPT_ATTN_CLUSTER = 1, 2, 3, 4, 5
-DFL_OPT_TEST_STALL, DFL_OPT_FUSE_STEPS = 6, 7
+DFL_OPT_TEST_STALL, DFL_OPT_FUSE_STEPS, DFL_OPT_PLE_SPLIT = 6, 7, 8
 ERRORS = {DFL_E_INVALID_ARG: "DFL_E_INVALID_ARG", DFL_E_STATE: "DFL_E_STATE", DFL_E_CAPACITY: "DFL_E_CAPACITY",
           DFL_E_UNSUPPORTED: "DFL_E_UNSUPPORTED", DFL_E_CUDA: "DFL_E_CUDA", DFL_E_TIMEOUT: "DFL_E_TIMEOUT"}
 

@@ -368,7 +368,7 @@ inline size_t act_words(int K) { return (size_t)kMaxRows * K; }          // frag
 inline size_t act_sums(int K) { return (size_t)(K / 16) * kMaxRows; }     // sum floats
 cudaError_t launch_pack_q41(const uint8_t *src, int K, int N, uint8_t *img, cudaStream_t s);
 cudaError_t launch_pack_bf16(const uint16_t *src, int K, int N, uint8_t *img, cudaStream_t s);
-inline int padded_k(int K) { return (K + 63) / 64 * 64; }
+__host__ __device__ inline int padded_k(int K) { return (K + 63) / 64 * 64; }
 inline size_t q41_image_bytes(int K, int N) { return size_t(N / 16) * (padded_k(K) / 64) * 640; }
 inline size_t bf16_image_bytes(int K, int N) { return size_t(N / 16) * (padded_k(K) / 64) * 2048; }
 
@@ -410,6 +410,20 @@ struct AttnArgs {
     Stamp ps;
 };
 
+// The per-layer-embedding tail's two products in one launch (rows.cu, k_ple)
+struct PleArgs {
+    int M, H, P;
+    const uint8_t *img_g;   // Q4_1 tile image of the gate, K = H, N = P
+    const uint8_t *img_p;   // Q4_1 tile image of the projection, K = P, N = H
+    const uint32_t *xf;     // the gate's input rows in operand format (H inputs, rows from 0)
+    const float *xs;        // their per-16 sums
+    const uint16_t *ext;    // the layer's per-layer-embedding rows: bf16, row m at ext + m * lde
+    int lde;
+    float *y;               // fp32 [M][H]: the projection's rows
+    Stamp ps;
+};
+bool ple_fused_ok(int M, int H, int P);
+
 struct SampleArgs {
     const float *logits;   // [M][V]
     int M, V, ld;
@@ -432,6 +446,7 @@ cudaError_t launch_cast_rows(const float *src, int ld_src, int M, int H, const u
                              cudaStream_t s);
 cudaError_t launch_copy_taps(const float *taps, int ld, const DevState *st, int M, uint32_t *dstf, cudaStream_t s);
 cudaError_t launch_plant(DevState *st, const int32_t *table, int count, cudaStream_t s);
+cudaError_t launch_ple(const PleArgs &a, cudaStream_t s);
 // fp32 rows of a long pass: out[m][j] = silu(y[m][j]) * y[m][F + j] (gate | up halves of a product row)
 cudaError_t launch_glu32(const float *y, int M, int F, float *out, cudaStream_t s);
 // out[m][j] = silu(y[m][j]) * e[m * lde + j] (bf16 e)

@@ -130,6 +130,7 @@ struct dfl_ctx {
     int32_t last_target[kMaxRows] = {};   // the target's tokens of the last verify
     bool test_stall = false;  // test of the give-up path: the products of the next passes issue no copies
     bool fuse_steps = false;  // the row and q/k steps run on the products' last CTAs (DFL_OPT_FUSE_STEPS)
+    bool ple_split = false;   // the PLE gate and projection as two products (DFL_OPT_PLE_SPLIT)
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
     int last_k = 0;
     int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
@@ -699,11 +700,29 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled, bool head_last = 
         r2.outf = c->h.f;
         r2.outs = c->h.s;
         const QMat *last = &L.d;
+        bool ple_one = false;   // the PLE gate and projection in one launch, its rows in c->y
         if (P) {
             DFL_CK(gemm_rows(c, L.d, c->a, k, r2));   // out = x: the gate's input
-            DFL_CK(gemm(c, L.pg, c->h, 0, k, EPI_SILU_MUL, nullptr, 0, &c->z, c->ple_rows + (size_t)l * P, NL * P));
+            ple_one = !c->ple_split && ple_fused_ok(k, H, P);
+            if (ple_one) {
+                PleArgs pa{};
+                pa.M = k;
+                pa.H = H;
+                pa.P = P;
+                pa.img_g = L.pg.img;
+                pa.img_p = L.pp.img;
+                pa.xf = c->h.f;
+                pa.xs = c->h.s;
+                pa.ext = c->ple_rows + (size_t)l * P;
+                pa.lde = NL * P;
+                pa.y = c->y;
+                pa.ps = stamp(c, 0, 2 * 0.625 * H * (double)P + 8.0 * k * H);
+                DFL_LAUNCH_C(0, launch_ple(pa, c->stream));
+            } else {
+                DFL_CK(gemm(c, L.pg, c->h, 0, k, EPI_SILU_MUL, nullptr, 0, &c->z, c->ple_rows + (size_t)l * P, NL * P));
+            }
             r2 = rows(c, k, c->x);
-            r2.y_out = c->y;
+            r2.y_out = ple_one ? nullptr : c->y;
             r2.w_post = L.ple_norm.p;
             r2.lambda = L.lambda;
             r2.outf = c->h.f;
@@ -716,7 +735,13 @@ int target_body(dfl_ctx *c, int k, bool do_head, bool sampled, bool head_last = 
             r2.ld_tap = c->TH;
             r2.tap_off = ti * H;
         }
-        DFL_CK(gemm_rows(c, *last, P ? c->z : c->a, k, r2));
+        if (ple_one) {
+            r2.y = c->y;   // the projection's rows, written by the PLE launch
+            r2.ldy = H;
+            DFL_LAUNCH_S(5, r2, launch_rows);
+        } else {
+            DFL_CK(gemm_rows(c, *last, P ? c->z : c->a, k, r2));
+        }
     }
     if (do_head) {
         float *lg = (c->keep_logits || sampled) ? c->logits : nullptr;
@@ -1486,6 +1511,14 @@ int dfl_set_option(dfl_ctx *c, int option, int value) {
         for (int i = 0; i < kProfClasses; ++i) c->prof_ms[i] = c->prof_bytes[i] = 0, c->prof_n[i] = 0;
     }
     else if (option == DFL_OPT_TEST_STALL) c->test_stall = value != 0;
+    else if (option == DFL_OPT_PLE_SPLIT) {
+        if ((value != 0) != c->ple_split) {
+            DFL_CK(cudaStreamSynchronize(c->stream));
+            for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second.exec);   // captured the other way
+            c->graphs.clear();
+            c->ple_split = value != 0;
+        }
+    }
     else if (option == DFL_OPT_FUSE_STEPS) {
         if ((value != 0) != c->fuse_steps) {
             DFL_CK(cudaStreamSynchronize(c->stream));

@@ -726,6 +726,242 @@ cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------------
+// The per-layer-embedding tail's two products in one launch: the gate z = silu(x Wg) * p_l (K = H,
+// N = P) and the projection y = z Wp (K = P, N = H). One cluster of P/16 CTAs:
+//   - CTA r computes the gate's 16-column tile r over all of K: its 8 warps take the 64-input chunks
+//     w, w + 8, ... and their sums are added in warp order; then silu * p_l, kept in shared memory.
+//   - After a cluster barrier every CTA gathers the whole z (tile r from rank r) into the operand
+//     format, then computes its share of the projection's 16-column tiles over all of K = P and
+//     writes y's rows (fp32).
+// Both weight matrices are requested (cp.async into shared memory) before the dependency wait. The
+// Q4_1 math is the product kernel's: codes enter the tensor cores as 128 + q, rows as bf16 hi + lo,
+// and each 32-block folds in y += d c + (m - 128 d) S. Every sum has a fixed order, so a row's
+// result does not depend on how many rows the pass carries.
+// ---------------------------------------------------------------------------------------------------
+constexpr int kPleWarps = 8;
+
+__host__ __device__ inline int ple_cluster(int P) { return P / 16; }
+__host__ __device__ inline int ple_tiles_per_cta(int H, int P) {
+    const int nt = H / 16, cl = ple_cluster(P);
+    return (nt + cl - 1) / cl;
+}
+static size_t ple_smem(int H, int P, int MT) {
+    const size_t cg = (size_t)padded_k(H) / 64, cp = (size_t)padded_k(P) / 64, gp = (size_t)padded_k(P) / 16;
+    const size_t gh = (size_t)H / 16;
+    return cg * 640 + (size_t)ple_tiles_per_cta(H, P) * cp * 640 + MT * gh * 512 + gh * kMaxRows * 4 +
+           (size_t)kPleWarps * MT * 4 * 32 * 4 + 16 * 16 * 4 + MT * gp * 512 + gp * kMaxRows * 4;
+}
+
+bool ple_fused_ok(int M, int H, int P) {
+    return M >= 1 && M <= kMaxRows && P >= 16 && P % 16 == 0 && P / 16 <= 16 && H % 128 == 0 &&
+           ple_smem(H, P, M > 8 ? 2 : 1) <= 200 * 1024;
+}
+
+// one 64-input chunk of one 16-column tile: codes and (d, m) from `t` (a 640-byte tile in shared
+// memory), rows from the operand fragments `xb` (MT row tiles, 4 k-steps) and sums `xsum` (16-input
+// groups of the chunk, kMaxRows each); adds into acc
+template <int MT>
+__device__ __forceinline__ void ple_chunk(float (&acc)[MT][4], const uint8_t *t, const uint4 (&xb)[MT][4],
+                                          const float *xsum, int lane) {
+    const int g = lane >> 2, tq = lane & 3;
+    const uint4 nb = *reinterpret_cast<const uint4 *>(t + 16 * lane);
+    const uint4 sc = *reinterpret_cast<const uint4 *>(t + 512 + 16 * g);
+    const uint32_t wv[4] = {nb.x, nb.y, nb.z, nb.w};
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        float c[MT][4];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t w = wv[2 * blk + kk];
+            const uint32_t a0 = nib_pair_bf16(w), a1 = nib_pair_bf16(w >> 4), a2 = nib_pair_bf16(w >> 8),
+                           a3 = nib_pair_bf16(w >> 12);
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt) {
+                const uint4 b = xb[tt][2 * blk + kk];
+                if (kk == 0) {
+                    c[tt][0] = c[tt][1] = c[tt][2] = c[tt][3] = 0.f;
+                }
+                mma_bf16(c[tt], a0, a1, a2, a3, b.x, b.y);
+                mma_bf16(c[tt], a0, a1, a2, a3, b.z, b.w);
+            }
+        }
+        uint32_t dlo = blk ? sc.z : sc.x, dhi = blk ? sc.w : sc.y;
+        const float2 flo = __half22float2(*reinterpret_cast<__half2 *>(&dlo));   // (d, m) of column g
+        const float2 fhi = __half22float2(*reinterpret_cast<__half2 *>(&dhi));   // column g + 8
+        const float mlo = fmaf(-128.f, flo.x, flo.y), mhi = fmaf(-128.f, fhi.x, fhi.y);
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt) {
+            const float *s0 = xsum + (2 * blk) * kMaxRows + 8 * tt + 2 * tq;
+            const float *s1 = xsum + (2 * blk + 1) * kMaxRows + 8 * tt + 2 * tq;
+            const float S0 = s0[0] + s1[0], S1 = s0[1] + s1[1];
+            acc[tt][0] = fmaf(mlo, S0, fmaf(flo.x, c[tt][0], acc[tt][0]));
+            acc[tt][1] = fmaf(mlo, S1, fmaf(flo.x, c[tt][1], acc[tt][1]));
+            acc[tt][2] = fmaf(mhi, S0, fmaf(fhi.x, c[tt][2], acc[tt][2]));
+            acc[tt][3] = fmaf(mhi, S1, fmaf(fhi.x, c[tt][3], acc[tt][3]));
+        }
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kPleWarps * 32) k_ple(PleArgs a) {
+    extern __shared__ __align__(16) uint8_t sm8[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+    const unsigned rank = cluster_rank();
+    const int CL = ple_cluster(a.P);
+    const int Cg = padded_k(a.H) / 64, Cp = padded_k(a.P) / 64, Gp = padded_k(a.P) / 16, G = a.P / 16;
+    const int NT = a.H / 16, tpc = ple_tiles_per_cta(a.H, a.P);
+    const int t0 = min(NT, int(rank) * tpc), t1 = min(NT, t0 + tpc);
+    uint8_t *wg = sm8;                                              // [Cg][640] gate tile `rank`
+    uint8_t *wp = wg + (size_t)Cg * 640;                            // [t1 - t0][Cp][640] projection tiles
+    uint32_t *xa = reinterpret_cast<uint32_t *>(wp + (size_t)tpc * Cp * 640);   // [MT][H/16][128] gate input
+    float *xas = reinterpret_cast<float *>(xa + (size_t)MT * (a.H / 16) * 128);   // [H/16][kMaxRows] its sums
+    float *red = xas + (size_t)(a.H / 16) * kMaxRows;               // [warp][tt][4][32]
+    float *zs = red + kPleWarps * MT * 4 * 32;                      // [16 rows][16 columns]
+    uint32_t *xo = reinterpret_cast<uint32_t *>(zs + 16 * 16);      // [MT][Gp][128 words] operand format
+    float *xos = reinterpret_cast<float *>(xo + (size_t)MT * Gp * 128);   // [Gp][kMaxRows] sums
+
+    // weights are immutable: requested before the dependency wait
+    {
+        const uint8_t *src = a.img_g + (size_t)rank * Cg * 640;
+        for (int e = threadIdx.x; e < Cg * 40; e += blockDim.x) cp_async16(wg + 16 * e, src + 16 * e);
+        const uint8_t *srp = a.img_p + (size_t)t0 * Cp * 640;
+        for (int e = threadIdx.x; e < (t1 - t0) * Cp * 40; e += blockDim.x) cp_async16(wp + 16 * e, srp + 16 * e);
+        cp_async_commit();
+    }
+    pdl_trigger();
+    pdl_wait();
+    stamp_ready(a.ps);
+    // the gate's input rows (all of K: each row block is one run of the operand format) and their sums
+    {
+        const int nx = MT * (a.H / 16) * 32, ns = (a.H / 16) * kMaxRows / 4;
+        for (int e = threadIdx.x; e < nx; e += blockDim.x) cp_async16(xa + 4 * e, a.xf + 4 * e);
+        for (int e = threadIdx.x; e < ns; e += blockDim.x) cp_async16(xas + 4 * e, a.xs + 4 * e);
+        cp_async_commit();
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- gate: tile `rank`, chunks split over the warps ----
+    float acc[MT][4];
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt) acc[tt][0] = acc[tt][1] = acc[tt][2] = acc[tt][3] = 0.f;
+    for (int c = warp; c < Cg; c += kPleWarps) {
+        uint4 xb[MT][4];
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                xb[tt][ks] = *reinterpret_cast<const uint4 *>(xa + act_group(a.H, 8 * tt, 4 * c + ks) + 4 * lane);
+        ple_chunk<MT>(acc, wg + (size_t)c * 640, xb, xas + (size_t)(4 * c) * kMaxRows, lane);
+    }
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[((warp * MT + tt) * 4 + i) * 32 + lane] = acc[tt][i];
+    __syncthreads();
+    // sum over warps in order, then z = silu(.) * p_l; rows past M are zero
+    for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x) {
+        const int tok = e >> 4, col = e & 15;
+        float z = 0.f;
+        if (tok < 8 * MT) {
+            const int tt = tok >> 3, i = (col >= 8 ? 2 : 0) + (tok & 1), ln = 4 * (col & 7) + ((tok & 7) >> 1);
+            float v = 0.f;
+            for (int w = 0; w < kPleWarps; ++w) v += red[((w * MT + tt) * 4 + i) * 32 + ln];
+            if (tok < a.M) z = silu_f(v) * bf16_to_f32(a.ext[(long)tok * a.lde + 16 * rank + col]);
+        }
+        zs[e] = z;
+    }
+    cluster_sync_all();   // every rank's tile of z is in its shared memory
+
+    // ---- the projection's input: z in operand format (group kb from rank kb), zero past P ----
+    for (int e = threadIdx.x; e < MT * Gp * 32; e += blockDim.x) {
+        const int ln = e & 31, kb = (e >> 5) % Gp, tt = (e >> 5) / Gp;
+        const int gg = ln >> 2, t = ln & 3, tok = 8 * tt + gg;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (kb < G) {
+            const int cols[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = ld_cluster(zs + tok * 16 + cols[q], unsigned(kb));
+        }
+        uint32_t hi[2], lo[2];
+        float hl = 0.f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+            const float2 hf = __bfloat1622float2(h);
+            const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * q] - hf.x, v[2 * q + 1] - hf.y);
+            const float2 lf = __bfloat1622float2(l);
+            hi[q] = *reinterpret_cast<const uint32_t *>(&h);
+            lo[q] = *reinterpret_cast<const uint32_t *>(&l);
+            hl += (hf.x + lf.x) + (hf.y + lf.y);
+        }
+        *reinterpret_cast<uint4 *>(xo + ((size_t)tt * Gp + kb) * 128 + 4 * ln) = make_uint4(hi[0], hi[1], lo[0], lo[1]);
+        // the row's 16-input sum: the four lanes t of row gg hold its four entries
+        hl += __shfl_xor_sync(0xffffffffu, hl, 1);
+        hl += __shfl_xor_sync(0xffffffffu, hl, 2);
+        if (t == 0) xos[kb * kMaxRows + tok] = hl;
+    }
+    cluster_arrive();   // no more reads of other ranks' shared memory
+    __syncthreads();
+
+    // ---- projection: this rank's tiles t0..t1-1 in pairs, all of K = P per warp ----
+    for (int p0 = t0 + 2 * warp; p0 < t1; p0 += 2 * kPleWarps) {
+        float ac[2][MT][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt) ac[j][tt][0] = ac[j][tt][1] = ac[j][tt][2] = ac[j][tt][3] = 0.f;
+        const bool two = p0 + 1 < t1;
+        for (int c = 0; c < Cp; ++c) {
+            uint4 xb[MT][4];
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    xb[tt][ks] = *reinterpret_cast<const uint4 *>(xo + ((size_t)tt * Gp + 4 * c + ks) * 128 + 4 * lane);
+            const float *xsum = xos + (size_t)(4 * c) * kMaxRows;
+            ple_chunk<MT>(ac[0], wp + ((size_t)(p0 - t0) * Cp + c) * 640, xb, xsum, lane);
+            if (two) ple_chunk<MT>(ac[1], wp + ((size_t)(p0 + 1 - t0) * Cp + c) * 640, xb, xsum, lane);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (j == 1 && !two) break;
+            const int tile = p0 + j;
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = 8 * tt + 2 * tq + (i & 1), col = 16 * tile + g + 8 * (i >> 1);
+                    if (tok < a.M) a.y[(long)tok * a.H + col] = ac[j][tt][i];
+                }
+        }
+    }
+    cluster_wait();   // no rank leaves while another may still read its tile of z
+    stamp_done(a.ps);
+}
+
+template <int MT>
+static cudaError_t launch_ple_t(const PleArgs &a, cudaStream_t s) {
+    static bool done[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    const size_t smem = ple_smem(a.H, a.P, MT);
+    if (!done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_ple<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ple<MT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    const int cl = ple_cluster(a.P);
+    return launch_cluster_pdl(k_ple<MT>, dim3(cl), cl, kPleWarps * 32, smem, s, a);
+}
+
+cudaError_t launch_ple(const PleArgs &a, cudaStream_t s) {
+    if (!ple_fused_ok(a.M, a.H, a.P)) return cudaErrorInvalidValue;
+    return a.M > 8 ? launch_ple_t<2>(a, s) : launch_ple_t<1>(a, s);
+}
+
+// ---------------------------------------------------------------------------------------------------
 // Elementwise steps of a long pass on fp32 rows (a pass of 16 rows or fewer runs them in the products'
 // epilogues): the FFN's gate, and the per-layer-embedding gate.
 // four consecutive outputs per thread (F is a multiple of 64)

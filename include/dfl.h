@@ -208,7 +208,12 @@ int64_t dfl_positions_held(const dfl_ctx *ctx);
  * the partial softmax states are added, so logits may differ in the last bits); other values are
  * DFL_E_INVALID_ARG. Changing it drops the captured graphs. */
 enum { DFL_OPT_KEEP_LOGITS = 1, DFL_OPT_GRAPHS = 2, DFL_OPT_STOP_LAYER = 3, DFL_OPT_PROFILE = 4,
-       DFL_OPT_ATTN_CLUSTER = 5, DFL_OPT_TEST_STALL = 6, DFL_OPT_FUSE_STEPS = 7 };
+       DFL_OPT_ATTN_CLUSTER = 5, DFL_OPT_TEST_STALL = 6, DFL_OPT_FUSE_STEPS = 7, DFL_OPT_PLE_SPLIT = 8 };
+/* DFL_OPT_PLE_SPLIT = 1 runs the per-layer-embedding tail's gate and projection (PR-batched "What
+ * changes": gate = silu(x Wg) times the layer's per-layer input, then its projection) as two products
+ * (0, the default, runs them as one launch on a cluster of ple_dim / 16 CTAs when the pass has at most
+ * 16 rows and ple_dim is a multiple of 16 up to 256). Both give results within the parity tolerance of
+ * each other. Changing it drops the captured graphs. */
 /* DFL_OPT_FUSE_STEPS = 1 runs the row steps (residual, norms, layer scalar, taps) and the q/k steps
  * (norm, rotation, KV store) on the last CTAs of the product that feeds them instead of as separate
  * kernels (0, the default). Both give results within the parity tolerance of each other (the sums are

@@ -377,6 +377,33 @@ def test_spec_decode_lockstep_fused_steps(pair):
     assert res.max_rel_l1 < 1e-4
 
 
+def test_ple_split_and_one_launch():
+    """The per-layer-embedding tail as one cluster launch (default) and as two products
+    (DFL_OPT_PLE_SPLIT): both in lockstep with the oracle, and their verify logits within the logit
+    tolerance of each other; 16-row passes take the one-launch path too (a 20-row prefill)."""
+    from dflash_speculative_decode_gb300 import DFL_OPT_KEEP_LOGITS
+    from dflash_speculative_decode_gb300._abi import DFL_OPT_PLE_SPLIT
+    from gpu_harness import check_logits, engine, lockstep
+    pc = gen.tiny_shared_pair()
+    W = gen.generate(pc)
+    eng = engine(pc, W)
+    eng.dfl_set_option(DFL_OPT_PLE_SPLIT, 1)
+    res, plain = lockstep(pc, W, gen.prompt(pc.target.vocab, 20), 24, p=0.3, eng=eng)
+    if res.near_ties == 0:
+        assert res.tokens == [int(t) for t in plain.tokens]
+    prompt = gen.prompt(pc.target.vocab, 20, request=4)
+    rows = [int(v) for v in gen.prompt(pc.target.vocab, 8, request=5)]
+    out = []
+    for split in (0, 1):
+        e = engine(pc, W)
+        e.dfl_set_option(DFL_OPT_KEEP_LOGITS, 1)
+        e.dfl_set_option(DFL_OPT_PLE_SPLIT, split)
+        t = e.dfl_prefill(prompt)
+        e.dfl_verify_block([t] + rows[1:])
+        out.append((t, e.dfl_read_logits(0, 8)))
+    check_logits(out[0][1], out[1][1], "one launch vs two products")
+
+
 def test_single_turn_serving_matches_oracle():
     """Single-turn serving on tiny-shared (KV-shared layers with empty planes, PLE, two KV widths): a
     prefix cache of two slots, requests P1:A, P2:B, P1:A, P1:B with a stop token, each against the
