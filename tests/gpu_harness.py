@@ -1,6 +1,7 @@
 """Helpers of the GPU parity tests: run the CUDA path through the C ABI and the oracle side by side."""
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -12,7 +13,8 @@ from dflash_speculative_decode_gb300 import DFL_OPT_KEEP_LOGITS, Engine, config_
 LOGIT_REL_L1 = 1e-3      # tolerance on logits: sum|gpu - ref| / sum|ref|
 LOGIT_MAX_ABS = 2e-2     # and max |gpu - ref|
 NEAR_TIE = 1e-3          # greedy: top-2 logit gap below which a differing argmax is allowed
-NEAR_TIE_SAMPLED = 1e-5  # sampled: relative distance of u*sum(p) to an interval edge
+NEAR_TIE_SAMPLED = 1e-5  # sampled: relative distance of u*sum(p) to an interval edge (at least; see
+                         # lockstep: widened to what the row's own logit error can move an edge)
 
 
 def rel_l1(a, b):
@@ -97,7 +99,13 @@ def lockstep(pc, W, prompt, n_gen, p=0.3, temperature=None, seed=3, eng=None, ch
         res.max_rel_l1, res.max_abs = max(res.max_rel_l1, r), max(res.max_abs, m)
         for i in range(B):
             if tt_g[i] != tt_o[i]:
-                assert cl[i] < lim, f"target token row {i} at n={n}: {tt_g[i]} vs {tt_o[i]} (closeness {cl[i]})"
+                lim_i = lim
+                if temperature is not None:
+                    # a logit error of at most d moves every p_j by a factor within exp(+-d/T), so each
+                    # cumulative edge, relative to the total, by at most expm1(2 d / T)
+                    d = float(np.abs(np.asarray(lg_g[i], np.float64) - np.asarray(lg_o[i], np.float64)).max())
+                    lim_i = max(lim, math.expm1(2.0 * d / temperature))
+                assert cl[i] < lim_i, f"target token row {i} at n={n}: {tt_g[i]} vs {tt_o[i]} (closeness {cl[i]})"
                 res.near_ties += 1
         a_o = oracle.accept_length(rows[1:], list(tt_g[:-1]))
         assert a_g == a_o, f"accepted {a_g} vs {a_o} at n={n}"
