@@ -377,7 +377,7 @@ def cpu_baseline(pc, W, args, tokens_per_step):
                           + t.n_heads * t.head_dim * t.hidden + t.hidden * 3 * t.ffn[l] + 2 * t.hidden * t.ple_dim
                           for l in range(t.n_layers)) + 8 * t.hidden * t.vocab
     share = _attention_share(pc, args.ctx) / weight_macs
-    # config 1 (the tiny pair), one thread
+    # the tiny pair, one speculative pass on one thread
     tiny = gen.tiny_pair()
     Wt = gen.generate(tiny)
     oracle.set_threads(1)
@@ -396,7 +396,7 @@ def cpu_baseline(pc, W, args, tokens_per_step):
             "sample": "one speculative pass (draft block + 8-row verify) of the E4B pair at a 4-token context, "
                       "scaled by the GPU run's tokens per pass",
             "seconds_per_pass": round(dt, 2), "attention_share_1024": round(share, 4),
-            "config1_one_thread": {"seconds_per_pass": round(dt1, 3), "threads": 1,
+            "tiny_pair_one_thread": {"seconds_per_pass": round(dt1, 3), "threads": 1,
                                    "sample": "tiny pair, one speculative pass after a 32-token prompt"}}
 
 
@@ -459,7 +459,7 @@ def bench_reference(args):
     print(json.dumps(out), flush=True)
 
 
-# Config 2 (the isolated product sweep): K x N shapes of the step's Q4_1 products and the bf16 head.
+# The isolated product sweep: K x N shapes of the step's Q4_1 products and the bf16 head.
 SWEEP_SHAPES = [("q41", 2560, 10240), ("q41", 10240, 2560), ("q41", 2560, 4096), ("q41", 2560, 20480),
                 ("q41", 20480, 2560), ("q41", 2560, 40960), ("q41", 3072, 2560), ("q41", 2560, 3584),
                 ("bf16_head", 2560, 262144)]
@@ -639,7 +639,7 @@ def bench_attn(args):
 
 
 def bench_gemm(args):
-    """Config 2 on its own: every shape of SWEEP_SHAPES (or --gemm-shape), rows --gemm-rows."""
+    """The isolated product sweep on its own: every shape of SWEEP_SHAPES (or --gemm-shape), rows --gemm-rows."""
     import torch
     from dflash_speculative_decode_gb300 import build
     build.build()
@@ -649,7 +649,7 @@ def bench_gemm(args):
         shapes = [("q41",) + tuple(int(v) for v in args.gemm_shape.split("x"))]
     rows = [int(v) for v in args.gemm_rows.split(",")]
     res = product_sweep(torch, shapes, rows, buf_bytes=args.gemm_bufs * 1e8, pk=pk)
-    print(json.dumps({"workload": "isolated Q4_1 product sweep (config 2) and the bf16 head", "peak_gbs": pk["hbm_gbs"],
+    print(json.dumps({"workload": "isolated Q4_1 product sweep and the bf16 head", "peak_gbs": pk["hbm_gbs"],
                       "results": res}), flush=True)
 
 

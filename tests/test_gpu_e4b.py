@@ -71,7 +71,7 @@ def test_e4b_commit_and_next_pass(e4b):
 
 
 def test_e4b_draft_alone_contexts(e4b):
-    """Config 3: the E4B draft on its own (5 layers, 32/8 heads of 128, window 1024, shared head of 262144)
+    """The E4B draft on its own (5 layers, 32/8 heads of 128, window 1024, shared head of 262144)
     over context rows made from N(0, 1) taps, at contexts of 30, 1024 and 4096 rows (the last wraps the
     1024-slot context ring four times): draft logits and proposals against the oracle's draft."""
     import torch

@@ -6,7 +6,7 @@ oracle finishes. One prefix of 1100 tokens, prefilled once on each side: the sli
 slots) have wrapped twice, the full layers read 35 key blocks spread over clusters of 16 CTAs.
 
 On top of that prefix: greedy speculative decode in lockstep with the oracle; the KV planes and the taps
-compared with the oracle's directly; and config 5 in miniature: sampled decode (T = 0.8) of requests A,
+compared with the oracle's directly; and long-context sampled serving in miniature: sampled decode (T = 0.8) of requests A,
 B, A, each after restoring the pinned prefix snapshot on both sides (FastFlowLM PR #899
 "gemma4e-dflash-flash", "Changes": a pinned prefix must not be overwritten by a request; the bug showed
 on a sequence A, B, A, B, A)."""
@@ -103,7 +103,7 @@ def test_cut_long_context_greedy_lockstep(cut):
 
 
 def test_cut_pinned_prefix_requests_a_b_a_sampled(cut):
-    """Config 5 in miniature: the prefix snapshot restored before each of requests A, B, A; sampled
+    """Long-context sampled serving in miniature: the prefix snapshot restored before each of requests A, B, A; sampled
     verify at T = 0.8 with planted drafts (p = 0.3); every pass against the oracle restored the same
     way. A's two runs give the same tokens."""
     from gpu_harness import lockstep
