@@ -7,10 +7,13 @@ calls (proposals copied in from host memory, proposals and target tokens copied 
 `roofline` reports the Q4_1 products (the dominant kernel) against the measured HBM copy bandwidth;
 `cpu_baseline` times the oracle on a bounded sample of the same workload.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference] [--workload e4b|gemm|cut|27b]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+                  [--workload e4b|gemm|cut|27b|prefill|attn|long]
 
 `--workload 27b` runs the same step on the 27B-class pair (62 dense layers of width 5376, 16 GB of Q4_1
-weights); `cut` is a 12-layer E4B cut for profiling captures; `gemm` the isolated product sweep.
+weights); `cut` is a 12-layer E4B cut for profiling captures; `gemm` the isolated product sweep;
+`prefill` the tcgen05 product at many rows; `attn` a short attention profiling workload; `long` sampled
+serving at long contexts over a pinned prefix (requests A, B, A). Only the default prints the bench line.
 """
 from __future__ import annotations
 
@@ -638,6 +641,129 @@ def bench_attn(args):
                       "attention_launches_per_step": pc.target.n_layers + pc.draft.n_layers}), flush=True)
 
 
+def _sampled_spec(eng, table, first, n_gen, temperature, seed):
+    """Speculative decode from the current state until n_gen tokens: draft block, planted proposals from
+    the device table, sampled verify of the block, commit of the accepted rows. Returns the tokens and
+    the passes."""
+    from dflash_speculative_decode_gb300 import DFL_KEEP_ACCEPTED
+    B = eng.cfg.block
+    out, last, passes = [first], first, 0
+    while len(out) < n_gen:
+        eng.dfl_draft_block(last, want=False)
+        eng.dfl_plant_proposals(table)
+        tt, a = eng.dfl_verify_block(None, k=B, temperature=temperature, seed=seed)
+        eng.dfl_commit_verify_rows(DFL_KEEP_ACCEPTED)
+        out += [int(v) for v in tt[:a + 1]]
+        last = int(tt[a])
+        passes += 1
+    return out, passes
+
+
+def bench_long(args):
+    """Long-context sampled serving of the E4B pair, at each context of --long-ctx: a prefix of --prefix
+    tokens is prefilled once and pinned as a device snapshot; requests A, B, A each restore the pin,
+    prefill their own prompt up to the context, and decode --gen tokens speculatively at temperature
+    --temperature with planted drafts (corruption p). Before each timed decode a plain sampled decode of
+    the same request (untimed) gives the target's own tokens; they plant the drafts, and the speculative
+    tokens must equal them exactly, since sampling is keyed by seed and absolute position and a row's
+    logits do not depend on the rows verified beside it. A's two runs must give the same tokens
+    (FastFlowLM PR #899 "gemma4e-dflash-flash", "Changes": the pinned prefix is restored, never
+    overwritten). Prints one JSON line (not the bench line)."""
+    import torch
+    from dflash_speculative_decode_gb300 import build
+    build.build()
+    T = args.temperature
+    requests = [("A", 1, 11), ("B", 2, 12), ("A", 1, 11)]   # (name, prompt request id, sampling seed)
+    clk = Clocks(0)
+    clk.start()
+    t_first = None
+    results = []
+    for ctx in [int(v) for v in args.long_ctx.split(",")]:
+        if ctx <= args.prefix + 16:
+            raise SystemExit(f"--long-ctx {ctx} must exceed --prefix {args.prefix} + 16")
+        pc = gen.e4b_pair(max_ctx=ctx + args.gen + 64)
+        eng, _, t_load = load_engine(pc, prefill_rows=args.prefill_rows)
+        V, L = pc.target.vocab, pc.max_ctx + 32
+        prefix = gen.prompt(V, args.prefix, request=100)
+        empty = eng.dfl_snapshot()
+        # warm-up: the prefix's passes, plain and speculative sampled passes (graphs, kernel attributes)
+        t = eng.dfl_prefill(prefix, T, 1)
+        eng.dfl_verify_block([t], temperature=T, seed=1)
+        eng.dfl_commit_verify_rows(1)
+        warm = torch.zeros(L, dtype=torch.int32, device="cuda")
+        _sampled_spec(eng, warm, t, 12, T, 1)
+        eng.dfl_restore(empty)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        eng.dfl_prefill(prefix, T, 1)
+        torch.cuda.synchronize()
+        t_prefix = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        pin = eng.dfl_snapshot()
+        torch.cuda.synchronize()
+        t_snap = time.perf_counter() - t0
+        reqs, tot_tok, tot_ms, tot_pass = [], 0, 0.0, 0
+        for name, rid, seed in requests:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            eng.dfl_restore(pin)
+            torch.cuda.synchronize()
+            t_restore = time.perf_counter() - t0
+            prompt = gen.prompt(V, ctx - args.prefix, request=rid)
+            t0 = time.perf_counter()
+            first = eng.dfl_prefill(prompt, T, seed)
+            torch.cuda.synchronize()
+            t_pf = time.perf_counter() - t0
+            n0 = eng.dfl_positions_held()
+            after_prompt = eng.dfl_snapshot()
+            plain = [first]                                  # the target's own sampled tokens (untimed)
+            while len(plain) < args.gen:
+                tt, _ = eng.dfl_verify_block([plain[-1]], temperature=T, seed=seed)
+                eng.dfl_commit_verify_rows(1)
+                plain.append(int(tt[0]))
+            G = np.zeros(L, np.int32)
+            G[n0:n0 + len(plain)] = plain
+            table = torch.from_numpy(gen.corruption(args.p, V, L, request=rid).propose(G, np.arange(L))).cuda()
+            eng.dfl_restore(after_prompt)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            tw = time.time()
+            t_first = t_first or tw
+            e0.record()
+            out, passes = _sampled_spec(eng, table, first, args.gen, T, seed)
+            e1.record()
+            torch.cuda.synchronize()
+            clk.window(t_first, time.time())
+            ms = e0.elapsed_time(e1)
+            emitted = len(out) - 1                            # the first token came from the prefill
+            tot_tok, tot_ms, tot_pass = tot_tok + emitted, tot_ms + ms, tot_pass + passes
+            reqs.append({"request": name, "seed": seed, "positions_before_decode": n0,
+                         "prefill_s": round(t_pf, 4), "prefill_tokens_per_s": round((ctx - args.prefix) / t_pf, 1),
+                         "restore_ms": round(t_restore * 1e3, 3), "decode_ms": round(ms, 3),
+                         "tokens_per_s": round(emitted / (ms / 1e3), 2), "passes": passes,
+                         "tokens_per_pass": round(emitted / passes, 3),
+                         "spec_equals_plain": out[:args.gen] == plain[:args.gen], "tokens": out[:args.gen]})
+        a_repeat = reqs[0]["tokens"] == reqs[2]["tokens"]
+        for r in reqs:
+            del r["tokens"]
+        results.append({"context": ctx, "tokens_per_s": round(tot_tok / (tot_ms / 1e3), 2),
+                        "ms_per_pass": round(tot_ms / tot_pass, 4), "tokens_per_pass": round(tot_tok / tot_pass, 3),
+                        "prefix_prefill_s": round(t_prefix, 4), "snapshot_bytes": int(pin.numel()),
+                        "snapshot_ms": round(t_snap * 1e3, 3), "load_s": round(t_load, 1),
+                        "a_repeats_exactly": a_repeat,
+                        "spec_equals_plain": all(r["spec_equals_plain"] for r in reqs), "requests": reqs})
+        del eng, pin, empty, after_prompt, table, warm
+        torch.cuda.empty_cache()
+    clocks = clk.stop()
+    print(json.dumps({"workload": "long-context sampled serving, e4b pair, pinned prefix, requests A, B, A",
+                      "metric": "decode tokens/s (device-timed speculative passes, prefill excluded)",
+                      "temperature": T, "prefix": args.prefix, "generated_per_request": args.gen,
+                      "corruption_p": args.p, "block": 8, "prefill_rows": args.prefill_rows,
+                      "dtype": "fp32 activations, Q4_1/bf16 weights",
+                      "data": "synthetic (seeded random-init weights of the E4B-shaped pair, uniform prompts)",
+                      "results": results, "clocks": clocks}), flush=True)
+
+
 def bench_gemm(args):
     """The isolated product sweep on its own: every shape of SWEEP_SHAPES (or --gemm-shape), rows --gemm-rows."""
     import torch
@@ -659,7 +785,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b", "prefill", "attn"])
+    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b", "prefill", "attn", "long"])
     ap.add_argument("--attn-pair", default="e4b", choices=["e4b", "27b"], help="layers of --workload attn")
     ap.add_argument("--prefill-rows", type=int, default=1024,
                     help="rows per long prefill pass (tcgen05 products); 0 = passes of 16 rows")
@@ -670,6 +796,9 @@ def main():
     ap.add_argument("--gemm-bufs", type=int, default=40, help="sweep: cycle at least this many x 100 MB of images")
     ap.add_argument("--gemm-shape", default="", help="one KxN shape for the product sweep")
     ap.add_argument("--gemm-rows", default="1,2,4,8,16", help="row counts of the product sweep")
+    ap.add_argument("--long-ctx", default="4096,16384", help="contexts of --workload long")
+    ap.add_argument("--prefix", type=int, default=512, help="pinned prefix tokens of --workload long")
+    ap.add_argument("--temperature", type=float, default=0.8, help="sampling temperature of --workload long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="leave the product sweep out of the bench line")
     args = ap.parse_args()
@@ -681,6 +810,8 @@ def main():
         return bench_prefill(args)
     if args.workload == "attn":
         return bench_attn(args)
+    if args.workload == "long":
+        return bench_long(args)
     return bench_cuda(args)
 
 

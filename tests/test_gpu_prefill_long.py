@@ -90,3 +90,33 @@ def test_long_prefill_full_shapes(cut):
     if res.near_ties == 0:
         assert res.tokens == [int(t) for t in plain.tokens]
     assert res.max_rel_l1 < 1e-3
+
+
+@pytest.mark.parametrize("temperature", [None, 0.8])
+def test_long_passes_after_restored_prefix(pair, temperature):
+    """Long passes that start past position 0, as single-turn serving runs them: a 40-token prefix on
+    both sides, pinned by snapshot; another request's 150-token prompt over it on the GPU (one long pass
+    at position 40); the prefix restored on both sides; then a 300-token prompt in two long passes of
+    128 rows (at positions 40 and 168) and 16-row passes for the rest, and speculative decode in
+    lockstep with the oracle."""
+    import dataclasses
+    import oracle
+    from gpu_harness import lockstep
+    pc0, W = pair
+    pc = dataclasses.replace(pc0, max_ctx=512)
+    V = pc.target.vocab
+    eng = _engine(pc, W, 128)
+    op = oracle.Pair(pc, W)
+    prefix = gen.prompt(V, 40, request=21)
+    eng.dfl_prefill(prefix, temperature, 5)
+    op.prefill(prefix, oracle.Sampler(temperature, 5))
+    snap_g, snap_o = eng.dfl_snapshot(), op.snapshot()
+    eng.dfl_prefill(gen.prompt(V, 150, request=22), temperature, 5)
+    assert eng.dfl_positions_held() == 190
+    eng.dfl_restore(snap_g)
+    op.restore(snap_o)
+    res, plain = lockstep(pc, W, gen.prompt(V, 300, request=23), 12, p=0.3, temperature=temperature, seed=5,
+                          eng=eng, op=op)
+    if res.near_ties == 0:
+        assert res.tokens == [int(t) for t in plain.tokens]
+    assert res.max_rel_l1 < 1e-3
