@@ -8,12 +8,13 @@ calls (proposals copied in from host memory, proposals and target tokens copied 
 `cpu_baseline` times the oracle on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
-                  [--workload e4b|gemm|cut|27b|prefill|attn|long]
+                  [--workload e4b|gemm|cut|27b|prefill|attn|long|draft]
 
 `--workload 27b` runs the same step on the 27B-class pair (62 dense layers of width 5376, 16 GB of Q4_1
 weights); `cut` is a 12-layer E4B cut for profiling captures; `gemm` the isolated product sweep;
 `prefill` the tcgen05 product at many rows; `attn` a short attention profiling workload; `long` sampled
-serving at long contexts over a pinned prefix (requests A, B, A). Only the default prints the bench line.
+serving at long contexts over a pinned prefix (requests A, B, A); `draft` the draft on its own at contexts
+of 30, 1024 and 4096 rows. Only the default prints the bench line.
 """
 from __future__ import annotations
 
@@ -764,6 +765,66 @@ def bench_long(args):
                       "results": results, "clocks": clocks}), flush=True)
 
 
+def draft_block_bytes(pc, ctx):
+    """Algorithmic bytes of one draft block: the draft layers' Q4_1 images (0.625 bytes per weight), the
+    shared bf16 head once, and the context keys and values the block's attention reads (fp32 planes,
+    at most the draft's window of rows)."""
+    d, H = pc.draft, pc.target.hidden
+    per_layer = (H * (d.n_heads + 2 * d.n_kv_heads) * d.head_dim + d.n_heads * d.head_dim * H
+                 + H * 2 * d.ffn + d.ffn * H)
+    rows = min(ctx, d.window) if d.window > 0 else ctx
+    kv = d.n_layers * rows * 2 * d.n_kv_heads * d.head_dim * 4
+    return d.n_layers * per_layer * 0.625 + pc.target.vocab * H * 2 + kv
+
+
+def bench_draft(args):
+    """The E4B draft on its own: its context made of --draft-ctx rows of N(0, 1) taps (not timed), then
+    --steps seeded blocks (8 rows: the last token and 7 mask tokens at the next positions; 5 layers;
+    proposals from the shared head) timed back to back with device events. Each block reads the
+    draft's weights and the 1.34 GB head once, so no L2 flush is needed. Prints one JSON line (not the
+    bench line)."""
+    import torch
+    from dflash_speculative_decode_gb300 import build
+    build.build()
+    pk = peaks()
+    ctxs = [int(v) for v in args.draft_ctx.split(",")]
+    pc = gen.e4b_pair(max_ctx=max(ctxs) + 64)
+    eng, _, t_load = load_engine(pc)
+    taps = torch.from_numpy(gen.fc_taps(max(ctxs), len(pc.draft.taps) * pc.target.hidden)).cuda()
+    toks = [int(v) for v in gen.prompt(pc.target.vocab, args.steps + args.warmup, request=7)]
+    clk = Clocks(0)
+    clk.start()
+    t_first, have, res = None, 0, []
+    for ctx in ctxs:
+        eng.dfl_draft_append_taps(taps[have:ctx])
+        have = ctx
+        for t in toks[:args.warmup]:
+            eng.dfl_draft_block(t, want=False)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tw = time.time()
+        t_first = t_first or tw
+        l0 = eng.dfl_launch_count()
+        e0.record()
+        for t in toks[args.warmup:]:
+            eng.dfl_draft_block(t, want=False)
+        e1.record()
+        torch.cuda.synchronize()
+        clk.window(t_first, time.time())
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        by = draft_block_bytes(pc, ctx)
+        res.append({"context": ctx, "us_per_block": round(us, 2), "blocks_per_s": round(1e6 / us, 1),
+                    "launches_per_block": round((eng.dfl_launch_count() - l0) / args.steps, 1),
+                    "algorithmic_bytes_per_block": int(by), "GB/s": round(by / us / 1e3, 1),
+                    "frac_measured": round(by / us / 1e3 / pk["hbm_gbs"], 4), "frac_8TBs": round(by / us / 8e6, 4)})
+    clocks = clk.stop()
+    print(json.dumps({"workload": "E4B draft alone (5 layers, window 1024, shared head 2560 x 262144), "
+                                  "context from N(0, 1) taps", "blocks_timed": args.steps, "warmup": args.warmup,
+                      "peak_gbs": pk["hbm_gbs"], "peak_source": pk["src"], "load_s": round(t_load, 1),
+                      "dtype": "fp32 activations, Q4_1/bf16 weights", "data": "synthetic",
+                      "results": res, "clocks": clocks}), flush=True)
+
+
 def bench_gemm(args):
     """The isolated product sweep on its own: every shape of SWEEP_SHAPES (or --gemm-shape), rows --gemm-rows."""
     import torch
@@ -785,7 +846,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b", "prefill", "attn", "long"])
+    ap.add_argument("--workload", default="e4b", choices=["e4b", "gemm", "cut", "27b", "prefill", "attn", "long", "draft"])
     ap.add_argument("--attn-pair", default="e4b", choices=["e4b", "27b"], help="layers of --workload attn")
     ap.add_argument("--prefill-rows", type=int, default=1024,
                     help="rows per long prefill pass (tcgen05 products); 0 = passes of 16 rows")
@@ -799,6 +860,7 @@ def main():
     ap.add_argument("--long-ctx", default="4096,16384", help="contexts of --workload long")
     ap.add_argument("--prefix", type=int, default=512, help="pinned prefix tokens of --workload long")
     ap.add_argument("--temperature", type=float, default=0.8, help="sampling temperature of --workload long")
+    ap.add_argument("--draft-ctx", default="30,1024,4096", help="contexts of --workload draft")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="leave the product sweep out of the bench line")
     args = ap.parse_args()
@@ -812,6 +874,8 @@ def main():
         return bench_attn(args)
     if args.workload == "long":
         return bench_long(args)
+    if args.workload == "draft":
+        return bench_draft(args)
     return bench_cuda(args)
 
 
