@@ -132,6 +132,9 @@ struct dfl_ctx {
     bool fuse_steps = false;  // the row and q/k steps run on the products' last CTAs (DFL_OPT_FUSE_STEPS)
     bool ple_split = false;   // the PLE gate and projection as two products (DFL_OPT_PLE_SPLIT)
     bool draft_only = false, keep_logits = false, have_logits = false, have_dlogits = false;
+    // a failed prefill may have overwritten ring slots (sliding planes, the draft context) that the
+    // positions held still need: passes and snapshots are refused until a restore
+    bool needs_restore = false;
     int last_k = 0;
     int stop_layer = -1;   // debug: a target pass runs layers 0..stop_layer only (no head)
     int attn_cluster = 16; // largest attention cluster size allowed: 16, 8 or 4
@@ -1100,6 +1103,8 @@ int check_tokens(dfl_ctx *c, const int32_t *t, int n) {
 }
 
 int ready(dfl_ctx *c) {
+    if (c->needs_restore)
+        return fail(c, DFL_E_STATE, "a failed prefill may have overwritten ring slots of the held positions: restore a snapshot");
     auto chk = [&](bool ok, const char *what) { return ok ? DFL_OK : fail(c, DFL_E_STATE, std::string("tensor not loaded: ") + what); };
     int rc;
     if ((rc = chk(c->emb.loaded && c->head.loaded && c->final_norm.loaded, "emb/head/final_norm"))) return rc;
@@ -1289,6 +1294,17 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
     if ((rc = check_tokens(c, tokens, n))) return rc;
     const bool sampled = s && s->temperature > 0.f;
     const int n_start = c->n;
+    // On an error after the first pass was enqueued none of the rows counts. The passes already run
+    // may have written ring slots that positions held still need (more rows than a ring's slack, or
+    // rows of the draft context's window), so the context also refuses passes until a restore.
+    auto failed = [&](int rc_) {
+        c->n = n_start;
+        c->draft_n = std::min(c->draft_n, n_start);
+        c->draft_n_ok = std::min(c->draft_n_ok, c->draft_n);
+        c->draft_at = -1;
+        c->needs_restore = n_start > 0;   // an empty context has no slot to lose
+        return rc_;
+    };
     int done = 0;
     const int PF = c->cfg.prefill_rows;
     while (done < n) {
@@ -1296,26 +1312,21 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
         const bool longp = PF > 0 && n - done >= 128;
         const int k = longp ? std::min(PF, n - done) : std::min(kMaxRows, n - done);
         const bool last = done + k == n;
-        if ((rc = set_state(c, k, tokens + done, false, 0, -1, s))) return rc;
+        if ((rc = set_state(c, k, tokens + done, false, 0, -1, s))) return failed(rc);
         if (longp) {
             if (cudaMemcpyAsync(c->pf_tok, tokens + done, sizeof(int32_t) * k, cudaMemcpyHostToDevice, c->stream) !=
                 cudaSuccess)
-                return fail(c, DFL_E_CUDA, "prefill token copy failed");
-            if ((rc = prefill_long(c, k, last, sampled))) return rc;
+                return failed(fail(c, DFL_E_CUDA, "prefill token copy failed"));
+            if ((rc = prefill_long(c, k, last, sampled))) return failed(rc);
         } else if ((rc = run_target(c, k, last, sampled, true))) {
-            return rc;
+            return failed(rc);
         }
         c->n += k;
         done += k;
     }
-    if ((rc = catch_up(c, 0))) return rc;
+    if ((rc = catch_up(c, 0))) return failed(rc);
     DevState hs;
-    if ((rc = read_state(c, &hs))) {
-        c->n = n_start;   // none of the chunks counts
-        c->draft_n = std::min(c->draft_n, n_start);
-        c->draft_n_ok = c->draft_n;
-        return rc;
-    }
+    if ((rc = read_state(c, &hs))) return failed(rc);
     if (next_tok) *next_tok = hs.target[0];   // the head ran on the last row only
     c->last_k = 1;                            // logits of that row
     c->draft_at = -1;
@@ -1410,6 +1421,7 @@ int64_t dfl_snapshot_bytes(const dfl_ctx *c) {
 int dfl_snapshot(dfl_ctx *c, void *dst, size_t bytes) {
     if (!c) return DFL_E_INVALID_ARG;
     if (c->pending) return fail(c, DFL_E_STATE, "snapshot needs the committed state");
+    if (c->needs_restore) return fail(c, DFL_E_STATE, "a failed prefill left the state unusable: restore first");
     if (!dst) return fail(c, DFL_E_INVALID_ARG, "null destination");
     const size_t need = snapshot_size(c, c->n, c->draft_n);
     if (bytes < need) return fail(c, DFL_E_INVALID_ARG, "snapshot buffer too small");
@@ -1487,6 +1499,7 @@ int dfl_restore(dfl_ctx *c, const void *src, size_t bytes) {
     c->draft_n_ok = hdr.draft_n;
     c->draft_at = -1;
     c->draft_only = false;
+    c->needs_restore = false;
     return DFL_OK;
 }
 

@@ -130,10 +130,15 @@ int dfl_load_tensor(dfl_ctx *ctx, const char *name, const void *dev_src, size_t 
 
 /* Prefill (extend the context; 1bit engine PR "npu forward: Gemma4 verifies a draft in one batched
  * pass; KV row width per layer", "What changes" item 1, extend_context): run the n tokens at positions
- * held..held+n-1 in chunks of at most DFL_MAX_ROWS rows, commit them, bring the draft context up to date,
+ * held..held+n-1 in passes, commit them, bring the draft context up to date,
  * and write the target's token for the next position to *next_tok (greedy or sampled). The output
- * head runs on the last prompt row only: only that row's token is needed. Fails with
- * DFL_E_CAPACITY if held + n exceeds max_ctx; on any error positions held stay as they were. */
+ * head runs on the last prompt row only: only that row's token is needed. Passes: with prefill_rows > 0,
+ * min(prefill_rows, remaining) rows while 128 or more remain (products on tcgen05), then passes of at
+ * most DFL_MAX_ROWS rows; with prefill_rows = 0, passes of at most DFL_MAX_ROWS rows. Fails with
+ * DFL_E_CAPACITY if held + n exceeds max_ctx; on any error positions held stay as they were. An error
+ * after the first pass was enqueued (DFL_E_TIMEOUT, DFL_E_CUDA) on a context that held positions
+ * leaves it refusing passes and snapshots with DFL_E_STATE until dfl_restore succeeds: the passes that
+ * ran may have overwritten sliding-ring and draft-context slots those positions still need. */
 int dfl_prefill(dfl_ctx *ctx, const int32_t *tokens, int n, const dfl_sampling *s, int32_t *next_tok);
 
 /* Draft block (model card "Nemotron-3.5-Bolt-E4B-DFlash-NPU2", "How it is used"; 1bit engine PR "a
