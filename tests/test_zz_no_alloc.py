@@ -1,7 +1,7 @@
 """The product with library-owned scratch (dfl_q41_gemm_noalloc) against dfl_q41_gemm.
 
-Collected last (file name), so it also runs after every other GPU test in the same process; it passes
-alone in a fresh process as well. Two calls in a row check that the shared static scratch is left in a
+Collected after the parity files (file name), so it also runs after them in the same process; it
+passes alone in a fresh process as well. Two calls in a row check that the shared static scratch is left in a
 usable state (arrival counters back at zero) by each call.
 """
 import ctypes
