@@ -24,6 +24,23 @@
 #include "dfl.h"
 #include "rowstep.cuh"
 
+// A named NVTX range around each pass-level call, so that a profiler's timeline (and ncu's --nvtx-include
+// filter) can tell prefill, draft and verify passes apart. The NVTX v3 header needs no library; without a
+// tool attached the calls do nothing. A toolkit without the header builds the ranges as no-ops.
+#if __has_include(<nvtx3/nvToolsExt.h>)
+#include <nvtx3/nvToolsExt.h>
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#else
+struct NvtxRange {
+    explicit NvtxRange(const char *) {}
+};
+#endif
+
 namespace dfl {
 size_t attn_smem(int M, int hd);
 }  // namespace dfl
@@ -1284,6 +1301,7 @@ int dfl_load_tensor(dfl_ctx *c, const char *name, const void *src, size_t bytes)
 }
 
 int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s, int32_t *next_tok) {
+    NvtxRange nvtx("dfl_prefill");
     if (!c) return DFL_E_INVALID_ARG;
     if (!tokens || n < 1) return fail(c, DFL_E_INVALID_ARG, "prefill needs at least one token");
     if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending: commit it first");
@@ -1334,6 +1352,7 @@ int dfl_prefill(dfl_ctx *c, const int32_t *tokens, int n, const dfl_sampling *s,
 }
 
 int dfl_draft_block(dfl_ctx *c, int32_t last_tok, int32_t *proposals) {
+    NvtxRange nvtx("dfl_draft_block");
     if (!c) return DFL_E_INVALID_ARG;
     if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending: commit it first");
     if (last_tok < 0 || last_tok >= c->cfg.vocab) return fail(c, DFL_E_INVALID_ARG, "token id out of range");
@@ -1353,6 +1372,7 @@ int dfl_draft_block(dfl_ctx *c, int32_t last_tok, int32_t *proposals) {
 
 int dfl_verify_block(dfl_ctx *c, const int32_t *rows_in, int k, const dfl_sampling *s, int32_t *target_tok,
                      int32_t *accepted) {
+    NvtxRange nvtx("dfl_verify_block");
     if (!c) return DFL_E_INVALID_ARG;
     if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending: commit it first");
     if (c->draft_only) return fail(c, DFL_E_STATE, "context holds draft-only rows");
@@ -1419,6 +1439,7 @@ int64_t dfl_snapshot_bytes(const dfl_ctx *c) {
 }
 
 int dfl_snapshot(dfl_ctx *c, void *dst, size_t bytes) {
+    NvtxRange nvtx("dfl_snapshot");
     if (!c) return DFL_E_INVALID_ARG;
     if (c->pending) return fail(c, DFL_E_STATE, "snapshot needs the committed state");
     if (c->needs_restore) return fail(c, DFL_E_STATE, "a failed prefill left the state unusable: restore first");
@@ -1460,6 +1481,7 @@ int dfl_snapshot(dfl_ctx *c, void *dst, size_t bytes) {
 }
 
 int dfl_restore(dfl_ctx *c, const void *src, size_t bytes) {
+    NvtxRange nvtx("dfl_restore");
     if (!c) return DFL_E_INVALID_ARG;
     if (c->pending) return fail(c, DFL_E_STATE, "restore needs the committed state");
     if (!src || bytes < sizeof(SnapHeader)) return fail(c, DFL_E_INVALID_ARG, "snapshot too small");
@@ -1581,6 +1603,7 @@ int dfl_read_taps(dfl_ctx *c, int pos0, int rows, float *dst) {
 }
 
 int dfl_draft_append_taps(dfl_ctx *c, const void *src, int rows) {
+    NvtxRange nvtx("dfl_draft_append_taps");
     if (!c) return DFL_E_INVALID_ARG;
     if (!src || rows < 1) return fail(c, DFL_E_INVALID_ARG, "bad taps");
     if (c->pending) return fail(c, DFL_E_STATE, "a verify is pending");
