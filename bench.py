@@ -164,10 +164,11 @@ def planted_table(torch, eng, pc, first, n_gen, p):
     return snap, toks, torch.from_numpy(table).cuda()
 
 
-def run_steps(eng, torch, table_dev, first_tok, snap, n0, steps, n_gen, host_rows=None):
+def run_steps(eng, torch, table_dev, first_tok, snap, n0, steps, n_gen, host_rows=None, accepted=None):
     """`steps` speculative passes; a 512-token decode that runs out restarts from the prefix snapshot.
     Device mode: proposals planted from the device table. Host mode (host_rows = host table): proposals
-    read back to host, planted there, and passed in host memory."""
+    read back to host, planted there, and passed in host memory. `accepted`, when a list, receives each
+    pass's accepted length."""
     from dflash_speculative_decode_gb300 import DFL_KEEP_ACCEPTED
     B = eng.cfg.block
     tokens = 0
@@ -190,7 +191,18 @@ def run_steps(eng, torch, table_dev, first_tok, snap, n0, steps, n_gen, host_row
         last = int(tt[a])
         tokens += a + 1
         produced += a + 1
+        if accepted is not None:
+            accepted.append(a)
     return tokens
+
+
+def acceptance(accepted, block):
+    """Accepted proposals per pass, their histogram over 0..block-1, and the first proposal's hit rate."""
+    n = max(len(accepted), 1)
+    hist = [sum(1 for a in accepted if a == i) for i in range(block)]
+    return {"accepted_per_pass": round(sum(accepted) / n, 4), "tokens_per_pass": round(1 + sum(accepted) / n, 4),
+            "histogram": hist, "first_proposal_hit_rate": round(sum(1 for a in accepted if a >= 1) / n, 4),
+            "passes": len(accepted)}
 
 
 def combine_ranks(torch, ms: float, toks: float, device) -> tuple:
@@ -289,7 +301,8 @@ def bench_cuda(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     e0.record(stream)
-    toks = run_steps(eng, torch, table, first, snap, n0, args.steps, args.gen)
+    acc = []
+    toks = run_steps(eng, torch, table, first, snap, n0, args.steps, args.gen, accepted=acc)
     e1.record(stream)
     torch.cuda.synchronize()
     clk.window(t_wall0, time.time())
@@ -327,6 +340,8 @@ def bench_cuda(args):
                    " pair, uniform prompt)",
            "config": dict(cfgdesc, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
            "tokens_per_step": round(toks_all / world / args.steps, 3),
+           "acceptance": dict(acceptance(acc, pc.draft.block), planted_p=args.p,
+                              expected_tokens_per_pass=round(1 + sum((1 - args.p) ** i for i in range(1, pc.draft.block)), 4)),
            "e2e": {"value": round(toks_e2e / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * pc.draft.block,
                    "d2h_bytes_per_step": 4 * (pc.draft.block - 1) + 4 * pc.draft.block + 4},
            "gpu_launches": launches, "roofline": roof, "clocks": clocks,

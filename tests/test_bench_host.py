@@ -1,8 +1,10 @@
 """The benchmark's host arithmetic on the CPU: the roofline figures it derives from the in-pass stamps,
-and the draft block's algorithmic bytes against the closed form of the draft's shapes."""
+the draft block's algorithmic bytes against the closed form of the draft's shapes, and the step loop's
+token and acceptance bookkeeping over a stand-in engine."""
 import hashlib
 import os
 
+import numpy as np
 import pytest
 
 import gen
@@ -67,3 +69,69 @@ def test_draft_block_bytes_closed_form():
         kv = 5 * min(ctx, 1024) * 2 * 8 * 128 * 4
         assert bench.draft_block_bytes(pc, ctx) == pytest.approx(weights * 0.625 + head + kv, rel=1e-12)
     assert bench.draft_block_bytes(pc, 4096) == bench.draft_block_bytes(pc, 1024)
+
+
+class _TruthEngine:
+    """Bookkeeping stand-in for run_steps: the target's token for position q is truth[q] whatever the
+    rows, proposals come from the planted table, and the calls keep positions held as the ABI does."""
+
+    def __init__(self, truth, block, n0):
+        from dflash_speculative_decode_gb300 import DFL_KEEP_ACCEPTED
+        self.truth, self.n, self.keep_code = truth, n0, DFL_KEEP_ACCEPTED
+        self.cfg = type("cfg", (), {"block": block})()
+        self.table = None
+        self.pending = None
+        self.restores = 0
+
+    def dfl_restore(self, snap):
+        self.n = snap
+        self.restores += 1
+
+    def dfl_positions_held(self):
+        return self.n
+
+    def dfl_draft_block(self, last, want=True):
+        return np.zeros(self.cfg.block - 1, np.int32) if want else None
+
+    def dfl_plant_proposals(self, table):
+        self.table = table
+
+    def dfl_verify_block(self, rows, k=None):
+        n, B = self.n, self.cfg.block
+        if rows is None:
+            rows = [0] + [int(v) for v in self.table[n + 1:n + B]]
+        tt = [int(self.truth[n + i + 1]) for i in range(len(rows))]
+        a = 0
+        while a < len(rows) - 1 and rows[1 + a] == tt[a]:
+            a += 1
+        self.pending = a
+        return np.asarray(tt, np.int32), a
+
+    def dfl_commit_verify_rows(self, keep):
+        assert keep == self.keep_code
+        self.n += self.pending + 1
+        self.pending = None
+
+
+@pytest.mark.parametrize("host", [False, True])
+def test_run_steps_counts_and_acceptance(host):
+    """run_steps counts a + 1 tokens per pass, restarts from the snapshot once a decode has produced
+    n_gen tokens, and reports every pass's accepted length; the first proposal's hit rate and the tokens
+    per pass match the planted corruption's expectations (1 - p, and 1 + sum_i (1 - p)^i)."""
+    B, p, n0, n_gen, steps = 8, 0.3, 40, 512, 3000
+    L = n0 + n_gen + 64
+    truth = np.random.default_rng(5).integers(0, 1000, size=L + 32).astype(np.int32)
+    table = gen.corruption(p, 1000, L + 32).propose(truth, np.arange(L + 32))
+    eng = _TruthEngine(truth, B, n0)
+    acc = []
+    toks = bench.run_steps(eng, None, table, int(truth[n0]), n0, n0, steps, n_gen,
+                           host_rows=table if host else None, accepted=acc)
+    assert len(acc) == steps and toks == sum(a + 1 for a in acc)
+    assert eng.restores >= toks // (n_gen + B) - 1
+    st = bench.acceptance(acc, B)
+    assert sum(st["histogram"]) == steps == st["passes"]
+    assert st["tokens_per_pass"] == pytest.approx(toks / steps, abs=1e-4)
+    # the corruption is keyed by position and every decode restarts from the same prefix, so the passes
+    # revisit one sample of about 170 pass positions: statistical tolerances of a few standard errors
+    assert st["first_proposal_hit_rate"] == pytest.approx(1 - p, abs=0.06)
+    assert st["tokens_per_pass"] == pytest.approx(1 + sum((1 - p) ** i for i in range(1, B)), rel=0.08)
