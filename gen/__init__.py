@@ -15,8 +15,9 @@ embeddings, double-wide MLP on shared layers).
 """
 from __future__ import annotations
 
+import json
 import zlib
-from dataclasses import dataclass, field, replace
+from dataclasses import asdict, dataclass, field, replace
 from typing import Dict, Iterator, Optional, Tuple
 
 import numpy as np
@@ -189,6 +190,33 @@ def b27_cut(max_ctx: int = 256, n_layers: int = 6, vocab: int = 32768) -> PairCo
 
 
 PAIRS = {"tiny": tiny_pair, "tiny-shared": tiny_shared_pair, "e4b": e4b_pair, "27b": b27_pair}
+
+_TYPE_NAMES = {SLIDING: "sliding", FULL: "full"}
+
+
+def pair_to_json(pc: PairConfig) -> str:
+    """The pair's configuration as one JSON document (layer types by name), the file form of a model
+    that config_from_pair mirrors into the library's dfl_config; pair_from_json reads it back."""
+    d = asdict(pc)
+    d["target"]["layer_type"] = [_TYPE_NAMES[t] for t in pc.target.layer_type]
+    return json.dumps(d, indent=1)
+
+
+def pair_from_json(text: str) -> PairConfig:
+    """A PairConfig from pair_to_json's document. Unknown or missing fields and unknown layer types are
+    refused (TypeError, ValueError) rather than defaulted."""
+    d = json.loads(text)
+    names = {v: k for k, v in _TYPE_NAMES.items()}
+    t = dict(d.pop("target"))
+    bad = [v for v in t.get("layer_type", []) if v not in names]
+    if bad:
+        raise ValueError(f"unknown layer types {bad}")
+    t["layer_type"] = tuple(names[v] for v in t["layer_type"])
+    for k in ("kv_heads", "kv_owner", "ffn"):
+        t[k] = tuple(int(v) for v in t[k])
+    dr = dict(d.pop("draft"))
+    dr["taps"] = tuple(int(v) for v in dr["taps"])
+    return PairConfig(TargetConfig(**t), DraftConfig(**dr), **d)
 
 
 # ----------------------------------------------------------------------------------------------
